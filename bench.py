@@ -1,0 +1,467 @@
+"""Benchmark of the block-float decode-in-kernel matmul on GB300.
+
+One step = one dense decode layer over MXFP4 weights at M = 1 token:
+fused QKV 10240x8192, FFN up/gate 57344x8192 and down 8192x28672, all
+through mx_qmv.  The headline value is weight GB/s (codes + block scales
+streamed per second); the same run also reports M = 4, the MoE decode layer
+(128 experts, top-8: gate-up, SwiGLU, down, combine) in tokens/s, the
+MXFP8 / NVFP4 format sweep and the prefill GEMM in TFLOP/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  Inputs are seeded synthetic tensors (see
+gemm_decode_register_gb300/synth.py).  The layer's 419 MB of weights are
+larger than the 129 MB L2, so each step streams them from HBM.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MXFP4 qmv weight GB/s (% of HBM peak); MoE tok/s; prefill qmm TFLOP/s"
+DENSE = [("qkv", 10240, 8192, 1), ("up_gate", 57344, 8192, 2), ("down", 8192, 28672, 3)]
+WORKLOAD = ("dense decode layer, MXFP4 weights (E2M1 codes, E8M0 scale per 32, exponents "
+            "uniform in [118,132]), bf16 activations N(0,1), M=1 token: fused QKV 10240x8192 + "
+            "FFN up/gate 57344x8192 + down 8192x28672 via mx_qmv")
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1939.6)), \
+            float(d.get("bf16_tflops_sustained", 1726.2)), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[tuple[float, str]] = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.index), "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.th = threading.Thread(target=self._read, daemon=True)
+        self.th.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for t, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((t, float(parts[0]), float(parts[1]), parts[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        inside = [r for r in rows if self.t0 and self.t1 and self.t0 <= r[0] <= self.t1]
+        use = inside or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside)}
+
+
+# ------------------------------------------------------------------ helpers
+
+def upload(torch, a):
+    return torch.from_numpy(np.ascontiguousarray(a).reshape(-1)).cuda()
+
+
+def bf16_dev(torch, bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def time_region(torch, fn, iters, stream):
+    """Average seconds per call of fn over iters calls (CUDA events)."""
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s.record(stream)
+    for _ in range(iters):
+        fn()
+    e.record(stream)
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / 1e3 / iters
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, rank, world, dist):
+    import torch
+
+    from gemm_decode_register_gb300 import build as b
+    from gemm_decode_register_gb300 import ops, synth
+
+    b.build()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    hbm, bf16_burst, bf16_sust, peak_kind = peaks()
+    F4 = synth.FMT_MXFP4
+
+    # ---- dense decode layer (the step)
+    layers = []
+    wbytes = 0
+    for name, N, K, seed in DENSE:
+        codes, scales = synth.weights(F4, N, K, seed, exp_lo=118, exp_hi=132)
+        x = synth.activations(1, K, 100 + seed)
+        layers.append({"name": name, "N": N, "K": K, "codes": upload(torch, codes),
+                       "scales": upload(torch, scales), "x": bf16_dev(torch, x),
+                       "x_host": torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory(),
+                       "y": torch.empty((1, N), dtype=torch.float32, device=dev),
+                       "y_host": torch.empty((1, N), dtype=torch.float32).pin_memory(),
+                       "bytes": codes.nbytes + scales.nbytes})
+        wbytes += codes.nbytes + scales.nbytes
+    alg_bytes = sum(L["bytes"] + L["K"] * 2 + L["N"] * 4 for L in layers)
+
+    def step():
+        for L in layers:
+            ops.qmv(F4, L["codes"], L["scales"], L["x"], L["N"], y=L["y"])
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+
+    clk = ClockSampler(dev.index)
+    clk.start()
+    time.sleep(0.3)
+    # per-launch events for the roofline of the qmv kernel
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(layers) + 1)] for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clk.mark("t0")
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        for j, L in enumerate(layers):
+            ops.qmv(F4, L["codes"], L["scales"], L["x"], L["N"], y=L["y"])
+            ev[i][j + 1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk.mark("t1")
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    if dist:
+        t = torch.tensor([elapsed], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+    launch_s = [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)) / 1e3 / args.steps
+                for j in range(len(layers))]
+    value = world * wbytes * args.steps / elapsed / 1e9
+    ms_per_step = elapsed / args.steps * 1e3
+    achieved = alg_bytes / sum(launch_s) / 1e9
+    per_layer = {L["name"]: round(L["bytes"] / s / 1e9, 1) for L, s in zip(layers, launch_s)}
+
+    # ---- end to end through the public API with host buffers
+    def e2e_step():
+        for L in layers:
+            L["x"].copy_(L["x_host"], non_blocking=True)
+            ops.qmv(F4, L["codes"], L["scales"], L["x"], L["N"], y=L["y"])
+            L["y_host"].copy_(L["y"], non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    e2e_t = time_region(torch, e2e_step, args.steps, stream)
+    clk.stop()
+    h2d = sum(L["K"] * 2 for L in layers)
+    d2h = sum(L["N"] * 4 for L in layers)
+
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16xf16->f32 (decoded MXFP4 x scaled bf16)", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "weight_bytes_per_step": wbytes,
+                   "l2": "inputs larger than L2: 419 MB of weights streamed per step (L2 129 MB)",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "per_projection_gbs": per_layer},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
+                     "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": None,
+                     "kernel": "qmv_kernel<MXFP4, MC=1>", "peak_source": peak_kind,
+                     "bytes_per_launch": round(alg_bytes / len(layers))},
+        "e2e": {"value": round(world * wbytes / e2e_t / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "note": "weights resident (model state); each step copies x in and y out"},
+        "gpu_launches": len(layers) * args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_extras and rank == 0:
+        out["extras"] = extras(torch, ops, synth, dev, stream, hbm, bf16_burst, bf16_sust, args)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        out["cpu_baseline"] = cpu_baseline(synth, budget_s=args.cpu_seconds)
+    return out
+
+
+def extras(torch, ops, synth, dev, stream, hbm, bf16_burst, bf16_sust, args):
+    """Secondary measurements of the other workloads (same run)."""
+    res = {}
+    F4, F8, NV = synth.FMT_MXFP4, synth.FMT_MXFP8, synth.FMT_NVFP4
+    iters = max(20, args.extra_iters)
+
+    # M = 4 dense layer
+    mats = []
+    for name, N, K, seed in DENSE:
+        codes, scales = synth.weights(F4, N, K, seed, exp_lo=118, exp_hi=132)
+        mats.append((N, K, upload(torch, codes), upload(torch, scales),
+                     bf16_dev(torch, synth.activations(4, K, 200 + seed)), codes.nbytes + scales.nbytes))
+    wb = sum(m[5] for m in mats)
+    for M in (1, 4):
+        def f(M=M):
+            for N, K, c, s, x, _ in mats:
+                ops.qmv(F4, c, s, x[: M * K].view(M, K), N)
+        for _ in range(3):
+            f()
+        t = time_region(torch, f, iters, stream)
+        res[f"dense_layer_M{M}"] = {"gbs": round(wb / t / 1e9, 1), "frac_hbm": round(wb / t / 1e9 / hbm, 4),
+                                   "us": round(t * 1e6, 2), "tok_s": round(M / t, 1)}
+    del mats
+
+    # format sweep on the FFN up/gate shape
+    N, K = 57344, 8192
+    for fmt, fname, seed in ((F4, "mxfp4", 2), (F8, "mxfp8", 6), (NV, "nvfp4", 7)):
+        codes, scales = synth.weights(fmt, N, K, seed, exp_lo=118, exp_hi=132)
+        c, s = upload(torch, codes), upload(torch, scales)
+        wbf = codes.nbytes + scales.nbytes
+        for M in (1, 4):
+            x = bf16_dev(torch, synth.activations(M, K, 300 + M)).view(M, K)
+            f = lambda: ops.qmv(fmt, c, s, x, N)  # noqa: E731
+            for _ in range(3):
+                f()
+            t = time_region(torch, f, iters, stream)  # 250-480 MB per call: larger than L2
+            res[f"sweep_{fname}_M{M}"] = {"gbs": round(wbf / t / 1e9, 1),
+                                         "frac_hbm": round(wbf / t / 1e9 / hbm, 4), "us": round(t * 1e6, 2)}
+        del c, s
+
+    # MoE decode layer: 128 experts, top-8, hidden 2048, expert intermediate 768
+    E, topk, H, I = 128, 8, 2048, 768
+    c1, s1 = synth.weights(F4, 2 * I, H, 40, E=E, exp_lo=118, exp_hi=132)
+    c2, s2 = synth.weights(F4, H, I, 41, E=E, exp_lo=118, exp_hi=132)
+    per_expert = (c1.nbytes + s1.nbytes + c2.nbytes + s2.nbytes) // E
+    d1, e1, d2, e2 = (upload(torch, a) for a in (c1, s1, c2, s2))
+    for T in (1, 4):
+        nsets = 64
+        ids_all = [synth.expert_ids(T, E, topk, 1000 * T + i) for i in range(nsets)]
+        uniq = [len(np.unique(a)) for a in ids_all]
+        ids_dev = [torch.from_numpy(a).cuda() for a in ids_all]
+        ids_flat = [a.reshape(-1, 1).contiguous() for a in ids_dev]
+        r = torch.from_numpy(synth.router_weights(T, topk, 77)).cuda()
+        x = bf16_dev(torch, synth.activations(T, H, 78)).view(T, H)
+        gu = torch.empty((T, topk, 2 * I), dtype=torch.float32, device=dev)
+        h = torch.empty((T * topk, I), dtype=torch.bfloat16, device=dev)
+        yd = torch.empty((T * topk, 1, H), dtype=torch.float32, device=dev)
+        out = torch.empty((T, H), dtype=torch.float32, device=dev)
+
+        def layer(i):
+            ops.moe_qmv(F4, d1, e1, x, ids_dev[i], E, 2 * I, y=gu)
+            ops.swiglu(gu, I, h=h)
+            ops.moe_qmv(F4, d2, e2, h, ids_flat[i], E, H, y=yd)
+            ops.moe_combine(yd, r, out=out)
+
+        def gemv_only(i):
+            ops.moe_qmv(F4, d1, e1, x, ids_dev[i], E, 2 * I, y=gu)
+            ops.moe_qmv(F4, d2, e2, h, ids_flat[i], E, H, y=yd)
+
+        # one CUDA graph per variant holds nsets layers, each with its own routing
+        graphs = {}
+        for name, fn in (("layer", layer), ("gemv", gemv_only)):
+            for i in range(3):
+                fn(i)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for i in range(nsets):
+                    fn(i)
+            graphs[name] = g
+        reps = max(4, iters // 8)
+        t = time_region(torch, graphs["layer"].replay, reps, stream) / nsets
+        t2 = time_region(torch, graphs["gemv"].replay, reps, stream) / nsets
+        ub = statistics.mean(uniq) * per_expert
+        res[f"moe_layer_T{T}"] = {"tok_s": round(T / t, 1), "us_layer": round(t * 1e6, 2),
+                                  "us_gemv_only": round(t2 * 1e6, 2),
+                                  "unique_expert_gbs": round(ub / t2 / 1e9, 1),
+                                  "frac_hbm_gemv": round(ub / t2 / 1e9 / hbm, 4),
+                                  "mean_unique_experts": round(statistics.mean(uniq), 2),
+                                  "note": "CUDA graph of 64 layers, each with freshly drawn expert ids"}
+    del d1, e1, d2, e2
+
+    # prefill qmm
+    try:
+        for N, K, seed in ((28672, 8192, 8), (8192, 28672, 9)):
+            M = 4096
+            codes, scales = synth.weights(F4, N, K, seed, exp_lo=118, exp_hi=132)
+            c, s = upload(torch, codes), upload(torch, scales)
+            X = torch.randn(M, K, device=dev).to(torch.bfloat16)
+            Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            f = lambda: ops.qmm(F4, c, s, X, N, Y=Y)  # noqa: E731
+            for _ in range(3):
+                f()
+            t = time_region(torch, f, max(5, iters // 4), stream)
+            tf = 2.0 * M * N * K / t / 1e12
+            res[f"prefill_qmm_{N}x{K}"] = {"tflops": round(tf, 1), "frac_bf16_burst": round(tf / bf16_burst, 4),
+                                          "frac_bf16_sustained": round(tf / bf16_sust, 4),
+                                          "ms": round(t * 1e3, 3)}
+            del c, s, X, Y
+    except Exception as exc:  # reported, not hidden
+        res["prefill_qmm"] = {"error": str(exc).splitlines()[0][:200]}
+    return res
+
+
+# ------------------------------------------------------------------ oracle
+
+def cpu_baseline(synth, budget_s=12.0):
+    """The oracle (single-threaded C, fp64) on a bounded sample of the same
+    layer: leading rows of each projection, growing until about budget_s of
+    CPU time; value in the same unit (weight GB/s)."""
+    import oracle
+
+    orc = oracle.get()
+    F4 = synth.FMT_MXFP4
+    data = []
+    for name, N, K, seed in DENSE:
+        codes, scales = synth.weights(F4, N, K, seed, exp_lo=118, exp_hi=132)
+        data.append((name, N, K, codes, scales, synth.activations(1, K, 100 + seed)))
+    rows = 16
+    spent = 0.0
+    done_bytes = 0
+    done_rows = 0
+    while spent < budget_s and rows <= 8192:
+        for name, N, K, codes, scales, x in data:
+            r = np.arange(min(rows, N))
+            t0 = time.perf_counter()
+            orc.qmv_rows(F4, codes, scales, x, 1, N, K, r)
+            spent += time.perf_counter() - t0
+            done_bytes += r.size * (K // 2 + K // 32)
+            done_rows += r.size
+        rows *= 2
+    return {"value": round(done_bytes / spent / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done_rows} weight rows (leading rows of QKV, up/gate, down), "
+                      f"{spent:.1f} s single-threaded"}
+
+
+def run_reference(args, rank, world):
+    """The oracle arm: the same metric on the host cores, each step a
+    bounded sample of the layer (leading rows of each projection)."""
+    from gemm_decode_register_gb300 import synth
+    import oracle
+
+    if rank != 0:
+        return None
+    orc = oracle.get()
+    F4 = synth.FMT_MXFP4
+    data = []
+    for name, N, K, seed in DENSE:
+        codes, scales = synth.weights(F4, N, K, seed, exp_lo=118, exp_hi=132)
+        data.append((N, K, codes, scales, synth.activations(1, K, 100 + seed)))
+    rows = args.ref_rows
+
+    def step():
+        b = 0
+        for N, K, codes, scales, x in data:
+            orc.qmv_rows(F4, codes, scales, x, 1, N, K, np.arange(rows))
+            b += rows * (K // 2 + K // 32)
+        return b
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    tot = 0
+    for _ in range(args.steps):
+        tot += step()
+    el = time.perf_counter() - t0
+    v = tot / el / 1e9
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": f"{rows} leading rows of each projection per step"},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{rows} leading rows of each projection per step"},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--extra-iters", type=int, default=100)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-rows", type=int, default=256)
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    out = run_ours(args, rank, world, dist)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

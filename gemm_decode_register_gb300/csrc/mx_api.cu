@@ -1,0 +1,169 @@
+// mx_api.cu -- the C ABI declared in include/mx.h: argument validation,
+// per-thread stream, per-device state and the device error word.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/mx.h"
+#include "mx_internal.h"
+
+namespace mx {
+
+static thread_local cudaStream_t t_stream = nullptr;
+static std::mutex g_mu;
+static DeviceState g_dev[64];
+
+cudaStream_t current_stream() { return t_stream; }
+
+DeviceState *device_state()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState &ds = g_dev[dev];
+    if (ds.device == dev) return &ds;
+    int sms = 0, smem = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return nullptr;
+    if (cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return nullptr;
+    void *scratch = nullptr;
+    if (cudaMalloc(&scratch, 256) != cudaSuccess) return nullptr;
+    if (cudaMemset(scratch, 0, 256) != cudaSuccess) {
+        cudaFree(scratch);
+        return nullptr;
+    }
+    ds.num_sms = sms;
+    ds.max_smem_optin = smem;
+    ds.err = static_cast<int *>(scratch);
+    ds.device = dev;
+    return &ds;
+}
+
+}  // namespace mx
+
+using namespace mx;
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static int block_of(int fmt) { return fmt == MX_FMT_NVFP4 ? 16 : 32; }
+static bool fmt_ok(int fmt) { return fmt == MX_FMT_MXFP4 || fmt == MX_FMT_MXFP8 || fmt == MX_FMT_NVFP4; }
+
+static int finish(cudaError_t e) { return e == cudaSuccess ? MX_OK : MX_ECUDA; }
+
+extern "C" int mx_set_stream(void *cuda_stream)
+{
+    t_stream = static_cast<cudaStream_t>(cuda_stream);
+    return MX_OK;
+}
+
+extern "C" int mx_qmv(int fmt, const void *codes, const void *scales, const void *x, float *y, int M,
+                      int N, int K)
+{
+    if (!fmt_ok(fmt)) return MX_EUNSUPPORTED;
+    if (!codes || !scales || !x || !y) return MX_EINVAL;
+    if (M <= 0 || N <= 0 || K <= 0 || K % block_of(fmt) != 0) return MX_EINVAL;
+    if (K > QMV_MAX_K) return MX_EUNSUPPORTED;
+    if (!aligned16(codes) || !aligned16(scales) || !aligned16(x) || !aligned16(y)) return MX_EALIGN;
+    DeviceState *ds = device_state();
+    if (!ds) return MX_ECUDA;
+    cudaError_t e = launch_qmv(*ds, t_stream, fmt, static_cast<const uint8_t *>(codes),
+                               static_cast<const uint8_t *>(scales), static_cast<const uint16_t *>(x), y,
+                               M, N, K);
+    if (e == cudaErrorInvalidValue) return MX_EUNSUPPORTED;
+    return finish(e);
+}
+
+extern "C" int mx_moe_qmv(int fmt, const void *expert_codes, const void *expert_scales, const void *x,
+                          const int32_t *expert_ids, float *y, int T, int E, int topk, int N, int K)
+{
+    if (!fmt_ok(fmt)) return MX_EUNSUPPORTED;
+    if (!expert_codes || !expert_scales || !x || !expert_ids || !y) return MX_EINVAL;
+    if (T <= 0 || E <= 0 || topk <= 0 || N <= 0 || K <= 0 || topk > E || K % block_of(fmt) != 0)
+        return MX_EINVAL;
+    if ((long long)T * topk > MOE_MAX_SLOTS || E > MOE_MAX_EXPERTS || K > QMV_MAX_K)
+        return MX_EUNSUPPORTED;
+    if (!aligned16(expert_codes) || !aligned16(expert_scales) || !aligned16(x) || !aligned16(y) ||
+        (reinterpret_cast<uintptr_t>(expert_ids) & 3u))
+        return MX_EALIGN;
+    DeviceState *ds = device_state();
+    if (!ds) return MX_ECUDA;
+    cudaError_t e = launch_moe_qmv(*ds, t_stream, fmt, static_cast<const uint8_t *>(expert_codes),
+                                   static_cast<const uint8_t *>(expert_scales),
+                                   static_cast<const uint16_t *>(x), expert_ids, y, T, E, topk, N, K);
+    if (e == cudaErrorInvalidValue) return MX_EUNSUPPORTED;
+    return finish(e);
+}
+
+extern "C" int mx_qmm(int fmt, const void *codes, const void *scales, const void *X, void *Y, int M,
+                      int N, int K)
+{
+    if (!fmt_ok(fmt)) return MX_EUNSUPPORTED;
+    if (!codes || !scales || !X || !Y) return MX_EINVAL;
+    if (M <= 0 || N <= 0 || K <= 0 || K % block_of(fmt) != 0) return MX_EINVAL;
+    if (M % 128 != 0 || N % 256 != 0 || K % 64 != 0) return MX_EUNSUPPORTED;
+    if (!aligned16(codes) || !aligned16(scales) || !aligned16(X) || !aligned16(Y)) return MX_EALIGN;
+    DeviceState *ds = device_state();
+    if (!ds) return MX_ECUDA;
+    cudaError_t e = launch_qmm(*ds, t_stream, fmt, static_cast<const uint8_t *>(codes),
+                               static_cast<const uint8_t *>(scales), static_cast<const uint16_t *>(X),
+                               static_cast<uint16_t *>(Y), M, N, K);
+    if (e == cudaErrorInvalidValue) return MX_EUNSUPPORTED;
+    return finish(e);
+}
+
+extern "C" int mx_dequant(int fmt, const void *codes, const void *scales, float *W, int N, int K)
+{
+    if (!fmt_ok(fmt)) return MX_EUNSUPPORTED;
+    if (!codes || !scales || !W) return MX_EINVAL;
+    if (N <= 0 || K <= 0 || K % block_of(fmt) != 0) return MX_EINVAL;
+    if (!aligned16(codes) || !aligned16(W)) return MX_EALIGN;
+    DeviceState *ds = device_state();
+    if (!ds) return MX_ECUDA;
+    return finish(launch_dequant(*ds, t_stream, fmt, static_cast<const uint8_t *>(codes),
+                                 static_cast<const uint8_t *>(scales), W, N, K));
+}
+
+extern "C" int mx_swiglu(const float *gu, void *h, int Q, int I)
+{
+    if (!gu || !h) return MX_EINVAL;
+    if (Q <= 0 || I <= 0) return MX_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(gu) & 3u) || (reinterpret_cast<uintptr_t>(h) & 1u)) return MX_EALIGN;
+    DeviceState *ds = device_state();
+    if (!ds) return MX_ECUDA;
+    return finish(launch_swiglu(*ds, t_stream, gu, static_cast<uint16_t *>(h), Q, I));
+}
+
+extern "C" int mx_moe_combine(const float *yd, const float *r, float *out, int T, int topk, int N)
+{
+    if (!yd || !r || !out) return MX_EINVAL;
+    if (T <= 0 || topk <= 0 || N <= 0) return MX_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(yd) & 3u) || (reinterpret_cast<uintptr_t>(r) & 3u) ||
+        (reinterpret_cast<uintptr_t>(out) & 3u))
+        return MX_EALIGN;
+    DeviceState *ds = device_state();
+    if (!ds) return MX_ECUDA;
+    return finish(launch_moe_combine(*ds, t_stream, yd, r, out, T, topk, N));
+}
+
+extern "C" int mx_device_error(void)
+{
+    DeviceState *ds = device_state();
+    if (!ds) return MX_ECUDA;
+    if (cudaStreamSynchronize(t_stream) != cudaSuccess) return MX_ECUDA;
+    int word = 0;
+    if (cudaMemcpy(&word, ds->err, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return MX_ECUDA;
+    if (word && cudaMemset(ds->err, 0, sizeof word) != cudaSuccess) return MX_ECUDA;
+    return word;
+}
+
+extern "C" const char *mx_strerror(int status)
+{
+    switch (status) {
+    case MX_OK: return "ok";
+    case MX_EINVAL: return "invalid argument (null pointer, size <= 0, or K not a multiple of the block)";
+    case MX_EUNSUPPORTED: return "unsupported format or size";
+    case MX_EALIGN: return "pointer not 16-byte aligned";
+    case MX_ECUDA: return "CUDA runtime error";
+    case MX_EDEVICE: return "device-side check fired";
+    default: return "unknown status";
+    }
+}

@@ -1,0 +1,45 @@
+// mx_internal.h -- host-side declarations shared by the library's
+// translation units (launchers, per-device state).  Not part of the ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mx {
+
+// Per-device state, created on first use of a device.
+struct DeviceState {
+    int device = -1;
+    int num_sms = 0;
+    int max_smem_optin = 0;  // bytes of dynamic shared memory a block may opt into
+    int *err = nullptr;      // device error word (first int of a 256-byte scratch block)
+};
+
+DeviceState *device_state();  // current device; nullptr on CUDA error
+cudaStream_t current_stream();
+
+// Launchers: validated arguments in, a CUDA error code out.
+cudaError_t launch_qmv(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,
+                       const uint8_t *scales, const uint16_t *x, float *y, int M, int N, int K);
+cudaError_t launch_moe_qmv(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,
+                           const uint8_t *scales, const uint16_t *x, const int32_t *ids, float *y,
+                           int T, int E, int topk, int N, int K);
+cudaError_t launch_dequant(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,
+                           const uint8_t *scales, float *W, int N, int K);
+cudaError_t launch_swiglu(const DeviceState &ds, cudaStream_t st, const float *gu, uint16_t *h,
+                          int Q, int I);
+cudaError_t launch_moe_combine(const DeviceState &ds, cudaStream_t st, const float *yd,
+                               const float *r, float *out, int T, int topk, int N);
+cudaError_t launch_qmm(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,
+                       const uint8_t *scales, const uint16_t *X, uint16_t *Y, int M, int N, int K);
+
+// Limits checked on the host.
+constexpr int QMV_MAX_K = 1 << 20;
+constexpr int MOE_MAX_SLOTS = 1024;  // T * topk
+constexpr int MOE_MAX_EXPERTS = 4096;
+
+// Shared-memory bytes the qmv kernel needs to stage `rows` activation rows
+// of length K (f16, padded), or -1 if that cannot fit.
+int qmv_stage_bytes(int rows, int K);
+
+}  // namespace mx

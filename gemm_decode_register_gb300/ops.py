@@ -1,0 +1,166 @@
+"""Python binding of the C ABI in include/mx.h (argument marshalling only).
+
+Each function takes torch CUDA tensors, passes their device pointers and
+the current torch stream to libmxgemm.so, and raises MxError on a non-zero
+status.  Every step of the computation runs in the library's kernels; there
+is no fallback path: if the library is missing, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+from .synth import FMT_MXFP4, FMT_MXFP8, FMT_NVFP4, block_of  # noqa: F401
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libmxgemm.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "mx.h")
+
+_lock = threading.Lock()
+_lib: ctypes.CDLL | None = None
+
+
+class MxError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn} failed: status {status} ({msg})")
+        self.status = status
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libmxgemm.so (built by ``gemm_decode_register_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"CUDA library not built: {p} is missing "
+                               "(run __graft_entry__.build() or python -m "
+                               "gemm_decode_register_gb300.build)")
+        lib = ctypes.CDLL(p)
+        P, I = ctypes.c_void_p, ctypes.c_int
+        sig = {
+            "mx_qmv": [I, P, P, P, P, I, I, I],
+            "mx_moe_qmv": [I, P, P, P, P, P, I, I, I, I, I],
+            "mx_qmm": [I, P, P, P, P, I, I, I],
+            "mx_set_stream": [P],
+            "mx_dequant": [I, P, P, P, I, I],
+            "mx_swiglu": [P, P, I, I],
+            "mx_moe_combine": [P, P, P, I, I, I],
+            "mx_device_error": [],
+        }
+        for name, args in sig.items():
+            f = getattr(lib, name)
+            f.argtypes = args
+            f.restype = I
+        lib.mx_strerror.argtypes = [I]
+        lib.mx_strerror.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def header_symbols() -> list[str]:
+    """Names of the functions include/mx.h declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    return re.findall(r"^\s*(?:const\s+char\s*\*|int)\s*(mx_\w+)\s*\(", text, flags=re.M)
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise MxError(fn, status, load().mx_strerror(status).decode())
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _stream() -> None:
+    load().mx_set_stream(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+
+
+def qmv(fmt: int, codes: torch.Tensor, scales: torch.Tensor, x: torch.Tensor, N: int,
+        y: torch.Tensor | None = None) -> torch.Tensor:
+    """y[M][N] fp32 = x (bf16 [M][K]) . W^T, W block-float [N][K]."""
+    M, K = x.shape
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _stream()
+    _check("mx_qmv", load().mx_qmv(fmt, _ptr(codes), _ptr(scales), _ptr(x), _ptr(y), M, N, K))
+    return y
+
+
+def moe_qmv(fmt: int, codes: torch.Tensor, scales: torch.Tensor, x: torch.Tensor,
+            expert_ids: torch.Tensor, E: int, N: int, y: torch.Tensor | None = None) -> torch.Tensor:
+    """y[T][topk][N] fp32 over the routed experts of each token."""
+    T, K = x.shape
+    topk = expert_ids.shape[1]
+    if y is None:
+        y = torch.empty((T, topk, N), dtype=torch.float32, device=x.device)
+    _stream()
+    _check("mx_moe_qmv", load().mx_moe_qmv(fmt, _ptr(codes), _ptr(scales), _ptr(x),
+                                           _ptr(expert_ids), _ptr(y), T, E, topk, N, K))
+    return y
+
+
+def qmm(fmt: int, codes: torch.Tensor, scales: torch.Tensor, X: torch.Tensor, N: int,
+        Y: torch.Tensor | None = None) -> torch.Tensor:
+    """Y[M][N] bf16 = X (bf16 [M][K]) . W^T with fp32 accumulation."""
+    M, K = X.shape
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    _stream()
+    _check("mx_qmm", load().mx_qmm(fmt, _ptr(codes), _ptr(scales), _ptr(X), _ptr(Y), M, N, K))
+    return Y
+
+
+def dequant(fmt: int, codes: torch.Tensor, scales: torch.Tensor, N: int, K: int,
+            W: torch.Tensor | None = None) -> torch.Tensor:
+    if W is None:
+        W = torch.empty((N, K), dtype=torch.float32, device=codes.device)
+    _stream()
+    _check("mx_dequant", load().mx_dequant(fmt, _ptr(codes), _ptr(scales), _ptr(W), N, K))
+    return W
+
+
+def swiglu(gu: torch.Tensor, I: int, h: torch.Tensor | None = None) -> torch.Tensor:
+    Q = gu.numel() // (2 * I)
+    if h is None:
+        h = torch.empty((Q, I), dtype=torch.bfloat16, device=gu.device)
+    _stream()
+    _check("mx_swiglu", load().mx_swiglu(_ptr(gu), _ptr(h), Q, I))
+    return h
+
+
+def moe_combine(yd: torch.Tensor, r: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    T, topk = r.shape
+    N = yd.numel() // (T * topk)
+    if out is None:
+        out = torch.empty((T, N), dtype=torch.float32, device=yd.device)
+    _stream()
+    _check("mx_moe_combine", load().mx_moe_combine(_ptr(yd), _ptr(r), _ptr(out), T, topk, N))
+    return out
+
+
+def device_error() -> int:
+    """Synchronise the current stream; return and clear the device error word."""
+    _stream()
+    s = load().mx_device_error()
+    if s < 0:
+        _check("mx_device_error", s)
+    return s
+
+
+def raw_call(name: str, *args) -> int:
+    """Call an ABI function with raw integer/pointer arguments (tests)."""
+    return getattr(load(), name)(*args)

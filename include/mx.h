@@ -1,0 +1,142 @@
+/*
+ * mx.h -- C ABI of the block-float decode-in-kernel matmul library
+ * (libmxgemm.so, sm_103a).
+ *
+ * The operation: y = x . W^T where the weight W[N][K] is stored as packed
+ * low-precision codes plus one shared scale per block, and is decoded
+ * inside the kernel.  Formats ("MLxcel 0.8 release", section "Decoding
+ * block-float formats in software"; talk "High-performance LLM/VLM
+ * inference on AMD Strix Halo with mlxcel engine", slide 7 "AMD Strix
+ * Halo: The Target Platform" and slide 12 "Software Decode for Block Float
+ * Formats" name MXFP4, MXFP8 and NVFP4 and fix the E2M1 element as 1 sign,
+ * 2 exponent and 1 mantissa bit, decoded exactly; the rest follows the
+ * OCP MX v1.0 and NVFP4 definitions those pages refer to):
+ *
+ *   MX_FMT_MXFP4  E2M1 codes, 2 per byte, one E8M0 scale per 32 elements
+ *   MX_FMT_MXFP8  E4M3 codes, 1 per byte, one E8M0 scale per 32 elements
+ *   MX_FMT_NVFP4  E2M1 codes, 2 per byte, one E4M3 scale per 16 elements,
+ *                 times one fp32 per-tensor scale
+ *
+ * Layouts (all row-major, little-endian):
+ *   codes   uint8 [N][K/2] (4-bit formats: element k in byte k/2, even k in
+ *           the low nibble) or [N][K] (MXFP8).
+ *   scales  uint8 [N][K/block].  NVFP4: the fp32 per-tensor scale follows
+ *           immediately after these N*K/16 bytes (any alignment).
+ *   x, X    bf16 [M][K];  y fp32 [M][N];  Y bf16 [M][N].
+ *   MoE     expert e's codes start at e*N*(bytes per row), its scales at
+ *           e*N*(K/block); NVFP4 stacks carry E fp32 tensor scales after the
+ *           whole [E][N][K/16] scale block, one per expert.
+ *
+ * Values: E8M0 byte e = 2^(e-127), 0xFF = NaN; E4M3 has bias 7, no
+ * infinities, S.1111.111 = NaN, max 448.  Decoding is exact (see
+ * mx_dequant).  Products accumulate in fp32; their rounding order is the
+ * kernel's, not a fixed sequential one.
+ *
+ * Ownership and execution: every pointer is a caller-owned DEVICE pointer
+ * on the current CUDA device.  The library allocates nothing per call; on
+ * first use of a device it allocates one 256-byte scratch block that holds
+ * the device error word.  Calls are asynchronous on the stream set with
+ * mx_set_stream (per host thread; default: the legacy default stream),
+ * re-entrant across host threads, and return as soon as the kernel is
+ * queued.
+ *
+ * Errors: 0 on success, otherwise a negative MX_E* code; the call then
+ * launched nothing.  Faults found on the device (an expert id out of range,
+ * a pipeline wait that timed out) do not trap: the kernel writes NaN to the
+ * affected outputs, sets a bit in the device error word and returns;
+ * mx_device_error() reads and clears it.
+ */
+#ifndef MX_H
+#define MX_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum mx_fmt { MX_FMT_MXFP4 = 0, MX_FMT_MXFP8 = 1, MX_FMT_NVFP4 = 2 };
+
+enum mx_status {
+    MX_OK = 0,
+    MX_EINVAL = -1,       /* null pointer, a size <= 0, K not a multiple of the block */
+    MX_EUNSUPPORTED = -2, /* unknown format, or a size beyond what the kernel handles */
+    MX_EALIGN = -3,       /* a pointer is not 16-byte aligned */
+    MX_ECUDA = -4,        /* a CUDA runtime call or the launch failed */
+    MX_EDEVICE = -5       /* (mx_device_error only) a device-side check fired */
+};
+
+/* Device error word bits, as returned by mx_device_error(). */
+#define MX_DEVERR_BAD_EXPERT 0x1 /* an expert id outside [0, E); that slot's y rows are NaN */
+#define MX_DEVERR_TIMEOUT 0x2    /* a bounded pipeline wait gave up; that tile of Y is NaN */
+
+/* Decode GEMV for a few tokens (the memory-bound decode step; "MLxcel 0.8
+ * release", section "Profiling set the porting order": the qmv kernel is 95%
+ * of dense decode GPU time):
+ *   y[m][n] = sum_k x[m][k] * W[n][k],   m < M, n < N.
+ * x bf16 [M][K], y fp32 [M][N].  Any M >= 1 is accepted; the weight is
+ * streamed once per group of up to 8 tokens.  K must be a multiple of 32
+ * (MXFP4, MXFP8) or 16 (NVFP4); K <= 2^20.  codes, scales, x, y 16-byte
+ * aligned. */
+int mx_qmv(int fmt, const void *codes, const void *scales, const void *x, float *y, int M, int N,
+           int K);
+
+/* MoE decode GEMV over routed experts only (talk slide 4 "UMA Advantage for
+ * MoE Architecture": each token reads only its active experts; manual page
+ * "Building from source", ROCm status table: single-token MoE decode runs
+ * a gate-up kernel then a down kernel):
+ *   y[t][j][n] = sum_k x[t][k] * W_{e}[n][k],  e = expert_ids[t][j].
+ * expert_codes / expert_scales hold E stacked [N][K] weights (layout
+ * above); x bf16 [T][K]; expert_ids int32 [T][topk]; y fp32 [T][topk][N].
+ * Slots that share an expert are served by one pass over that expert's
+ * weights.  The routing is read on the device (no host copy).  T*topk <=
+ * 4096.  An id outside [0, E) sets MX_DEVERR_BAD_EXPERT and fills that
+ * slot's N outputs with NaN.  For the down projection call with T' = T*topk
+ * rows of x, topk = 1 and the ids flattened to [T*topk][1]. */
+int mx_moe_qmv(int fmt, const void *expert_codes, const void *expert_scales, const void *x,
+               const int32_t *expert_ids, float *y, int T, int E, int topk, int N, int K);
+
+/* Prefill GEMM over the same weights (release post, section "Decoding
+ * block-float formats in software": dequantise on the GPU and multiply on
+ * matrix units):
+ *   Y[m][n] = bf16_rne( sum_k X[m][k] * W[n][k] ),  fp32 accumulation.
+ * X bf16 [M][K], Y bf16 [M][N].  The weight tile is decoded exactly to bf16
+ * in shared memory and multiplied by tcgen05 tensor-core MMA with the
+ * accumulator in tensor memory.  Requires M, N, K multiples of 128, 256
+ * and 64; the NVFP4 tensor scale is applied in the epilogue. */
+int mx_qmm(int fmt, const void *codes, const void *scales, const void *X, void *Y, int M, int N,
+           int K);
+
+/* ---- support calls (not on the pages; part of this library's contract) */
+
+/* Stream for subsequent calls from this host thread (a cudaStream_t; NULL =
+ * the legacy default stream). */
+int mx_set_stream(void *cuda_stream);
+
+/* Bit-exact dequantisation W[n][k] = fp32(code * scale) (NVFP4: then one
+ * round-to-nearest-even multiply by the fp32 tensor scale), W fp32 [N][K].
+ * Exposes the kernels' decode for exactness tests. */
+int mx_dequant(int fmt, const void *codes, const void *scales, float *W, int N, int K);
+
+/* MoE FFN glue used between the two projections:
+ *   h[q][i] = bf16_rne( silu(gu[q][i]) * gu[q][I + i] ),  silu(v) = v / (1 + e^-v),
+ * gu fp32 [Q][2I] (gate rows then up rows), h bf16 [Q][I]. */
+int mx_swiglu(const float *gu, void *h, int Q, int I);
+
+/* Router-weighted combine: out[t][n] = sum_j r[t][j] * yd[t*topk + j][n],
+ * yd fp32 [T*topk][N], r fp32 [T][topk], out fp32 [T][N]. */
+int mx_moe_combine(const float *yd, const float *r, float *out, int T, int topk, int N);
+
+/* Synchronise the calling thread's stream, then return the device error
+ * word of the current device (0 = none; MX_DEVERR_* bits) and clear it.
+ * Returns MX_ECUDA if the synchronisation fails. */
+int mx_device_error(void);
+
+/* Static description of a status code. */
+const char *mx_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MX_H */
