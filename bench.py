@@ -257,7 +257,7 @@ def extras(torch, ops, synth, dev, stream, hbm, bf16_burst, bf16_sust, args):
     for M in (1, 4):
         def f(M=M):
             for N, K, c, s, x, _ in mats:
-                ops.qmv(F4, c, s, x[: M * K].view(M, K), N)
+                ops.qmv(F4, c, s, x.reshape(-1)[: M * K].view(M, K), N)
         for _ in range(3):
             f()
         t = time_region(torch, f, iters, stream)
@@ -334,6 +334,8 @@ def extras(torch, ops, synth, dev, stream, hbm, bf16_burst, bf16_sust, args):
     del d1, e1, d2, e2
 
     # prefill qmm
+    if args.no_qmm:
+        return res
     try:
         for N, K, seed in ((28672, 8192, 8), (8192, 28672, 9)):
             M = 4096
@@ -436,6 +438,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-qmm", action="store_true")
     ap.add_argument("--extra-iters", type=int, default=100)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=256)

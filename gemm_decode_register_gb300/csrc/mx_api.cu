@@ -99,7 +99,7 @@ extern "C" int mx_qmm(int fmt, const void *codes, const void *scales, const void
     if (!fmt_ok(fmt)) return MX_EUNSUPPORTED;
     if (!codes || !scales || !X || !Y) return MX_EINVAL;
     if (M <= 0 || N <= 0 || K <= 0 || K % block_of(fmt) != 0) return MX_EINVAL;
-    if (M % 128 != 0 || N % 256 != 0 || K % 64 != 0) return MX_EUNSUPPORTED;
+    if (N % 256 != 0 || K % 64 != 0) return MX_EUNSUPPORTED;
     if (!aligned16(codes) || !aligned16(scales) || !aligned16(X) || !aligned16(Y)) return MX_EALIGN;
     DeviceState *ds = device_state();
     if (!ds) return MX_ECUDA;

@@ -75,8 +75,10 @@ cudaError_t launch_dequant(const DeviceState &ds, cudaStream_t st, int fmt, cons
     return cudaGetLastError();
 }
 
-// h = bf16(silu(gate) * up), fp32 arithmetic: silu(v) = v / (1 + e^-v) with
-// the correctly rounded division and CUDA's expf.
+// h = bf16(silu(gate) * up), fp32 arithmetic: silu(v) = v * sigmoid(v), the
+// sigmoid evaluated from e = exp(-|v|) (CUDA's expf, never overflows) as
+// 1 / (1 + e) for v >= 0 and e / (1 + e) below, with correctly rounded
+// division.
 __global__ void swiglu_kernel(const float *__restrict__ gu, uint16_t *__restrict__ h, int Q, int I)
 {
     const size_t total = (size_t)Q * I;
@@ -84,8 +86,9 @@ __global__ void swiglu_kernel(const float *__restrict__ gu, uint16_t *__restrict
          i += (size_t)gridDim.x * blockDim.x) {
         const size_t q = i / I, j = i - q * I;
         const float gv = gu[q * 2 * I + j], uv = gu[q * 2 * I + I + j];
-        const float s = __fdiv_rn(gv, __fadd_rn(1.0f, expf(-gv)));
-        const float p = __fmul_rn(s, uv);
+        const float e = expf(-fabsf(gv));
+        const float sig = __fdiv_rn(gv >= 0.0f ? 1.0f : e, __fadd_rn(1.0f, e));
+        const float p = __fmul_rn(__fmul_rn(gv, sig), uv);
         h[i] = (uint16_t)(f32x2_to_bf16x2(p, 0.0f) & 0xFFFFu);
     }
 }

@@ -102,8 +102,9 @@ int mx_moe_qmv(int fmt, const void *expert_codes, const void *expert_scales, con
  *   Y[m][n] = bf16_rne( sum_k X[m][k] * W[n][k] ),  fp32 accumulation.
  * X bf16 [M][K], Y bf16 [M][N].  The weight tile is decoded exactly to bf16
  * in shared memory and multiplied by tcgen05 tensor-core MMA with the
- * accumulator in tensor memory.  Requires M, N, K multiples of 128, 256
- * and 64; the NVFP4 tensor scale is applied in the epilogue. */
+ * accumulator in tensor memory.  Any M >= 1; N must be a multiple of 256
+ * and K of 64 (else MX_EUNSUPPORTED); the NVFP4 tensor scale is applied in
+ * the epilogue. */
 int mx_qmm(int fmt, const void *codes, const void *scales, const void *X, void *Y, int M, int N,
            int K);
 
@@ -120,7 +121,9 @@ int mx_dequant(int fmt, const void *codes, const void *scales, float *W, int N, 
 
 /* MoE FFN glue used between the two projections:
  *   h[q][i] = bf16_rne( silu(gu[q][i]) * gu[q][I + i] ),  silu(v) = v / (1 + e^-v),
- * gu fp32 [Q][2I] (gate rows then up rows), h bf16 [Q][I]. */
+ * gu fp32 [Q][2I] (gate rows then up rows), h bf16 [Q][I].  Evaluated in
+ * fp32 as v * sigmoid(v) with the sigmoid formed from e^-|v|, so it never
+ * overflows. */
 int mx_swiglu(const float *gu, void *h, int Q, int I);
 
 /* Router-weighted combine: out[t][n] = sum_j r[t][j] * yd[t*topk + j][n],

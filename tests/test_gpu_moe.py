@@ -6,8 +6,8 @@ import numpy as np
 import pytest
 
 from gemm_decode_register_gb300 import synth
-from gpu_util import (bf16_host, check_close, dev_bf16, dev_i32, dev_u8, need_gpu,
-                      same_values)
+from gpu_util import (bf16_bits_to_f64, bf16_host, check_close, dev_bf16, dev_i32, dev_u8,
+                      need_gpu, same_values)
 
 pytestmark = pytest.mark.gpu
 
@@ -56,18 +56,22 @@ def test_moe_ragged(orc, fmt, T, E, topk, N, K):
 
 @pytest.mark.parametrize("fmt", [0, 2])
 @pytest.mark.parametrize("T", [1, 3, 8])
-def test_moe_single_expert_equals_qmv(fmt, T):
-    """E = 1, topk = 1: every token routes to the one expert, so the MoE
-    kernel runs the same tile code on the same token group as qmv."""
+def test_moe_single_expert_equals_qmv(orc, fmt, T):
+    """E = 1, topk = 1: every token routes to the one expert, so MoE reduces
+    to qmv.  The two kernels may split K differently (qmv spreads a tile's K
+    over several warps), so they agree within the tolerance gate, and both
+    match the oracle."""
     need_gpu()
     from gemm_decode_register_gb300 import ops
 
     N, K = 200, 512
     codes, scales = synth.weights(fmt, N, K, 9)
     x = synth.activations(T, K, 10)
-    y_moe = run_moe(fmt, codes, scales, x, np.zeros((T, 1), np.int32), 1, N)
+    y_moe = run_moe(fmt, codes, scales, x, np.zeros((T, 1), np.int32), 1, N).reshape(T, N)
     y_qmv = ops.qmv(fmt, dev_u8(codes), dev_u8(scales), dev_bf16(x), N).cpu().numpy()
-    assert np.array_equal(y_moe.reshape(T, N), y_qmv)
+    want = orc.qmv(fmt, codes, scales, x, T, N, K)
+    check_close(y_moe, y_qmv.astype(np.float64), "moe vs qmv")
+    check_close(y_moe, want, "moe vs oracle")
 
 
 def test_moe_bad_expert_id(orc):
@@ -120,9 +124,14 @@ def test_moe_ffn_composite(orc, T):
     out_o = orc.moe_combine(yd_o.reshape(T * topk, H), r, T, topk, H)
     check_close(out, out_o, f"moe ffn T{T}")
     # SwiGLU alone on the GPU's own gate/up output: bf16 within one ulp
+    # wherever the value is not vanishingly small (fp32 exp underflows near
+    # 2^-126, where the oracle's fp64 still resolves digits)
     h_chk = orc.swiglu_bf16(gu.cpu().numpy().astype(np.float64).reshape(T * topk, 2 * I), I)
-    diff = np.abs(bf16_host(h).astype(np.int32) - h_chk.astype(np.int32))
+    hb = bf16_host(h)
+    big = np.abs(bf16_bits_to_f64(h_chk)) >= 2.0 ** -100
+    diff = np.abs(hb.astype(np.int32) - h_chk.astype(np.int32))[big]
     assert diff.max() <= 1
+    assert np.all(np.abs(bf16_bits_to_f64(hb[~big])) < 2.0 ** -99)
 
 
 def test_combine_exact_one_hot_router():
