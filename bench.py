@@ -430,6 +430,58 @@ def run_reference(args, rank, world):
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+CASES = {
+    # name: (kind, fmt, M or T, N, K)
+    "qmv_upgate_m1": ("qmv", 0, 1, 57344, 8192),
+    "qmv_upgate_m4": ("qmv", 0, 4, 57344, 8192),
+    "qmv_down_m1": ("qmv", 0, 1, 8192, 28672),
+    "qmv_down_m4": ("qmv", 0, 4, 8192, 28672),
+    "qmv_mxfp8_m1": ("qmv", 1, 1, 57344, 8192),
+    "qmv_nvfp4_m1": ("qmv", 2, 1, 57344, 8192),
+    "moe_gateup_t4": ("moe", 0, 4, 1536, 2048),
+    "qmm_up": ("qmm", 0, 4096, 28672, 8192),
+    "qmm_small": ("qmm", 0, 1024, 4096, 4096),
+}
+
+
+def run_case(args):
+    """One kernel configuration for a few launches (profiling runs); prints
+    the mean launch time."""
+    import torch
+
+    from gemm_decode_register_gb300 import build as b
+    from gemm_decode_register_gb300 import ops, synth
+
+    b.build()
+    kind, fmt, M, N, K = CASES[args.case]
+    stream = torch.cuda.current_stream()
+    if kind == "moe":
+        E, topk = 128, 8
+        codes, scales = synth.weights(fmt, N, K, 40, E=E)
+        c, s = upload(torch, codes), upload(torch, scales)
+        ids = torch.from_numpy(synth.expert_ids(M, E, topk, 5)).cuda()
+        x = bf16_dev(torch, synth.activations(M, K, 6)).view(M, K)
+        f = lambda: ops.moe_qmv(fmt, c, s, x, ids, E, N)  # noqa: E731
+        wb = (codes.nbytes + scales.nbytes) / E * len(np.unique(ids.cpu().numpy()))
+    else:
+        codes, scales = synth.weights(fmt, N, K, 2, exp_lo=118, exp_hi=132)
+        c, s = upload(torch, codes), upload(torch, scales)
+        if kind == "qmv":
+            x = bf16_dev(torch, synth.activations(M, K, 3)).view(M, K)
+            f = lambda: ops.qmv(fmt, c, s, x, N)  # noqa: E731
+        else:
+            X = torch.randn(M, K, device="cuda").to(torch.bfloat16)
+            Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+            f = lambda: ops.qmm(fmt, c, s, X, N, Y=Y)  # noqa: E731
+        wb = codes.nbytes + scales.nbytes
+    t = time_region(torch, f, args.iters, stream)
+    out = {"case": args.case, "iters": args.iters, "us": round(t * 1e6, 2),
+           "weight_gbs": round(wb / t / 1e9, 1)}
+    if kind == "qmm":
+        out["tflops"] = round(2.0 * M * N * K / t / 1e12, 1)
+    print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -442,7 +494,12 @@ def main():
     ap.add_argument("--extra-iters", type=int, default=100)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=256)
+    ap.add_argument("--case", choices=sorted(CASES), help="time one kernel configuration only")
+    ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
+    if args.case:
+        run_case(args)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

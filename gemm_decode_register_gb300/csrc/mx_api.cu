@@ -27,14 +27,16 @@ DeviceState *device_state()
     if (cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
         return nullptr;
     void *scratch = nullptr;
-    if (cudaMalloc(&scratch, 256) != cudaSuccess) return nullptr;
-    if (cudaMemset(scratch, 0, 256) != cudaSuccess) {
+    if (cudaMalloc(&scratch, SCRATCH_BYTES) != cudaSuccess) return nullptr;
+    if (cudaMemset(scratch, 0, SCRATCH_BYTES) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
         cudaFree(scratch);
         return nullptr;
     }
     ds.num_sms = sms;
     ds.max_smem_optin = smem;
     ds.err = static_cast<int *>(scratch);
+    ds.ws = reinterpret_cast<float *>(static_cast<char *>(scratch) + 256);
+    ds.ws_count = reinterpret_cast<int *>(ds.ws + WS_FLOATS);
     ds.device = dev;
     return &ds;
 }

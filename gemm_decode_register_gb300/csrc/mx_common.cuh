@@ -34,6 +34,33 @@ __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte)
     return out;
 }
 
+// Eight E2M1 nibbles of a word (nibble i = element i) -> four f16x2 words
+// (word j holds elements 2j, 2j+1).  The bytes are split with a vector
+// move, so the conversion reads them in place.
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t &o0, uint32_t &o1, uint32_t &o2,
+                                                uint32_t &o3)
+{
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(o0), "=r"(o1), "=r"(o2), "=r"(o3)
+        : "r"(w));
+}
+
+// Four E4M3 bytes of a word -> two f16x2 words (elements 0,1 and 2,3).
+__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t w, uint32_t &o0, uint32_t &o1)
+{
+    asm("{\n\t.reg .b16 h0, h1;\n\t"
+        "mov.b32 {h0, h1}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, h0;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, h1;\n\t}"
+        : "=r"(o0), "=r"(o1)
+        : "r"(w));
+}
+
 // Two E4M3 bytes (low byte = first element) -> f16x2 (low half = first).
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes)
 {

@@ -12,18 +12,32 @@ struct DeviceState {
     int device = -1;
     int num_sms = 0;
     int max_smem_optin = 0;  // bytes of dynamic shared memory a block may opt into
-    int *err = nullptr;      // device error word (first int of a 256-byte scratch block)
+    int *err = nullptr;      // device error word (first int of the scratch block)
+    float *ws = nullptr;     // split-K partial sums (WS_FLOATS floats)
+    int *ws_count = nullptr; // split-K arrival counters (WS_COUNTERS ints, kept at zero between calls)
 };
+
+// Device scratch: error word (256 bytes), split-K partials, counters.
+constexpr size_t WS_FLOATS = (size_t)4 << 20;  // 16 MiB
+constexpr int WS_COUNTERS = 4096;
+constexpr size_t SCRATCH_BYTES = 256 + WS_FLOATS * 4 + WS_COUNTERS * 4;
 
 DeviceState *device_state();  // current device; nullptr on CUDA error
 cudaStream_t current_stream();
 
-// Launchers: validated arguments in, a CUDA error code out.
+// Launchers: validated arguments in, a CUDA error code out.  The plain
+// launch_qmv / launch_moe_qmv pick the streaming kernels when the shape
+// allows and fall back to the direct-load kernels otherwise.
 cudaError_t launch_qmv(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,
                        const uint8_t *scales, const uint16_t *x, float *y, int M, int N, int K);
 cudaError_t launch_moe_qmv(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,
                            const uint8_t *scales, const uint16_t *x, const int32_t *ids, float *y,
                            int T, int E, int topk, int N, int K);
+cudaError_t launch_qmv_direct(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,
+                              const uint8_t *scales, const uint16_t *x, float *y, int M, int N, int K);
+cudaError_t launch_moe_qmv_direct(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,
+                                  const uint8_t *scales, const uint16_t *x, const int32_t *ids, float *y,
+                                  int T, int E, int topk, int N, int K);
 cudaError_t launch_dequant(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,
                            const uint8_t *scales, float *W, int N, int K);
 cudaError_t launch_swiglu(const DeviceState &ds, cudaStream_t st, const float *gu, uint16_t *h,

@@ -1,0 +1,479 @@
+// mx_qmv_core.cuh -- device pieces shared by the decode-GEMV kernels
+// (direct-load and streaming variants): activation staging, the m16n8k16
+// fragment mapping for block-float weights, and the warp reductions.
+//
+// What is computed: y[t][n] = sum_k x[t][k] * W[n][k] for a handful of
+// tokens t, with W streamed from HBM exactly once per call ("MLxcel 0.8
+// release", section "Profiling set the porting order": in dense decode one
+// GEMV kernel takes 95% of GPU time and runs at the memory roofline; talk
+// slide 13).  The weight is never materialised: each 32-element block of
+// codes is decoded in registers and its block scale is applied to the
+// block's partial sum.
+//
+// sm_103a design.  Decoding dominates the instruction budget of a GEMV at
+// HBM speed (about 12 G weights/ms at 6.4 TB/s of MXFP4), so the
+// multiply-accumulate runs on the tensor pipe: codes are converted by
+// cvt.rn.f16x2.e2m1x2 / .e4m3x2 straight into the A fragment of an
+// m16n8k16 f16 MMA with fp32 accumulation, and the activations, scaled per
+// token by a power of two into fp16 range (exact for bf16 inputs), form
+// the B fragment.  To keep one block scale per MMA output while loads stay
+// contiguous, the 16 A rows of an MMA are (weight row, block) pairs and the
+// 8 B columns are (token, block) pairs with the same block set:
+//
+//     BPM = 8 / MC blocks per MMA, MC = tokens per pass (1, 2, 4 or 8)
+//     A row a (0..15): weight row  (a / 8) * MC + (a % 8) / BPM,  block a % BPM
+//     B col n (0..7):  token       n / BPM,                        block n % BPM
+//
+// Only entries whose A-row block equals the B-column block are used; the
+// others are discarded (the tensor pipe has ample headroom).  Lane
+// (g = lane/4, q = lane%4) then reads, for A rows g and g+8, the 4-byte
+// (MXFP4) or 8-byte (MXFP8) slice [8q, 8q+8) of the block: for MC = 1 the 32
+// lanes read 128 contiguous bytes of one row per load.  Inside a 32-element
+// unit, fragment slot p = 8q + 4s + i (MMA step s, element i) holds element
+// p for MX formats and element 16s + 4q + i for NVFP4, so each MMA step
+// stays inside one 16-element NVFP4 block; the staged activations use the
+// same permutation.
+#pragma once
+
+#include "mx_common.cuh"
+#include "mx_internal.h"
+
+namespace mx {
+
+constexpr int QMV_WARPS = 16;
+constexpr int QMV_THREADS = QMV_WARPS * 32;
+// Pipeline depth (MMA iterations loaded ahead) of the dense and MoE kernels.
+template <int FMT>
+__host__ __device__ constexpr int dense_uf() { return FMT == FMT_MXFP8 ? 6 : 8; }
+constexpr int MOE_UF = 4;
+
+// f16 row stride of staged activations: units*32 rounded so that the byte
+// stride is an odd multiple of 64 (conflict-free B loads for 8 tokens).
+__host__ __device__ inline int stage_stride(int K)
+{
+    int U = (K + 31) / 32;
+    int ks = U * 32;
+    if ((ks / 32) % 2 == 0) ks += 32;
+    return ks;
+}
+
+
+// -------------------------------------------------------------- staging
+
+// Stage activation rows (bf16 -> scaled f16, permuted per unit) into
+// shared memory.  Row r of xs holds elements [0, len) of source row src[r]
+// (or r when src is null) of x, whose rows are ld elements apart.  sh[r]
+// receives the per-row power-of-two exponent: the staged values are
+// x * 2^-sh[r] with max |.| in [1, 2) (exact: bf16 has 8 significant bits,
+// f16 11).  Elements past len up to the next 32-element unit are zero.
+template <int FMT>
+__device__ void stage_x(const uint16_t *__restrict__ x, size_t ld, int len, int nrows, const int *src,
+                        uint16_t *xs, int ks, int *sh, unsigned *maxbits)
+{
+    for (int r = threadIdx.x; r < nrows; r += blockDim.x) maxbits[r] = 0u;
+    __syncthreads();
+    // pass 1: largest magnitude per row (as bf16 bits; NaN > inf > finite)
+    const int kp = len / 2;  // bf16 pairs per row
+    for (int r = 0; r < nrows; ++r) {
+        const uint32_t *row = reinterpret_cast<const uint32_t *>(x + (size_t)(src ? src[r] : r) * ld);
+        unsigned m = 0;
+        for (int i = threadIdx.x; i < kp; i += blockDim.x) {
+            uint32_t v = row[i];
+            m = max(m, max(v & 0x7FFFu, (v >> 16) & 0x7FFFu));
+        }
+        if (m) atomicMax(&maxbits[r], m);
+    }
+    __syncthreads();
+    for (int r = threadIdx.x; r < nrows; r += blockDim.x) {
+        unsigned mb = maxbits[r];
+        int ef = (int)(mb >> 7);
+        int s = 0;
+        if (mb != 0u && ef != 255) s = ef == 0 ? -126 : ef - 127;
+        sh[r] = s;
+    }
+    __syncthreads();
+    // pass 2: convert and permute (zero past len)
+    const int U = (len + 31) / 32;
+    const int pairs = U * 16;
+    for (int idx = threadIdx.x; idx < nrows * pairs; idx += blockDim.x) {
+        const int r = idx / pairs, pp = idx - r * pairs;
+        const int k = 2 * pp;
+        const int u = k >> 5, p = k & 31;
+        int slot = p;
+        if (FMT == FMT_NVFP4) slot = 8 * ((p & 15) >> 2) + 4 * (p >> 4) + (p & 3);
+        uint32_t out = 0u;
+        if (k < len) {
+            uint32_t v = reinterpret_cast<const uint32_t *>(x + (size_t)(src ? src[r] : r) * ld)[pp];
+            float f = pow2f(-sh[r]);
+            out = f32x2_to_f16x2(bf16_to_f32(v & 0xFFFFu) * f, bf16_to_f32(v >> 16) * f);
+        }
+        *reinterpret_cast<uint32_t *>(xs + (size_t)r * ks + u * 32 + slot) = out;
+    }
+}
+
+// -------------------------------------------------------------- loads
+
+template <int FMT>
+struct Ld;
+
+template <>
+struct Ld<FMT_MXFP4> {
+    uint32_t c[2];
+    uint32_t s;  // scale bytes of A rows g (low byte) and g+8
+};
+template <>
+struct Ld<FMT_NVFP4> {
+    uint32_t c[2];
+    uint32_t s[2];  // two E4M3 block scales per A row (low byte: step 0)
+};
+template <>
+struct Ld<FMT_MXFP8> {
+    uint2 c[2];
+    uint32_t s;
+};
+
+// Per-lane constants of one tile.
+struct TileCtx {
+    const uint8_t *cp[2];  // code pointer of A rows g, g+8, lane offset applied
+    const uint8_t *sp[2];  // block-scale row pointer
+    bool rv[2];            // weight row exists
+    int b;                 // block offset within an MMA group
+    int U;                 // 32-element units per row
+    int KB16;              // NVFP4 16-element blocks per row
+};
+
+template <int FMT>
+__device__ __forceinline__ void load_unit(const TileCtx &t, int u, bool ok, Ld<FMT> &l)
+{
+    if constexpr (FMT == FMT_MXFP4) {
+        uint32_t s0 = 127u, s1 = 127u;
+        l.c[0] = l.c[1] = 0u;
+        if (ok && t.rv[0]) { l.c[0] = ld_nc_u32(t.cp[0] + (size_t)u * 16); s0 = ld_nc_u8(t.sp[0] + u); }
+        if (ok && t.rv[1]) { l.c[1] = ld_nc_u32(t.cp[1] + (size_t)u * 16); s1 = ld_nc_u8(t.sp[1] + u); }
+        l.s = s0 | (s1 << 8);
+    } else if constexpr (FMT == FMT_MXFP8) {
+        uint32_t s0 = 127u, s1 = 127u;
+        l.c[0] = l.c[1] = make_uint2(0u, 0u);
+        if (ok && t.rv[0]) { l.c[0] = ld_nc_u64(t.cp[0] + (size_t)u * 32); s0 = ld_nc_u8(t.sp[0] + u); }
+        if (ok && t.rv[1]) { l.c[1] = ld_nc_u64(t.cp[1] + (size_t)u * 32); s1 = ld_nc_u8(t.sp[1] + u); }
+        l.s = s0 | (s1 << 8);
+    } else {
+        const bool two = 2 * u + 1 < t.KB16;  // the unit's second 16-block exists
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t c = 0u, s = 0x3838u;  // E4M3 1.0, 1.0
+            if (ok && t.rv[h]) {
+                const uint8_t *cp = t.cp[h] + (size_t)u * 16;
+                const uint8_t *sp = t.sp[h] + 2 * u;
+                c = ld_nc_u16(cp);
+                s = ld_nc_u8(sp) | 0x3800u;
+                if (two) {
+                    c |= ld_nc_u16(cp + 8) << 16;
+                    s = (s & 0xFFu) | (ld_nc_u8(sp + 1) << 8);
+                }
+            }
+            l.c[h] = c;
+            l.s[h] = s;
+        }
+    }
+}
+
+// One MMA group: BPM units (one per A-row block offset) -> acc[h][c].
+// ok = false: the lane's unit lies outside the work; its fragments may hold
+// stale data, so nothing is accumulated (the quad that shares the A rows
+// and B column has the same ok).
+template <int FMT>
+__device__ __forceinline__ void compute_unit(const Ld<FMT> &l, const uint32_t (&B)[4], float (&acc)[2][2],
+                                             bool ok = true)
+{
+    const float z[4] = {0.f, 0.f, 0.f, 0.f};
+    if constexpr (FMT == FMT_MXFP8) {
+        float d[4];
+        uint32_t a[4];
+        // step 0 uses word .x of each A row, step 1 word .y
+        e4m3x4_to_f16x2(l.c[0].x, a[0], a[2]);
+        e4m3x4_to_f16x2(l.c[1].x, a[1], a[3]);
+        mma_f16_16816(d, a, B[0], B[1], z);
+        e4m3x4_to_f16x2(l.c[0].y, a[0], a[2]);
+        e4m3x4_to_f16x2(l.c[1].y, a[1], a[3]);
+        mma_f16_16816(d, a, B[2], B[3], d);
+        float s0, s1;
+        e8m0x2_to_f32(l.s, s0, s1);
+        if (ok) {
+            acc[0][0] = fmaf(d[0], s0, acc[0][0]);
+            acc[0][1] = fmaf(d[1], s0, acc[0][1]);
+            acc[1][0] = fmaf(d[2], s1, acc[1][0]);
+            acc[1][1] = fmaf(d[3], s1, acc[1][1]);
+        }
+    } else {
+        // bytes 0,1 of a row's word feed MMA step 0 (A cols 2q.. and 2q+8..),
+        // bytes 2,3 feed step 1
+        uint32_t a0[4], a1[4];
+        e2m1x8_to_f16x2(l.c[0], a0[0], a0[2], a1[0], a1[2]);
+        e2m1x8_to_f16x2(l.c[1], a0[1], a0[3], a1[1], a1[3]);
+        if constexpr (FMT == FMT_MXFP4) {
+            float d[4];
+            mma_f16_16816(d, a0, B[0], B[1], z);
+            mma_f16_16816(d, a1, B[2], B[3], d);
+            float s0, s1;
+            e8m0x2_to_f32(l.s, s0, s1);
+            if (ok) {
+                acc[0][0] = fmaf(d[0], s0, acc[0][0]);
+                acc[0][1] = fmaf(d[1], s0, acc[0][1]);
+                acc[1][0] = fmaf(d[2], s1, acc[1][0]);
+                acc[1][1] = fmaf(d[3], s1, acc[1][1]);
+            }
+        } else {
+            float d0[4], d1[4];
+            mma_f16_16816(d0, a0, B[0], B[1], z);
+            mma_f16_16816(d1, a1, B[2], B[3], z);
+            const uint32_t f0 = e4m3x2_to_f16x2(l.s[0]), f1 = e4m3x2_to_f16x2(l.s[1]);
+            const float s00 = f16_lo_to_f32(f0), s01 = f16_hi_to_f32(f0);
+            const float s10 = f16_lo_to_f32(f1), s11 = f16_hi_to_f32(f1);
+            if (ok) {
+                acc[0][0] = fmaf(d1[0], s01, fmaf(d0[0], s00, acc[0][0]));
+                acc[0][1] = fmaf(d1[1], s01, fmaf(d0[1], s00, acc[0][1]));
+                acc[1][0] = fmaf(d1[2], s11, fmaf(d0[2], s10, acc[1][0]));
+                acc[1][1] = fmaf(d1[3], s11, fmaf(d0[3], s10, acc[1][1]));
+            }
+        }
+    }
+}
+
+// Stream MMA iterations [it0, it1) of one tile (2*MC weight rows from row0)
+// and accumulate the lane's fragment partial sums into acc[h][c].
+// xrow: this lane's B-column activation row in xs, or -1 for a padding
+// column.
+template <int FMT, int MC, int UF>
+__device__ __forceinline__ void qmv_tile(const uint8_t *__restrict__ codes,
+                                         const uint8_t *__restrict__ scales, int N, int K,
+                                         int row0, int it0, int it1, const uint16_t *xs, int ks,
+                                         int xrow, float (&acc)[2][2])
+{
+    constexpr int BPM = 8 / MC;
+    const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+    TileCtx t;
+    t.b = g % BPM;
+    t.U = (K + 31) / 32;
+    t.KB16 = K / 16;
+    const size_t rb = FMT == FMT_MXFP8 ? (size_t)K : (size_t)K / 2;
+    const size_t sb = FMT == FMT_NVFP4 ? (size_t)(K / 16) : (size_t)(K / 32);
+    const int lane_off = FMT == FMT_MXFP8 ? 8 * q : (FMT == FMT_NVFP4 ? 2 * q : 4 * q);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int row = row0 + h * MC + g / BPM;
+        t.rv[h] = row < N;
+        const int rr = t.rv[h] ? row : 0;
+        t.cp[h] = codes + (size_t)rr * rb + lane_off;
+        t.sp[h] = scales + (size_t)rr * sb;
+    }
+    const uint16_t *xp = xrow >= 0 ? xs + (size_t)xrow * ks + 8 * q : nullptr;
+
+    Ld<FMT> cur[UF], nxt[UF];
+#pragma unroll
+    for (int j = 0; j < UF; ++j) {
+        const int it = it0 + j, u = it * BPM + t.b;
+        load_unit<FMT>(t, u, it < it1 && u < t.U, cur[j]);
+    }
+    for (int itb = it0; itb < it1; itb += UF) {
+        const bool more = itb + UF < it1;
+#pragma unroll
+        for (int j = 0; j < UF; ++j) {
+            const int it = itb + UF + j, u = it * BPM + t.b;
+            if (more) load_unit<FMT>(t, u, it < it1 && u < t.U, nxt[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < UF; ++j) {
+            const int it = itb + j, u = it * BPM + t.b;
+            if (it < it1) {
+                uint32_t B[4] = {0u, 0u, 0u, 0u};
+                if (xp && u < t.U) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(xp + (size_t)u * 32);
+                    B[0] = v.x; B[1] = v.y; B[2] = v.z; B[3] = v.w;
+                }
+                compute_unit<FMT>(cur[j], B, acc);
+            }
+        }
+        if (more) {
+#pragma unroll
+            for (int j = 0; j < UF; ++j) cur[j] = nxt[j];
+        }
+    }
+}
+
+// Reduce a lane's fragment partials over the lanes that share a
+// (weight row, token) pair.  After the call, lanes for which
+// tile_out() returns true hold finished sums in v[h][c].
+template <int MC>
+__device__ __forceinline__ void qmv_warp_reduce(const float (&acc)[2][2], float (&v)[2][2])
+{
+    const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        if constexpr (MC == 8) {
+            v[h][0] = acc[h][0];
+            v[h][1] = acc[h][1];
+        } else {
+            float x;
+            if constexpr (MC == 1) x = (q == (g >> 1)) ? acc[h][g & 1] : 0.f;
+            else if constexpr (MC == 2) x = ((q & 1) == ((g >> 1) & 1)) ? acc[h][g & 1] : 0.f;
+            else x = acc[h][g & 1];
+            if constexpr (MC == 1) {
+                x += __shfl_xor_sync(0xFFFFFFFFu, x, 16);
+                x += __shfl_xor_sync(0xFFFFFFFFu, x, 8);
+                x += __shfl_xor_sync(0xFFFFFFFFu, x, 4);
+                x += __shfl_xor_sync(0xFFFFFFFFu, x, 2);
+                x += __shfl_xor_sync(0xFFFFFFFFu, x, 1);
+            } else if constexpr (MC == 2) {
+                x += __shfl_xor_sync(0xFFFFFFFFu, x, 8);
+                x += __shfl_xor_sync(0xFFFFFFFFu, x, 4);
+                x += __shfl_xor_sync(0xFFFFFFFFu, x, 1);
+            } else {
+                x += __shfl_xor_sync(0xFFFFFFFFu, x, 4);
+            }
+            v[h][0] = x;
+            v[h][1] = 0.f;
+        }
+    }
+}
+
+// Which (tile row r, token t) a lane's finished v[h][c] belongs to; false
+// when the lane holds no finished value for it.
+template <int MC>
+__device__ __forceinline__ bool tile_out(int h, int c, int &r, int &t)
+{
+    const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+    constexpr int BPM = 8 / MC;
+    r = h * MC + g / BPM;
+    if constexpr (MC == 8) {
+        t = 2 * q + c;
+        return true;
+    } else if constexpr (MC == 1) {
+        t = 0;
+        return c == 0 && lane == 0;  // after the full-warp sum lane 0 holds both rows
+    } else if constexpr (MC == 2) {
+        t = q >> 1;
+        return c == 0 && (g & 3) == 0 && (q & 1) == 0;
+    } else {
+        t = q;
+        return c == 0 && (g & 1) == 0;
+    }
+}
+
+// The lane's B column: which token (0..MC-1) it carries.
+template <int MC>
+__device__ __forceinline__ int lane_token()
+{
+    return ((threadIdx.x & 31) >> 2) / (8 / MC);
+}
+
+__device__ __forceinline__ int warp_incl_scan(int v)
+{
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int n = __shfl_up_sync(0xFFFFFFFFu, v, o);
+        if (lane >= o) v += n;
+    }
+    return v;
+}
+
+// Exclusive prefix sum of a[0..n) in shared memory (whole block calls);
+// returns the total.  tmp: >= 33 ints of shared scratch.
+__device__ inline int block_excl_scan(int *a, int n, int *tmp)
+{
+    const int per = (n + blockDim.x - 1) / blockDim.x;
+    const int lo = min(n, (int)threadIdx.x * per), hi = min(n, lo + per);
+    int s = 0;
+    for (int i = lo; i < hi; ++i) s += a[i];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int inc = warp_incl_scan(s);
+    if (lane == 31) tmp[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = blockDim.x >> 5;
+        int w = lane < nw ? tmp[lane] : 0;
+        int wi = warp_incl_scan(w);
+        if (lane < nw) tmp[lane] = wi - w;
+        if (lane == 31) tmp[32] = wi;
+    }
+    __syncthreads();
+    int run = tmp[warp] + inc - s;
+    for (int i = lo; i < hi; ++i) {
+        int v = a[i];
+        a[i] = run;
+        run += v;
+    }
+    const int total = tmp[32];
+    __syncthreads();
+    return total;
+}
+
+// Shared-memory arrays of the MoE routing step.
+struct RouteSmem {
+    int *cnt;       // [E]  per-expert counts, then first index in `sorted`
+    int *wgs;       // [E]  first work group of each expert
+    int *pos;       // [E]  placement cursors
+    int *sorted;    // [P]  valid slots grouped by expert, increasing slot order inside a group
+    int *wg_e;      // [P]  work group -> expert
+    int *wg_first;  // [P]  work group -> first index in `sorted`
+    int *wg_mc;     // [P]  work group -> member count (1..cap)
+    int *tmp;       // [40] scan scratch
+};
+
+// Group the routed slots by expert on the device (every CTA computes the
+// same result from expert_ids; nothing is copied to the host).  Slots with
+// an id outside [0, E) are left out.  Work group w serves expert wg_e[w]
+// for the slots sorted[wg_first[w] .. + wg_mc[w]), at most `cap` of them,
+// so an expert routed from several tokens is streamed once per group.
+// Whole block calls; returns the number of work groups.
+__device__ inline int moe_route(const int32_t *ids, int P, int E, int cap, const RouteSmem &r)
+{
+    for (int e = threadIdx.x; e < E; e += blockDim.x) r.cnt[e] = 0;
+    __syncthreads();
+    for (int p = threadIdx.x; p < P; p += blockDim.x) {
+        const int e = ids[p];
+        if (e >= 0 && e < E) atomicAdd(&r.cnt[e], 1);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) r.wgs[e] = (r.cnt[e] + cap - 1) / cap;
+    __syncthreads();
+    const int nwg = block_excl_scan(r.wgs, E, r.tmp);
+    block_excl_scan(r.cnt, E, r.tmp);  // counts -> starts
+    for (int e = threadIdx.x; e < E; e += blockDim.x) r.pos[e] = r.cnt[e];
+    __syncthreads();
+    // stable placement (one warp, in slot order)
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        for (int base = 0; base < P; base += 32) {
+            const int p = base + lane;
+            int e = p < P ? ids[p] : -1;
+            const bool valid = p < P && e >= 0 && e < E;
+            if (!valid) e = -1 - (p & 0xFFFF);  // distinct keys for invalid lanes
+            const unsigned m = __match_any_sync(0xFFFFFFFFu, e);
+            const int rank = __popc(m & ((1u << lane) - 1u));
+            int at = 0;
+            if (valid) at = r.pos[e] + rank;
+            __syncwarp();
+            if (valid) {
+                r.sorted[at] = p;
+                if (rank == 0) r.pos[e] += __popc(m);
+            }
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int n = (e + 1 < E ? r.cnt[e + 1] : r.pos[e]) - r.cnt[e];  // members of e
+        for (int c = 0; c * cap < n; ++c) {
+            const int w = r.wgs[e] + c;
+            r.wg_e[w] = e;
+            r.wg_first[w] = r.cnt[e] + cap * c;
+            r.wg_mc[w] = min(cap, n - cap * c);
+        }
+    }
+    __syncthreads();
+    return nwg;
+}
+
+}  // namespace mx

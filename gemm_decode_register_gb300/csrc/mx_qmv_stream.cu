@@ -1,0 +1,649 @@
+// mx_qmv_stream.cu -- decode GEMV and MoE decode GEMV, streaming variant.
+//
+// Same arithmetic as the direct-load kernels (mx_qmv_core.cuh: codes decoded
+// by cvt into m16n8k16 fragments, block scale applied per block), but the
+// weight bytes reach the SM through a per-warp shared-memory ring fed by
+// 16-byte cp.async copies: every warp keeps two ~2.4 KB stages (codes plus
+// block scales of its rows) in flight while it decodes the third, so an SM
+// with 16 warps has ~80 KB of HBM reads outstanding without spending
+// registers on them, and each copy instruction moves 512 contiguous bytes.
+//
+// Work is cut into units (2*MC weight rows x a run of K) that each warp
+// streams back to back: the ring runs continuously across units, so short
+// units cost nothing extra and the CTAs stay balanced to within one unit.
+//   * dense: units are (tile, K chunk); the chunks of a tile are summed in a
+//     fixed order in shared memory.  When the tokens' activations do not
+//     fit in shared memory, K is also split across CTAs (windows); the
+//     windows' partial sums go to a device workspace and the last CTA of a
+//     tile group adds them in window order (deterministic).
+//   * MoE: units are (work group of up to MC slots routed to one expert,
+//     tile) over the whole K of that expert.
+#include "mx_qmv_core.cuh"
+
+namespace mx {
+
+constexpr int ST_STAGES = 3;
+constexpr int ST_RED_BUDGET = 24 * 1024;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Stage geometry for one (format, tokens-per-pass) pair.
+template <int FMT, int MC>
+struct SGeo {
+    static constexpr int BPM = 8 / MC;                             // units per MMA
+    static constexpr int RT = 2 * MC;                              // weight rows per tile
+    static constexpr int UCB = FMT == FMT_MXFP8 ? 32 : 16;        // code bytes per 32-element unit
+    static constexpr int IPS = FMT == FMT_MXFP8 ? 4 : 8;          // MMA iterations per stage
+    static constexpr int UPS = IPS * BPM;                          // units per row per stage
+    static constexpr int CB = UPS * UCB;                           // code bytes per row per stage
+    static constexpr int RS = CB + (FMT == FMT_MXFP8 ? 256 : 128) / MC;  // padded row stride
+    static constexpr int SPU = FMT == FMT_NVFP4 ? 2 : 1;           // scale bytes per unit
+    static constexpr int SB = UPS * SPU;                           // scale bytes per row per stage
+    static constexpr int CODE_BYTES = RT * RS;
+    static constexpr int STAGE_BYTES = CODE_BYTES + RT * SB;
+    static constexpr int PIECES = RT * CB / 16;                    // 16-byte code copies per stage
+    static constexpr int SWORDS = RT * SB / 4;                     // 4-byte scale copies per stage
+    static_assert(PIECES % 32 == 0, "code copies per lane");
+    static_assert(STAGE_BYTES % 16 == 0, "stage alignment");
+};
+
+// One unit of a warp's stream.
+struct SUnit {
+    const uint8_t *codes;   // matrix (expert) base
+    const uint8_t *scales;  // block-scale base
+    int row0;               // first weight row of the tile
+    int ub, ul;             // units [ub, ul)
+};
+
+template <int FMT, int MC>
+__device__ __forceinline__ int unit_stages(const SUnit &u)
+{
+    using G = SGeo<FMT, MC>;
+    return u.ul > u.ub ? (u.ul - u.ub + G::UPS - 1) / G::UPS : 0;
+}
+
+// A lane's share of the copies of one unit, resolved once per unit:
+// source pointers at the unit's first stage, bytes left in the row after
+// them, and destination offsets within a ring slot.
+template <int FMT, int MC>
+struct CopyPlan {
+    using G = SGeo<FMT, MC>;
+    static constexpr int NP = G::PIECES / 32;
+    static constexpr int NW = (G::SWORDS + 31) / 32;
+    const uint8_t *src[NP];
+    long long left[NP];  // row bytes from src to the row end (<= 0: none)
+    uint32_t dst[NP];
+    const uint8_t *ssrc[NW];
+    long long sleft[NW];
+    uint32_t sdst[NW];
+};
+
+template <int FMT, int MC>
+__device__ __forceinline__ void plan_copies(const SUnit &u, int N, size_t RB, size_t KS, CopyPlan<FMT, MC> &c)
+{
+    using G = SGeo<FMT, MC>;
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int j = 0; j < c.NP; ++j) {
+        const int p = lane + 32 * j;
+        const int row = p / (G::CB / 16), off = (p % (G::CB / 16)) * 16;
+        const int grow = u.row0 + row;
+        const size_t col = (size_t)u.ub * G::UCB + off;
+        c.src[j] = u.codes + (size_t)(grow < N ? grow : 0) * RB + col;
+        c.left[j] = grow < N ? (long long)RB - (long long)col : 0;
+        c.dst[j] = row * G::RS + off;
+    }
+#pragma unroll
+    for (int j = 0; j < c.NW; ++j) {
+        const int w = lane + 32 * j;
+        const int row = w / (G::SB / 4), off = (w % (G::SB / 4)) * 4;
+        const int grow = u.row0 + row;
+        const size_t col = (size_t)u.ub * G::SPU + off;
+        c.ssrc[j] = u.scales + (size_t)(grow < N ? grow : 0) * KS + col;
+        c.sleft[j] = (grow < N && w < G::SWORDS) ? (long long)KS - (long long)col : 0;
+        c.sdst[j] = G::CODE_BYTES + row * G::SB + off;
+    }
+}
+
+// Copy stage s of the planned unit into the ring slot at shared address dst.
+template <int FMT, int MC>
+__device__ __forceinline__ void copy_stage(const CopyPlan<FMT, MC> &c, int s, uint32_t dst)
+{
+    using G = SGeo<FMT, MC>;
+    const long long cs = (long long)s * G::CB, ss = (long long)s * G::SB;
+#pragma unroll
+    for (int j = 0; j < c.NP; ++j)
+        if (cs < c.left[j]) cp_async16(dst + c.dst[j], c.src[j] + cs);
+#pragma unroll
+    for (int j = 0; j < c.NW; ++j)
+        if (ss < c.sleft[j]) cp_async4(dst + c.sdst[j], c.ssrc[j] + ss);
+}
+
+// Decode-and-multiply one stage from shared memory into acc.
+// xrow: the lane's staged activation row (-1: padding column); xu0: the
+// first unit held by the staged activations.  FULL: every unit of the stage
+// lies inside the unit's range (no per-iteration checks).
+template <int FMT, int MC, bool FULL>
+__device__ __forceinline__ void compute_stage_impl(const SUnit &u, int s, const uint8_t *buf, const uint16_t *xs,
+                                                   int ks, int xu0, int xrow, float (&acc)[2][2])
+{
+    using G = SGeo<FMT, MC>;
+    const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+    const int b = g % G::BPM;
+    const int r0 = g / G::BPM, r1 = MC + g / G::BPM;
+    const int u0 = u.ub + s * G::UPS;
+    const int lane_off = FMT == FMT_MXFP8 ? 8 * q : (FMT == FMT_NVFP4 ? 2 * q : 4 * q);
+    const uint8_t *a0 = buf + r0 * G::RS + b * G::UCB + lane_off;
+    const uint8_t *a1 = buf + r1 * G::RS + b * G::UCB + lane_off;
+    const uint8_t *s0 = buf + G::CODE_BYTES + r0 * G::SB + b * G::SPU;
+    const uint8_t *s1 = buf + G::CODE_BYTES + r1 * G::SB + b * G::SPU;
+    const uint16_t *xp = xrow >= 0 ? xs + (size_t)xrow * ks + 8 * q + (size_t)(u0 + b - xu0) * 32 : nullptr;
+#pragma unroll
+    for (int it = 0; it < G::IPS; ++it) {
+        const int rel = it * G::BPM;
+        bool ok = true;
+        if constexpr (!FULL) {
+            if (rel >= u.ul - u0) break;  // warp-uniform end of the unit
+            ok = u0 + rel + b < u.ul;
+        }
+        Ld<FMT> l;
+        if constexpr (FMT == FMT_MXFP4) {
+            l.c[0] = *reinterpret_cast<const uint32_t *>(a0 + rel * 16);
+            l.c[1] = *reinterpret_cast<const uint32_t *>(a1 + rel * 16);
+            l.s = __byte_perm(s0[rel], s1[rel], 0x0040);
+        } else if constexpr (FMT == FMT_MXFP8) {
+            l.c[0] = *reinterpret_cast<const uint2 *>(a0 + rel * 32);
+            l.c[1] = *reinterpret_cast<const uint2 *>(a1 + rel * 32);
+            l.s = __byte_perm(s0[rel], s1[rel], 0x0040);
+        } else {
+            l.c[0] = __byte_perm(*reinterpret_cast<const uint16_t *>(a0 + rel * 16),
+                                 *reinterpret_cast<const uint16_t *>(a0 + rel * 16 + 8), 0x5410);
+            l.c[1] = __byte_perm(*reinterpret_cast<const uint16_t *>(a1 + rel * 16),
+                                 *reinterpret_cast<const uint16_t *>(a1 + rel * 16 + 8), 0x5410);
+            l.s[0] = *reinterpret_cast<const uint16_t *>(s0 + rel * 2);
+            l.s[1] = *reinterpret_cast<const uint16_t *>(s1 + rel * 2);
+        }
+        uint32_t B[4] = {0u, 0u, 0u, 0u};
+        if (xp && ok) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(xp + (size_t)rel * 32);
+            B[0] = v.x;
+            B[1] = v.y;
+            B[2] = v.z;
+            B[3] = v.w;
+        }
+        compute_unit<FMT>(l, B, acc, ok);
+    }
+}
+
+template <int FMT, int MC>
+__device__ __forceinline__ void compute_stage(const SUnit &u, int s, const uint8_t *buf, const uint16_t *xs,
+                                              int ks, int xu0, int xrow, float (&acc)[2][2])
+{
+    using G = SGeo<FMT, MC>;
+    if (u.ul - (u.ub + s * G::UPS) >= G::UPS)
+        compute_stage_impl<FMT, MC, true>(u, s, buf, xs, ks, xu0, xrow, acc);
+    else
+        compute_stage_impl<FMT, MC, false>(u, s, buf, xs, ks, xu0, xrow, acc);
+}
+
+// Stream a warp's units through its ring.  next(i) -> SUnit, xrow_of(i) ->
+// the lane's activation row for unit i, done(i, acc) receives the lane's
+// fragment partial sums at the end of unit i.
+template <int FMT, int MC, class Next, class XRow, class Done>
+__device__ __forceinline__ void stream_units(int n_units, const Next &next, const XRow &xrow_of, const Done &done,
+                                             uint8_t *ring, const uint16_t *xs, int ks, int xu0, int N, size_t RB,
+                                             size_t KS)
+{
+    using G = SGeo<FMT, MC>;
+    const uint32_t ring_s = smem_addr(ring);
+    // issue cursor
+    int iu = -1, is = 0, ins = 0, slot_issue = 0;
+    CopyPlan<FMT, MC> plan;
+    auto issue = [&]() {
+        while (iu < n_units && (iu < 0 || is >= ins)) {
+            ++iu;
+            is = 0;
+            if (iu < n_units) {
+                const SUnit iud = next(iu);
+                ins = unit_stages<FMT, MC>(iud);
+                plan_copies<FMT, MC>(iud, N, RB, KS, plan);
+            }
+        }
+        if (iu < n_units) {
+            copy_stage<FMT, MC>(plan, is, ring_s + slot_issue * G::STAGE_BYTES);
+            ++is;
+        }
+        cp_async_commit();
+        slot_issue = slot_issue + 1 == ST_STAGES ? 0 : slot_issue + 1;
+    };
+#pragma unroll
+    for (int s = 0; s < ST_STAGES - 1; ++s) issue();
+    int slot = 0;
+    for (int cu = 0; cu < n_units; ++cu) {
+        const SUnit cd = next(cu);
+        const int nst = unit_stages<FMT, MC>(cd);
+        const int xrow = xrow_of(cu);
+        float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+        for (int cs = 0; cs < nst; ++cs) {
+            cp_async_wait<ST_STAGES - 2>();
+            __syncwarp();
+            issue();  // refills the slot consumed one stage ago
+            compute_stage<FMT, MC>(cd, cs, ring + slot * G::STAGE_BYTES, xs, ks, xu0, xrow, acc);
+            slot = slot + 1 == ST_STAGES ? 0 : slot + 1;
+        }
+        done(cu, acc);
+    }
+    cp_async_wait<0>();
+    __syncwarp();
+}
+
+// ------------------------------------------------------------------ dense
+
+struct QmvSArgs {
+    const uint8_t *codes;
+    const uint8_t *scales;
+    const uint16_t *x;  // bf16 [M][K]
+    float *y;           // [M][N]
+    float *ws;          // window partials [nwin][mc][N]
+    int *ws_count;      // [G]
+    int N, K;
+    int m0, mc;
+    int tiles;     // ceil(N / RT)
+    int G;         // CTAs per window
+    int nwin;      // K windows
+    int WU;        // units per window (multiple of UPS)
+    int wk;        // chunks per tile per window (a power of two)
+    int wk_log2;
+    int CU;        // units per chunk (multiple of UPS)
+    int ntl_max;   // tiles per CTA (upper bound)
+    int ks;        // staged row stride (f16 elements)
+};
+
+template <int FMT, int MC>
+__global__ void __launch_bounds__(QMV_THREADS, 1) qmv_stream_kernel(QmvSArgs a)
+{
+    using G = SGeo<FMT, MC>;
+    extern __shared__ __align__(16) uint8_t smem[];
+    uint16_t *xs = reinterpret_cast<uint16_t *>(smem);
+    size_t off = (size_t)MC * a.ks * 2;
+    int *sh = reinterpret_cast<int *>(smem + off);
+    unsigned *maxbits = reinterpret_cast<unsigned *>(sh + 8);
+    int *flag = reinterpret_cast<int *>(maxbits + 8);
+    off += 80;
+    float *red = reinterpret_cast<float *>(smem + off);
+    off += (((size_t)a.ntl_max * a.wk * G::RT * MC * 4) + 15) & ~(size_t)15;
+    uint8_t *rings = smem + off;
+
+    const int gb = blockIdx.x % a.G, win = blockIdx.x / a.G;
+    const int U = (a.K + 31) / 32;
+    const int xu0 = win * a.WU, xu1 = min(U, xu0 + a.WU);
+    const int len = min(a.K - xu0 * 32, (xu1 - xu0) * 32);
+    stage_x<FMT>(a.x + (size_t)a.m0 * a.K + (size_t)xu0 * 32, (size_t)a.K, len, a.mc, nullptr, xs, a.ks, sh,
+                 maxbits);
+    __syncthreads();
+
+    const int warp = threadIdx.x >> 5;
+    const int ntl = gb < a.tiles ? (a.tiles - gb + a.G - 1) / a.G : 0;
+    const int nv = ntl * a.wk;
+    const int n_my = warp < nv ? (nv - warp + QMV_WARPS - 1) / QMV_WARPS : 0;
+    const size_t RB = FMT == FMT_MXFP8 ? (size_t)a.K : (size_t)a.K / 2;
+    const size_t KS = FMT == FMT_NVFP4 ? (size_t)(a.K / 16) : (size_t)(a.K / 32);
+    const int tok = lane_token<MC>();
+    const int xrow = tok < a.mc ? tok : -1;
+
+    auto next = [&](int i) {
+        const int v = warp + QMV_WARPS * i;
+        const int ti = v >> a.wk_log2, c = v & (a.wk - 1);
+        SUnit u;
+        u.codes = a.codes;
+        u.scales = a.scales;
+        u.row0 = (gb + ti * a.G) * G::RT;
+        u.ub = xu0 + c * a.CU;
+        u.ul = min(xu1, u.ub + a.CU);
+        if (u.ub > u.ul) u.ub = u.ul;
+        return u;
+    };
+    auto xrow_of = [&](int) { return xrow; };
+    auto done = [&](int i, const float (&acc)[2][2]) {
+        const int v = warp + QMV_WARPS * i;
+        float vv[2][2];
+        qmv_warp_reduce<MC>(acc, vv);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                int r, t;
+                if (tile_out<MC>(h, c, r, t)) red[((size_t)v * G::RT + r) * MC + t] = vv[h][c];
+            }
+    };
+    stream_units<FMT, MC>(n_my, next, xrow_of, done, rings + (size_t)warp * ST_STAGES * G::STAGE_BYTES, xs, a.ks,
+                          xu0, a.N, RB, KS);
+    __syncthreads();
+
+    float g = 1.0f;
+    if (FMT == FMT_NVFP4) g = load_f32_unaligned(a.scales + (size_t)a.N * (a.K / 16));
+    const int total = ntl * G::RT * a.mc;
+    for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
+        const int ti = idx / (G::RT * a.mc), rt = idx - ti * G::RT * a.mc;
+        const int r = rt / a.mc, t = rt - r * a.mc;
+        const int row = (gb + ti * a.G) * G::RT + r;
+        if (row >= a.N) continue;
+        float s = 0.f;
+        for (int c = 0; c < a.wk; ++c) s += red[((size_t)(ti * a.wk + c) * G::RT + r) * MC + t];
+        s *= pow2f(sh[t]);
+        if (a.nwin == 1) {
+            if (FMT == FMT_NVFP4) s *= g;
+            a.y[(size_t)(a.m0 + t) * a.N + row] = s;
+        } else {
+            a.ws[((size_t)win * a.mc + t) * a.N + row] = s;
+        }
+    }
+    if (a.nwin == 1) return;
+    // split-K over windows: the last CTA of this tile group adds the windows
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) *flag = atomicAdd(&a.ws_count[gb], 1) == a.nwin - 1;
+    __syncthreads();
+    if (!*flag) return;
+    __threadfence();
+    for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
+        const int ti = idx / (G::RT * a.mc), rt = idx - ti * G::RT * a.mc;
+        const int r = rt / a.mc, t = rt - r * a.mc;
+        const int row = (gb + ti * a.G) * G::RT + r;
+        if (row >= a.N) continue;
+        float s = 0.f;
+        for (int w = 0; w < a.nwin; ++w) s += __ldcg(&a.ws[((size_t)w * a.mc + t) * a.N + row]);
+        if (FMT == FMT_NVFP4) s *= g;
+        a.y[(size_t)(a.m0 + t) * a.N + row] = s;
+    }
+    if (threadIdx.x == 0) atomicExch(&a.ws_count[gb], 0);
+}
+
+template <int FMT, int MC>
+static cudaError_t run_qmv_stream(const DeviceState &ds, cudaStream_t st, QmvSArgs a, size_t smem)
+{
+    static int configured_dev[64] = {0};
+    if (ds.device < 64 && !configured_dev[ds.device]) {
+        cudaError_t e = cudaFuncSetAttribute(qmv_stream_kernel<FMT, MC>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, ds.max_smem_optin);
+        if (e != cudaSuccess) return e;
+        configured_dev[ds.device] = 1;
+    }
+    qmv_stream_kernel<FMT, MC><<<a.G * a.nwin, QMV_THREADS, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+// Plan and launch one token chunk; returns cudaErrorNotSupported when the
+// streaming kernel cannot take this shape (the caller falls back).
+template <int FMT, int MC>
+static cudaError_t plan_qmv_stream(const DeviceState &ds, cudaStream_t st, const uint8_t *codes,
+                                   const uint8_t *scales, const uint16_t *x, float *y, int m0, int mc, int N, int K)
+{
+    using G = SGeo<FMT, MC>;
+    const int U = K / 32;
+    const int rings = QMV_WARPS * ST_STAGES * G::STAGE_BYTES;
+    const long long avail = (long long)ds.max_smem_optin - rings - ST_RED_BUDGET - 128;
+    if (avail < 8192) return cudaErrorNotSupported;
+    // K windows so that the staged activations fit
+    int nwin = 1, WU = 0, ks = 0;
+    for (;; ++nwin) {
+        WU = (U + nwin - 1) / nwin;
+        WU = (WU + G::UPS - 1) / G::UPS * G::UPS;
+        ks = WU * 32;
+        if ((ks / 32) % 2 == 0) ks += 32;
+        if ((long long)MC * ks * 2 <= avail) break;
+        if (nwin > 64) return cudaErrorNotSupported;
+    }
+    nwin = (U + WU - 1) / WU;
+    QmvSArgs a;
+    a.codes = codes;
+    a.scales = scales;
+    a.x = x;
+    a.y = y;
+    a.ws = ds.ws;
+    a.ws_count = ds.ws_count;
+    a.N = N;
+    a.K = K;
+    a.m0 = m0;
+    a.mc = mc;
+    a.tiles = (N + G::RT - 1) / G::RT;
+    a.nwin = nwin;
+    a.G = nwin == 1 ? ds.num_sms : (ds.num_sms / nwin > 0 ? ds.num_sms / nwin : 1);
+    if (a.G > a.tiles) a.G = a.tiles;
+    a.WU = WU;
+    a.ntl_max = (a.tiles + a.G - 1) / a.G;
+    if (nwin > 1 && ((size_t)nwin * mc * N > WS_FLOATS || a.G > WS_COUNTERS)) return cudaErrorNotSupported;
+    // chunks per tile: as fine as one stage, within the reduction budget
+    const int spw = (WU + G::UPS - 1) / G::UPS;  // stages per row per window
+    int wk = 1, wl = 0;
+    while (wk * 2 <= spw && wk < 16) { wk *= 2; ++wl; }
+    const long long per = (long long)a.ntl_max * G::RT * MC * 4;
+    if (per > ST_RED_BUDGET) return cudaErrorNotSupported;
+    while (wk > 1 && per * wk > ST_RED_BUDGET) { wk /= 2; --wl; }
+    a.wk = wk;
+    a.wk_log2 = wl;
+    a.CU = ((spw + wk - 1) / wk) * G::UPS;
+    a.ks = ks;
+    const size_t red = (((size_t)a.ntl_max * wk * G::RT * MC * 4) + 15) & ~(size_t)15;
+    const size_t smem = (size_t)MC * ks * 2 + 80 + red + rings;
+    if (smem > (size_t)ds.max_smem_optin) return cudaErrorNotSupported;
+    return run_qmv_stream<FMT, MC>(ds, st, a, smem);
+}
+
+static int round_mc_s(int m) { return m <= 1 ? 1 : m <= 2 ? 2 : m <= 4 ? 4 : 8; }
+
+template <int FMT>
+static cudaError_t qmv_stream_chunk(const DeviceState &ds, cudaStream_t st, const uint8_t *codes,
+                                    const uint8_t *scales, const uint16_t *x, float *y, int m0, int mc, int N, int K)
+{
+    switch (round_mc_s(mc)) {
+    case 1: return plan_qmv_stream<FMT, 1>(ds, st, codes, scales, x, y, m0, mc, N, K);
+    case 2: return plan_qmv_stream<FMT, 2>(ds, st, codes, scales, x, y, m0, mc, N, K);
+    case 4: return plan_qmv_stream<FMT, 4>(ds, st, codes, scales, x, y, m0, mc, N, K);
+    default: return plan_qmv_stream<FMT, 8>(ds, st, codes, scales, x, y, m0, mc, N, K);
+    }
+}
+
+// Rows must be 128-element aligned for the 16-byte copies of codes and the
+// 4-byte copies of scales.
+static bool stream_ok(int, int K) { return K % 128 == 0; }
+
+cudaError_t launch_qmv(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,
+                       const uint8_t *scales, const uint16_t *x, float *y, int M, int N, int K)
+{
+    if (!stream_ok(fmt, K)) return launch_qmv_direct(ds, st, fmt, codes, scales, x, y, M, N, K);
+    for (int m0 = 0; m0 < M; m0 += 8) {
+        const int mc = M - m0 < 8 ? M - m0 : 8;
+        cudaError_t e;
+        if (fmt == FMT_MXFP4) e = qmv_stream_chunk<FMT_MXFP4>(ds, st, codes, scales, x, y, m0, mc, N, K);
+        else if (fmt == FMT_MXFP8) e = qmv_stream_chunk<FMT_MXFP8>(ds, st, codes, scales, x, y, m0, mc, N, K);
+        else e = qmv_stream_chunk<FMT_NVFP4>(ds, st, codes, scales, x, y, m0, mc, N, K);
+        if (e == cudaErrorNotSupported)
+            e = launch_qmv_direct(ds, st, fmt, codes, scales, x + (size_t)m0 * K, y + (size_t)m0 * N, mc, N, K);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+// ------------------------------------------------------------------ MoE
+
+struct MoeSArgs {
+    const uint8_t *codes;
+    const uint8_t *scales;
+    const uint16_t *x;
+    const int32_t *ids;
+    float *y;
+    int *err;
+    int T, E, topk, N, K;
+    int ks;
+};
+
+template <int FMT, int MC>
+__global__ void __launch_bounds__(QMV_THREADS, 1) moe_stream_kernel(MoeSArgs a)
+{
+    using G = SGeo<FMT, MC>;
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int P = a.T * a.topk;
+    int *cnt = reinterpret_cast<int *>(smem);
+    int *wgs = cnt + a.E;
+    int *pos = wgs + a.E;
+    int *sorted = pos + a.E;
+    int *wg_e = sorted + P;
+    int *wg_first = wg_e + P;
+    int *wg_mc = wg_first + P;
+    int *tmp = wg_mc + P;
+    int *sh = tmp + 40;
+    unsigned *maxbits = reinterpret_cast<unsigned *>(sh + a.T);
+    size_t off = (((size_t)(3 * a.E + 4 * P + 40 + 2 * a.T) * 4) + 15) & ~(size_t)15;
+    uint16_t *xs = reinterpret_cast<uint16_t *>(smem + off);
+    off += (size_t)a.T * a.ks * 2;
+    uint8_t *rings = smem + off;
+
+    RouteSmem rs{cnt, wgs, pos, sorted, wg_e, wg_first, wg_mc, tmp};
+    const int nwg = moe_route(a.ids, P, a.E, MC, rs);
+    for (int p = blockIdx.x; p < P; p += gridDim.x) {
+        const int e = a.ids[p];
+        if (e < 0 || e >= a.E) {
+            if (threadIdx.x == 0) set_device_error(a.err, DEVERR_BAD_EXPERT);
+            for (int n = threadIdx.x; n < a.N; n += blockDim.x) a.y[(size_t)p * a.N + n] = __int_as_float(0x7FC00000);
+        }
+    }
+    stage_x<FMT>(a.x, (size_t)a.K, a.K, a.T, nullptr, xs, a.ks, sh, maxbits);
+    __syncthreads();
+
+    const int tiles = (a.N + G::RT - 1) / G::RT;
+    const int items = nwg * tiles;
+    const int warp = threadIdx.x >> 5;
+    const int gw = blockIdx.x * QMV_WARPS + warp, stride = gridDim.x * QMV_WARPS;
+    const int n_my = gw < items ? (items - gw + stride - 1) / stride : 0;
+    const size_t RB = FMT == FMT_MXFP8 ? (size_t)a.K : (size_t)a.K / 2;
+    const size_t KS = FMT == FMT_NVFP4 ? (size_t)(a.K / 16) : (size_t)(a.K / 32);
+    const int U = (a.K + 31) / 32;
+    const int tok = lane_token<MC>();
+
+    auto next = [&](int i) {
+        const int item = gw + stride * i;
+        const int w = item / tiles, tile = item - w * tiles;
+        const int e = wg_e[w];
+        SUnit u;
+        u.codes = a.codes + (size_t)e * a.N * RB;
+        u.scales = a.scales + (size_t)e * a.N * KS;
+        u.row0 = tile * G::RT;
+        u.ub = 0;
+        u.ul = U;
+        return u;
+    };
+    auto xrow_of = [&](int i) {
+        const int w = (gw + stride * i) / tiles;
+        return tok < wg_mc[w] ? sorted[wg_first[w] + tok] / a.topk : -1;
+    };
+    auto done = [&](int i, const float (&acc)[2][2]) {
+        const int item = gw + stride * i;
+        const int w = item / tiles, tile = item - w * tiles;
+        float vv[2][2];
+        qmv_warp_reduce<MC>(acc, vv);
+        float g = 1.0f;
+        if (FMT == FMT_NVFP4)
+            g = load_f32_unaligned(a.scales + (size_t)a.E * a.N * KS + 4 * (size_t)wg_e[w]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                int r, t;
+                if (tile_out<MC>(h, c, r, t)) {
+                    const int row = tile * G::RT + r;
+                    if (row < a.N && t < wg_mc[w]) {
+                        const int slot = sorted[wg_first[w] + t];
+                        float s = vv[h][c] * pow2f(sh[slot / a.topk]);
+                        if (FMT == FMT_NVFP4) s *= g;
+                        a.y[(size_t)slot * a.N + row] = s;
+                    }
+                }
+            }
+    };
+    stream_units<FMT, MC>(n_my, next, xrow_of, done, rings + (size_t)warp * ST_STAGES * G::STAGE_BYTES, xs, a.ks,
+                          0, a.N, RB, KS);
+}
+
+template <int FMT, int MC>
+static cudaError_t run_moe_stream(const DeviceState &ds, cudaStream_t st, const MoeSArgs &a)
+{
+    using G = SGeo<FMT, MC>;
+    const int P = a.T * a.topk;
+    const size_t head = (((size_t)(3 * a.E + 4 * P + 40 + 2 * a.T) * 4) + 15) & ~(size_t)15;
+    const size_t smem = head + (size_t)a.T * a.ks * 2 + (size_t)QMV_WARPS * ST_STAGES * G::STAGE_BYTES;
+    if (smem > (size_t)ds.max_smem_optin) return cudaErrorNotSupported;
+    static int configured_dev[64] = {0};
+    if (ds.device < 64 && !configured_dev[ds.device]) {
+        cudaError_t e = cudaFuncSetAttribute(moe_stream_kernel<FMT, MC>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, ds.max_smem_optin);
+        if (e != cudaSuccess) return e;
+        configured_dev[ds.device] = 1;
+    }
+    moe_stream_kernel<FMT, MC><<<ds.num_sms, QMV_THREADS, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <int FMT>
+static cudaError_t moe_stream_dispatch(const DeviceState &ds, cudaStream_t st, const MoeSArgs &a, int MC)
+{
+    switch (MC) {
+    case 1: return run_moe_stream<FMT, 1>(ds, st, a);
+    case 2: return run_moe_stream<FMT, 2>(ds, st, a);
+    case 4: return run_moe_stream<FMT, 4>(ds, st, a);
+    default: return run_moe_stream<FMT, 8>(ds, st, a);
+    }
+}
+
+cudaError_t launch_moe_qmv(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,
+                           const uint8_t *scales, const uint16_t *x, const int32_t *ids, float *y, int T, int E,
+                           int topk, int N, int K)
+{
+    if (stream_ok(fmt, K)) {
+        MoeSArgs a;
+        a.codes = codes;
+        a.scales = scales;
+        a.x = x;
+        a.ids = ids;
+        a.y = y;
+        a.err = ds.err;
+        a.T = T;
+        a.E = E;
+        a.topk = topk;
+        a.N = N;
+        a.K = K;
+        a.ks = stage_stride(K);
+        // a work group holds the slots of one expert, at most one per token
+        // when each token's experts are distinct; the pass width follows T
+        const int MC = round_mc_s(T < 8 ? T : 8);
+        cudaError_t e;
+        if (fmt == FMT_MXFP4) e = moe_stream_dispatch<FMT_MXFP4>(ds, st, a, MC);
+        else if (fmt == FMT_MXFP8) e = moe_stream_dispatch<FMT_MXFP8>(ds, st, a, MC);
+        else e = moe_stream_dispatch<FMT_NVFP4>(ds, st, a, MC);
+        if (e != cudaErrorNotSupported) return e;
+    }
+    return launch_moe_qmv_direct(ds, st, fmt, codes, scales, x, ids, y, T, E, topk, N, K);
+}
+
+}  // namespace mx

@@ -11,6 +11,11 @@ import pytest
 
 REL_L2 = 2e-3
 MAX_ROWNORM = 1e-2
+# A bf16 output is rounded to 8 significant bits: that alone moves each
+# element by up to 2^-9 of itself, so for bf16 outputs the per-row relative
+# L2 allows that rounding on top of the 2e-3 budget (the per-tensor relL2 and
+# the max-error bound stay as they are).
+BF16_ROUNDING = 2.0 ** -9
 
 
 def need_gpu():
@@ -54,7 +59,7 @@ def bf16_bits_to_f64(bits):
         return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-def check_close(got, want, what=""):
+def check_close(got, want, what="", bf16_out=False):
     """Tolerance gate on [rows][cols] arrays (got fp32/bf16-as-float, want fp64)."""
     got = np.asarray(got, dtype=np.float64).reshape(want.shape[0], -1)
     want = np.asarray(want, dtype=np.float64).reshape(want.shape[0], -1)
@@ -65,7 +70,8 @@ def check_close(got, want, what=""):
     rel_rows = np.linalg.norm(err, axis=1) / rn
     mx = np.abs(err).max(axis=1) / rn
     assert tot <= REL_L2, f"{what}: relL2 {tot:.3e}"
-    assert rel_rows.max() <= REL_L2, f"{what}: worst row relL2 {rel_rows.max():.3e}"
+    row_lim = REL_L2 + (BF16_ROUNDING if bf16_out else 0.0)
+    assert rel_rows.max() <= row_lim, f"{what}: worst row relL2 {rel_rows.max():.3e}"
     assert mx.max() <= MAX_ROWNORM, f"{what}: max |err| / row norm {mx.max():.3e}"
     return tot, rel_rows.max(), mx.max()
 

@@ -26,7 +26,7 @@ def test_qmm_parity(orc, fmt, M, N, K):
     codes, scales = synth.weights(fmt, N, K, M + K, exp_lo=118, exp_hi=132)
     X = synth.activations(M, K, N + K)
     check_close(run_qmm(fmt, codes, scales, X, N), orc.qmv(fmt, codes, scales, X, M, N, K),
-                f"qmm fmt{fmt} {M}x{N}x{K}")
+                f"qmm fmt{fmt} {M}x{N}x{K}", bf16_out=True)
 
 
 @pytest.mark.parametrize("fmt", [0, 1, 2])
@@ -55,7 +55,7 @@ def test_qmm_agrees_with_qmv():
     X = synth.activations(M, K, 18)
     Y = run_qmm(fmt, codes, scales, X, N)
     y = ops.qmv(fmt, dev_u8(codes), dev_u8(scales), dev_bf16(X[:4]), N).cpu().numpy()
-    check_close(Y[:4], y.astype(np.float64), "qmm vs qmv")
+    check_close(Y[:4], y.astype(np.float64), "qmm vs qmv", bf16_out=True)
 
 
 @pytest.mark.parametrize("N,K,seed", [(28672, 8192, 8), (8192, 28672, 9)])
@@ -71,5 +71,5 @@ def test_qmm_prefill_full_size(orc, N, K, seed):
     ms = np.repeat(rows, N)
     ns = np.tile(np.arange(N), rows.size)
     want = orc.qmm_points(0, codes, scales, X, M, N, K, ms, ns).reshape(rows.size, N)
-    check_close(Y[rows], want, f"qmm full {N}x{K}")
+    check_close(Y[rows], want, f"qmm full {N}x{K}", bf16_out=True)
     assert np.all(np.isfinite(Y))
