@@ -85,59 +85,77 @@ __device__ __forceinline__ int unit_stages(const SUnit &u)
 
 // A lane's share of the copies of one unit, resolved once per unit:
 // source pointers at the unit's first stage, bytes left in the row after
-// them, and destination offsets within a ring slot.
+// them (<= 0: nothing to copy), and destination offsets within a ring slot.
 template <int FMT, int MC>
 struct CopyPlan {
     using G = SGeo<FMT, MC>;
     static constexpr int NP = G::PIECES / 32;
     static constexpr int NW = (G::SWORDS + 31) / 32;
     const uint8_t *src[NP];
-    long long left[NP];  // row bytes from src to the row end (<= 0: none)
-    uint32_t dst[NP];
+    int left[NP];
     const uint8_t *ssrc[NW];
-    long long sleft[NW];
-    uint32_t sdst[NW];
+    int sleft[NW];
+};
+
+// Lane constants of the copy mapping (independent of the unit).
+template <int FMT, int MC>
+struct CopyLane {
+    using G = SGeo<FMT, MC>;
+    int row[CopyPlan<FMT, MC>::NP], off[CopyPlan<FMT, MC>::NP];
+    int srow[CopyPlan<FMT, MC>::NW], soff[CopyPlan<FMT, MC>::NW];
+    __device__ __forceinline__ CopyLane()
+    {
+        const int lane = threadIdx.x & 31;
+#pragma unroll
+        for (int j = 0; j < CopyPlan<FMT, MC>::NP; ++j) {
+            const int p = lane + 32 * j;
+            row[j] = p / (G::CB / 16);
+            off[j] = (p % (G::CB / 16)) * 16;
+        }
+#pragma unroll
+        for (int j = 0; j < CopyPlan<FMT, MC>::NW; ++j) {
+            const int w = lane + 32 * j;
+            srow[j] = w < G::SWORDS ? w / (G::SB / 4) : 0;
+            soff[j] = (w % (G::SB / 4)) * 4;
+        }
+    }
 };
 
 template <int FMT, int MC>
-__device__ __forceinline__ void plan_copies(const SUnit &u, int N, size_t RB, size_t KS, CopyPlan<FMT, MC> &c)
+__device__ __forceinline__ void plan_copies(const SUnit &u, const CopyLane<FMT, MC> &cl, int N, int RB, int KS,
+                                            CopyPlan<FMT, MC> &c)
 {
     using G = SGeo<FMT, MC>;
     const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int j = 0; j < c.NP; ++j) {
-        const int p = lane + 32 * j;
-        const int row = p / (G::CB / 16), off = (p % (G::CB / 16)) * 16;
-        const int grow = u.row0 + row;
-        const size_t col = (size_t)u.ub * G::UCB + off;
+        const int grow = u.row0 + cl.row[j];
+        const int col = u.ub * G::UCB + cl.off[j];
         c.src[j] = u.codes + (size_t)(grow < N ? grow : 0) * RB + col;
-        c.left[j] = grow < N ? (long long)RB - (long long)col : 0;
-        c.dst[j] = row * G::RS + off;
+        c.left[j] = grow < N ? RB - col : 0;
     }
 #pragma unroll
     for (int j = 0; j < c.NW; ++j) {
-        const int w = lane + 32 * j;
-        const int row = w / (G::SB / 4), off = (w % (G::SB / 4)) * 4;
-        const int grow = u.row0 + row;
-        const size_t col = (size_t)u.ub * G::SPU + off;
+        const int grow = u.row0 + cl.srow[j];
+        const int col = u.ub * G::SPU + cl.soff[j];
         c.ssrc[j] = u.scales + (size_t)(grow < N ? grow : 0) * KS + col;
-        c.sleft[j] = (grow < N && w < G::SWORDS) ? (long long)KS - (long long)col : 0;
-        c.sdst[j] = G::CODE_BYTES + row * G::SB + off;
+        c.sleft[j] = (grow < N && lane + 32 * j < G::SWORDS) ? KS - col : 0;
     }
 }
 
 // Copy stage s of the planned unit into the ring slot at shared address dst.
 template <int FMT, int MC>
-__device__ __forceinline__ void copy_stage(const CopyPlan<FMT, MC> &c, int s, uint32_t dst)
+__device__ __forceinline__ void copy_stage(const CopyPlan<FMT, MC> &c, const CopyLane<FMT, MC> &cl, int s,
+                                           uint32_t dst)
 {
     using G = SGeo<FMT, MC>;
-    const long long cs = (long long)s * G::CB, ss = (long long)s * G::SB;
+    const int cs = s * G::CB, ss = s * G::SB;
 #pragma unroll
     for (int j = 0; j < c.NP; ++j)
-        if (cs < c.left[j]) cp_async16(dst + c.dst[j], c.src[j] + cs);
+        if (cs < c.left[j]) cp_async16(dst + cl.row[j] * G::RS + cl.off[j], c.src[j] + cs);
 #pragma unroll
     for (int j = 0; j < c.NW; ++j)
-        if (ss < c.sleft[j]) cp_async4(dst + c.sdst[j], c.ssrc[j] + ss);
+        if (ss < c.sleft[j]) cp_async4(dst + G::CODE_BYTES + cl.srow[j] * G::SB + cl.soff[j], c.ssrc[j] + ss);
 }
 
 // Decode-and-multiply one stage from shared memory into acc.
@@ -212,11 +230,12 @@ __device__ __forceinline__ void compute_stage(const SUnit &u, int s, const uint8
 // fragment partial sums at the end of unit i.
 template <int FMT, int MC, class Next, class XRow, class Done>
 __device__ __forceinline__ void stream_units(int n_units, const Next &next, const XRow &xrow_of, const Done &done,
-                                             uint8_t *ring, const uint16_t *xs, int ks, int xu0, int N, size_t RB,
-                                             size_t KS)
+                                             uint8_t *ring, const uint16_t *xs, int ks, int xu0, int N, int RB,
+                                             int KS)
 {
     using G = SGeo<FMT, MC>;
     const uint32_t ring_s = smem_addr(ring);
+    const CopyLane<FMT, MC> cl;
     // issue cursor
     int iu = -1, is = 0, ins = 0, slot_issue = 0;
     CopyPlan<FMT, MC> plan;
@@ -227,11 +246,11 @@ __device__ __forceinline__ void stream_units(int n_units, const Next &next, cons
             if (iu < n_units) {
                 const SUnit iud = next(iu);
                 ins = unit_stages<FMT, MC>(iud);
-                plan_copies<FMT, MC>(iud, N, RB, KS, plan);
+                plan_copies<FMT, MC>(iud, cl, N, RB, KS, plan);
             }
         }
         if (iu < n_units) {
-            copy_stage<FMT, MC>(plan, is, ring_s + slot_issue * G::STAGE_BYTES);
+            copy_stage<FMT, MC>(plan, cl, is, ring_s + slot_issue * G::STAGE_BYTES);
             ++is;
         }
         cp_async_commit();
@@ -307,8 +326,8 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) qmv_stream_kernel(QmvSArgs a)
     const int ntl = gb < a.tiles ? (a.tiles - gb + a.G - 1) / a.G : 0;
     const int nv = ntl * a.wk;
     const int n_my = warp < nv ? (nv - warp + QMV_WARPS - 1) / QMV_WARPS : 0;
-    const size_t RB = FMT == FMT_MXFP8 ? (size_t)a.K : (size_t)a.K / 2;
-    const size_t KS = FMT == FMT_NVFP4 ? (size_t)(a.K / 16) : (size_t)(a.K / 32);
+    const int RB = FMT == FMT_MXFP8 ? a.K : a.K / 2;
+    const int KS = FMT == FMT_NVFP4 ? a.K / 16 : a.K / 32;
     const int tok = lane_token<MC>();
     const int xrow = tok < a.mc ? tok : -1;
 
@@ -437,7 +456,10 @@ static cudaError_t plan_qmv_stream(const DeviceState &ds, cudaStream_t st, const
     // chunks per tile: as fine as one stage, within the reduction budget
     const int spw = (WU + G::UPS - 1) / G::UPS;  // stages per row per window
     int wk = 1, wl = 0;
-    while (wk * 2 <= spw && wk < 16) { wk *= 2; ++wl; }
+    while ((long long)a.ntl_max * wk < 6LL * QMV_WARPS && wk * 2 <= spw && wk < 16) {
+        wk *= 2;
+        ++wl;
+    }
     const long long per = (long long)a.ntl_max * G::RT * MC * 4;
     if (per > ST_RED_BUDGET) return cudaErrorNotSupported;
     while (wk > 1 && per * wk > ST_RED_BUDGET) { wk /= 2; --wl; }
@@ -537,8 +559,8 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) moe_stream_kernel(MoeSArgs a)
     const int warp = threadIdx.x >> 5;
     const int gw = blockIdx.x * QMV_WARPS + warp, stride = gridDim.x * QMV_WARPS;
     const int n_my = gw < items ? (items - gw + stride - 1) / stride : 0;
-    const size_t RB = FMT == FMT_MXFP8 ? (size_t)a.K : (size_t)a.K / 2;
-    const size_t KS = FMT == FMT_NVFP4 ? (size_t)(a.K / 16) : (size_t)(a.K / 32);
+    const int RB = FMT == FMT_MXFP8 ? a.K : a.K / 2;
+    const int KS = FMT == FMT_NVFP4 ? a.K / 16 : a.K / 32;
     const int U = (a.K + 31) / 32;
     const int tok = lane_token<MC>();
 
