@@ -66,22 +66,65 @@ __host__ __device__ inline int stage_stride(int K)
 // receives the per-row power-of-two exponent: the staged values are
 // x * 2^-sh[r] with max |.| in [1, 2) (exact: bf16 has 8 significant bits,
 // f16 11).  Elements past len up to the next 32-element unit are zero.
+// When the rows fit in registers (<= 8 chunks of 8 elements per thread)
+// global memory is read once; otherwise twice.
+constexpr int STAGE_REG_CHUNKS = 8;
+
+__device__ __forceinline__ void stage_store(uint16_t *xs, int ks, int r, int k0, int len, uint4 v, float f,
+                                            int fmt)
+{
+    // elements k0 .. k0+7 of row r (k0 a multiple of 8), zero past len
+    const int u = k0 >> 5, p0 = k0 & 31;
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int p = p0 + 2 * j;
+        int slot = p;
+        if (fmt == FMT_NVFP4) slot = 8 * ((p & 15) >> 2) + 4 * (p >> 4) + (p & 3);
+        uint32_t out = 0u;
+        if (k0 + 2 * j < len)
+            out = f32x2_to_f16x2(bf16_to_f32(w[j] & 0xFFFFu) * f, bf16_to_f32(w[j] >> 16) * f);
+        *reinterpret_cast<uint32_t *>(xs + (size_t)r * ks + u * 32 + slot) = out;
+    }
+}
+
 template <int FMT>
 __device__ void stage_x(const uint16_t *__restrict__ x, size_t ld, int len, int nrows, const int *src,
                         uint16_t *xs, int ks, int *sh, unsigned *maxbits)
 {
     for (int r = threadIdx.x; r < nrows; r += blockDim.x) maxbits[r] = 0u;
     __syncthreads();
+    const int cpr = (len + 31) / 32 * 4;  // 8-element chunks per row (whole units)
+    const int total = nrows * cpr;
+    const bool in_regs = total <= (int)blockDim.x * STAGE_REG_CHUNKS && (len % 8) == 0 && (ld % 8) == 0;
+    uint4 cache[STAGE_REG_CHUNKS];
     // pass 1: largest magnitude per row (as bf16 bits; NaN > inf > finite)
-    const int kp = len / 2;  // bf16 pairs per row
-    for (int r = 0; r < nrows; ++r) {
+    for (int r = 0; r < nrows && !in_regs; ++r) {
         const uint32_t *row = reinterpret_cast<const uint32_t *>(x + (size_t)(src ? src[r] : r) * ld);
         unsigned m = 0;
-        for (int i = threadIdx.x; i < kp; i += blockDim.x) {
+        for (int i = threadIdx.x; i < len / 2; i += blockDim.x) {
             uint32_t v = row[i];
             m = max(m, max(v & 0x7FFFu, (v >> 16) & 0x7FFFu));
         }
         if (m) atomicMax(&maxbits[r], m);
+    }
+    if (in_regs) {
+        // one read: each thread caches its chunks and reduces per row
+#pragma unroll
+        for (int j = 0; j < STAGE_REG_CHUNKS; ++j) {
+            const int idx = threadIdx.x + j * blockDim.x;
+            cache[j] = make_uint4(0u, 0u, 0u, 0u);
+            if (idx < total) {
+                const int r = idx / cpr, k0 = (idx - r * cpr) * 8;
+                if (k0 < len) {
+                    cache[j] = *reinterpret_cast<const uint4 *>(x + (size_t)(src ? src[r] : r) * ld + k0);
+                    const uint4 v = cache[j];
+                    unsigned m = max(max(v.x & 0x7FFFu, (v.x >> 16) & 0x7FFFu), max(v.y & 0x7FFFu, (v.y >> 16) & 0x7FFFu));
+                    m = max(m, max(max(v.z & 0x7FFFu, (v.z >> 16) & 0x7FFFu), max(v.w & 0x7FFFu, (v.w >> 16) & 0x7FFFu)));
+                    if (m) atomicMax(&maxbits[r], m);
+                }
+            }
+        }
     }
     __syncthreads();
     for (int r = threadIdx.x; r < nrows; r += blockDim.x) {
@@ -92,22 +135,31 @@ __device__ void stage_x(const uint16_t *__restrict__ x, size_t ld, int len, int 
         sh[r] = s;
     }
     __syncthreads();
-    // pass 2: convert and permute (zero past len)
-    const int U = (len + 31) / 32;
-    const int pairs = U * 16;
-    for (int idx = threadIdx.x; idx < nrows * pairs; idx += blockDim.x) {
-        const int r = idx / pairs, pp = idx - r * pairs;
-        const int k = 2 * pp;
-        const int u = k >> 5, p = k & 31;
-        int slot = p;
-        if (FMT == FMT_NVFP4) slot = 8 * ((p & 15) >> 2) + 4 * (p >> 4) + (p & 3);
-        uint32_t out = 0u;
-        if (k < len) {
-            uint32_t v = reinterpret_cast<const uint32_t *>(x + (size_t)(src ? src[r] : r) * ld)[pp];
-            float f = pow2f(-sh[r]);
-            out = f32x2_to_f16x2(bf16_to_f32(v & 0xFFFFu) * f, bf16_to_f32(v >> 16) * f);
+    if (in_regs) {
+#pragma unroll
+        for (int j = 0; j < STAGE_REG_CHUNKS; ++j) {
+            const int idx = threadIdx.x + j * blockDim.x;
+            if (idx < total) {
+                const int r = idx / cpr, k0 = (idx - r * cpr) * 8;
+                stage_store(xs, ks, r, k0, len, cache[j], pow2f(-sh[r]), FMT);
+            }
         }
-        *reinterpret_cast<uint32_t *>(xs + (size_t)r * ks + u * 32 + slot) = out;
+        return;
+    }
+    // pass 2: convert and permute (zero past len)
+    for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
+        const int r = idx / cpr, k0 = (idx - r * cpr) * 8;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        const uint16_t *row = x + (size_t)(src ? src[r] : r) * ld;
+        if (k0 + 8 <= len && (ld % 8) == 0) {
+            v = *reinterpret_cast<const uint4 *>(row + k0);
+        } else {
+            uint32_t w[4] = {0u, 0u, 0u, 0u};
+            for (int j = 0; j < 4; ++j)
+                if (k0 + 2 * j < len) w[j] = *reinterpret_cast<const uint32_t *>(row + k0 + 2 * j);
+            v = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        stage_store(xs, ks, r, k0, len, v, pow2f(-sh[r]), FMT);
     }
 }
 

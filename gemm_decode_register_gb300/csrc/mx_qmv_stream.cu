@@ -18,11 +18,12 @@
 //     tile group adds them in window order (deterministic).
 //   * MoE: units are (work group of up to MC slots routed to one expert,
 //     tile) over the whole K of that expert.
+#include <algorithm>
+
 #include "mx_qmv_core.cuh"
 
 namespace mx {
 
-constexpr int ST_STAGES = 3;
 constexpr int ST_RED_BUDGET = 24 * 1024;
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p)
@@ -62,6 +63,9 @@ struct SGeo {
     static constexpr int SB = UPS * SPU;                           // scale bytes per row per stage
     static constexpr int CODE_BYTES = RT * RS;
     static constexpr int STAGE_BYTES = CODE_BYTES + RT * SB;
+    // ring depth: one stage in decode, the rest in flight (short tiles leave
+    // room in shared memory for a deeper ring)
+    static constexpr int STAGES = MC <= 2 ? 4 : 3;
     static constexpr int PIECES = RT * CB / 16;                    // 16-byte code copies per stage
     static constexpr int SWORDS = RT * SB / 4;                     // 4-byte scale copies per stage
     static_assert(PIECES % 32 == 0, "code copies per lane");
@@ -225,28 +229,35 @@ __device__ __forceinline__ void compute_stage(const SUnit &u, int s, const uint8
         compute_stage_impl<FMT, MC, false>(u, s, buf, xs, ks, xu0, xrow, acc);
 }
 
-// Stream a warp's units through its ring.  next(i) -> SUnit, xrow_of(i) ->
-// the lane's activation row for unit i, done(i, acc) receives the lane's
-// fragment partial sums at the end of unit i.
-template <int FMT, int MC, class Next, class XRow, class Done>
-__device__ __forceinline__ void stream_units(int n_units, const Next &next, const XRow &xrow_of, const Done &done,
-                                             uint8_t *ring, const uint16_t *xs, int ks, int xu0, int N, int RB,
-                                             int KS)
-{
+// A warp's stream of units through its ring: copies run S-1 stages ahead
+// of the decode.  prime() issues the first copies (it may run before the
+// activations are staged: the weights do not depend on them); run()
+// decodes every stage and refills the ring as it goes.
+// next(i) -> SUnit for the warp's unit i.
+template <int FMT, int MC, class Next>
+struct Streamer {
     using G = SGeo<FMT, MC>;
-    const uint32_t ring_s = smem_addr(ring);
-    const CopyLane<FMT, MC> cl;
-    // issue cursor
-    int iu = -1, is = 0, ins = 0, slot_issue = 0;
+    const Next &next;
+    int n_units, N, RB, KS;
+    uint32_t ring_s;
+    CopyLane<FMT, MC> cl;
     CopyPlan<FMT, MC> plan;
-    auto issue = [&]() {
+    int iu = -1, is = 0, ins = 0, slot_issue = 0;
+
+    __device__ __forceinline__ Streamer(const Next &nx, int n, uint8_t *ring, int n_rows, int rb, int kscale)
+        : next(nx), n_units(n), N(n_rows), RB(rb), KS(kscale), ring_s(smem_addr(ring))
+    {
+    }
+
+    __device__ __forceinline__ void issue()
+    {
         while (iu < n_units && (iu < 0 || is >= ins)) {
             ++iu;
             is = 0;
             if (iu < n_units) {
-                const SUnit iud = next(iu);
-                ins = unit_stages<FMT, MC>(iud);
-                plan_copies<FMT, MC>(iud, cl, N, RB, KS, plan);
+                const SUnit u = next(iu);
+                ins = unit_stages<FMT, MC>(u);
+                plan_copies<FMT, MC>(u, cl, N, RB, KS, plan);
             }
         }
         if (iu < n_units) {
@@ -254,28 +265,40 @@ __device__ __forceinline__ void stream_units(int n_units, const Next &next, cons
             ++is;
         }
         cp_async_commit();
-        slot_issue = slot_issue + 1 == ST_STAGES ? 0 : slot_issue + 1;
-    };
-#pragma unroll
-    for (int s = 0; s < ST_STAGES - 1; ++s) issue();
-    int slot = 0;
-    for (int cu = 0; cu < n_units; ++cu) {
-        const SUnit cd = next(cu);
-        const int nst = unit_stages<FMT, MC>(cd);
-        const int xrow = xrow_of(cu);
-        float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-        for (int cs = 0; cs < nst; ++cs) {
-            cp_async_wait<ST_STAGES - 2>();
-            __syncwarp();
-            issue();  // refills the slot consumed one stage ago
-            compute_stage<FMT, MC>(cd, cs, ring + slot * G::STAGE_BYTES, xs, ks, xu0, xrow, acc);
-            slot = slot + 1 == ST_STAGES ? 0 : slot + 1;
-        }
-        done(cu, acc);
+        slot_issue = slot_issue + 1 == G::STAGES ? 0 : slot_issue + 1;
     }
-    cp_async_wait<0>();
-    __syncwarp();
-}
+
+    __device__ __forceinline__ void prime()
+    {
+#pragma unroll
+        for (int s = 0; s < G::STAGES - 1; ++s) issue();
+    }
+
+    // xrow_of(i): the lane's activation row for unit i; done(i, acc): the
+    // lane's fragment partial sums at the end of unit i.
+    template <class XRow, class Done>
+    __device__ __forceinline__ void run(const XRow &xrow_of, const Done &done, const uint8_t *ring,
+                                        const uint16_t *xs, int ks, int xu0)
+    {
+        int slot = 0;
+        for (int cu = 0; cu < n_units; ++cu) {
+            const SUnit cd = next(cu);
+            const int nst = unit_stages<FMT, MC>(cd);
+            const int xrow = xrow_of(cu);
+            float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+            for (int cs = 0; cs < nst; ++cs) {
+                cp_async_wait<G::STAGES - 2>();
+                __syncwarp();
+                issue();  // refills the slot consumed one stage ago
+                compute_stage<FMT, MC>(cd, cs, ring + slot * G::STAGE_BYTES, xs, ks, xu0, xrow, acc);
+                slot = slot + 1 == G::STAGES ? 0 : slot + 1;
+            }
+            done(cu, acc);
+        }
+        cp_async_wait<0>();
+        __syncwarp();
+    }
+};
 
 // ------------------------------------------------------------------ dense
 
@@ -318,9 +341,6 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) qmv_stream_kernel(QmvSArgs a)
     const int U = (a.K + 31) / 32;
     const int xu0 = win * a.WU, xu1 = min(U, xu0 + a.WU);
     const int len = min(a.K - xu0 * 32, (xu1 - xu0) * 32);
-    stage_x<FMT>(a.x + (size_t)a.m0 * a.K + (size_t)xu0 * 32, (size_t)a.K, len, a.mc, nullptr, xs, a.ks, sh,
-                 maxbits);
-    __syncthreads();
 
     const int warp = threadIdx.x >> 5;
     const int ntl = gb < a.tiles ? (a.tiles - gb + a.G - 1) / a.G : 0;
@@ -356,8 +376,13 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) qmv_stream_kernel(QmvSArgs a)
                 if (tile_out<MC>(h, c, r, t)) red[((size_t)v * G::RT + r) * MC + t] = vv[h][c];
             }
     };
-    stream_units<FMT, MC>(n_my, next, xrow_of, done, rings + (size_t)warp * ST_STAGES * G::STAGE_BYTES, xs, a.ks,
-                          xu0, a.N, RB, KS);
+    uint8_t *ring = rings + (size_t)warp * G::STAGES * G::STAGE_BYTES;
+    Streamer<FMT, MC, decltype(next)> st(next, n_my, ring, a.N, RB, KS);
+    st.prime();  // weight copies overlap the activation staging below
+    stage_x<FMT>(a.x + (size_t)a.m0 * a.K + (size_t)xu0 * 32, (size_t)a.K, len, a.mc, nullptr, xs, a.ks, sh,
+                 maxbits);
+    __syncthreads();
+    st.run(xrow_of, done, ring, xs, a.ks, xu0);
     __syncthreads();
 
     float g = 1.0f;
@@ -421,8 +446,12 @@ static cudaError_t plan_qmv_stream(const DeviceState &ds, cudaStream_t st, const
 {
     using G = SGeo<FMT, MC>;
     const int U = K / 32;
-    const int rings = QMV_WARPS * ST_STAGES * G::STAGE_BYTES;
-    const long long avail = (long long)ds.max_smem_optin - rings - ST_RED_BUDGET - 128;
+    const int rings = QMV_WARPS * G::STAGES * G::STAGE_BYTES;
+    const int tiles = (N + G::RT - 1) / G::RT;
+    // reduction slots needed at most (one window, 16 chunks per tile)
+    const long long red_est =
+        std::min<long long>(ST_RED_BUDGET, (long long)((tiles + ds.num_sms - 1) / ds.num_sms) * 16 * G::RT * MC * 4);
+    const long long avail = (long long)ds.max_smem_optin - rings - red_est - 128;
     if (avail < 8192) return cudaErrorNotSupported;
     // K windows so that the staged activations fit
     int nwin = 1, WU = 0, ks = 0;
@@ -461,8 +490,9 @@ static cudaError_t plan_qmv_stream(const DeviceState &ds, cudaStream_t st, const
         ++wl;
     }
     const long long per = (long long)a.ntl_max * G::RT * MC * 4;
-    if (per > ST_RED_BUDGET) return cudaErrorNotSupported;
-    while (wk > 1 && per * wk > ST_RED_BUDGET) { wk /= 2; --wl; }
+    const long long red_cap = (long long)ds.max_smem_optin - rings - 128 - (long long)MC * ks * 2;
+    if (per > red_cap) return cudaErrorNotSupported;
+    while (wk > 1 && per * wk > red_cap) { wk /= 2; --wl; }
     a.wk = wk;
     a.wk_log2 = wl;
     a.CU = ((spw + wk - 1) / wk) * G::UPS;
@@ -604,8 +634,10 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) moe_stream_kernel(MoeSArgs a)
                 }
             }
     };
-    stream_units<FMT, MC>(n_my, next, xrow_of, done, rings + (size_t)warp * ST_STAGES * G::STAGE_BYTES, xs, a.ks,
-                          0, a.N, RB, KS);
+    uint8_t *ring = rings + (size_t)warp * G::STAGES * G::STAGE_BYTES;
+    Streamer<FMT, MC, decltype(next)> st(next, n_my, ring, a.N, RB, KS);
+    st.prime();
+    st.run(xrow_of, done, ring, xs, a.ks, 0);
 }
 
 template <int FMT, int MC>
@@ -614,7 +646,7 @@ static cudaError_t run_moe_stream(const DeviceState &ds, cudaStream_t st, const 
     using G = SGeo<FMT, MC>;
     const int P = a.T * a.topk;
     const size_t head = (((size_t)(3 * a.E + 4 * P + 40 + 2 * a.T) * 4) + 15) & ~(size_t)15;
-    const size_t smem = head + (size_t)a.T * a.ks * 2 + (size_t)QMV_WARPS * ST_STAGES * G::STAGE_BYTES;
+    const size_t smem = head + (size_t)a.T * a.ks * 2 + (size_t)QMV_WARPS * G::STAGES * G::STAGE_BYTES;
     if (smem > (size_t)ds.max_smem_optin) return cudaErrorNotSupported;
     static int configured_dev[64] = {0};
     if (ds.device < 64 && !configured_dev[ds.device]) {

@@ -33,6 +33,8 @@ class MxError(RuntimeError):
 def load(path: str | None = None) -> ctypes.CDLL:
     """Load libmxgemm.so (built by ``gemm_decode_register_gb300.build``)."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is not None:
             return _lib
