@@ -52,6 +52,13 @@ constexpr int QMV_MAX_K = 1 << 20;
 constexpr int MOE_MAX_SLOTS = 1024;  // T * topk
 constexpr int MOE_MAX_EXPERTS = 4096;
 
+// Split-K workspace a launch_qmv call would use (0 when it needs none).
+struct QmvScratchNeed {
+    size_t floats = 0;  // window partial sums
+    int counters = 0;   // arrival counters, zero before the launch
+};
+QmvScratchNeed qmv_scratch_need(const DeviceState &ds, int fmt, int M, int N, int K);
+
 // Shared-memory bytes the qmv kernel needs to stage `rows` activation rows
 // of length K (f16, padded), or -1 if that cannot fit.
 int qmv_stage_bytes(int rows, int K);

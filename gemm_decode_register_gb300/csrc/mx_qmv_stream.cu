@@ -439,10 +439,13 @@ static cudaError_t run_qmv_stream(const DeviceState &ds, cudaStream_t st, QmvSAr
 }
 
 // Plan and launch one token chunk; returns cudaErrorNotSupported when the
-// streaming kernel cannot take this shape (the caller falls back).
+// streaming kernel cannot take this shape (the caller falls back).  With a
+// query, nothing is launched: the workspace the launch would use is
+// reported instead.
 template <int FMT, int MC>
 static cudaError_t plan_qmv_stream(const DeviceState &ds, cudaStream_t st, const uint8_t *codes,
-                                   const uint8_t *scales, const uint16_t *x, float *y, int m0, int mc, int N, int K)
+                                   const uint8_t *scales, const uint16_t *x, float *y, int m0, int mc, int N, int K,
+                                   QmvScratchNeed *query = nullptr)
 {
     using G = SGeo<FMT, MC>;
     const int U = K / 32;
@@ -500,6 +503,11 @@ static cudaError_t plan_qmv_stream(const DeviceState &ds, cudaStream_t st, const
     const size_t red = (((size_t)a.ntl_max * wk * G::RT * MC * 4) + 15) & ~(size_t)15;
     const size_t smem = (size_t)MC * ks * 2 + 80 + red + rings;
     if (smem > (size_t)ds.max_smem_optin) return cudaErrorNotSupported;
+    if (query) {
+        query->floats = nwin > 1 ? (size_t)nwin * mc * N : 0;
+        query->counters = nwin > 1 ? a.G : 0;
+        return cudaSuccess;
+    }
     return run_qmv_stream<FMT, MC>(ds, st, a, smem);
 }
 
@@ -507,13 +515,14 @@ static int round_mc_s(int m) { return m <= 1 ? 1 : m <= 2 ? 2 : m <= 4 ? 4 : 8; 
 
 template <int FMT>
 static cudaError_t qmv_stream_chunk(const DeviceState &ds, cudaStream_t st, const uint8_t *codes,
-                                    const uint8_t *scales, const uint16_t *x, float *y, int m0, int mc, int N, int K)
+                                    const uint8_t *scales, const uint16_t *x, float *y, int m0, int mc, int N, int K,
+                                    QmvScratchNeed *query = nullptr)
 {
     switch (round_mc_s(mc)) {
-    case 1: return plan_qmv_stream<FMT, 1>(ds, st, codes, scales, x, y, m0, mc, N, K);
-    case 2: return plan_qmv_stream<FMT, 2>(ds, st, codes, scales, x, y, m0, mc, N, K);
-    case 4: return plan_qmv_stream<FMT, 4>(ds, st, codes, scales, x, y, m0, mc, N, K);
-    default: return plan_qmv_stream<FMT, 8>(ds, st, codes, scales, x, y, m0, mc, N, K);
+    case 1: return plan_qmv_stream<FMT, 1>(ds, st, codes, scales, x, y, m0, mc, N, K, query);
+    case 2: return plan_qmv_stream<FMT, 2>(ds, st, codes, scales, x, y, m0, mc, N, K, query);
+    case 4: return plan_qmv_stream<FMT, 4>(ds, st, codes, scales, x, y, m0, mc, N, K, query);
+    default: return plan_qmv_stream<FMT, 8>(ds, st, codes, scales, x, y, m0, mc, N, K, query);
     }
 }
 
@@ -536,6 +545,24 @@ cudaError_t launch_qmv(const DeviceState &ds, cudaStream_t st, int fmt, const ui
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+QmvScratchNeed qmv_scratch_need(const DeviceState &ds, int fmt, int M, int N, int K)
+{
+    QmvScratchNeed need;
+    if (!stream_ok(fmt, K)) return need;  // the direct-load kernels use no workspace
+    for (int m0 = 0; m0 < M; m0 += 8) {
+        const int mc = M - m0 < 8 ? M - m0 : 8;
+        QmvScratchNeed q;
+        cudaError_t e;
+        if (fmt == FMT_MXFP4) e = qmv_stream_chunk<FMT_MXFP4>(ds, nullptr, nullptr, nullptr, nullptr, nullptr, m0, mc, N, K, &q);
+        else if (fmt == FMT_MXFP8) e = qmv_stream_chunk<FMT_MXFP8>(ds, nullptr, nullptr, nullptr, nullptr, nullptr, m0, mc, N, K, &q);
+        else e = qmv_stream_chunk<FMT_NVFP4>(ds, nullptr, nullptr, nullptr, nullptr, nullptr, m0, mc, N, K, &q);
+        if (e != cudaSuccess) continue;  // that chunk falls back to the direct-load kernel
+        if (q.floats > need.floats) need.floats = q.floats;
+        if (q.counters > need.counters) need.counters = q.counters;
+    }
+    return need;
 }
 
 // ------------------------------------------------------------------ MoE

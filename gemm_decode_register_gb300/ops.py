@@ -47,6 +47,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         P, I = ctypes.c_void_p, ctypes.c_int
         sig = {
             "mx_qmv": [I, P, P, P, P, I, I, I],
+            "mx_qmv_noalloc": [I, P, P, P, P, I, I, I],
             "mx_moe_qmv": [I, P, P, P, P, P, I, I, I, I, I],
             "mx_qmm": [I, P, P, P, P, I, I, I],
             "mx_set_stream": [P],
@@ -99,6 +100,17 @@ def qmv(fmt: int, codes: torch.Tensor, scales: torch.Tensor, x: torch.Tensor, N:
         y = torch.empty((M, N), dtype=torch.float32, device=x.device)
     _stream()
     _check("mx_qmv", load().mx_qmv(fmt, _ptr(codes), _ptr(scales), _ptr(x), _ptr(y), M, N, K))
+    return y
+
+
+def qmv_noalloc(fmt: int, codes: torch.Tensor, scales: torch.Tensor, x: torch.Tensor, N: int,
+                y: torch.Tensor | None = None) -> torch.Tensor:
+    """mx_qmv_noalloc: the same product, with no device allocation."""
+    M, K = x.shape
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _stream()
+    _check("mx_qmv_noalloc", load().mx_qmv_noalloc(fmt, _ptr(codes), _ptr(scales), _ptr(x), _ptr(y), M, N, K))
     return y
 
 

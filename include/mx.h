@@ -34,8 +34,10 @@
  *
  * Ownership and execution: every pointer is a caller-owned DEVICE pointer
  * on the current CUDA device.  The library allocates nothing per call; on
- * first use of a device it allocates one 256-byte scratch block that holds
- * the device error word.  Calls are asynchronous on the stream set with
+ * first use of a device it allocates one 16 MiB scratch block that holds the
+ * device error word and the split-K workspace of mx_qmv (the first call on a
+ * device should therefore come before any stream capture; see
+ * mx_qmv_noalloc for a variant that never allocates).  Calls are asynchronous on the stream set with
  * mx_set_stream (per host thread; default: the legacy default stream),
  * re-entrant across host threads, and return as soon as the kernel is
  * queued.
@@ -129,6 +131,25 @@ int mx_swiglu(const float *gu, void *h, int Q, int I);
 /* Router-weighted combine: out[t][n] = sum_j r[t][j] * yd[t*topk + j][n],
  * yd fp32 [T*topk][N], r fp32 [T][topk], out fp32 [T][N]. */
 int mx_moe_combine(const float *yd, const float *r, float *out, int T, int topk, int N);
+
+/* Decode GEMV for callers that cannot allocate device memory.  Same
+ * operation, arguments, layouts and errors as mx_qmv, which on its first call
+ * on a device cudaMalloc's a 16 MiB workspace; some callers cannot allow
+ * that (an engine whose own allocator already owns the whole device pool, or
+ * a latency-critical decode loop that cannot take the device
+ * synchronisation of a first-call allocation).  This variant allocates
+ * nothing: its split-K workspace is a fixed ~1 MiB array inside the library
+ * image (262,144 fp32 partial sums plus 4,096 counters), held by every GPU
+ * that loads the library until the process exits.  Shapes whose workspace
+ * would not fit (many tokens times large N with K split into windows)
+ * return MX_EUNSUPPORTED.  The first call on a device looks up the array's
+ * device address and the device attributes; make that first call before any
+ * stream capture.  Every call shares the one array, so two calls that
+ * overlap on the GPU (for example on two streams) race; each call clears
+ * the counters it uses before launching.  No counterpart on the pages: this
+ * is an interface variant of mx_qmv, not a different computation. */
+int mx_qmv_noalloc(int fmt, const void *codes, const void *scales, const void *x, float *y, int M, int N,
+                   int K);
 
 /* Synchronise the calling thread's stream, then return the device error
  * word of the current device (0 = none; MX_DEVERR_* bits) and clear it.
