@@ -47,6 +47,45 @@ def peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+QMV_SOURCES = ["gemm_decode_register_gb300/csrc/mx_qmv_stream.cu", "gemm_decode_register_gb300/csrc/mx_qmv_core.cuh",
+               "gemm_decode_register_gb300/csrc/mx_common.cuh", "gemm_decode_register_gb300/csrc/mx_internal.h"]
+TRAFFIC_PROFILE = "profiles/qmv_decode_layer_traffic.md"
+
+
+def measured_traffic():
+    """DRAM bytes per qmv launch from the committed ncu summary, or None when
+    the kernel sources changed since that capture."""
+    import hashlib
+
+    try:
+        h = hashlib.sha256()
+        for f in QMV_SOURCES:
+            with open(os.path.join(ROOT, f), "rb") as fh:
+                h.update(fh.read())
+        fields = {}
+        with open(os.path.join(ROOT, TRAFFIC_PROFILE)) as fh:
+            for line in fh:
+                if ":" in line and line.strip().split(":")[0] in ("source_sha256", "traffic_bytes_per_launch"):
+                    k, v = line.strip().split(":", 1)
+                    fields[k.strip()] = v.strip()
+        if fields.get("source_sha256") != h.hexdigest():
+            return None
+        return int(fields["traffic_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+def max_over_ranks(dist, value, device=None):
+    """The largest value across ranks (the job's time is its slowest rank's)."""
+    if dist is None:
+        return value
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -210,11 +249,7 @@ def run_ours(args, rank, world, dist):
     t_end.record(stream)
     torch.cuda.synchronize()
     clk.mark("t1")
-    elapsed = t_start.elapsed_time(t_end) / 1e3
-    if dist:
-        t = torch.tensor([elapsed], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = max_over_ranks(dist, t_start.elapsed_time(t_end) / 1e3, dev)
     launch_s = [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)) / 1e3 / args.steps
                 for j in range(len(layers))]
     value = world * wbytes * args.steps / elapsed / 1e9
@@ -246,9 +281,10 @@ def run_ours(args, rank, world, dist):
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "per_projection_gbs": per_layer},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
-                     "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": None,
-                     "kernel": "qmv_kernel<MXFP4, MC=1>", "peak_source": peak_kind,
-                     "bytes_per_launch": round(alg_bytes / len(layers))},
+                     "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": measured_traffic(),
+                     "kernel": "qmv_stream_kernel<MXFP4, MC=1>", "peak_source": peak_kind,
+                     "bytes_per_launch": round(alg_bytes / len(layers)),
+                     "traffic_source": TRAFFIC_PROFILE},
         "e2e": {"value": round(world * wbytes / e2e_t / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "weights resident (model state); each step copies x in from pinned host "
