@@ -15,6 +15,25 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+// Launch a kernel of this library with programmatic stream serialisation
+// (see pdl_trigger / pdl_wait).
+template <typename... KArgs, typename... Args>
+static inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                   Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 namespace mx {
 
 enum : int { FMT_MXFP4 = 0, FMT_MXFP8 = 1, FMT_NVFP4 = 2 };
@@ -148,6 +167,18 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]),
                    "f"(c[1]), "f"(c[2]), "f"(c[3]));
 }
+
+// ---------------------------------------------------------- launch overlap
+//
+// Programmatic dependent launch: every kernel of this library lets the next
+// kernel on its stream start as soon as it begins (pdl_trigger), and waits
+// for the previous kernel's completion and memory (pdl_wait) before it reads
+// activations, routing or outputs.  Weights (codes, block scales) may be
+// read before the wait: no kernel of this library writes them, and a kernel
+// from elsewhere never triggers early, so it is always complete by then.
+// Both are no-ops when the launch carries no programmatic dependency.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ---------------------------------------------------------- misc
 

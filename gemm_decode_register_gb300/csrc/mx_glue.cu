@@ -15,6 +15,8 @@ template <int FMT>
 __global__ void dequant_kernel(const uint8_t *__restrict__ codes, const uint8_t *__restrict__ scales,
                                float *__restrict__ W, int N, int K)
 {
+    pdl_trigger();
+    pdl_wait();
     const size_t groups = (size_t)N * (K / 8);
     float g = 1.0f;
     if (FMT == FMT_NVFP4) g = load_f32_unaligned(scales + (size_t)N * (K / 16));
@@ -69,10 +71,9 @@ cudaError_t launch_dequant(const DeviceState &ds, cudaStream_t st, int fmt, cons
     const size_t cap = (size_t)ds.num_sms * 8;
     if (blocks > cap) blocks = cap;
     if (blocks == 0) blocks = 1;
-    if (fmt == FMT_MXFP4) dequant_kernel<FMT_MXFP4><<<(unsigned)blocks, 256, 0, st>>>(codes, scales, W, N, K);
-    else if (fmt == FMT_MXFP8) dequant_kernel<FMT_MXFP8><<<(unsigned)blocks, 256, 0, st>>>(codes, scales, W, N, K);
-    else dequant_kernel<FMT_NVFP4><<<(unsigned)blocks, 256, 0, st>>>(codes, scales, W, N, K);
-    return cudaGetLastError();
+    if (fmt == FMT_MXFP4) return launch_k(dequant_kernel<FMT_MXFP4>, dim3((unsigned)blocks), dim3(256), 0, st, codes, scales, W, N, K);
+    if (fmt == FMT_MXFP8) return launch_k(dequant_kernel<FMT_MXFP8>, dim3((unsigned)blocks), dim3(256), 0, st, codes, scales, W, N, K);
+    return launch_k(dequant_kernel<FMT_NVFP4>, dim3((unsigned)blocks), dim3(256), 0, st, codes, scales, W, N, K);
 }
 
 // h = bf16(silu(gate) * up), fp32 arithmetic: silu(v) = v * sigmoid(v), the
@@ -81,6 +82,8 @@ cudaError_t launch_dequant(const DeviceState &ds, cudaStream_t st, int fmt, cons
 // division.
 __global__ void swiglu_kernel(const float *__restrict__ gu, uint16_t *__restrict__ h, int Q, int I)
 {
+    pdl_trigger();
+    pdl_wait();
     const size_t total = (size_t)Q * I;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
          i += (size_t)gridDim.x * blockDim.x) {
@@ -100,14 +103,15 @@ cudaError_t launch_swiglu(const DeviceState &ds, cudaStream_t st, const float *g
     const size_t cap = (size_t)ds.num_sms * 8;
     if (blocks > cap) blocks = cap;
     if (blocks == 0) blocks = 1;
-    swiglu_kernel<<<(unsigned)blocks, 256, 0, st>>>(gu, h, Q, I);
-    return cudaGetLastError();
+    return launch_k(swiglu_kernel, dim3((unsigned)blocks), dim3(256), 0, st, gu, h, Q, I);
 }
 
 // out[t][n] = sum_j r[t][j] * yd[t*topk + j][n] (fp32, increasing j).
 __global__ void combine_kernel(const float *__restrict__ yd, const float *__restrict__ r,
                                float *__restrict__ out, int T, int topk, int N)
 {
+    pdl_trigger();
+    pdl_wait();
     const size_t total = (size_t)T * N;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
          i += (size_t)gridDim.x * blockDim.x) {
@@ -125,8 +129,7 @@ cudaError_t launch_moe_combine(const DeviceState &ds, cudaStream_t st, const flo
     const size_t cap = (size_t)ds.num_sms * 8;
     if (blocks > cap) blocks = cap;
     if (blocks == 0) blocks = 1;
-    combine_kernel<<<(unsigned)blocks, 256, 0, st>>>(yd, r, out, T, topk, N);
-    return cudaGetLastError();
+    return launch_k(combine_kernel, dim3((unsigned)blocks), dim3(256), 0, st, yd, r, out, T, topk, N);
 }
 
 }  // namespace mx

@@ -35,11 +35,24 @@ constexpr int QMM_BM = 256;   // two M=128 halves
 constexpr int QMM_BN = 256;   // UMMA N
 constexpr int QMM_BK = 64;    // bf16 elements per 128-byte swizzle row
 constexpr int QMM_STAGES = 3;
+constexpr int QMM_PF = 4;  // k-blocks of codes each decoder keeps in flight
 constexpr int QMM_THREADS = 320;  // 10 warps
 constexpr int QMM_A_BYTES = 128 * QMM_BK * 2;         // one M=128 half
 constexpr int QMM_B_BYTES = QMM_BN * QMM_BK * 2;
-constexpr int QMM_STAGE_BYTES = 2 * QMM_A_BYTES + QMM_B_BYTES;
-constexpr int QMM_SMEM = QMM_STAGES * QMM_STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int QMM_C_BYTES = QMM_BN * 32;  // packed 4-bit codes of one weight tile per k-block
+
+// Per-format stage layout: [X half 0][X half 1][decoded W (bf16)][packed codes].
+// The 4-bit formats bring their codes in by TMA with the X tiles; MXFP8
+// (twice the code bytes, which would not leave room for three stages) loads
+// them per thread.
+template <int FMT>
+struct QmmGeo {
+    static constexpr bool TMA_CODES = FMT != FMT_MXFP8;
+    static constexpr int C_BYTES = TMA_CODES ? QMM_C_BYTES : 0;
+    static constexpr int STAGE = 2 * QMM_A_BYTES + QMM_B_BYTES + C_BYTES;
+    static constexpr int SMEM = QMM_STAGES * STAGE + 1024 /*align*/ + 256 /*barriers*/;
+    static_assert(STAGE % 1024 == 0, "stages keep 1024-byte alignment");
+};
 constexpr unsigned long long QMM_WAIT_NS = 2000000000ull;
 
 // ------------------------------------------------------------ primitives
@@ -218,13 +231,66 @@ __device__ __forceinline__ uint32_t scaled_bf16x2(uint32_t h2, float s)
     return f32x2_to_bf16x2(__fmul_rn(f16_lo_to_f32(h2), s), __fmul_rn(f16_hi_to_f32(h2), s));
 }
 
+// Exact f16x2 -> bf16x2 of (value * 2^-112) for values decoded from E2M1 or
+// E4M3: those are zero or normal f16 numbers with at most 3 mantissa bits
+// (f16 bits 7-9), so the f16 exponent and mantissa bits, moved 3 places
+// right, are a normal bf16 number 2^-112 times the value (bf16 bias 127 =
+// f16 bias 15 + 112) and zero stays zero; the signs are kept in place.
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2_m112(uint32_t h2)
+{
+    return ((h2 & 0x7F807F80u) >> 3) | (h2 & 0x80008000u);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// bf16x2 holding 2^(e-15) twice, for e in [-111, 142] (normal bf16).
+__device__ __forceinline__ uint32_t bf16x2_pow2_m15(int e)
+{
+    const uint32_t b = (uint32_t)(e + 112) << 7;
+    return b | (b << 16);
+}
+
 // Decode the row's 64 elements to bf16 and store the 128-byte row at
 // `row_base` (row r of a 128-byte-swizzled tile: chunk c at c ^ (r & 7)).
+// Fast path: hardware cvt to f16, exact move to bf16 (scaled by 2^-112),
+// one bf16 multiply by the block scale times 2^112 (exact: the result has at
+// most 6 significant bits and stays in bf16's range).  Scales outside the
+// fast path's range (E8M0 below 2 (10 for MXFP8) or above 142, NaN scales)
+// use exact fp32 products.
 template <int FMT>
 __device__ __forceinline__ void qrow_store(const QRow<FMT> &r, uint8_t *row_base, int row)
 {
     const int sw = row & 7;
     if constexpr (FMT == FMT_MXFP8) {
+        // fast path while every product stays a normal bf16 number
+        const uint32_t e0 = r.s & 0xFFu, e1 = (r.s >> 8) & 0xFFu;
+        if (e0 - 10u <= 132u && e1 - 10u <= 132u) {
+            const uint32_t m0 = bf16x2_pow2_m15((int)e0), m1 = bf16x2_pow2_m15((int)e1);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t m = i < 2 ? m0 : m1;
+                const uint32_t w[4] = {r.c[i].x, r.c[i].y, r.c[i].z, r.c[i].w};
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t h0, h1, h2, h3;
+                    e4m3x4_to_f16x2(w[2 * half], h0, h1);
+                    e4m3x4_to_f16x2(w[2 * half + 1], h2, h3);
+                    uint4 o;
+                    o.x = bf16x2_mul(f16x2_to_bf16x2_m112(h0), m);
+                    o.y = bf16x2_mul(f16x2_to_bf16x2_m112(h1), m);
+                    o.z = bf16x2_mul(f16x2_to_bf16x2_m112(h2), m);
+                    o.w = bf16x2_mul(f16x2_to_bf16x2_m112(h3), m);
+                    const int chunk = 2 * i + half;
+                    *reinterpret_cast<uint4 *>(row_base + ((chunk ^ sw) << 4)) = o;
+                }
+            }
+            return;
+        }
         float s0, s1;
         e8m0x2_to_f32(r.s, s0, s1);
 #pragma unroll
@@ -243,6 +309,49 @@ __device__ __forceinline__ void qrow_store(const QRow<FMT> &r, uint8_t *row_base
             }
         }
     } else {
+        // per 16-element quarter: the bf16x2 multiplier (fast path) or fp32 scale
+        uint32_t mul[4];
+        bool fast;
+        if constexpr (FMT == FMT_NVFP4) {
+            // E4M3 scale s: bf16(s * 2^112) is exact (4 significant bits); NaN codes are 0x7F / 0xFF
+            fast = ((r.s & 0x7F7F7F7Fu) + 0x01010101u & 0x80808080u) == 0u;  // no byte is S.1111.111
+            const uint32_t a = e4m3x2_to_f16x2(r.s), b = e4m3x2_to_f16x2(r.s >> 16);
+            const uint32_t a2 = f16x2_to_bf16x2_m112(a), b2 = f16x2_to_bf16x2_m112(b);
+            // f16x2_to_bf16x2_m112 gives s * 2^-112: square the shift away with 2^224 as two 2^112 factors
+            const uint32_t p112 = bf16x2_pow2_m15(127);  // 2^112
+            const uint32_t as = bf16x2_mul(bf16x2_mul(a2, p112), p112);
+            const uint32_t bs = bf16x2_mul(bf16x2_mul(b2, p112), p112);
+            mul[0] = (as & 0xFFFFu) | (as << 16);
+            mul[1] = (as >> 16) | (as & 0xFFFF0000u);
+            mul[2] = (bs & 0xFFFFu) | (bs << 16);
+            mul[3] = (bs >> 16) | (bs & 0xFFFF0000u);
+        } else {
+            const uint32_t e0 = r.s & 0xFFu, e1 = (r.s >> 8) & 0xFFu;
+            fast = e0 - 2u <= 140u && e1 - 2u <= 140u;  // 2 <= e <= 142: products normal bf16
+            mul[0] = mul[1] = bf16x2_pow2_m15((int)e0);
+            mul[2] = mul[3] = bf16x2_pow2_m15((int)e1);
+        }
+        if (fast) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const uint32_t w[4] = {r.c[i].x, r.c[i].y, r.c[i].z, r.c[i].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    // word j of 16-byte half i: elements 32i + 8j .. +7 (16-element block 2i + j/2)
+                    const uint32_t m = mul[2 * i + (j >> 1)];
+                    uint32_t h0, h1, h2, h3;
+                    e2m1x8_to_f16x2(w[j], h0, h1, h2, h3);
+                    uint4 o;
+                    o.x = bf16x2_mul(f16x2_to_bf16x2_m112(h0), m);
+                    o.y = bf16x2_mul(f16x2_to_bf16x2_m112(h1), m);
+                    o.z = bf16x2_mul(f16x2_to_bf16x2_m112(h2), m);
+                    o.w = bf16x2_mul(f16x2_to_bf16x2_m112(h3), m);
+                    const int chunk = 4 * i + j;
+                    *reinterpret_cast<uint4 *>(row_base + ((chunk ^ sw) << 4)) = o;
+                }
+            }
+            return;
+        }
         float sc[4];
         if constexpr (FMT == FMT_NVFP4) {
             const uint32_t a = e4m3x2_to_f16x2(r.s), b = e4m3x2_to_f16x2(r.s >> 16);
@@ -260,7 +369,6 @@ __device__ __forceinline__ void qrow_store(const QRow<FMT> &r, uint8_t *row_base
             const uint32_t w[4] = {r.c[i].x, r.c[i].y, r.c[i].z, r.c[i].w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                // word j of 16-byte half i: elements 32i + 8j .. +7 (16-element block 2i + j/2)
                 const float s = sc[2 * i + (j >> 1)];
                 uint4 o;
                 o.x = scaled_bf16x2(e2m1x2_to_f16x2(w[j]), s);
@@ -286,8 +394,11 @@ struct QmmArgs {
 };
 
 template <int FMT>
-__global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_constant__ CUtensorMap tmap_x, QmmArgs a)
+__global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                                                             const __grid_constant__ CUtensorMap tmap_c, QmmArgs a)
 {
+    using QG = QmmGeo<FMT>;
+    constexpr int QMM_STAGE_BYTES = QG::STAGE;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + QMM_STAGES * QMM_STAGE_BYTES);
@@ -323,6 +434,8 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_trigger();
+    pdl_wait();  // X and Y may be used by the neighbouring kernels
 
     int issued_a = 0;  // producer: stages whose TMA was issued
     if (warp == 0) {
@@ -333,9 +446,11 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_consta
                 if (kb >= QMM_STAGES && !mbar_wait(&empty[s], ((kb / QMM_STAGES) - 1) & 1, abort_flag, a.wait_ns))
                     break;
                 uint8_t *st = smem + s * QMM_STAGE_BYTES;
-                mbar_arrive_expect_tx(&full_a[s], 2 * QMM_A_BYTES);
+                mbar_arrive_expect_tx(&full_a[s], 2 * QMM_A_BYTES + QG::C_BYTES);
                 tma_load_2d(st, &tmap_x, kb * QMM_BK, m0, &full_a[s]);
                 tma_load_2d(st + QMM_A_BYTES, &tmap_x, kb * QMM_BK, m0 + 128, &full_a[s]);
+                if constexpr (QG::TMA_CODES)  // 256 weight rows x 32 code bytes
+                    tma_load_2d(st + 2 * QMM_A_BYTES + QMM_B_BYTES, &tmap_c, kb * 32, n0, &full_a[s]);
                 issued_a = kb + 1;
             }
             // drain: every issued TMA must land before the CTA may exit
@@ -377,23 +492,62 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_consta
         const size_t sb = FMT == FMT_NVFP4 ? (size_t)(a.K / 16) : (size_t)(a.K / 32);
         const uint8_t *crow = a.codes + (size_t)n * rb;
         const uint8_t *srow = a.scales + (size_t)n * sb;
-        QRow<FMT> r0, r1;
-        qrow_load<FMT>(crow, srow, 0, r0);
-        if (KB > 1) qrow_load<FMT>(crow, srow, 1, r1);
-        for (int kb = 0; kb < KB; ++kb) {
-            const int s = kb % QMM_STAGES;
-            QRow<FMT> r2;
-            if (kb + 2 < KB) qrow_load<FMT>(crow, srow, kb + 2, r2);
-            if (kb >= QMM_STAGES && !mbar_wait(&empty[s], ((kb / QMM_STAGES) - 1) & 1, abort_flag, a.wait_ns))
-                break;
-            uint8_t *b_tile = smem + s * QMM_STAGE_BYTES + 2 * QMM_A_BYTES;
-            qrow_store<FMT>(r0, b_tile + d * 128, d);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&full_b[s]);
-            r0 = r1;
-            r1 = r2;
+        if constexpr (QG::TMA_CODES) {
+            // codes arrive by TMA with the stage; the scale bytes of the next
+            // QMM_PF k-blocks stay in flight in registers
+            constexpr int SPK = FMT == FMT_NVFP4 ? 4 : 2;  // scale bytes per k-block
+            uint32_t sv[QMM_PF];
+#pragma unroll
+            for (int j = 0; j < QMM_PF; ++j)
+                if (j < KB) sv[j] = SPK == 4 ? ld_nc_u32(srow + 4 * j) : ld_nc_u16(srow + 2 * j);
+            for (int kb0 = 0; kb0 < KB; kb0 += QMM_PF) {
+#pragma unroll
+                for (int j = 0; j < QMM_PF; ++j) {
+                    const int kb = kb0 + j;
+                    if (kb >= KB) break;
+                    const int s = kb % QMM_STAGES;
+                    // the stage's TMA was issued after the MMAs released it, so its
+                    // arrival also means the decoded-tile slot is free
+                    if (!mbar_wait(&full_a[s], (kb / QMM_STAGES) & 1, abort_flag, a.wait_ns)) goto decode_done;
+                    uint8_t *stage = smem + s * QMM_STAGE_BYTES;
+                    const uint4 *cp = reinterpret_cast<const uint4 *>(stage + 2 * QMM_A_BYTES + QMM_B_BYTES + d * 32);
+                    QRow<FMT> rr;
+                    rr.c[0] = cp[0];
+                    rr.c[1] = cp[1];
+                    rr.s = sv[j];
+                    if (kb + QMM_PF < KB)
+                        sv[j] = SPK == 4 ? ld_nc_u32(srow + 4 * (kb + QMM_PF)) : ld_nc_u16(srow + 2 * (kb + QMM_PF));
+                    qrow_store<FMT>(rr, stage + 2 * QMM_A_BYTES + d * 128, d);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&full_b[s]);
+                }
+            }
+        } else {
+            // codes and scales of the next QMM_PF k-blocks stay in flight in registers
+            QRow<FMT> r[QMM_PF];
+#pragma unroll
+            for (int j = 0; j < QMM_PF; ++j)
+                if (j < KB) qrow_load<FMT>(crow, srow, j, r[j]);
+            for (int kb0 = 0; kb0 < KB; kb0 += QMM_PF) {
+#pragma unroll
+                for (int j = 0; j < QMM_PF; ++j) {
+                    const int kb = kb0 + j;
+                    if (kb >= KB) break;
+                    const int s = kb % QMM_STAGES;
+                    if (kb >= QMM_STAGES &&
+                        !mbar_wait(&empty[s], ((kb / QMM_STAGES) - 1) & 1, abort_flag, a.wait_ns))
+                        goto decode_done;
+                    uint8_t *b_tile = smem + s * QMM_STAGE_BYTES + 2 * QMM_A_BYTES;
+                    qrow_store<FMT>(r[j], b_tile + d * 128, d);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&full_b[s]);
+                    if (kb + QMM_PF < KB) qrow_load<FMT>(crow, srow, kb + QMM_PF, r[j]);
+                }
+            }
         }
+    decode_done:;
     }
 
     // ---------------- epilogue (decoder warps): TMEM -> bf16 -> Y
@@ -464,24 +618,25 @@ static EncodeTiledFn encode_fn()
 }
 
 template <int FMT>
-static cudaError_t run_qmm(const DeviceState &ds, cudaStream_t st, const CUtensorMap &map, const QmmArgs &a)
+static cudaError_t run_qmm(const DeviceState &ds, cudaStream_t st, const CUtensorMap &map, const CUtensorMap &cmap,
+                           const QmmArgs &a)
 {
+    using QG = QmmGeo<FMT>;
+    if (QG::SMEM > ds.max_smem_optin) return cudaErrorInvalidValue;
     static int configured_dev[64] = {0};
     if (ds.device < 64 && !configured_dev[ds.device]) {
-        cudaError_t e = cudaFuncSetAttribute(qmm_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, QMM_SMEM);
+        cudaError_t e = cudaFuncSetAttribute(qmm_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, QG::SMEM);
         if (e != cudaSuccess) return e;
         configured_dev[ds.device] = 1;
     }
     const int grid = ((a.M + QMM_BM - 1) / QMM_BM) * (a.N / QMM_BN);
-    qmm_kernel<FMT><<<grid, QMM_THREADS, QMM_SMEM, st>>>(map, a);
-    return cudaGetLastError();
+    return launch_k(qmm_kernel<FMT>, dim3(grid), dim3(QMM_THREADS), (size_t)QG::SMEM, st, map, cmap, a);
 }
 
 cudaError_t launch_qmm(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,
                        const uint8_t *scales, const uint16_t *X, uint16_t *Y, int M, int N, int K)
 {
     if (N % QMM_BN != 0 || K % QMM_BK != 0) return cudaErrorInvalidValue;
-    if (QMM_SMEM > ds.max_smem_optin) return cudaErrorInvalidValue;
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     CUtensorMap map;
@@ -493,6 +648,19 @@ cudaError_t launch_qmm(const DeviceState &ds, cudaStream_t st, int fmt, const ui
                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    // packed codes of the 4-bit formats: [N][K/2] bytes, box of 32 bytes x 256 rows
+    CUtensorMap cmap;
+    if (fmt != FMT_MXFP8) {
+        const cuuint64_t cdims[2] = {(cuuint64_t)K / 2, (cuuint64_t)N};
+        const cuuint64_t cstrides[1] = {(cuuint64_t)K / 2};
+        const cuuint32_t cbox[2] = {32u, (cuuint32_t)QMM_BN};
+        r = enc(&cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(codes), cdims, cstrides, cbox, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    } else {
+        cmap = map;  // unused
+    }
     QmmArgs a;
     a.codes = codes;
     a.scales = scales;
@@ -502,9 +670,9 @@ cudaError_t launch_qmm(const DeviceState &ds, cudaStream_t st, int fmt, const ui
     a.N = N;
     a.K = K;
     a.wait_ns = QMM_WAIT_NS;
-    if (fmt == FMT_MXFP4) return run_qmm<FMT_MXFP4>(ds, st, map, a);
-    if (fmt == FMT_MXFP8) return run_qmm<FMT_MXFP8>(ds, st, map, a);
-    return run_qmm<FMT_NVFP4>(ds, st, map, a);
+    if (fmt == FMT_MXFP4) return run_qmm<FMT_MXFP4>(ds, st, map, cmap, a);
+    if (fmt == FMT_MXFP8) return run_qmm<FMT_MXFP8>(ds, st, map, cmap, a);
+    return run_qmm<FMT_NVFP4>(ds, st, map, cmap, a);
 }
 
 }  // namespace mx

@@ -34,6 +34,8 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) qmv_kernel(QmvArgs a)
     int *sh = reinterpret_cast<int *>(red + QMV_WARPS * 2 * MC * MC);     // [MC]
     unsigned *maxbits = reinterpret_cast<unsigned *>(sh + 8);              // [MC]
 
+    pdl_trigger();
+    pdl_wait();
     stage_x<FMT>(a.x + (size_t)a.m0 * a.K, (size_t)a.K, a.K, a.mc, nullptr, xs, a.ks, sh, maxbits);
     __syncthreads();
 
@@ -97,8 +99,7 @@ static cudaError_t run_qmv(const DeviceState &ds, cudaStream_t st, const QmvArgs
     const int WR = QMV_WARPS / a.wk;
     int rounds = (a.tiles + WR - 1) / WR;
     int grid = rounds < ds.num_sms ? rounds : ds.num_sms;
-    qmv_kernel<FMT, MC><<<grid, QMV_THREADS, smem, st>>>(a);
-    return cudaGetLastError();
+    return launch_k(qmv_kernel<FMT, MC>, dim3(grid), dim3(QMV_THREADS), smem, st, a);
 }
 
 template <int FMT>
@@ -225,6 +226,8 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) moe_qmv_kernel(MoeArgs a)
     uint16_t *xs = reinterpret_cast<uint16_t *>(
         smem + ((((size_t)(3 * a.E + 5 * P + 41 + 2 * a.T) * 4) + 15) & ~(size_t)15));
 
+    pdl_trigger();
+    pdl_wait();
     RouteSmem rs{cnt, wgs, pos, sorted, wg_e, wg_first, wg_mc, tmp};
     const int nwg = moe_route(a.ids, P, a.E, 8, rs);
     __syncthreads();
@@ -288,8 +291,7 @@ static cudaError_t run_moe(const DeviceState &ds, cudaStream_t st, const MoeArgs
         if (e != cudaSuccess) return e;
         configured_dev[ds.device] = 1;
     }
-    moe_qmv_kernel<FMT><<<ds.num_sms, QMV_THREADS, smem, st>>>(a);
-    return cudaGetLastError();
+    return launch_k(moe_qmv_kernel<FMT>, dim3(ds.num_sms), dim3(QMV_THREADS), smem, st, a);
 }
 
 cudaError_t launch_moe_qmv_direct(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,

@@ -376,9 +376,11 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) qmv_stream_kernel(QmvSArgs a)
                 if (tile_out<MC>(h, c, r, t)) red[((size_t)v * G::RT + r) * MC + t] = vv[h][c];
             }
     };
+    pdl_trigger();
     uint8_t *ring = rings + (size_t)warp * G::STAGES * G::STAGE_BYTES;
     Streamer<FMT, MC, decltype(next)> st(next, n_my, ring, a.N, RB, KS);
-    st.prime();  // weight copies overlap the activation staging below
+    st.prime();  // weight copies overlap the previous kernel's tail and the staging below
+    pdl_wait();
     stage_x<FMT>(a.x + (size_t)a.m0 * a.K + (size_t)xu0 * 32, (size_t)a.K, len, a.mc, nullptr, xs, a.ks, sh,
                  maxbits);
     __syncthreads();
@@ -434,8 +436,7 @@ static cudaError_t run_qmv_stream(const DeviceState &ds, cudaStream_t st, QmvSAr
         if (e != cudaSuccess) return e;
         configured_dev[ds.device] = 1;
     }
-    qmv_stream_kernel<FMT, MC><<<a.G * a.nwin, QMV_THREADS, smem, st>>>(a);
-    return cudaGetLastError();
+    return launch_k(qmv_stream_kernel<FMT, MC>, dim3(a.G * a.nwin), dim3(QMV_THREADS), smem, st, a);
 }
 
 // Plan and launch one token chunk; returns cudaErrorNotSupported when the
@@ -599,6 +600,8 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) moe_stream_kernel(MoeSArgs a)
     off += (size_t)a.T * a.ks * 2;
     uint8_t *rings = smem + off;
 
+    pdl_trigger();
+    pdl_wait();  // routing and activations may come from the previous kernel
     RouteSmem rs{cnt, wgs, pos, sorted, wg_e, wg_first, wg_mc, tmp};
     const int nwg = moe_route(a.ids, P, a.E, MC, rs);
     for (int p = blockIdx.x; p < P; p += gridDim.x) {
@@ -682,8 +685,7 @@ static cudaError_t run_moe_stream(const DeviceState &ds, cudaStream_t st, const 
         if (e != cudaSuccess) return e;
         configured_dev[ds.device] = 1;
     }
-    moe_stream_kernel<FMT, MC><<<ds.num_sms, QMV_THREADS, smem, st>>>(a);
-    return cudaGetLastError();
+    return launch_k(moe_stream_kernel<FMT, MC>, dim3(ds.num_sms), dim3(QMV_THREADS), smem, st, a);
 }
 
 template <int FMT>
