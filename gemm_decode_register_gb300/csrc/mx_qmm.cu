@@ -1,29 +1,43 @@
 // mx_qmm.cu -- prefill GEMM over block-float weights on the 5th-generation
-// tensor cores (tcgen05), sm_103a.
+// tensor cores (tcgen05, CTA pairs), sm_103a.
 //
 //   Y[m][n] = bf16_rne( sum_k X[m][k] * W[n][k] ),  X bf16, fp32 accumulate.
 //
 // The pages move block-float dequantisation onto the GPU and feed the
 // matrix units from it ("MLxcel 0.8 release", section "Decoding block-float
 // formats in software": NVFP4 prefill 3.1x from GPU dequant + WMMA; talk
-// slide 12).  Here each CTA owns a 256 x 256 output tile and streams K in
-// 64-wide k-blocks through a 3-stage shared-memory ring:
+// slide 12).  Here a cluster of two CTAs (a CTA pair on neighbouring SMs)
+// owns a (256 * NACC) x 256 output tile and runs tcgen05.mma.cta_group::2
+// with M = 256, N = 256, K = 16: CTA r holds rows 128r .. 128r+127 of each
+// 256-row slab of X (its half of operand A) and weight rows
+// n0 + 128r .. +127 decoded to bf16 (its half of operand B); the pair's MMA
+// reads both CTAs' shared memory and CTA r's tensor memory receives its 128
+// rows of the accumulator.  Against one CTA running 128 x 256 MMAs this
+// halves each SM's decode work and shared-memory operand reads per flop.
+// Per CTA, K streams in 64-wide k-blocks through two rings of shared memory
+// (X slabs; decoded weights with their codes and scales):
 //
-//   warp 0      TMA: two 128 x 64 bf16 tiles of X per stage (128-byte swizzle)
-//   warp 1      one elected thread issues tcgen05.mma.kind::f16 (bf16 x bf16
-//               -> fp32): per k-block 4 K=16 steps for each of the two M=128
-//               halves, both sharing the decoded weight tile; the fp32
-//               accumulators live in tensor memory (2 x 256 columns)
-//   warps 2-9   decoders: thread d loads the packed codes and block scales of
-//               weight row n0+d for the k-block, decodes them exactly to bf16
-//               (code * scale has at most 6 significant bits) and stores the
-//               128-byte row in the same 128-byte-swizzled K-major layout TMA
-//               produces; then the epilogue: tcgen05.ld of the accumulator,
-//               NVFP4 tensor scale, round to bf16, store.
+//   warp 10     X: NACC 128 x 64 bf16 slabs per k-block by TMA (128-byte
+//               swizzle); both CTAs' slabs complete on CTA 0's barrier
+//   warp 0      W: the packed codes of the CTA's 128 weight rows by TMA, and
+//               their block scales through registers into shared memory
+//   warp 1      CTA 0: one thread issues the pair's MMAs (NACC accumulators
+//               of 256 columns sharing the decoded weights) and commits each
+//               k-block to the empty barriers of both CTAs;
+//               CTA 1: one thread relays the completion of CTA 1's decoded
+//               tiles to CTA 0 (one cluster-scope fence per batch)
+//   warps 2-9   decoders: two threads per weight row, 32 elements each; they
+//               wait for the codes, decode them exactly to bf16 (code * scale
+//               has at most 6 significant bits), store them in the
+//               128-byte-swizzled K-major layout TMA produces and arrive on
+//               their CTA's barrier; then the epilogue: tcgen05.ld of the
+//               CTA's accumulator rows, NVFP4 tensor scale, round to bf16,
+//               store.
 //
 // Every mbarrier wait is bounded (about two seconds of %globaltimer); a wait
 // that gives up sets MX_DEVERR_TIMEOUT in the device error word, the CTA
-// drains what it has in flight, writes NaN to its Y tile and returns.
+// drains what it has in flight, both CTAs of the pair write NaN to their Y
+// rows and return.
 #include <cuda.h>
 
 #include "mx_common.cuh"
@@ -31,29 +45,46 @@
 
 namespace mx {
 
-constexpr int QMM_BM = 256;   // two M=128 halves
-constexpr int QMM_BN = 256;   // UMMA N
-constexpr int QMM_BK = 64;    // bf16 elements per 128-byte swizzle row
-constexpr int QMM_STAGES = 3;
-constexpr int QMM_PF = 4;  // k-blocks of codes each decoder keeps in flight
-constexpr int QMM_THREADS = 320;  // 10 warps
-constexpr int QMM_A_BYTES = 128 * QMM_BK * 2;         // one M=128 half
-constexpr int QMM_B_BYTES = QMM_BN * QMM_BK * 2;
-constexpr int QMM_C_BYTES = QMM_BN * 32;  // packed 4-bit codes of one weight tile per k-block
-
-// Per-format stage layout: [X half 0][X half 1][decoded W (bf16)][packed codes].
-// The 4-bit formats bring their codes in by TMA with the X tiles; MXFP8
-// (twice the code bytes, which would not leave room for three stages) loads
-// them per thread.
-template <int FMT>
-struct QmmGeo {
-    static constexpr bool TMA_CODES = FMT != FMT_MXFP8;
-    static constexpr int C_BYTES = TMA_CODES ? QMM_C_BYTES : 0;
-    static constexpr int STAGE = 2 * QMM_A_BYTES + QMM_B_BYTES + C_BYTES;
-    static constexpr int SMEM = QMM_STAGES * STAGE + 1024 /*align*/ + 256 /*barriers*/;
-    static_assert(STAGE % 1024 == 0, "stages keep 1024-byte alignment");
-};
+constexpr int QMM_BN = 256;                    // UMMA N: 128 weight rows from each CTA
+constexpr int QMM_BK = 64;                     // bf16 elements per 128-byte swizzle row
+constexpr int QMM_THREADS = 352;               // 11 warps
+constexpr int QMM_SPF = 4;                     // k-blocks of block scales the producer keeps in flight
+constexpr int QMM_X_BYTES = 128 * QMM_BK * 2;  // a CTA's 128 rows of one 256-row X slab
+constexpr int QMM_W_BYTES = 128 * QMM_BK * 2;  // a CTA's 128 decoded weight rows
+constexpr int QMM_SMEM_LIMIT = 232448;         // 227 KB of dynamic shared memory per CTA
 constexpr unsigned long long QMM_WAIT_NS = 2000000000ull;
+
+// Per-format, per-tile-height geometry.  Two rings of k-blocks:
+//   X ring (SX slots): NACC slabs of 128 x 64 bf16 X rows, by TMA;
+//   W ring (SW slots): the decoded 128 x 64 bf16 weight tile, the packed
+//     codes it is decoded from (TMA) and the block scales.
+// The W ring is deeper: a W slot is held from its codes' TMA through the
+// decode and the hand-over to CTA 0 until the MMA finishes, an X slot only
+// from its TMA until the MMA finishes.
+template <int FMT, int NACC>
+struct QmmGeo {
+    static constexpr int BM = 256 * NACC;  // output rows per pair tile
+    static constexpr int CODE_ROW = FMT == FMT_MXFP8 ? QMM_BK : QMM_BK / 2;  // code bytes per row per k-block
+    static constexpr int C_BYTES = 128 * CODE_ROW;
+    static constexpr int SPK = FMT == FMT_NVFP4 ? 4 : 2;  // scale bytes per row per k-block
+    static constexpr int SC_BYTES = 128 * SPK;
+    static constexpr int X_STAGE = NACC * QMM_X_BYTES;
+    static constexpr int SX = NACC == 2 ? 3 : 4;
+    static constexpr int RESERVED = 1024 /*align*/ + 512 /*barriers*/;
+    static constexpr int W_FIT = (QMM_SMEM_LIMIT - RESERVED - SX * X_STAGE) / (QMM_W_BYTES + C_BYTES + SC_BYTES);
+    static constexpr int SW = W_FIT > 8 ? 8 : W_FIT;
+    // layout: [X ring][decoded W ring][codes ring][scales ring][barriers]
+    static constexpr int OFF_W = SX * X_STAGE;
+    static constexpr int OFF_C = OFF_W + SW * QMM_W_BYTES;
+    static constexpr int OFF_S = OFF_C + SW * C_BYTES;
+    static constexpr int OFF_BAR = OFF_S + SW * SC_BYTES;
+    static constexpr int SMEM = OFF_BAR + RESERVED;
+    static constexpr int TMEM_COLS = 256 * NACC;
+    static_assert(OFF_C % 1024 == 0 && OFF_S % 16 == 0 && OFF_BAR % 8 == 0, "ring alignment");
+    static_assert(SW >= 4, "W ring too shallow");
+    static_assert((2 * SX + 4 * SW + 1) * 8 + 16 <= 512, "barrier area");
+    static_assert(SMEM <= QMM_SMEM_LIMIT, "shared memory");
+};
 
 // ------------------------------------------------------------ primitives
 
@@ -69,10 +100,55 @@ __device__ __forceinline__ unsigned long long globaltimer()
     return t;
 }
 
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_id_x()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+
+// Every thread of both CTAs: release what it wrote, acquire the peer's.
+__device__ __forceinline__ void cluster_sync_all()
+{
+    __syncwarp();
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// Address of the same shared-memory variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_cta(uint32_t saddr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ int ld_cluster_s32(uint32_t caddr)
+{
+    int v;
+    asm volatile("ld.shared::cluster.b32 %0, [%1];" : "=r"(v) : "r"(caddr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
 {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
+
+// Relaxed arrive on a barrier given by its cluster address (own or peer
+// CTA); after fence_acq_rel_cluster it is a release at cluster scope.
+__device__ __forceinline__ void mbar_arrive_relaxed_cluster(uint32_t caddr)
+{
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+}
+
+__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
 {
@@ -85,11 +161,13 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
+// Cluster-scope acquire: phases may be completed by the peer CTA's threads
+// or by the pair's MMA commits.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
                  "selp.u32 %0, 1, 0, p;\n\t}"
                  : "=r"(ok)
                  : "r"(smem_u32(bar)), "r"(parity)
@@ -100,15 +178,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 // Bounded wait on a phase; false when it timed out or (with
 // respect_abort) when another role of the CTA has given up.  Drains of work
 // already in flight pass respect_abort = false so they still wait for it.
-__device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                       unsigned long long limit_ns, bool respect_abort = true)
+// The clock is read only once a wait has gone on for a while: a phase that
+// is already complete costs one try_wait.
+__device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                            unsigned long long limit_ns, bool respect_abort)
 {
-    const unsigned long long t0 = globaltimer();
-    for (uint32_t i = 0;; ++i) {
+    unsigned long long t0 = 0;
+    for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 63u) {
+        if ((i & 63u) == 0u) {
             if (respect_abort && *abort_flag) return false;
-            if (globaltimer() - t0 > limit_ns) {
+            const unsigned long long t = globaltimer();
+            if (t0 == 0) {
+                t0 = t;
+            } else if (t - t0 > limit_ns) {
                 *abort_flag = 1;
                 return false;
             }
@@ -116,11 +199,20 @@ __device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile 
     }
 }
 
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                          unsigned long long limit_ns, bool respect_abort = true)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, abort_flag, limit_ns, respect_abort);
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// 2-D tiled TMA load into this CTA's shared memory, completing on this CTA's
+// barrier.
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar)
 {
     asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
@@ -129,11 +221,33 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
                  : "memory");
 }
 
+// 2-D tiled TMA load into this CTA's shared memory that completes on a
+// barrier of either CTA of the pair (`bar_cluster`: a cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *map, int c0, int c1,
+                                                 uint32_t bar_cluster)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 "
+                 "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster)
+                 : "memory");
+}
+
+// Arrive on a barrier of either CTA (cluster address) and announce `bytes`
+// of TMA data that will complete on it.  Relaxed: the data itself arrives
+// by TMA, whose completion the barrier tracks.
+__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t caddr, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(caddr),
+                 "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
-// 1024 bytes apart (rows of 128 bytes), sm_100 descriptor version.
+// 1024 bytes apart (rows of 128 bytes), sm_100 descriptor version.  For the
+// pair MMA the same address names the tile in both CTAs.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
 {
     uint64_t d = 0;
@@ -146,30 +260,33 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
 }
 
 // Instruction descriptor, kind::f16: bf16 A and B (K-major), fp32 D,
-// M = 128, N = 256.
+// M = 256 (the pair), N = 256.
 __host__ __device__ constexpr uint32_t qmm_idesc()
 {
-    return (1u << 4)               // D format fp32
-           | (1u << 7)             // A format bf16
-           | (1u << 10)            // B format bf16
+    return (1u << 4)                // D format fp32
+           | (1u << 7)              // A format bf16
+           | (1u << 10)             // B format bf16
            | ((QMM_BN >> 3) << 17)  // N / 8
-           | ((128 >> 4) << 24);    // M / 16
+           | ((256 >> 4) << 24);    // M / 16
 }
 
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                          uint32_t accumulate)
+__device__ __forceinline__ void umma2_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate)
 {
     asm volatile("{\n\t.reg .pred p;\n\t"
                  "setp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
                  "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
                  : "memory");
 }
 
-__device__ __forceinline__ void umma_commit(uint64_t *bar)
+// Arrive (once) on the barrier at this address in both CTAs of the pair when
+// every MMA issued so far has completed.
+__device__ __forceinline__ void umma2_commit_both(uint64_t *bar)
 {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     smem_u32(bar))
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+                 "[%0], %1;" ::"r"(smem_u32(bar)),
+                 "h"((unsigned short)3)
                  : "memory");
 }
 
@@ -189,42 +306,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
 }
 
 // ------------------------------------------------------------ decode
-
-// Codes + scales of one weight row for one 64-wide k-block.
-template <int FMT>
-struct QRow;
-template <>
-struct QRow<FMT_MXFP4> {
-    uint4 c[2];
-    uint32_t s;  // 2 E8M0 bytes
-};
-template <>
-struct QRow<FMT_NVFP4> {
-    uint4 c[2];
-    uint32_t s;  // 4 E4M3 bytes
-};
-template <>
-struct QRow<FMT_MXFP8> {
-    uint4 c[4];
-    uint32_t s;  // 2 E8M0 bytes
-};
-
-template <int FMT>
-__device__ __forceinline__ void qrow_load(const uint8_t *crow, const uint8_t *srow, int kb, QRow<FMT> &r)
-{
-    if constexpr (FMT == FMT_MXFP8) {
-        const uint4 *p = reinterpret_cast<const uint4 *>(crow + (size_t)kb * 64);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) r.c[i] = __ldg(p + i);
-        r.s = ld_nc_u16(srow + 2 * kb);
-    } else {
-        const uint4 *p = reinterpret_cast<const uint4 *>(crow + (size_t)kb * 32);
-        r.c[0] = __ldg(p);
-        r.c[1] = __ldg(p + 1);
-        if constexpr (FMT == FMT_NVFP4) r.s = ld_nc_u32(srow + 4 * kb);
-        else r.s = ld_nc_u16(srow + 2 * kb);
-    }
-}
 
 __device__ __forceinline__ uint32_t scaled_bf16x2(uint32_t h2, float s)
 {
@@ -255,137 +336,108 @@ __device__ __forceinline__ uint32_t bf16x2_pow2_m15(int e)
     return b | (b << 16);
 }
 
-// Decode the row's 64 elements to bf16 and store the 128-byte row at
-// `row_base` (row r of a 128-byte-swizzled tile: chunk c at c ^ (r & 7)).
-// Fast path: hardware cvt to f16, exact move to bf16 (scaled by 2^-112),
-// one bf16 multiply by the block scale times 2^112 (exact: the result has at
-// most 6 significant bits and stays in bf16's range).  Scales outside the
-// fast path's range (E8M0 below 2 (10 for MXFP8) or above 142, NaN scales)
-// use exact fp32 products.
-template <int FMT>
-__device__ __forceinline__ void qrow_store(const QRow<FMT> &r, uint8_t *row_base, int row)
+__device__ __forceinline__ void store_chunk(uint8_t *row_base, int chunk, int sw, uint32_t x, uint32_t y,
+                                            uint32_t z, uint32_t w)
 {
-    const int sw = row & 7;
+    *reinterpret_cast<uint4 *>(row_base + ((chunk ^ sw) << 4)) = make_uint4(x, y, z, w);
+}
+
+// Decode 32 elements of one weight row (half `half` of a 64-wide k-block)
+// to bf16 and store them as chunks 4*half .. 4*half+3 of the row's 128 bytes
+// at `row_base` (row r of a 128-byte-swizzled tile: chunk c at c ^ (r & 7)).
+// w[]: the packed codes (4 words for E2M1, 8 for E4M3); sbits: the block
+// scale byte (MX) or the two E4M3 scale bytes (NVFP4).
+// Fast path: hardware cvt to f16, exact move to bf16 (scaled by 2^-112), one
+// bf16 multiply by the block scale times 2^112 (exact: the result has at most
+// 6 significant bits and stays a normal bf16 number).  Scales outside its
+// range (E8M0 below 2 (10 for MXFP8) or above 142, NaN scales) use exact fp32
+// products.
+template <int FMT>
+__device__ __forceinline__ void qhalf_store(const uint32_t *w, uint32_t sbits, uint8_t *row_base, int half, int sw)
+{
     if constexpr (FMT == FMT_MXFP8) {
-        // fast path while every product stays a normal bf16 number
-        const uint32_t e0 = r.s & 0xFFu, e1 = (r.s >> 8) & 0xFFu;
-        if (e0 - 10u <= 132u && e1 - 10u <= 132u) {
-            const uint32_t m0 = bf16x2_pow2_m15((int)e0), m1 = bf16x2_pow2_m15((int)e1);
+        const uint32_t e = sbits & 0xFFu;
+        if (e - 10u <= 132u) {
+            const uint32_t m = bf16x2_pow2_m15((int)e);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t m = i < 2 ? m0 : m1;
-                const uint32_t w[4] = {r.c[i].x, r.c[i].y, r.c[i].z, r.c[i].w};
+            for (int c = 0; c < 4; ++c) {
+                uint32_t h0, h1, h2, h3;
+                e4m3x4_to_f16x2(w[2 * c], h0, h1);
+                e4m3x4_to_f16x2(w[2 * c + 1], h2, h3);
+                store_chunk(row_base, 4 * half + c, sw, bf16x2_mul(f16x2_to_bf16x2_m112(h0), m),
+                            bf16x2_mul(f16x2_to_bf16x2_m112(h1), m), bf16x2_mul(f16x2_to_bf16x2_m112(h2), m),
+                            bf16x2_mul(f16x2_to_bf16x2_m112(h3), m));
+            }
+            return;
+        }
+        const float s = e8m0_to_f32(e);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t h0, h1, h2, h3;
-                    e4m3x4_to_f16x2(w[2 * half], h0, h1);
-                    e4m3x4_to_f16x2(w[2 * half + 1], h2, h3);
-                    uint4 o;
-                    o.x = bf16x2_mul(f16x2_to_bf16x2_m112(h0), m);
-                    o.y = bf16x2_mul(f16x2_to_bf16x2_m112(h1), m);
-                    o.z = bf16x2_mul(f16x2_to_bf16x2_m112(h2), m);
-                    o.w = bf16x2_mul(f16x2_to_bf16x2_m112(h3), m);
-                    const int chunk = 2 * i + half;
-                    *reinterpret_cast<uint4 *>(row_base + ((chunk ^ sw) << 4)) = o;
-                }
+        for (int c = 0; c < 4; ++c)
+            store_chunk(row_base, 4 * half + c, sw, scaled_bf16x2(e4m3x2_to_f16x2(w[2 * c]), s),
+                        scaled_bf16x2(e4m3x2_to_f16x2(w[2 * c] >> 16), s),
+                        scaled_bf16x2(e4m3x2_to_f16x2(w[2 * c + 1]), s),
+                        scaled_bf16x2(e4m3x2_to_f16x2(w[2 * c + 1] >> 16), s));
+    } else {
+        // multiplier of words 0-1 (m0) and 2-3 (m1): one 32-element E8M0
+        // block, or two 16-element E4M3 blocks
+        uint32_t m0, m1;
+        bool fast;
+        if constexpr (FMT == FMT_NVFP4) {
+            // E4M3 scale s: bf16(s * 2^112) is exact (4 significant bits); NaN codes are 0x7F / 0xFF
+            fast = (((sbits & 0x7F7Fu) + 0x0101u) & 0x8080u) == 0u;
+            const uint32_t a2 = f16x2_to_bf16x2_m112(e4m3x2_to_f16x2(sbits));
+            // a2 holds s * 2^-112: multiply by 2^112 twice to get s * 2^112
+            const uint32_t p112 = bf16x2_pow2_m15(127);
+            const uint32_t as = bf16x2_mul(bf16x2_mul(a2, p112), p112);
+            m0 = (as & 0xFFFFu) | (as << 16);
+            m1 = (as >> 16) | (as & 0xFFFF0000u);
+        } else {
+            const uint32_t e = sbits & 0xFFu;
+            fast = e - 2u <= 140u;  // 2 <= e <= 142: products normal bf16
+            m0 = m1 = bf16x2_pow2_m15((int)e);
+        }
+        if (fast) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                // word j: elements 8j .. 8j+7 of the half row
+                const uint32_t m = j < 2 ? m0 : m1;
+                uint32_t h0, h1, h2, h3;
+                e2m1x8_to_f16x2(w[j], h0, h1, h2, h3);
+                store_chunk(row_base, 4 * half + j, sw, bf16x2_mul(f16x2_to_bf16x2_m112(h0), m),
+                            bf16x2_mul(f16x2_to_bf16x2_m112(h1), m), bf16x2_mul(f16x2_to_bf16x2_m112(h2), m),
+                            bf16x2_mul(f16x2_to_bf16x2_m112(h3), m));
             }
             return;
         }
         float s0, s1;
-        e8m0x2_to_f32(r.s, s0, s1);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float s = i < 2 ? s0 : s1;
-            const uint32_t w[4] = {r.c[i].x, r.c[i].y, r.c[i].z, r.c[i].w};
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint4 o;
-                o.x = scaled_bf16x2(e4m3x2_to_f16x2(w[2 * half]), s);
-                o.y = scaled_bf16x2(e4m3x2_to_f16x2(w[2 * half] >> 16), s);
-                o.z = scaled_bf16x2(e4m3x2_to_f16x2(w[2 * half + 1]), s);
-                o.w = scaled_bf16x2(e4m3x2_to_f16x2(w[2 * half + 1] >> 16), s);
-                const int chunk = 2 * i + half;
-                *reinterpret_cast<uint4 *>(row_base + ((chunk ^ sw) << 4)) = o;
-            }
-        }
-    } else {
-        // per 16-element quarter: the bf16x2 multiplier (fast path) or fp32 scale
-        uint32_t mul[4];
-        bool fast;
         if constexpr (FMT == FMT_NVFP4) {
-            // E4M3 scale s: bf16(s * 2^112) is exact (4 significant bits); NaN codes are 0x7F / 0xFF
-            fast = ((r.s & 0x7F7F7F7Fu) + 0x01010101u & 0x80808080u) == 0u;  // no byte is S.1111.111
-            const uint32_t a = e4m3x2_to_f16x2(r.s), b = e4m3x2_to_f16x2(r.s >> 16);
-            const uint32_t a2 = f16x2_to_bf16x2_m112(a), b2 = f16x2_to_bf16x2_m112(b);
-            // f16x2_to_bf16x2_m112 gives s * 2^-112: square the shift away with 2^224 as two 2^112 factors
-            const uint32_t p112 = bf16x2_pow2_m15(127);  // 2^112
-            const uint32_t as = bf16x2_mul(bf16x2_mul(a2, p112), p112);
-            const uint32_t bs = bf16x2_mul(bf16x2_mul(b2, p112), p112);
-            mul[0] = (as & 0xFFFFu) | (as << 16);
-            mul[1] = (as >> 16) | (as & 0xFFFF0000u);
-            mul[2] = (bs & 0xFFFFu) | (bs << 16);
-            mul[3] = (bs >> 16) | (bs & 0xFFFF0000u);
+            const uint32_t a = e4m3x2_to_f16x2(sbits);
+            s0 = f16_lo_to_f32(a);
+            s1 = f16_hi_to_f32(a);
         } else {
-            const uint32_t e0 = r.s & 0xFFu, e1 = (r.s >> 8) & 0xFFu;
-            fast = e0 - 2u <= 140u && e1 - 2u <= 140u;  // 2 <= e <= 142: products normal bf16
-            mul[0] = mul[1] = bf16x2_pow2_m15((int)e0);
-            mul[2] = mul[3] = bf16x2_pow2_m15((int)e1);
-        }
-        if (fast) {
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const uint32_t w[4] = {r.c[i].x, r.c[i].y, r.c[i].z, r.c[i].w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    // word j of 16-byte half i: elements 32i + 8j .. +7 (16-element block 2i + j/2)
-                    const uint32_t m = mul[2 * i + (j >> 1)];
-                    uint32_t h0, h1, h2, h3;
-                    e2m1x8_to_f16x2(w[j], h0, h1, h2, h3);
-                    uint4 o;
-                    o.x = bf16x2_mul(f16x2_to_bf16x2_m112(h0), m);
-                    o.y = bf16x2_mul(f16x2_to_bf16x2_m112(h1), m);
-                    o.z = bf16x2_mul(f16x2_to_bf16x2_m112(h2), m);
-                    o.w = bf16x2_mul(f16x2_to_bf16x2_m112(h3), m);
-                    const int chunk = 4 * i + j;
-                    *reinterpret_cast<uint4 *>(row_base + ((chunk ^ sw) << 4)) = o;
-                }
-            }
-            return;
-        }
-        float sc[4];
-        if constexpr (FMT == FMT_NVFP4) {
-            const uint32_t a = e4m3x2_to_f16x2(r.s), b = e4m3x2_to_f16x2(r.s >> 16);
-            sc[0] = f16_lo_to_f32(a);
-            sc[1] = f16_hi_to_f32(a);
-            sc[2] = f16_lo_to_f32(b);
-            sc[3] = f16_hi_to_f32(b);
-        } else {
-            e8m0x2_to_f32(r.s, sc[0], sc[2]);
-            sc[1] = sc[0];
-            sc[3] = sc[2];
+            s0 = s1 = e8m0_to_f32(sbits);
         }
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const uint32_t w[4] = {r.c[i].x, r.c[i].y, r.c[i].z, r.c[i].w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float s = sc[2 * i + (j >> 1)];
-                uint4 o;
-                o.x = scaled_bf16x2(e2m1x2_to_f16x2(w[j]), s);
-                o.y = scaled_bf16x2(e2m1x2_to_f16x2(w[j] >> 8), s);
-                o.z = scaled_bf16x2(e2m1x2_to_f16x2(w[j] >> 16), s);
-                o.w = scaled_bf16x2(e2m1x2_to_f16x2(w[j] >> 24), s);
-                const int chunk = 4 * i + j;
-                *reinterpret_cast<uint4 *>(row_base + ((chunk ^ sw) << 4)) = o;
-            }
+        for (int j = 0; j < 4; ++j) {
+            const float s = j < 2 ? s0 : s1;
+            store_chunk(row_base, 4 * half + j, sw, scaled_bf16x2(e2m1x2_to_f16x2(w[j]), s),
+                        scaled_bf16x2(e2m1x2_to_f16x2(w[j] >> 8), s),
+                        scaled_bf16x2(e2m1x2_to_f16x2(w[j] >> 16), s),
+                        scaled_bf16x2(e2m1x2_to_f16x2(w[j] >> 24), s));
         }
     }
 }
 
 // ------------------------------------------------------------ kernel
 
+// One row's block scales of one k-block: 2 E8M0 bytes or 4 E4M3 bytes.
+template <int SPK>
+__device__ __forceinline__ uint32_t scale_load(const uint8_t *p)
+{
+    return SPK == 4 ? ld_nc_u32(p) : ld_nc_u16(p);
+}
+
 struct QmmArgs {
-    const uint8_t *codes;
     const uint8_t *scales;
     uint16_t *Y;
     int *err;
@@ -393,42 +445,63 @@ struct QmmArgs {
     unsigned long long wait_ns;
 };
 
-template <int FMT>
+template <int FMT, int NACC>
 __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_constant__ CUtensorMap tmap_x,
                                                              const __grid_constant__ CUtensorMap tmap_c, QmmArgs a)
 {
-    using QG = QmmGeo<FMT>;
-    constexpr int QMM_STAGE_BYTES = QG::STAGE;
+    using QG = QmmGeo<FMT, NACC>;
+    constexpr int SX = QG::SX, SW = QG::SW, SPK = QG::SPK;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + QMM_STAGES * QMM_STAGE_BYTES);
-    uint64_t *full_a = bars;                    // [STAGES] TMA bytes landed
-    uint64_t *full_b = bars + QMM_STAGES;       // [STAGES] decoded tile stored (8 warps)
-    uint64_t *empty = bars + 2 * QMM_STAGES;    // [STAGES] MMAs that read the stage finished
-    uint64_t *acc_full = bars + 3 * QMM_STAGES; // accumulators complete
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * QMM_STAGES + 1);
+    uint8_t *xring = smem;
+    uint8_t *wring = smem + QG::OFF_W;
+    uint8_t *cring = smem + QG::OFF_C;
+    uint8_t *sring = smem + QG::OFF_S;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + QG::OFF_BAR);
+    uint64_t *full_x = bars;                    // [SX] (CTA 0) both CTAs' X slabs landed: 2 arrivals + bytes
+    uint64_t *empty_x = bars + SX;              // [SX] the pair's MMAs that read the X slot finished
+    uint64_t *full_w = bars + 2 * SX;           // [SW] this CTA's codes (TMA) and scales landed
+    uint64_t *dec_full = full_w + SW;           // [SW] this CTA's decoded tile stored (8 warps)
+    uint64_t *peer_full = full_w + 2 * SW;      // [SW] (CTA 0) CTA 1's decoded tile stored (relayed)
+    uint64_t *empty_w = full_w + 3 * SW;        // [SW] the pair's MMAs that read the W slot finished
+    uint64_t *acc_full = full_w + 4 * SW;       // accumulators complete
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *x_issued = reinterpret_cast<volatile int *>(tmem_slot + 2);  // X k-blocks this CTA loaded
+    volatile int *x_taken = reinterpret_cast<volatile int *>(tmem_slot + 3);   // (CTA 0) X k-blocks the MMAs took
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m_tiles = (a.M + QMM_BM - 1) / QMM_BM;
-    const int m0 = (blockIdx.x % m_tiles) * QMM_BM;
-    const int n0 = (blockIdx.x / m_tiles) * QMM_BN;
+    const uint32_t rank = cluster_ctarank();
+    const int cid = (int)cluster_id_x();
+    const int m_tiles = (a.M + QG::BM - 1) / QG::BM;
+    const int m0 = (cid % m_tiles) * QG::BM;
+    const int n0 = (cid / m_tiles) * QMM_BN;
     const int KB = a.K / QMM_BK;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < QMM_STAGES; ++s) {
-            mbar_init(&full_a[s], 1);
-            mbar_init(&full_b[s], 8);
-            mbar_init(&empty[s], 1);
+        for (int s = 0; s < SX; ++s) {
+            mbar_init(&full_x[s], 2);
+            mbar_init(&empty_x[s], 1);
+        }
+        for (int s = 0; s < SW; ++s) {
+            mbar_init(&full_w[s], 2);
+            mbar_init(&dec_full[s], 8);
+            mbar_init(&peer_full[s], 1);
+            mbar_init(&empty_w[s], 1);
         }
         mbar_init(acc_full, 1);
         *abort_flag = 0;
+        *x_issued = 0;
+        *x_taken = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    cluster_sync_all();  // both CTAs' barriers exist before either arrives remotely
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(tmem_slot))
+        // one warp of each CTA allocates the pair's columns together
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(QG::TMEM_COLS)
                      : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
         tc_fence_before();
     }
     __syncthreads();
@@ -437,135 +510,191 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_consta
     pdl_trigger();
     pdl_wait();  // X and Y may be used by the neighbouring kernels
 
-    int issued_a = 0;  // producer: stages whose TMA was issued
-    if (warp == 0) {
-        // ---------------- TMA producer
+    if (warp == 10) {
+        // ---------------- X producer: both CTAs' slabs complete on CTA 0's
+        // barrier, each CTA adding one arrival and its own bytes
         if (lane == 0) {
+            const uint32_t fx0 = map_to_cta(smem_u32(full_x), 0);
+            int issued = 0;
             for (int kb = 0; kb < KB; ++kb) {
-                const int s = kb % QMM_STAGES;
-                if (kb >= QMM_STAGES && !mbar_wait(&empty[s], ((kb / QMM_STAGES) - 1) & 1, abort_flag, a.wait_ns))
-                    break;
-                uint8_t *st = smem + s * QMM_STAGE_BYTES;
-                mbar_arrive_expect_tx(&full_a[s], 2 * QMM_A_BYTES + QG::C_BYTES);
-                tma_load_2d(st, &tmap_x, kb * QMM_BK, m0, &full_a[s]);
-                tma_load_2d(st + QMM_A_BYTES, &tmap_x, kb * QMM_BK, m0 + 128, &full_a[s]);
-                if constexpr (QG::TMA_CODES)  // 256 weight rows x 32 code bytes
-                    tma_load_2d(st + 2 * QMM_A_BYTES + QMM_B_BYTES, &tmap_c, kb * 32, n0, &full_a[s]);
-                issued_a = kb + 1;
+                const int s = kb % SX;
+                if (kb >= SX && !mbar_wait(&empty_x[s], ((kb / SX) - 1) & 1, abort_flag, a.wait_ns)) break;
+                const uint32_t bar = fx0 + 8u * (uint32_t)s;
+                mbar_arrive_expect_tx_cluster(bar, NACC * QMM_X_BYTES);
+#pragma unroll
+                for (int h = 0; h < NACC; ++h)
+                    tma_load_2d_pair(xring + s * QG::X_STAGE + h * QMM_X_BYTES, &tmap_x, kb * QMM_BK,
+                                     m0 + 256 * h + 128 * (int)rank, bar);
+                issued = kb + 1;
             }
-            // drain: every issued TMA must land before the CTA may exit
-            for (int kb = (issued_a > QMM_STAGES ? issued_a - QMM_STAGES : 0); kb < issued_a; ++kb)
-                mbar_wait(&full_a[kb % QMM_STAGES], (kb / QMM_STAGES) & 1, abort_flag, a.wait_ns, false);
+            *x_issued = issued;
         }
+    } else if (warp == 0) {
+        // ---------------- W producer: codes by TMA (lane 0), block scales
+        // (whole warp, QMM_SPF k-blocks in flight).  The scales come through
+        // shared memory so that the decoders hold no global loads in flight
+        // when they release their stores.
+        const size_t srow_bytes = (size_t)KB * SPK;
+        const uint8_t *sbase = a.scales + (size_t)(n0 + 128 * (int)rank + lane) * srow_bytes;
+        uint32_t pv[QMM_SPF][4];
+#pragma unroll
+        for (int j = 0; j < QMM_SPF; ++j)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (j < KB) pv[j][i] = scale_load<SPK>(sbase + (size_t)(32 * i) * srow_bytes + SPK * j);
+        int issued = 0;
+        bool go = true;
+        for (int kb0 = 0; kb0 < KB && go; kb0 += QMM_SPF) {
+#pragma unroll
+            for (int j = 0; j < QMM_SPF; ++j) {
+                const int kb = kb0 + j;
+                if (kb >= KB) break;
+                const int s = kb % SW;
+                int ok = 1;
+                if (lane == 0 && kb >= SW) ok = mbar_wait(&empty_w[s], ((kb / SW) - 1) & 1, abort_flag, a.wait_ns);
+                if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
+                    go = false;
+                    break;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&full_w[s], QG::C_BYTES);
+                    tma_load_2d(cring + s * QG::C_BYTES, &tmap_c, kb * QG::CODE_ROW, n0 + 128 * (int)rank,
+                                &full_w[s]);
+                }
+                uint8_t *sc = sring + s * QG::SC_BYTES;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if constexpr (SPK == 4) *reinterpret_cast<uint32_t *>(sc + 4 * (lane + 32 * i)) = pv[j][i];
+                    else *reinterpret_cast<uint16_t *>(sc + 2 * (lane + 32 * i)) = (uint16_t)pv[j][i];
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full_w[s]);
+                issued = kb + 1;
+                if (kb + QMM_SPF < KB)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        pv[j][i] = scale_load<SPK>(sbase + (size_t)(32 * i) * srow_bytes + SPK * (kb + QMM_SPF));
+            }
+        }
+        // drain: every issued codes TMA must land before the CTA may exit
+        if (lane == 0)
+            for (int kb = (issued > SW ? issued - SW : 0); kb < issued; ++kb)
+                mbar_wait(&full_w[kb % SW], (kb / SW) & 1, abort_flag, a.wait_ns, false);
     } else if (warp == 1) {
-        // ---------------- MMA issuer
-        if (lane == 0) {
+        if (rank == 0 && lane == 0) {
+            // ---------------- MMA issuer (CTA 0)
             constexpr uint32_t idesc = qmm_idesc();
-            int done = 0;
+            int taken = 0;
             for (int kb = 0; kb < KB; ++kb) {
-                const int s = kb % QMM_STAGES;
-                const uint32_t ph = (kb / QMM_STAGES) & 1;
-                if (!mbar_wait(&full_a[s], ph, abort_flag, a.wait_ns)) break;
-                if (!mbar_wait(&full_b[s], ph, abort_flag, a.wait_ns)) break;
+                const int sx = kb % SX, sw = kb % SW;
+                if (!mbar_wait(&full_x[sx], (kb / SX) & 1, abort_flag, a.wait_ns)) break;
+                taken = kb + 1;
+                if (!mbar_wait(&dec_full[sw], (kb / SW) & 1, abort_flag, a.wait_ns)) break;
+                if (!mbar_wait(&peer_full[sw], (kb / SW) & 1, abort_flag, a.wait_ns)) break;
                 tc_fence_after();
-                const uint32_t sa0 = smem_u32(smem + s * QMM_STAGE_BYTES);
-                const uint32_t sa1 = sa0 + QMM_A_BYTES;
-                const uint32_t sb = sa0 + 2 * QMM_A_BYTES;
+                const uint32_t xa = smem_u32(xring + sx * QG::X_STAGE);
+                const uint32_t wa = smem_u32(wring + sw * QMM_W_BYTES);
 #pragma unroll
                 for (int kk = 0; kk < QMM_BK / 16; ++kk) {
-                    const uint64_t bd = sw128_desc(sb + kk * 32);
+                    const uint64_t bd = sw128_desc(wa + kk * 32);
                     const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-                    umma_bf16(tmem, sw128_desc(sa0 + kk * 32), bd, idesc, acc);
-                    umma_bf16(tmem + QMM_BN, sw128_desc(sa1 + kk * 32), bd, idesc, acc);
+#pragma unroll
+                    for (int h = 0; h < NACC; ++h)
+                        umma2_bf16(tmem + h * QMM_BN, sw128_desc(xa + h * QMM_X_BYTES + kk * 32), bd, idesc, acc);
                 }
-                umma_commit(&empty[s]);
-                done = kb + 1;
+                umma2_commit_both(&empty_x[sx]);
+                umma2_commit_both(&empty_w[sw]);
             }
-            umma_commit(acc_full);  // fires once every MMA issued so far has completed
-            (void)done;
+            umma2_commit_both(acc_full);  // fires once every MMA issued so far has completed
+            *x_taken = taken;
+        } else if (rank == 1 && lane == 0) {
+            // ---------------- relay (CTA 1): pass the completion of this CTA's
+            // decoded tiles to CTA 0.  The decoders release their stores at
+            // CTA scope; one cluster-scope fence per batch of completed slots
+            // then makes them visible to the pair's MMA issuer.  (A cluster-
+            // scope release in every decoder warp stalls each of them on the
+            // fence for every k-block.)
+            const uint32_t peer0 = map_to_cta(smem_u32(peer_full), 0);
+            int kb = 0;
+            while (kb < KB) {
+                if (!mbar_wait(&dec_full[kb % SW], (kb / SW) & 1, abort_flag, a.wait_ns)) break;
+                int end = kb + 1;
+                while (end < KB && end < kb + SW && mbar_try_wait(&dec_full[end % SW], (end / SW) & 1)) ++end;
+                fence_acq_rel_cluster();
+                for (int k = kb; k < end; ++k) mbar_arrive_relaxed_cluster(peer0 + 8u * (uint32_t)(k % SW));
+                kb = end;
+            }
         }
     } else {
-        // ---------------- decoders (warps 2..9), one weight row per thread
-        const int d = threadIdx.x - 64;  // 0..255
-        const int n = n0 + d;
-        const size_t rb = FMT == FMT_MXFP8 ? (size_t)a.K : (size_t)a.K / 2;
-        const size_t sb = FMT == FMT_NVFP4 ? (size_t)(a.K / 16) : (size_t)(a.K / 32);
-        const uint8_t *crow = a.codes + (size_t)n * rb;
-        const uint8_t *srow = a.scales + (size_t)n * sb;
-        if constexpr (QG::TMA_CODES) {
-            // codes arrive by TMA with the stage; the scale bytes of the next
-            // QMM_PF k-blocks stay in flight in registers
-            constexpr int SPK = FMT == FMT_NVFP4 ? 4 : 2;  // scale bytes per k-block
-            uint32_t sv[QMM_PF];
-#pragma unroll
-            for (int j = 0; j < QMM_PF; ++j)
-                if (j < KB) sv[j] = SPK == 4 ? ld_nc_u32(srow + 4 * j) : ld_nc_u16(srow + 2 * j);
-            for (int kb0 = 0; kb0 < KB; kb0 += QMM_PF) {
-#pragma unroll
-                for (int j = 0; j < QMM_PF; ++j) {
-                    const int kb = kb0 + j;
-                    if (kb >= KB) break;
-                    const int s = kb % QMM_STAGES;
-                    // the stage's TMA was issued after the MMAs released it, so its
-                    // arrival also means the decoded-tile slot is free
-                    if (!mbar_wait(&full_a[s], (kb / QMM_STAGES) & 1, abort_flag, a.wait_ns)) goto decode_done;
-                    uint8_t *stage = smem + s * QMM_STAGE_BYTES;
-                    const uint4 *cp = reinterpret_cast<const uint4 *>(stage + 2 * QMM_A_BYTES + QMM_B_BYTES + d * 32);
-                    QRow<FMT> rr;
-                    rr.c[0] = cp[0];
-                    rr.c[1] = cp[1];
-                    rr.s = sv[j];
-                    if (kb + QMM_PF < KB)
-                        sv[j] = SPK == 4 ? ld_nc_u32(srow + 4 * (kb + QMM_PF)) : ld_nc_u16(srow + 2 * (kb + QMM_PF));
-                    qrow_store<FMT>(rr, stage + 2 * QMM_A_BYTES + d * 128, d);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&full_b[s]);
-                }
+        // ---------------- decoders (warps 2..9): thread d decodes half (d & 1)
+        // of weight row n0 + 128 rank + (d >> 1)
+        const int d = threadIdx.x - 64;
+        const int row = d >> 1, half = d & 1;
+        for (int kb = 0; kb < KB; ++kb) {
+            const int s = kb % SW;
+            // the codes' TMA was issued after the MMAs released the slot, so
+            // its arrival also means the decoded-tile slot is free
+            if (!mbar_wait(&full_w[s], (kb / SW) & 1, abort_flag, a.wait_ns)) break;
+            const uint8_t *cp = cring + s * QG::C_BYTES + row * QG::CODE_ROW + half * (QG::CODE_ROW / 2);
+            uint32_t w[FMT == FMT_MXFP8 ? 8 : 4];
+            if constexpr (FMT == FMT_MXFP8) {
+                // the two 16-byte reads in a row-dependent order spread a
+                // warp's reads over all banks
+                const int f = (row >> 1) & 1;
+                const uint4 v0 = *reinterpret_cast<const uint4 *>(cp + 16 * f);
+                const uint4 v1 = *reinterpret_cast<const uint4 *>(cp + 16 * (f ^ 1));
+                const uint4 lo = f ? v1 : v0, hi = f ? v0 : v1;
+                w[0] = lo.x; w[1] = lo.y; w[2] = lo.z; w[3] = lo.w;
+                w[4] = hi.x; w[5] = hi.y; w[6] = hi.z; w[7] = hi.w;
+            } else {
+                const uint4 v = *reinterpret_cast<const uint4 *>(cp);
+                w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
             }
-        } else {
-            // codes and scales of the next QMM_PF k-blocks stay in flight in registers
-            QRow<FMT> r[QMM_PF];
-#pragma unroll
-            for (int j = 0; j < QMM_PF; ++j)
-                if (j < KB) qrow_load<FMT>(crow, srow, j, r[j]);
-            for (int kb0 = 0; kb0 < KB; kb0 += QMM_PF) {
-#pragma unroll
-                for (int j = 0; j < QMM_PF; ++j) {
-                    const int kb = kb0 + j;
-                    if (kb >= KB) break;
-                    const int s = kb % QMM_STAGES;
-                    if (kb >= QMM_STAGES &&
-                        !mbar_wait(&empty[s], ((kb / QMM_STAGES) - 1) & 1, abort_flag, a.wait_ns))
-                        goto decode_done;
-                    uint8_t *b_tile = smem + s * QMM_STAGE_BYTES + 2 * QMM_A_BYTES;
-                    qrow_store<FMT>(r[j], b_tile + d * 128, d);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&full_b[s]);
-                    if (kb + QMM_PF < KB) qrow_load<FMT>(crow, srow, kb + QMM_PF, r[j]);
-                }
-            }
+            const uint8_t *scp = sring + s * QG::SC_BYTES + SPK * row + (SPK / 2) * half;
+            const uint32_t sbits = SPK == 4 ? *reinterpret_cast<const uint16_t *>(scp) : *scp;
+            qhalf_store<FMT>(w, sbits, wring + s * QMM_W_BYTES + row * 128, half, row & 7);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&dec_full[s]);
         }
-    decode_done:;
     }
 
     // ---------------- epilogue (decoder warps): TMEM -> bf16 -> Y
-    if (warp >= 2) {
+    bool acc_ok = true;
+    if (warp >= 2 && warp <= 9) {
         // the MMAs must have finished (even on abort) before TMEM is read or freed
-        const bool ok = mbar_wait(acc_full, 0, abort_flag, a.wait_ns, false) && !*abort_flag;
-        tc_fence_after();
-        const int half = warp < 6 ? 0 : 1;      // accumulator (M half)
-        const int quarter = warp & 3;           // TMEM lanes 32*quarter .. +31
-        const int m = m0 + half * 128 + quarter * 32 + lane;
+        acc_ok = mbar_wait(acc_full, 0, abort_flag, a.wait_ns, false);
+    }
+    // every role of both CTAs is done: settle whether the pair gave up
+    tc_fence_before();
+    cluster_sync_all();
+    tc_fence_after();
+    const int aborted = *abort_flag | ld_cluster_s32(map_to_cta(smem_u32((const void *)abort_flag), rank ^ 1u));
+    if (aborted && rank == 0 && threadIdx.x == 320) {
+        // X slabs the MMAs did not take may still be landing in either CTA:
+        // supply the arrival of a CTA that did not load a k-block, then wait
+        // for each outstanding slot (its bytes complete on this barrier)
+        const int i0 = *x_issued, i1 = ld_cluster_s32(map_to_cta(smem_u32((const void *)x_issued), 1u));
+        const int hi = i0 > i1 ? i0 : i1;
+        for (int kb = *x_taken; kb < hi; ++kb) {
+            const int s = kb % SX;
+            if (kb >= i0) mbar_arrive_expect_tx_cluster(smem_u32(&full_x[s]), 0);
+            if (kb >= i1) mbar_arrive_expect_tx_cluster(smem_u32(&full_x[s]), 0);
+            mbar_wait(&full_x[s], (kb / SX) & 1, abort_flag, a.wait_ns, false);
+        }
+    }
+    if (warp >= 2 && warp <= 9) {
+        const bool ok = acc_ok && !aborted;
+        const int quarter = warp & 3;   // TMEM lanes 32*quarter .. +31
+        const int group = (warp - 2) >> 2;  // which half of the accumulator columns
         float g = 1.0f;
         if (FMT == FMT_NVFP4) g = load_f32_unaligned(a.scales + (size_t)a.N * (a.K / 16));
-        uint16_t *yrow = a.Y + (size_t)m * a.N + n0;
-        const bool store = m < a.M;  // rows past M were zero-filled by TMA
-        for (int c = 0; c < QMM_BN; c += 32) {
+        for (int c = group * NACC * 128; c < (group + 1) * NACC * 128; c += 32) {
+            const int h = c / QMM_BN, nc = c % QMM_BN;
+            const int m = m0 + 256 * h + 128 * (int)rank + 32 * quarter + lane;
             uint32_t v[32];
             if (ok) {
-                tmem_ld32(tmem + half * QMM_BN + c + ((uint32_t)(quarter * 32) << 16), v);
+                tmem_ld32(tmem + (uint32_t)c + ((uint32_t)(quarter * 32) << 16), v);
             } else {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = 0x7FC00000u;
@@ -580,19 +709,21 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_consta
                 }
                 o[i] = f32x2_to_bf16x2(lo, hi);
             }
-            uint4 *dst = reinterpret_cast<uint4 *>(yrow + c);
-            if (store) {
+            if (m < a.M) {  // rows past M were zero-filled by TMA
+                uint4 *dst = reinterpret_cast<uint4 *>(a.Y + (size_t)m * a.N + n0 + nc);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
             }
         }
-        tc_fence_before();
     }
-    __syncthreads();
+    // neither CTA frees tensor memory or exits while its peer may still use it
+    tc_fence_before();
+    cluster_sync_all();
     if (threadIdx.x == 0 && *abort_flag) set_device_error(a.err, DEVERR_TIMEOUT);
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(QG::TMEM_COLS)
+                     : "memory");
     }
 }
 
@@ -617,20 +748,56 @@ static EncodeTiledFn encode_fn()
     return fn;
 }
 
-template <int FMT>
-static cudaError_t run_qmm(const DeviceState &ds, cudaStream_t st, const CUtensorMap &map, const CUtensorMap &cmap,
+template <int FMT, int NACC>
+static cudaError_t run_qmm(const DeviceState &ds, cudaStream_t st, const CUtensorMap &xmap, const CUtensorMap &cmap,
                            const QmmArgs &a)
 {
-    using QG = QmmGeo<FMT>;
+    using QG = QmmGeo<FMT, NACC>;
     if (QG::SMEM > ds.max_smem_optin) return cudaErrorInvalidValue;
     static int configured_dev[64] = {0};
     if (ds.device < 64 && !configured_dev[ds.device]) {
-        cudaError_t e = cudaFuncSetAttribute(qmm_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, QG::SMEM);
+        cudaError_t e =
+            cudaFuncSetAttribute(qmm_kernel<FMT, NACC>, cudaFuncAttributeMaxDynamicSharedMemorySize, QG::SMEM);
         if (e != cudaSuccess) return e;
         configured_dev[ds.device] = 1;
     }
-    const int grid = ((a.M + QMM_BM - 1) / QMM_BM) * (a.N / QMM_BN);
-    return launch_k(qmm_kernel<FMT>, dim3(grid), dim3(QMM_THREADS), (size_t)QG::SMEM, st, map, cmap, a);
+    const int pairs = ((a.M + QG::BM - 1) / QG::BM) * (a.N / QMM_BN);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * pairs);
+    cfg.blockDim = dim3(QMM_THREADS);
+    cfg.dynamicSmemBytes = QG::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, qmm_kernel<FMT, NACC>, xmap, cmap, a);
+}
+
+// Pair tiles of 512 rows halve each SM's decode and shared-memory writes per
+// flop against 256-row tiles, but come in half as many; take them unless the
+// coarser wave quantisation costs more (a 512-row tile taken as 1.85 times a
+// 256-row one; num_sms / 2 pairs per wave).
+static int qmm_nacc(const DeviceState &ds, int M, int N)
+{
+    if (M <= 256) return 1;
+    const long long slots = ds.num_sms / 2 > 0 ? ds.num_sms / 2 : 1;
+    const long long p1 = (long long)((M + 255) / 256) * (N / QMM_BN);
+    const long long p2 = (long long)((M + 511) / 512) * (N / QMM_BN);
+    const long long w1 = (p1 + slots - 1) / slots, w2 = (p2 + slots - 1) / slots;
+    return w2 * 185 <= w1 * 100 ? 2 : 1;
+}
+
+template <int FMT>
+static cudaError_t run_qmm_fmt(const DeviceState &ds, cudaStream_t st, const CUtensorMap &xmap,
+                               const CUtensorMap &cmap, const QmmArgs &a)
+{
+    return qmm_nacc(ds, a.M, a.N) == 2 ? run_qmm<FMT, 2>(ds, st, xmap, cmap, a) : run_qmm<FMT, 1>(ds, st, xmap, cmap, a);
 }
 
 cudaError_t launch_qmm(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,
@@ -639,30 +806,27 @@ cudaError_t launch_qmm(const DeviceState &ds, cudaStream_t st, int fmt, const ui
     if (N % QMM_BN != 0 || K % QMM_BK != 0) return cudaErrorInvalidValue;
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
-    CUtensorMap map;
+    // X: [M][K] bf16, boxes of 64 x 128 rows, 128-byte swizzle; rows past M read as zero
+    CUtensorMap xmap;
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
     const cuuint32_t box[2] = {(cuuint32_t)QMM_BK, 128u};
     const cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(X), dims, strides, box,
+    CUresult r = enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(X), dims, strides, box,
                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    // packed codes of the 4-bit formats: [N][K/2] bytes, box of 32 bytes x 256 rows
+    // packed codes: [N][row bytes], boxes of one k-block's bytes x 128 rows
+    const cuuint64_t row_bytes = fmt == FMT_MXFP8 ? (cuuint64_t)K : (cuuint64_t)K / 2;
     CUtensorMap cmap;
-    if (fmt != FMT_MXFP8) {
-        const cuuint64_t cdims[2] = {(cuuint64_t)K / 2, (cuuint64_t)N};
-        const cuuint64_t cstrides[1] = {(cuuint64_t)K / 2};
-        const cuuint32_t cbox[2] = {32u, (cuuint32_t)QMM_BN};
-        r = enc(&cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(codes), cdims, cstrides, cbox, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    } else {
-        cmap = map;  // unused
-    }
+    const cuuint64_t cdims[2] = {row_bytes, (cuuint64_t)N};
+    const cuuint64_t cstrides[1] = {row_bytes};
+    const cuuint32_t cbox[2] = {fmt == FMT_MXFP8 ? (cuuint32_t)QMM_BK : (cuuint32_t)QMM_BK / 2, 128u};
+    r = enc(&cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(codes), cdims, cstrides, cbox, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     QmmArgs a;
-    a.codes = codes;
     a.scales = scales;
     a.Y = Y;
     a.err = ds.err;
@@ -670,9 +834,9 @@ cudaError_t launch_qmm(const DeviceState &ds, cudaStream_t st, int fmt, const ui
     a.N = N;
     a.K = K;
     a.wait_ns = QMM_WAIT_NS;
-    if (fmt == FMT_MXFP4) return run_qmm<FMT_MXFP4>(ds, st, map, cmap, a);
-    if (fmt == FMT_MXFP8) return run_qmm<FMT_MXFP8>(ds, st, map, cmap, a);
-    return run_qmm<FMT_NVFP4>(ds, st, map, cmap, a);
+    if (fmt == FMT_MXFP4) return run_qmm_fmt<FMT_MXFP4>(ds, st, xmap, cmap, a);
+    if (fmt == FMT_MXFP8) return run_qmm_fmt<FMT_MXFP8>(ds, st, xmap, cmap, a);
+    return run_qmm_fmt<FMT_NVFP4>(ds, st, xmap, cmap, a);
 }
 
 }  // namespace mx

@@ -20,8 +20,10 @@ def run_qmm(fmt, codes, scales, X, N):
 
 @pytest.mark.parametrize("fmt", [0, 1, 2])
 @pytest.mark.parametrize("M,N,K", [(256, 256, 64), (256, 512, 256), (512, 256, 1024), (100, 256, 128),
-                                   (300, 768, 320)])
+                                   (300, 768, 320), (1000, 9728, 192)])
 def test_qmm_parity(orc, fmt, M, N, K):
+    """Pair tiles of 256 rows, and (1000 x 9728: 76 pairs, one wave) of 512
+    rows with a ragged last tile."""
     need_gpu()
     codes, scales = synth.weights(fmt, N, K, M + K, exp_lo=118, exp_hi=132)
     X = synth.activations(M, K, N + K)
