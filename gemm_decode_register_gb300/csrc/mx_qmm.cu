@@ -14,25 +14,23 @@
 // reads both CTAs' shared memory and CTA r's tensor memory receives its 128
 // rows of the accumulator.  Against one CTA running 128 x 256 MMAs this
 // halves each SM's decode work and shared-memory operand reads per flop.
-// Per CTA, K streams in 64-wide k-blocks through two rings of shared memory
-// (X slabs; decoded weights with their codes and scales):
+// Per CTA, K streams in 64-wide k-blocks through three rings of shared
+// memory (X slabs, decoded weights, packed codes with their scales):
 //
 //   warp 10     X: NACC 128 x 64 bf16 slabs per k-block by TMA (128-byte
 //               swizzle); both CTAs' slabs complete on CTA 0's barrier
-//   warp 0      W: the packed codes of the CTA's 128 weight rows by TMA, and
-//               their block scales through registers into shared memory
+//   warp 0      codes of the CTA's 128 weight rows by TMA, and their block
+//               scales through registers into shared memory
 //   warp 1      CTA 0: one thread issues the pair's MMAs (NACC accumulators
 //               of 256 columns sharing the decoded weights) and commits each
-//               k-block to the empty barriers of both CTAs;
-//               CTA 1: one thread relays the completion of CTA 1's decoded
-//               tiles to CTA 0 (one cluster-scope fence per batch)
+//               k-block to the empty barriers of both CTAs
 //   warps 2-9   decoders: two threads per weight row, 32 elements each; they
-//               wait for the codes, decode them exactly to bf16 (code * scale
-//               has at most 6 significant bits), store them in the
-//               128-byte-swizzled K-major layout TMA produces and arrive on
-//               their CTA's barrier; then the epilogue: tcgen05.ld of the
-//               CTA's accumulator rows, NVFP4 tensor scale, round to bf16,
-//               store.
+//               decode the codes exactly to bf16 (code * scale has at most 6
+//               significant bits) into the 128-byte-swizzled K-major layout
+//               TMA produces; CTA 0's warps then arrive on CTA 0's barrier,
+//               CTA 1's signal it with a 16-byte bulk copy that completes
+//               there.  Then the epilogue: tcgen05.ld of the CTA's
+//               accumulator rows, NVFP4 tensor scale, round to bf16, store.
 //
 // Every mbarrier wait is bounded (about two seconds of %globaltimer); a wait
 // that gives up sets MX_DEVERR_TIMEOUT in the device error word, the CTA
@@ -54,13 +52,12 @@ constexpr int QMM_W_BYTES = 128 * QMM_BK * 2;  // a CTA's 128 decoded weight row
 constexpr int QMM_SMEM_LIMIT = 232448;         // 227 KB of dynamic shared memory per CTA
 constexpr unsigned long long QMM_WAIT_NS = 2000000000ull;
 
-// Per-format, per-tile-height geometry.  Two rings of k-blocks:
+// Per-format, per-tile-height geometry.  Three rings of k-blocks:
 //   X ring (SX slots): NACC slabs of 128 x 64 bf16 X rows, by TMA;
-//   W ring (SW slots): the decoded 128 x 64 bf16 weight tile, the packed
-//     codes it is decoded from (TMA) and the block scales.
-// The W ring is deeper: a W slot is held from its codes' TMA through the
-// decode and the hand-over to CTA 0 until the MMA finishes, an X slot only
-// from its TMA until the MMA finishes.
+//   D ring (SD slots): the decoded 128 x 64 bf16 weight tile;
+//   C ring (SC slots): the packed codes (TMA) and block scales of a k-block.
+// A D slot is held from its decode through the hand-over to CTA 0 until the
+// MMA finishes; a C slot only until its codes are decoded.
 template <int FMT, int NACC>
 struct QmmGeo {
     static constexpr int BM = 256 * NACC;  // output rows per pair tile
@@ -69,20 +66,22 @@ struct QmmGeo {
     static constexpr int SPK = FMT == FMT_NVFP4 ? 4 : 2;  // scale bytes per row per k-block
     static constexpr int SC_BYTES = 128 * SPK;
     static constexpr int X_STAGE = NACC * QMM_X_BYTES;
-    static constexpr int SX = NACC == 2 ? 3 : 4;
-    static constexpr int RESERVED = 1024 /*align*/ + 512 /*barriers*/;
-    static constexpr int W_FIT = (QMM_SMEM_LIMIT - RESERVED - SX * X_STAGE) / (QMM_W_BYTES + C_BYTES + SC_BYTES);
-    static constexpr int SW = W_FIT > 8 ? 8 : W_FIT;
-    // layout: [X ring][decoded W ring][codes ring][scales ring][barriers]
-    static constexpr int OFF_W = SX * X_STAGE;
-    static constexpr int OFF_C = OFF_W + SW * QMM_W_BYTES;
-    static constexpr int OFF_S = OFF_C + SW * C_BYTES;
-    static constexpr int OFF_BAR = OFF_S + SW * SC_BYTES;
-    static constexpr int SMEM = OFF_BAR + RESERVED;
+    static constexpr int SX = NACC == 2 ? 4 : 6;
+    static constexpr int SD = NACC == 2 ? 5 : 6;
+    static constexpr int RESERVED = 1024 /*align*/ + 128 /*signal landing*/ + 512 /*barriers*/;
+    static constexpr int C_FIT = (QMM_SMEM_LIMIT - RESERVED - SX * X_STAGE - SD * QMM_W_BYTES) / (C_BYTES + SC_BYTES);
+    static constexpr int SC = C_FIT > 4 ? 4 : C_FIT;
+    // layout: [X ring][D ring][codes ring][scales ring][signal landing][barriers]
+    static constexpr int OFF_D = SX * X_STAGE;
+    static constexpr int OFF_C = OFF_D + SD * QMM_W_BYTES;
+    static constexpr int OFF_S = OFF_C + SC * C_BYTES;
+    static constexpr int OFF_SIG = OFF_S + SC * SC_BYTES;
+    static constexpr int OFF_BAR = OFF_SIG + 128;
+    static constexpr int SMEM = OFF_BAR + 512 + 1024;
     static constexpr int TMEM_COLS = 256 * NACC;
-    static_assert(OFF_C % 1024 == 0 && OFF_S % 16 == 0 && OFF_BAR % 8 == 0, "ring alignment");
-    static_assert(SW >= 4, "W ring too shallow");
-    static_assert((2 * SX + 4 * SW + 1) * 8 + 16 <= 512, "barrier area");
+    static_assert(OFF_C % 1024 == 0 && OFF_S % 128 == 0 && OFF_SIG % 128 == 0, "ring alignment");
+    static_assert(SC >= 2, "codes ring too shallow");
+    static_assert((2 * SX + 2 * SC + 3 * SD + 1) * 8 + 16 <= 512, "barrier area");
     static_assert(SMEM <= QMM_SMEM_LIMIT, "shared memory");
 };
 
@@ -141,14 +140,19 @@ __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
 
-// Relaxed arrive on a barrier given by its cluster address (own or peer
-// CTA); after fence_acq_rel_cluster it is a release at cluster scope.
-__device__ __forceinline__ void mbar_arrive_relaxed_cluster(uint32_t caddr)
+// Signal a barrier of the peer CTA through the async proxy: copy 16 bytes
+// of this CTA's shared memory to `dst_cluster` and complete 16 bytes of
+// transactions on `bar_cluster` (both cluster addresses in the peer).  After
+// fence.proxy.async, the copy's completion orders this thread's earlier
+// shared-memory writes before whatever the waiter on the barrier does next,
+// without stalling this thread on a cluster-scope fence.
+__device__ __forceinline__ void bulk_signal(uint32_t dst_cluster, const void *src, uint32_t bar_cluster)
 {
-    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], 16, [%2];" ::"r"(
+                     dst_cluster),
+                 "r"(smem_u32(src)), "r"(bar_cluster)
+                 : "memory");
 }
-
-__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
 {
@@ -450,21 +454,24 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_consta
                                                              const __grid_constant__ CUtensorMap tmap_c, QmmArgs a)
 {
     using QG = QmmGeo<FMT, NACC>;
-    constexpr int SX = QG::SX, SW = QG::SW, SPK = QG::SPK;
+    constexpr int SX = QG::SX, SD = QG::SD, SC = QG::SC, SPK = QG::SPK;
+    constexpr uint32_t SIG_BYTES = 8 * 16;  // one 16-byte signal per decoder warp of CTA 1
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t *xring = smem;
-    uint8_t *wring = smem + QG::OFF_W;
+    uint8_t *dring = smem + QG::OFF_D;
     uint8_t *cring = smem + QG::OFF_C;
     uint8_t *sring = smem + QG::OFF_S;
+    uint8_t *sig = smem + QG::OFF_SIG;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + QG::OFF_BAR);
-    uint64_t *full_x = bars;                    // [SX] (CTA 0) both CTAs' X slabs landed: 2 arrivals + bytes
-    uint64_t *empty_x = bars + SX;              // [SX] the pair's MMAs that read the X slot finished
-    uint64_t *full_w = bars + 2 * SX;           // [SW] this CTA's codes (TMA) and scales landed
-    uint64_t *dec_full = full_w + SW;           // [SW] this CTA's decoded tile stored (8 warps)
-    uint64_t *peer_full = full_w + 2 * SW;      // [SW] (CTA 0) CTA 1's decoded tile stored (relayed)
-    uint64_t *empty_w = full_w + 3 * SW;        // [SW] the pair's MMAs that read the W slot finished
-    uint64_t *acc_full = full_w + 4 * SW;       // accumulators complete
+    uint64_t *full_x = bars;                // [SX] (CTA 0) both CTAs' X slabs landed: 2 arrivals + bytes
+    uint64_t *empty_x = bars + SX;          // [SX] the pair's MMAs that read the X slot finished
+    uint64_t *full_c = bars + 2 * SX;       // [SC] this CTA's codes (TMA) and scales landed
+    uint64_t *empty_c = full_c + SC;        // [SC] this CTA's decoders read the codes (8 warps)
+    uint64_t *dec_full = full_c + 2 * SC;   // [SD] this CTA's decoded tile stored (8 warps)
+    uint64_t *peer_full = dec_full + SD;    // [SD] (CTA 0) CTA 1's decoded tile stored (8 signals)
+    uint64_t *empty_d = dec_full + 2 * SD;  // [SD] the pair's MMAs that read the D slot finished
+    uint64_t *acc_full = dec_full + 3 * SD; // accumulators complete
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *x_issued = reinterpret_cast<volatile int *>(tmem_slot + 2);  // X k-blocks this CTA loaded
@@ -483,19 +490,24 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_consta
             mbar_init(&full_x[s], 2);
             mbar_init(&empty_x[s], 1);
         }
-        for (int s = 0; s < SW; ++s) {
-            mbar_init(&full_w[s], 2);
+        for (int s = 0; s < SC; ++s) {
+            mbar_init(&full_c[s], 2);
+            mbar_init(&empty_c[s], 8);
+        }
+        for (int s = 0; s < SD; ++s) {
             mbar_init(&dec_full[s], 8);
             mbar_init(&peer_full[s], 1);
-            mbar_init(&empty_w[s], 1);
+            mbar_init(&empty_d[s], 1);
         }
         mbar_init(acc_full, 1);
         *abort_flag = 0;
         *x_issued = 0;
         *x_taken = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        // first use of each peer_full: its one arrival, and the signal bytes to wait for
+        for (int s = 0; s < SD; ++s) mbar_arrive_expect_tx(&peer_full[s], SIG_BYTES);
     }
-    cluster_sync_all();  // both CTAs' barriers exist before either arrives remotely
+    cluster_sync_all();  // both CTAs' barriers exist before either signals remotely
     if (warp == 1) {
         // one warp of each CTA allocates the pair's columns together
         asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -530,10 +542,9 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_consta
             *x_issued = issued;
         }
     } else if (warp == 0) {
-        // ---------------- W producer: codes by TMA (lane 0), block scales
+        // ---------------- codes producer: codes by TMA (lane 0), block scales
         // (whole warp, QMM_SPF k-blocks in flight).  The scales come through
-        // shared memory so that the decoders hold no global loads in flight
-        // when they release their stores.
+        // shared memory so that the decoders hold no global loads in flight.
         const size_t srow_bytes = (size_t)KB * SPK;
         const uint8_t *sbase = a.scales + (size_t)(n0 + 128 * (int)rank + lane) * srow_bytes;
         uint32_t pv[QMM_SPF][4];
@@ -549,17 +560,17 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_consta
             for (int j = 0; j < QMM_SPF; ++j) {
                 const int kb = kb0 + j;
                 if (kb >= KB) break;
-                const int s = kb % SW;
+                const int s = kb % SC;
                 int ok = 1;
-                if (lane == 0 && kb >= SW) ok = mbar_wait(&empty_w[s], ((kb / SW) - 1) & 1, abort_flag, a.wait_ns);
+                if (lane == 0 && kb >= SC) ok = mbar_wait(&empty_c[s], ((kb / SC) - 1) & 1, abort_flag, a.wait_ns);
                 if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
                     go = false;
                     break;
                 }
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&full_w[s], QG::C_BYTES);
+                    mbar_arrive_expect_tx(&full_c[s], QG::C_BYTES);
                     tma_load_2d(cring + s * QG::C_BYTES, &tmap_c, kb * QG::CODE_ROW, n0 + 128 * (int)rank,
-                                &full_w[s]);
+                                &full_c[s]);
                 }
                 uint8_t *sc = sring + s * QG::SC_BYTES;
 #pragma unroll
@@ -568,7 +579,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_consta
                     else *reinterpret_cast<uint16_t *>(sc + 2 * (lane + 32 * i)) = (uint16_t)pv[j][i];
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&full_w[s]);
+                if (lane == 0) mbar_arrive(&full_c[s]);
                 issued = kb + 1;
                 if (kb + QMM_SPF < KB)
 #pragma unroll
@@ -578,64 +589,50 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_consta
         }
         // drain: every issued codes TMA must land before the CTA may exit
         if (lane == 0)
-            for (int kb = (issued > SW ? issued - SW : 0); kb < issued; ++kb)
-                mbar_wait(&full_w[kb % SW], (kb / SW) & 1, abort_flag, a.wait_ns, false);
+            for (int kb = (issued > SC ? issued - SC : 0); kb < issued; ++kb)
+                mbar_wait(&full_c[kb % SC], (kb / SC) & 1, abort_flag, a.wait_ns, false);
     } else if (warp == 1) {
         if (rank == 0 && lane == 0) {
             // ---------------- MMA issuer (CTA 0)
             constexpr uint32_t idesc = qmm_idesc();
             int taken = 0;
             for (int kb = 0; kb < KB; ++kb) {
-                const int sx = kb % SX, sw = kb % SW;
+                const int sx = kb % SX, sd = kb % SD;
                 if (!mbar_wait(&full_x[sx], (kb / SX) & 1, abort_flag, a.wait_ns)) break;
                 taken = kb + 1;
-                if (!mbar_wait(&dec_full[sw], (kb / SW) & 1, abort_flag, a.wait_ns)) break;
-                if (!mbar_wait(&peer_full[sw], (kb / SW) & 1, abort_flag, a.wait_ns)) break;
+                if (!mbar_wait(&dec_full[sd], (kb / SD) & 1, abort_flag, a.wait_ns)) break;
+                if (!mbar_wait(&peer_full[sd], (kb / SD) & 1, abort_flag, a.wait_ns)) break;
+                // arm the slot's next use: its arrival, and the signal bytes to wait for
+                mbar_arrive_expect_tx(&peer_full[sd], SIG_BYTES);
                 tc_fence_after();
                 const uint32_t xa = smem_u32(xring + sx * QG::X_STAGE);
-                const uint32_t wa = smem_u32(wring + sw * QMM_W_BYTES);
+                const uint32_t da = smem_u32(dring + sd * QMM_W_BYTES);
 #pragma unroll
                 for (int kk = 0; kk < QMM_BK / 16; ++kk) {
-                    const uint64_t bd = sw128_desc(wa + kk * 32);
+                    const uint64_t bd = sw128_desc(da + kk * 32);
                     const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
 #pragma unroll
                     for (int h = 0; h < NACC; ++h)
                         umma2_bf16(tmem + h * QMM_BN, sw128_desc(xa + h * QMM_X_BYTES + kk * 32), bd, idesc, acc);
                 }
                 umma2_commit_both(&empty_x[sx]);
-                umma2_commit_both(&empty_w[sw]);
+                umma2_commit_both(&empty_d[sd]);
             }
             umma2_commit_both(acc_full);  // fires once every MMA issued so far has completed
             *x_taken = taken;
-        } else if (rank == 1 && lane == 0) {
-            // ---------------- relay (CTA 1): pass the completion of this CTA's
-            // decoded tiles to CTA 0.  The decoders release their stores at
-            // CTA scope; one cluster-scope fence per batch of completed slots
-            // then makes them visible to the pair's MMA issuer.  (A cluster-
-            // scope release in every decoder warp stalls each of them on the
-            // fence for every k-block.)
-            const uint32_t peer0 = map_to_cta(smem_u32(peer_full), 0);
-            int kb = 0;
-            while (kb < KB) {
-                if (!mbar_wait(&dec_full[kb % SW], (kb / SW) & 1, abort_flag, a.wait_ns)) break;
-                int end = kb + 1;
-                while (end < KB && end < kb + SW && mbar_try_wait(&dec_full[end % SW], (end / SW) & 1)) ++end;
-                fence_acq_rel_cluster();
-                for (int k = kb; k < end; ++k) mbar_arrive_relaxed_cluster(peer0 + 8u * (uint32_t)(k % SW));
-                kb = end;
-            }
         }
     } else {
         // ---------------- decoders (warps 2..9): thread d decodes half (d & 1)
-        // of weight row n0 + 128 rank + (d >> 1)
+        // of weight row n0 + 128 rank + (d >> 1).  CTA 0's decoders arrive on
+        // their own barrier; CTA 1's signal CTA 0 with a 16-byte bulk copy.
         const int d = threadIdx.x - 64;
         const int row = d >> 1, half = d & 1;
+        const uint32_t sig0 = map_to_cta(smem_u32(sig + 16 * (warp - 2)), 0);
+        const uint32_t pf0 = map_to_cta(smem_u32(peer_full), 0);
         for (int kb = 0; kb < KB; ++kb) {
-            const int s = kb % SW;
-            // the codes' TMA was issued after the MMAs released the slot, so
-            // its arrival also means the decoded-tile slot is free
-            if (!mbar_wait(&full_w[s], (kb / SW) & 1, abort_flag, a.wait_ns)) break;
-            const uint8_t *cp = cring + s * QG::C_BYTES + row * QG::CODE_ROW + half * (QG::CODE_ROW / 2);
+            const int sc = kb % SC, sd = kb % SD;
+            if (!mbar_wait(&full_c[sc], (kb / SC) & 1, abort_flag, a.wait_ns)) break;
+            const uint8_t *cp = cring + sc * QG::C_BYTES + row * QG::CODE_ROW + half * (QG::CODE_ROW / 2);
             uint32_t w[FMT == FMT_MXFP8 ? 8 : 4];
             if constexpr (FMT == FMT_MXFP8) {
                 // the two 16-byte reads in a row-dependent order spread a
@@ -650,12 +647,22 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_consta
                 const uint4 v = *reinterpret_cast<const uint4 *>(cp);
                 w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
             }
-            const uint8_t *scp = sring + s * QG::SC_BYTES + SPK * row + (SPK / 2) * half;
+            const uint8_t *scp = sring + sc * QG::SC_BYTES + SPK * row + (SPK / 2) * half;
             const uint32_t sbits = SPK == 4 ? *reinterpret_cast<const uint16_t *>(scp) : *scp;
-            qhalf_store<FMT>(w, sbits, wring + s * QMM_W_BYTES + row * 128, half, row & 7);
+            // the codes slot may be refilled (by TMA) once every warp has read it
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&dec_full[s]);
+            if (lane == 0) mbar_arrive(&empty_c[sc]);
+            // the decoded slot is free once the pair's MMAs of k-block kb - SD finished
+            if (kb >= SD && !mbar_wait(&empty_d[sd], ((kb / SD) - 1) & 1, abort_flag, a.wait_ns)) break;
+            uint8_t *dslot = dring + sd * QMM_W_BYTES;
+            qhalf_store<FMT>(w, sbits, dslot + row * 128, half, row & 7);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                if (rank == 0) mbar_arrive(&dec_full[sd]);
+                else bulk_signal(sig0, dslot + 16 * (warp - 2), pf0 + 8u * (uint32_t)sd);
+            }
         }
     }
 
@@ -682,6 +689,9 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_consta
             if (kb >= i1) mbar_arrive_expect_tx_cluster(smem_u32(&full_x[s]), 0);
             mbar_wait(&full_x[s], (kb / SX) & 1, abort_flag, a.wait_ns, false);
         }
+        // CTA 1's 16-byte signals issued before it stopped land within
+        // microseconds; give them that long before this CTA may exit
+        __nanosleep(20000);
     }
     if (warp >= 2 && warp <= 9) {
         const bool ok = acc_ok && !aborted;
@@ -780,9 +790,10 @@ static cudaError_t run_qmm(const DeviceState &ds, cudaStream_t st, const CUtenso
 }
 
 // Pair tiles of 512 rows halve each SM's decode and shared-memory writes per
-// flop against 256-row tiles, but come in half as many; take them unless the
-// coarser wave quantisation costs more (a 512-row tile taken as 1.85 times a
-// 256-row one; num_sms / 2 pairs per wave).
+// flop against 256-row tiles but come in half as many; take them unless the
+// coarser wave quantisation costs more.  On GB300 a 256-row tile takes about
+// 0.83 times as long as a 512-row one (M = 4096, N = 28672, K = 8192: 85 us
+// against 102 us per wave of num_sms / 2 pairs).
 static int qmm_nacc(const DeviceState &ds, int M, int N)
 {
     if (M <= 256) return 1;
@@ -790,7 +801,7 @@ static int qmm_nacc(const DeviceState &ds, int M, int N)
     const long long p1 = (long long)((M + 255) / 256) * (N / QMM_BN);
     const long long p2 = (long long)((M + 511) / 512) * (N / QMM_BN);
     const long long w1 = (p1 + slots - 1) / slots, w2 = (p2 + slots - 1) / slots;
-    return w2 * 185 <= w1 * 100 ? 2 : 1;
+    return w2 * 120 <= w1 * 100 ? 2 : 1;
 }
 
 template <int FMT>
