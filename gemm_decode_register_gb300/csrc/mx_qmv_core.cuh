@@ -88,9 +88,16 @@ __device__ __forceinline__ void stage_store(uint16_t *xs, int ks, int r, int k0,
     }
 }
 
-template <int FMT>
+struct NoMid {
+    __device__ void operator()() const {}
+};
+
+// mid() runs once the activation loads are in flight and before they are
+// used: a caller issues its weight copies there, so that the activations do
+// not queue behind them in the memory system.
+template <int FMT, class Mid = NoMid>
 __device__ void stage_x(const uint16_t *__restrict__ x, size_t ld, int len, int nrows, const int *src,
-                        uint16_t *xs, int ks, int *sh, unsigned *maxbits)
+                        uint16_t *xs, int ks, int *sh, unsigned *maxbits, const Mid &mid = Mid())
 {
     for (int r = threadIdx.x; r < nrows; r += blockDim.x) maxbits[r] = 0u;
     __syncthreads();
@@ -98,6 +105,7 @@ __device__ void stage_x(const uint16_t *__restrict__ x, size_t ld, int len, int 
     const int total = nrows * cpr;
     const bool in_regs = total <= (int)blockDim.x * STAGE_REG_CHUNKS && (len % 8) == 0 && (ld % 8) == 0;
     uint4 cache[STAGE_REG_CHUNKS];
+    if (!in_regs) mid();
     // pass 1: largest magnitude per row (as bf16 bits; NaN > inf > finite)
     for (int r = 0; r < nrows && !in_regs; ++r) {
         const uint32_t *row = reinterpret_cast<const uint32_t *>(x + (size_t)(src ? src[r] : r) * ld);
@@ -109,15 +117,23 @@ __device__ void stage_x(const uint16_t *__restrict__ x, size_t ld, int len, int 
         if (m) atomicMax(&maxbits[r], m);
     }
     if (in_regs) {
-        // one read: each thread caches its chunks and reduces per row
+        // one read: each thread caches its chunks, then reduces per row
 #pragma unroll
         for (int j = 0; j < STAGE_REG_CHUNKS; ++j) {
             const int idx = threadIdx.x + j * blockDim.x;
             cache[j] = make_uint4(0u, 0u, 0u, 0u);
             if (idx < total) {
                 const int r = idx / cpr, k0 = (idx - r * cpr) * 8;
+                if (k0 < len) cache[j] = *reinterpret_cast<const uint4 *>(x + (size_t)(src ? src[r] : r) * ld + k0);
+            }
+        }
+        mid();
+#pragma unroll
+        for (int j = 0; j < STAGE_REG_CHUNKS; ++j) {
+            const int idx = threadIdx.x + j * blockDim.x;
+            if (idx < total) {
+                const int r = idx / cpr, k0 = (idx - r * cpr) * 8;
                 if (k0 < len) {
-                    cache[j] = *reinterpret_cast<const uint4 *>(x + (size_t)(src ? src[r] : r) * ld + k0);
                     const uint4 v = cache[j];
                     unsigned m = max(max(v.x & 0x7FFFu, (v.x >> 16) & 0x7FFFu), max(v.y & 0x7FFFu, (v.y >> 16) & 0x7FFFu));
                     m = max(m, max(max(v.z & 0x7FFFu, (v.z >> 16) & 0x7FFFu), max(v.w & 0x7FFFu, (v.w >> 16) & 0x7FFFu)));

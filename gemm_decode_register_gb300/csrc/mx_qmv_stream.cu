@@ -268,10 +268,13 @@ struct Streamer {
         slot_issue = slot_issue + 1 == G::STAGES ? 0 : slot_issue + 1;
     }
 
-    __device__ __forceinline__ void prime()
+    // Issue `n` of the STAGES - 1 stages in flight when the stream starts
+    // (n over all calls before run() adds up to STAGES - 1).
+    __device__ __forceinline__ void prime(int n = G::STAGES - 1)
     {
 #pragma unroll
-        for (int s = 0; s < G::STAGES - 1; ++s) issue();
+        for (int s = 0; s < G::STAGES - 1; ++s)
+            if (s < n) issue();
     }
 
     // xrow_of(i): the lane's activation row for unit i; done(i, acc): the
@@ -379,10 +382,14 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) qmv_stream_kernel(QmvSArgs a)
     pdl_trigger();
     uint8_t *ring = rings + (size_t)warp * G::STAGES * G::STAGE_BYTES;
     Streamer<FMT, MC, decltype(next)> st(next, n_my, ring, a.N, RB, KS);
-    st.prime();  // weight copies overlap the previous kernel's tail and the staging below
+    // One stage of weight copies overlaps the previous kernel's tail; the
+    // rest is issued once the activation loads are in flight (behind a
+    // ring's worth of weight copies the activations take microseconds
+    // longer to arrive).
+    st.prime(1);
     pdl_wait();
     stage_x<FMT>(a.x + (size_t)a.m0 * a.K + (size_t)xu0 * 32, (size_t)a.K, len, a.mc, nullptr, xs, a.ks, sh,
-                 maxbits);
+                 maxbits, [&]() { st.prime(G::STAGES - 2); });
     __syncthreads();
     st.run(xrow_of, done, ring, xs, a.ks, xu0);
     __syncthreads();
