@@ -618,9 +618,6 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) moe_stream_kernel(MoeSArgs a)
             for (int n = threadIdx.x; n < a.N; n += blockDim.x) a.y[(size_t)p * a.N + n] = __int_as_float(0x7FC00000);
         }
     }
-    stage_x<FMT>(a.x, (size_t)a.K, a.K, a.T, nullptr, xs, a.ks, sh, maxbits);
-    __syncthreads();
-
     const int tiles = (a.N + G::RT - 1) / G::RT;
     const int items = nwg * tiles;
     const int warp = threadIdx.x >> 5;
@@ -673,7 +670,9 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) moe_stream_kernel(MoeSArgs a)
     };
     uint8_t *ring = rings + (size_t)warp * G::STAGES * G::STAGE_BYTES;
     Streamer<FMT, MC, decltype(next)> st(next, n_my, ring, a.N, RB, KS);
-    st.prime();
+    // weight copies are issued once the activation loads are in flight
+    stage_x<FMT>(a.x, (size_t)a.K, a.K, a.T, nullptr, xs, a.ks, sh, maxbits, [&]() { st.prime(); });
+    __syncthreads();
     st.run(xrow_of, done, ring, xs, a.ks, 0);
 }
 
