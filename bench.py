@@ -371,9 +371,15 @@ def extras(torch, ops, synth, dev, stream, hbm, bf16_burst, bf16_sust, args):
             ops.moe_qmv(F4, d1, e1, x, ids_dev[i], E, 2 * I, y=gu)
             ops.moe_qmv(F4, d2, e2, h, ids_flat[i], E, H, y=yd)
 
+        hf = torch.empty((T, topk, I), dtype=torch.bfloat16, device=dev)
+
+        def fused(i):
+            ops.moe_gate_up_swiglu(F4, d1, e1, x, ids_dev[i], E, I, h=hf)
+            ops.moe_down_combine(F4, d2, e2, hf.view(T * topk, I), ids_dev[i], r, E, H, out=out)
+
         # one CUDA graph per variant holds nsets layers, each with its own routing
         graphs = {}
-        for name, fn in (("layer", layer), ("gemv", gemv_only)):
+        for name, fn in (("layer", layer), ("gemv", gemv_only), ("fused", fused)):
             def allsets(fn=fn):
                 for i in range(nsets):
                     fn(i)
@@ -381,11 +387,14 @@ def extras(torch, ops, synth, dev, stream, hbm, bf16_burst, bf16_sust, args):
         reps = max(4, iters // 8)
         t = time_region(torch, graphs["layer"].replay, reps, stream) / nsets
         t2 = time_region(torch, graphs["gemv"].replay, reps, stream) / nsets
+        tf = time_region(torch, graphs["fused"].replay, reps, stream) / nsets
         ub = statistics.mean(uniq) * per_expert
-        res[f"moe_layer_T{T}"] = {"tok_s": round(T / t, 1), "us_layer": round(t * 1e6, 2),
-                                  "us_gemv_only": round(t2 * 1e6, 2),
-                                  "unique_expert_gbs": round(ub / t2 / 1e9, 1),
-                                  "frac_hbm_gemv": round(ub / t2 / 1e9 / hbm, 4),
+        res[f"moe_layer_T{T}"] = {"tok_s": round(T / tf, 1), "us_layer": round(tf * 1e6, 2),
+                                  "unique_expert_gbs": round(ub / tf / 1e9, 1),
+                                  "frac_hbm": round(ub / tf / 1e9 / hbm, 4),
+                                  "path": "mx_moe_gate_up_swiglu + mx_moe_down_combine (2 launches)",
+                                  "tok_s_unfused": round(T / t, 1), "us_layer_unfused": round(t * 1e6, 2),
+                                  "us_gemv_only_unfused": round(t2 * 1e6, 2),
                                   "mean_unique_experts": round(statistics.mean(uniq), 2),
                                   "note": "CUDA graph of 64 layers, each with freshly drawn expert ids"}
     del d1, e1, d2, e2

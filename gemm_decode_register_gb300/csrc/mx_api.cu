@@ -95,6 +95,51 @@ extern "C" int mx_moe_qmv(int fmt, const void *expert_codes, const void *expert_
     return finish(e);
 }
 
+extern "C" int mx_moe_gate_up_swiglu(int fmt, const void *expert_codes, const void *expert_scales, const void *x,
+                                     const int32_t *expert_ids, void *h, int T, int E, int topk, int I, int K)
+{
+    if (!fmt_ok(fmt)) return MX_EUNSUPPORTED;
+    if (!expert_codes || !expert_scales || !x || !expert_ids || !h) return MX_EINVAL;
+    if (T <= 0 || E <= 0 || topk <= 0 || I <= 0 || K <= 0 || topk > E || K % block_of(fmt) != 0)
+        return MX_EINVAL;
+    if ((long long)T * topk > MOE_MAX_SLOTS || E > MOE_MAX_EXPERTS || K > QMV_MAX_K || K % 128 != 0)
+        return MX_EUNSUPPORTED;
+    if (!aligned16(expert_codes) || !aligned16(expert_scales) || !aligned16(x) || !aligned16(h) ||
+        (reinterpret_cast<uintptr_t>(expert_ids) & 3u))
+        return MX_EALIGN;
+    DeviceState *ds = device_state();
+    if (!ds) return MX_ECUDA;
+    cudaError_t e = launch_moe_gate_up_swiglu(*ds, t_stream, fmt, static_cast<const uint8_t *>(expert_codes),
+                                              static_cast<const uint8_t *>(expert_scales),
+                                              static_cast<const uint16_t *>(x), expert_ids,
+                                              static_cast<uint16_t *>(h), T, E, topk, I, K);
+    if (e == cudaErrorInvalidValue) return MX_EUNSUPPORTED;
+    return finish(e);
+}
+
+extern "C" int mx_moe_down_combine(int fmt, const void *expert_codes, const void *expert_scales, const void *h,
+                                   const int32_t *expert_ids, const float *router_weights, float *out, int T,
+                                   int E, int topk, int N, int K)
+{
+    if (!fmt_ok(fmt)) return MX_EUNSUPPORTED;
+    if (!expert_codes || !expert_scales || !h || !expert_ids || !router_weights || !out) return MX_EINVAL;
+    if (T <= 0 || E <= 0 || topk <= 0 || N <= 0 || K <= 0 || topk > E || K % block_of(fmt) != 0)
+        return MX_EINVAL;
+    if ((long long)T * topk > MOE_MAX_SLOTS || E > MOE_MAX_EXPERTS || K > QMV_MAX_K || K % 128 != 0)
+        return MX_EUNSUPPORTED;
+    if (!aligned16(expert_codes) || !aligned16(expert_scales) || !aligned16(h) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(expert_ids) & 3u) || (reinterpret_cast<uintptr_t>(router_weights) & 3u))
+        return MX_EALIGN;
+    DeviceState *ds = device_state();
+    if (!ds) return MX_ECUDA;
+    cudaError_t e = launch_moe_down_combine(*ds, t_stream, fmt, static_cast<const uint8_t *>(expert_codes),
+                                            static_cast<const uint8_t *>(expert_scales),
+                                            static_cast<const uint16_t *>(h), expert_ids, router_weights, out, T,
+                                            E, topk, N, K);
+    if (e == cudaErrorInvalidValue) return MX_EUNSUPPORTED;
+    return finish(e);
+}
+
 extern "C" int mx_qmm(int fmt, const void *codes, const void *scales, const void *X, void *Y, int M,
                       int N, int K)
 {

@@ -180,6 +180,20 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// ---------------------------------------------------------- activation
+
+// SwiGLU of one (gate, up) pair rounded to bf16 (bits in the low half):
+// bf16(silu(g) * u) in fp32 arithmetic, silu(v) = v * sigmoid(v) with the
+// sigmoid evaluated from e = exp(-|v|) (CUDA's expf, never overflows) as
+// 1 / (1 + e) for v >= 0 and e / (1 + e) below, correctly rounded division.
+__device__ __forceinline__ uint32_t swiglu_bf16(float g, float u)
+{
+    const float e = expf(-fabsf(g));
+    const float sig = __fdiv_rn(g >= 0.0f ? 1.0f : e, __fadd_rn(1.0f, e));
+    const float p = __fmul_rn(__fmul_rn(g, sig), u);
+    return f32x2_to_bf16x2(p, 0.0f) & 0xFFFFu;
+}
+
 // ---------------------------------------------------------- misc
 
 __device__ __forceinline__ void set_device_error(int *err, int bits)

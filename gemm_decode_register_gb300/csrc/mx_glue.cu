@@ -76,10 +76,7 @@ cudaError_t launch_dequant(const DeviceState &ds, cudaStream_t st, int fmt, cons
     return launch_k(dequant_kernel<FMT_NVFP4>, dim3((unsigned)blocks), dim3(256), 0, st, codes, scales, W, N, K);
 }
 
-// h = bf16(silu(gate) * up), fp32 arithmetic: silu(v) = v * sigmoid(v), the
-// sigmoid evaluated from e = exp(-|v|) (CUDA's expf, never overflows) as
-// 1 / (1 + e) for v >= 0 and e / (1 + e) below, with correctly rounded
-// division.
+// h = bf16(silu(gate) * up) (swiglu_bf16).
 __global__ void swiglu_kernel(const float *__restrict__ gu, uint16_t *__restrict__ h, int Q, int I)
 {
     pdl_trigger();
@@ -88,11 +85,7 @@ __global__ void swiglu_kernel(const float *__restrict__ gu, uint16_t *__restrict
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
          i += (size_t)gridDim.x * blockDim.x) {
         const size_t q = i / I, j = i - q * I;
-        const float gv = gu[q * 2 * I + j], uv = gu[q * 2 * I + I + j];
-        const float e = expf(-fabsf(gv));
-        const float sig = __fdiv_rn(gv >= 0.0f ? 1.0f : e, __fadd_rn(1.0f, e));
-        const float p = __fmul_rn(__fmul_rn(gv, sig), uv);
-        h[i] = (uint16_t)(f32x2_to_bf16x2(p, 0.0f) & 0xFFFFu);
+        h[i] = (uint16_t)swiglu_bf16(gu[q * 2 * I + j], gu[q * 2 * I + I + j]);
     }
 }
 

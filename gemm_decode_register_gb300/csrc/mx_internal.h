@@ -44,6 +44,12 @@ cudaError_t launch_swiglu(const DeviceState &ds, cudaStream_t st, const float *g
                           int Q, int I);
 cudaError_t launch_moe_combine(const DeviceState &ds, cudaStream_t st, const float *yd,
                                const float *r, float *out, int T, int topk, int N);
+cudaError_t launch_moe_gate_up_swiglu(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,
+                                      const uint8_t *scales, const uint16_t *x, const int32_t *ids, uint16_t *h,
+                                      int T, int E, int topk, int I, int K);
+cudaError_t launch_moe_down_combine(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,
+                                    const uint8_t *scales, const uint16_t *h, const int32_t *ids, const float *rw,
+                                    float *out, int T, int E, int topk, int N, int K);
 cudaError_t launch_qmm(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,
                        const uint8_t *scales, const uint16_t *X, uint16_t *Y, int M, int N, int K);
 

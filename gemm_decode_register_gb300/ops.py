@@ -49,6 +49,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "mx_qmv": [I, P, P, P, P, I, I, I],
             "mx_qmv_noalloc": [I, P, P, P, P, I, I, I],
             "mx_moe_qmv": [I, P, P, P, P, P, I, I, I, I, I],
+            "mx_moe_gate_up_swiglu": [I, P, P, P, P, P, I, I, I, I, I],
+            "mx_moe_down_combine": [I, P, P, P, P, P, P, I, I, I, I, I],
             "mx_qmm": [I, P, P, P, P, I, I, I],
             "mx_set_stream": [P],
             "mx_dequant": [I, P, P, P, I, I],
@@ -125,6 +127,34 @@ def moe_qmv(fmt: int, codes: torch.Tensor, scales: torch.Tensor, x: torch.Tensor
     _check("mx_moe_qmv", load().mx_moe_qmv(fmt, _ptr(codes), _ptr(scales), _ptr(x),
                                            _ptr(expert_ids), _ptr(y), T, E, topk, N, K))
     return y
+
+
+def moe_gate_up_swiglu(fmt: int, codes: torch.Tensor, scales: torch.Tensor, x: torch.Tensor,
+                       expert_ids: torch.Tensor, E: int, I: int, h: torch.Tensor | None = None) -> torch.Tensor:
+    """h[T][topk][I] bf16 = SwiGLU of the routed experts' gate and up rows."""
+    T, K = x.shape
+    topk = expert_ids.shape[1]
+    if h is None:
+        h = torch.empty((T, topk, I), dtype=torch.bfloat16, device=x.device)
+    _stream()
+    _check("mx_moe_gate_up_swiglu", load().mx_moe_gate_up_swiglu(fmt, _ptr(codes), _ptr(scales), _ptr(x),
+                                                                 _ptr(expert_ids), _ptr(h), T, E, topk, I, K))
+    return h
+
+
+def moe_down_combine(fmt: int, codes: torch.Tensor, scales: torch.Tensor, h: torch.Tensor,
+                     expert_ids: torch.Tensor, router_weights: torch.Tensor, E: int, N: int,
+                     out: torch.Tensor | None = None) -> torch.Tensor:
+    """out[T][N] fp32 = router-weighted sum of the routed experts' down rows."""
+    T, topk = expert_ids.shape
+    K = h.shape[-1]
+    if out is None:
+        out = torch.empty((T, N), dtype=torch.float32, device=h.device)
+    _stream()
+    _check("mx_moe_down_combine", load().mx_moe_down_combine(fmt, _ptr(codes), _ptr(scales), _ptr(h),
+                                                             _ptr(expert_ids), _ptr(router_weights), _ptr(out),
+                                                             T, E, topk, N, K))
+    return out
 
 
 def qmm(fmt: int, codes: torch.Tensor, scales: torch.Tensor, X: torch.Tensor, N: int,

@@ -92,11 +92,45 @@ int mx_qmv(int fmt, const void *codes, const void *scales, const void *x, float 
  * above); x bf16 [T][K]; expert_ids int32 [T][topk]; y fp32 [T][topk][N].
  * Slots that share an expert are served by one pass over that expert's
  * weights.  The routing is read on the device (no host copy).  T*topk <=
- * 4096.  An id outside [0, E) sets MX_DEVERR_BAD_EXPERT and fills that
+ * 1024, E <= 4096.  An id outside [0, E) sets MX_DEVERR_BAD_EXPERT and fills that
  * slot's N outputs with NaN.  For the down projection call with T' = T*topk
  * rows of x, topk = 1 and the ids flattened to [T*topk][1]. */
 int mx_moe_qmv(int fmt, const void *expert_codes, const void *expert_scales, const void *x,
                const int32_t *expert_ids, float *y, int T, int E, int topk, int N, int K);
+
+/* Fused MoE FFN, first half: gate and up projections of the routed experts
+ * with the SwiGLU applied as the outputs are formed (the pages' fused
+ * gate-up path: manual page "Building from source", ROCm status table, and
+ * release post, section "MoE decode": a gate-up kernel and a down kernel
+ * per layer):
+ *   h[t][j][i] = bf16_rne( silu(g) * u ),  g = sum_k x[t][k] * W_e[i][k],
+ *                                          u = sum_k x[t][k] * W_e[I + i][k],
+ * e = expert_ids[t][j].  Each expert's weight is [2I][K]: rows 0..I-1 gate,
+ * rows I..2I-1 up (NVFP4: E fp32 tensor scales after the whole
+ * [E][2I][K/16] scale block).  x bf16 [T][K]; h bf16 [T][topk][I].  silu and
+ * the rounding are those of mx_swiglu, so h equals mx_swiglu applied to
+ * mx_moe_qmv's output with N = 2I.  K must be a multiple of 128 (else
+ * MX_EUNSUPPORTED); other limits and the bad-id behaviour (h rows NaN) as in
+ * mx_moe_qmv.  codes, scales, x, h 16-byte aligned; ids 4-byte aligned. */
+int mx_moe_gate_up_swiglu(int fmt, const void *expert_codes, const void *expert_scales, const void *x,
+                          const int32_t *expert_ids, void *h, int T, int E, int topk, int I, int K);
+
+/* Fused MoE FFN, second half: down projection of each routed slot and the
+ * router-weighted sum over the token's slots:
+ *   out[t][n] = sum_j r[t][j] * ( sum_k h[t*topk + j][k] * W_e[n][k] ),
+ * e = expert_ids[t][j], summed over j in increasing order with fused
+ * multiply-adds (as mx_moe_combine).  Expert weights [N][K]; h bf16
+ * [T*topk][K] (mx_moe_gate_up_swiglu's output, K = I); r fp32 [T][topk];
+ * out fp32 [T][N].  Slots that share an expert are served by one pass over
+ * its weights; the per-slot partial sums go through the library's device
+ * workspace (T*topk*N <= 4 Mi floats), whose counters are re-armed by the
+ * call itself.  A bad id sets MX_DEVERR_BAD_EXPERT and makes that token's
+ * outputs NaN.  K a multiple of 128; h, out, codes, scales 16-byte aligned,
+ * ids and r 4-byte aligned.  Calls that use the workspace (this one and
+ * mx_qmv) must not run concurrently on one device. */
+int mx_moe_down_combine(int fmt, const void *expert_codes, const void *expert_scales, const void *h,
+                        const int32_t *expert_ids, const float *router_weights, float *out, int T, int E,
+                        int topk, int N, int K);
 
 /* Prefill GEMM over the same weights (release post, section "Decoding
  * block-float formats in software": dequantise on the GPU and multiply on

@@ -1,0 +1,197 @@
+"""Fused MoE FFN kernels on the GPU: mx_moe_gate_up_swiglu (gate and up
+rows of each routed expert with the SwiGLU in the epilogue) and
+mx_moe_down_combine (down rows with the router-weighted sum over a token's
+slots), against the oracle chain and against the unfused GPU path."""
+import numpy as np
+import pytest
+
+from gemm_decode_register_gb300 import synth
+from gpu_util import bf16_bits_to_f64, bf16_host, check_close, dev_bf16, dev_i32, dev_u8, need_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def fused_gate_up(fmt, codes, scales, x, ids, E, I):
+    from gemm_decode_register_gb300 import ops
+
+    return ops.moe_gate_up_swiglu(fmt, dev_u8(codes), dev_u8(scales), dev_bf16(x), dev_i32(ids), E, I)
+
+
+def fused_down(fmt, codes, scales, h, ids, r, E, N):
+    import torch
+    from gemm_decode_register_gb300 import ops
+
+    hd = h if isinstance(h, torch.Tensor) else dev_bf16(h)
+    return ops.moe_down_combine(fmt, dev_u8(codes), dev_u8(scales), hd.reshape(-1, hd.shape[-1]).contiguous(),
+                                dev_i32(ids), torch.from_numpy(np.ascontiguousarray(r, np.float32)).cuda(), E, N)
+
+
+def oracle_h(orc, fmt, codes, scales, x, ids, T, E, topk, I, K):
+    gu, rc = orc.moe_qmv(fmt, codes, scales, x, ids, T, E, topk, 2 * I, K)
+    assert rc == 0
+    return orc.swiglu_bf16(gu.reshape(T * topk, 2 * I), I)
+
+
+def oracle_out(orc, fmt, codes, scales, h_bits, ids, r, T, E, topk, N, K):
+    yd, rc = orc.moe_qmv(fmt, codes, scales, h_bits, ids.reshape(-1, 1), T * topk, E, 1, N, K)
+    assert rc == 0
+    return orc.moe_combine(yd.reshape(T * topk, N), r, T, topk, N)
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_gate_up_swiglu_config(orc, T):
+    """128 experts, top-8, hidden 2048, intermediate 768: h against the
+    oracle (gate/up in fp64, SwiGLU rounded to bf16) within the gate for
+    bf16 outputs, and against the unfused GPU path (mx_moe_qmv, then
+    mx_swiglu) to within one bf16 ulp."""
+    need_gpu()
+    from gemm_decode_register_gb300 import ops
+
+    fmt, E, topk, H, I = 0, 128, 8, 2048, 768
+    codes, scales = synth.weights(fmt, 2 * I, H, 90, E=E)
+    x = synth.activations(T, H, 91 + T)
+    ids = synth.expert_ids(T, E, topk, 92 + T)
+    h = fused_gate_up(fmt, codes, scales, x, ids, E, I)
+    hb = bf16_host(h).reshape(T * topk, I)
+    want = oracle_h(orc, fmt, codes, scales, x, ids, T, E, topk, I, H)
+    check_close(bf16_bits_to_f64(hb), bf16_bits_to_f64(want), f"gate-up swiglu T{T}", bf16_out=True)
+    gu = ops.moe_qmv(fmt, dev_u8(codes), dev_u8(scales), dev_bf16(x), dev_i32(ids), E, 2 * I)
+    h2 = bf16_host(ops.swiglu(gu, I)).reshape(T * topk, I)
+    assert np.abs(hb.astype(np.int32) - h2.astype(np.int32)).max() <= 1
+
+
+@pytest.mark.parametrize("fmt", [0, 1, 2])
+@pytest.mark.parametrize("T,E,topk,I,K", [(3, 5, 2, 37, 256), (9, 4, 3, 64, 128), (2, 7, 7, 19, 384),
+                                         (12, 6, 4, 24, 128)])
+def test_gate_up_swiglu_ragged(orc, fmt, T, E, topk, I, K):
+    """Experts shared across tokens (groups above one slot, groups split at
+    eight), intermediate sizes that leave the last gate/up tile partly
+    empty, and more than 32 slots (block-wide routing)."""
+    need_gpu()
+    codes, scales = synth.weights(fmt, 2 * I, K, T + E + I, E=E)
+    x = synth.activations(T, K, 5 * T)
+    ids = synth.expert_ids(T, E, topk, 6 * T)
+    hb = bf16_host(fused_gate_up(fmt, codes, scales, x, ids, E, I)).reshape(T * topk, I)
+    want = oracle_h(orc, fmt, codes, scales, x, ids, T, E, topk, I, K)
+    check_close(bf16_bits_to_f64(hb), bf16_bits_to_f64(want), f"gate-up fmt{fmt}", bf16_out=True)
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_down_combine_config(orc, T):
+    """down 2048 x 768 over the routed experts, router-weighted sum: against
+    the oracle (fp64 products and sum) and against the unfused GPU path
+    (mx_moe_qmv per slot, then mx_moe_combine)."""
+    need_gpu()
+    import torch
+    from gemm_decode_register_gb300 import ops
+
+    fmt, E, topk, H, I = 0, 128, 8, 2048, 768
+    codes, scales = synth.weights(fmt, H, I, 93, E=E)
+    h = synth.activations(T * topk, I, 94 + T)
+    ids = synth.expert_ids(T, E, topk, 95 + T)
+    r = synth.router_weights(T, topk, 96 + T)
+    out = fused_down(fmt, codes, scales, h, ids, r, E, H).cpu().numpy()
+    want = oracle_out(orc, fmt, codes, scales, h, ids, r, T, E, topk, H, I)
+    check_close(out, want, f"down combine T{T}")
+    yd = ops.moe_qmv(fmt, dev_u8(codes), dev_u8(scales), dev_bf16(h), dev_i32(ids.reshape(-1, 1)), E, H)
+    out2 = ops.moe_combine(yd, torch.from_numpy(r).cuda()).cpu().numpy()
+    check_close(out, out2.astype(np.float64), f"down combine vs unfused T{T}")
+
+
+@pytest.mark.parametrize("fmt", [0, 1, 2])
+@pytest.mark.parametrize("T,E,topk,N,K", [(3, 5, 2, 37, 128), (9, 4, 3, 70, 256), (5, 6, 6, 19, 128),
+                                         (12, 6, 4, 33, 128)])
+def test_down_combine_ragged(orc, fmt, T, E, topk, N, K):
+    need_gpu()
+    codes, scales = synth.weights(fmt, N, K, T + E + N, E=E)
+    h = synth.activations(T * topk, K, 7 * T)
+    ids = synth.expert_ids(T, E, topk, 8 * T)
+    r = synth.router_weights(T, topk, 9 * T)
+    out = fused_down(fmt, codes, scales, h, ids, r, E, N).cpu().numpy()
+    want = oracle_out(orc, fmt, codes, scales, h, ids, r, T, E, topk, N, K)
+    check_close(out, want, f"down combine fmt{fmt}")
+
+
+def test_down_combine_deterministic():
+    """The partial sums are combined in slot order by whichever warp closes a
+    tile: repeated calls give the same bits."""
+    need_gpu()
+    fmt, E, topk, T, N, K = 0, 16, 4, 4, 512, 256
+    codes, scales = synth.weights(fmt, N, K, 31, E=E)
+    h = synth.activations(T * topk, K, 32)
+    ids = synth.expert_ids(T, E, topk, 33)
+    r = synth.router_weights(T, topk, 34)
+    a = fused_down(fmt, codes, scales, h, ids, r, E, N).cpu().numpy()
+    for _ in range(3):
+        b = fused_down(fmt, codes, scales, h, ids, r, E, N).cpu().numpy()
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_fused_ffn_composite(orc, T):
+    """The two fused kernels chained (the MoE FFN in two launches) against
+    the oracle chain."""
+    need_gpu()
+    fmt, E, topk, H, I = 0, 128, 8, 2048, 768
+    c1, s1 = synth.weights(fmt, 2 * I, H, 80, E=E)
+    c2, s2 = synth.weights(fmt, H, I, 81, E=E)
+    x = synth.activations(T, H, 82 + T)
+    ids = synth.expert_ids(T, E, topk, 83 + T)
+    r = synth.router_weights(T, topk, 84 + T)
+    h = fused_gate_up(fmt, c1, s1, x, ids, E, I)
+    out = fused_down(fmt, c2, s2, h, ids, r, E, H).cpu().numpy()
+    h_o = oracle_h(orc, fmt, c1, s1, x, ids, T, E, topk, I, H)
+    out_o = oracle_out(orc, fmt, c2, s2, h_o, ids, r, T, E, topk, H, I)
+    check_close(out, out_o, f"fused moe ffn T{T}")
+
+
+def test_fused_bad_expert_ids(orc):
+    """An id outside [0, E): the gate-up kernel writes NaN for that slot's
+    h row, the down kernel NaN for that token's outputs; the other slots and
+    tokens are unaffected and the device error word records it."""
+    need_gpu()
+    from gemm_decode_register_gb300 import ops
+
+    ops.device_error()  # clear
+    fmt, T, E, topk, I, K, N = 0, 3, 6, 2, 40, 128, 64
+    c1, s1 = synth.weights(fmt, 2 * I, K, 41, E=E)
+    x = synth.activations(T, K, 42)
+    ids = synth.expert_ids(T, E, topk, 43)
+    ids[1, 0] = E + 3
+    hb = bf16_host(fused_gate_up(fmt, c1, s1, x, ids, E, I)).reshape(T * topk, I)
+    assert ops.device_error() & 0x1
+    assert np.all(np.isnan(bf16_bits_to_f64(hb[1 * topk + 0])))
+    good = np.ones(T * topk, bool)
+    good[1 * topk + 0] = False
+    ids_ok = ids.copy()
+    ids_ok[1, 0] = 0
+    want = oracle_h(orc, fmt, c1, s1, x, ids_ok, T, E, topk, I, K)
+    check_close(bf16_bits_to_f64(hb[good]), bf16_bits_to_f64(want[good]), "gate-up good slots", bf16_out=True)
+
+    c2, s2 = synth.weights(fmt, N, K, 44, E=E)
+    h = synth.activations(T * topk, K, 45)
+    r = synth.router_weights(T, topk, 46)
+    out = fused_down(fmt, c2, s2, h, ids, r, E, N).cpu().numpy()
+    assert ops.device_error() & 0x1
+    assert np.all(np.isnan(out[1]))
+    want = oracle_out(orc, fmt, c2, s2, h, ids_ok, r, T, E, topk, N, K)
+    check_close(out[[0, 2]], want[[0, 2]], "down good tokens")
+    # every id bad: no work group at all, every output NaN
+    bad = np.full((T, topk), -1, np.int32)
+    out = fused_down(fmt, c2, s2, h, bad, r, E, N).cpu().numpy()
+    assert ops.device_error() & 0x1
+    assert np.all(np.isnan(out))
+
+
+def test_fused_rejects_unsupported_k():
+    """K not a multiple of 128 has no fused kernel: MX_EUNSUPPORTED."""
+    need_gpu()
+    from gemm_decode_register_gb300 import ops
+
+    fmt, T, E, topk, I, K = 0, 1, 4, 2, 16, 96
+    c1, s1 = synth.weights(fmt, 2 * I, K, 47, E=E)
+    x = synth.activations(T, K, 48)
+    ids = synth.expert_ids(T, E, topk, 49)
+    with pytest.raises(ops.MxError) as ei:
+        fused_gate_up(fmt, c1, s1, x, ids, E, I)
+    assert ei.value.status == -2
