@@ -508,9 +508,12 @@ CASES = {
     "qmv_mxfp8_m1": ("qmv", 1, 1, 57344, 8192),
     "qmv_nvfp4_m1": ("qmv", 2, 1, 57344, 8192),
     "moe_gateup_t4": ("moe", 0, 4, 1536, 2048),
+    "moe_ffn_t1": ("moe_ffn", 0, 1, 2048, 768),  # fused gate-up/SwiGLU + down/combine, hidden 2048, I 768
+    "moe_ffn_t4": ("moe_ffn", 0, 4, 2048, 768),
     "qmm_up": ("qmm", 0, 4096, 28672, 8192),
     "qmm_down": ("qmm", 0, 4096, 8192, 28672),
     "qmm_small": ("qmm", 0, 1024, 4096, 4096),
+    "qmm_mid": ("qmm", 0, 2048, 8192, 4096),
 }
 
 
@@ -525,7 +528,23 @@ def run_case(args):
     b.build()
     kind, fmt, M, N, K = CASES[args.case]
     stream = torch.cuda.current_stream()
-    if kind == "moe":
+    if kind == "moe_ffn":
+        E, topk, H, I = 128, 8, N, K
+        c1, s1 = synth.weights(fmt, 2 * I, H, 40, E=E)
+        c2, s2 = synth.weights(fmt, H, I, 41, E=E)
+        d1, e1, d2, e2 = (upload(torch, a) for a in (c1, s1, c2, s2))
+        ids = torch.from_numpy(synth.expert_ids(M, E, topk, 5)).cuda()
+        r = torch.from_numpy(synth.router_weights(M, topk, 7)).cuda()
+        x = bf16_dev(torch, synth.activations(M, H, 6)).view(M, H)
+        hf = torch.empty((M * topk, I), dtype=torch.bfloat16, device="cuda")
+        out = torch.empty((M, H), dtype=torch.float32, device="cuda")
+
+        def f():
+            ops.moe_gate_up_swiglu(fmt, d1, e1, x, ids, E, I, h=hf)
+            ops.moe_down_combine(fmt, d2, e2, hf, ids, r, E, H, out=out)
+        nu = len(np.unique(ids.cpu().numpy()))
+        wb = (c1.nbytes + s1.nbytes + c2.nbytes + s2.nbytes) / E * nu
+    elif kind == "moe":
         E, topk = 128, 8
         codes, scales = synth.weights(fmt, N, K, 40, E=E)
         c, s = upload(torch, codes), upload(torch, scales)

@@ -99,10 +99,10 @@ int mx_moe_qmv(int fmt, const void *expert_codes, const void *expert_scales, con
                const int32_t *expert_ids, float *y, int T, int E, int topk, int N, int K);
 
 /* Fused MoE FFN, first half: gate and up projections of the routed experts
- * with the SwiGLU applied as the outputs are formed (the pages' fused
- * gate-up path: manual page "Building from source", ROCm status table, and
- * release post, section "MoE decode": a gate-up kernel and a down kernel
- * per layer):
+ * with the SwiGLU applied as the outputs are formed (the pages' fused MoE
+ * decode: manual page "Building from source", ROCm status table, a gate-up
+ * kernel then a down kernel per layer; talk slide 13 "Porting Order Set by
+ * Profiling", the fused-MoE port):
  *   h[t][j][i] = bf16_rne( silu(g) * u ),  g = sum_k x[t][k] * W_e[i][k],
  *                                          u = sum_k x[t][k] * W_e[I + i][k],
  * e = expert_ids[t][j].  Each expert's weight is [2I][K]: rows 0..I-1 gate,
