@@ -173,9 +173,9 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)
 // Programmatic dependent launch: every kernel of this library lets the next
 // kernel on its stream start as soon as it begins (pdl_trigger), and waits
 // for the previous kernel's completion and memory (pdl_wait) before it reads
-// activations, routing or outputs.  Weights (codes, block scales) may be
-// read before the wait: no kernel of this library writes them, and a kernel
-// from elsewhere never triggers early, so it is always complete by then.
+// activations or writes outputs.  Weights (codes, block scales) and MoE
+// expert ids may be read before the wait: no kernel of this library writes
+// them, and the ABI requires them to be complete when a call is issued.
 // Both are no-ops when the launch carries no programmatic dependency.
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

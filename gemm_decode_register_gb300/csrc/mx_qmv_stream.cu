@@ -637,22 +637,17 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) moe_stream_kernel(MoeSArgs a)
     off += (size_t)XR * a.ks * 2;
     uint8_t *rings = smem + off;
 
+    // The routing and the routed experts' weights do not depend on the
+    // previous kernel (no kernel of this library writes expert ids; the
+    // caller's ids are complete when the call is issued): the grouping and
+    // the first weight copies overlap its tail.  Activations and outputs wait.
     pdl_trigger();
-    pdl_wait();  // routing and activations may come from the previous kernel
     RouteSmem rs{cnt, wgs, pos, sorted, wg_e, wg_first, wg_mc, tmp};
     const int nwg = moe_route(a.ids, P, a.E, MC, rs);
-    for (int p = blockIdx.x; p < P; p += gridDim.x) {
-        const int e = a.ids[p];
-        if (e < 0 || e >= a.E) {
-            if (threadIdx.x == 0) set_device_error(a.err, DEVERR_BAD_EXPERT);
-            if (MODE == MOE_PLAIN)
-                for (int n = threadIdx.x; n < a.N; n += blockDim.x) a.y[(size_t)p * a.N + n] = __int_as_float(0x7FC00000);
-            if (MODE == MOE_GATE_UP_SWIGLU)
-                for (int i = threadIdx.x; i < a.I; i += blockDim.x) a.h[(size_t)p * a.I + i] = 0x7FC0u;
-        }
-    }
     if (MODE == MOE_DOWN_COMBINE && nwg == 0) {
         // no valid slot at all: every token's sum has a NaN term
+        pdl_wait();
+        if (blockIdx.x == 0 && threadIdx.x == 0) set_device_error(a.err, DEVERR_BAD_EXPERT);
         for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < (size_t)a.T * a.N;
              i += (size_t)gridDim.x * blockDim.x)
             a.out[i] = __int_as_float(0x7FC00000);
@@ -745,8 +740,20 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) moe_stream_kernel(MoeSArgs a)
     };
     uint8_t *ring = rings + (size_t)warp * G::STAGES * G::STAGE_BYTES;
     Streamer<FMT, MC, decltype(next)> st(next, n_my, ring, R, RB, KS);
-    // weight copies are issued once the activation loads are in flight
-    stage_x<FMT>(a.x, (size_t)a.K, a.K, XR, nullptr, xs, a.ks, sh, maxbits, [&]() { st.prime(); });
+    st.prime(1);
+    pdl_wait();
+    for (int p = blockIdx.x; p < P; p += gridDim.x) {
+        const int e = a.ids[p];
+        if (e < 0 || e >= a.E) {
+            if (threadIdx.x == 0) set_device_error(a.err, DEVERR_BAD_EXPERT);
+            if (MODE == MOE_PLAIN)
+                for (int n = threadIdx.x; n < a.N; n += blockDim.x) a.y[(size_t)p * a.N + n] = __int_as_float(0x7FC00000);
+            if (MODE == MOE_GATE_UP_SWIGLU)
+                for (int i = threadIdx.x; i < a.I; i += blockDim.x) a.h[(size_t)p * a.I + i] = 0x7FC0u;
+        }
+    }
+    // the rest of the weight copies are issued once the activation loads are in flight
+    stage_x<FMT>(a.x, (size_t)a.K, a.K, XR, nullptr, xs, a.ks, sh, maxbits, [&]() { st.prime(G::STAGES - 2); });
     __syncthreads();
     st.run(xrow_of, done, ring, xs, a.ks, 0);
 

@@ -92,7 +92,13 @@ int mx_qmv(int fmt, const void *codes, const void *scales, const void *x, float 
  * above); x bf16 [T][K]; expert_ids int32 [T][topk]; y fp32 [T][topk][N].
  * Slots that share an expert are served by one pass over that expert's
  * weights.  The routing is read on the device (no host copy).  T*topk <=
- * 1024, E <= 4096.  An id outside [0, E) sets MX_DEVERR_BAD_EXPERT and fills that
+ * 1024, E <= 4096.  The ids are read as soon as the kernel starts, before it
+ * waits for the preceding kernel on the stream (the routed experts' weights
+ * start streaming under that kernel's tail): they must be complete when the
+ * call is issued, i.e. not written by a kernel that lets its dependents start
+ * early (no kernel of this library writes expert ids; activations and outputs
+ * do wait).  The same holds for mx_moe_gate_up_swiglu and
+ * mx_moe_down_combine.  An id outside [0, E) sets MX_DEVERR_BAD_EXPERT and fills that
  * slot's N outputs with NaN.  For the down projection call with T' = T*topk
  * rows of x, topk = 1 and the ids flattened to [T*topk][1]. */
 int mx_moe_qmv(int fmt, const void *expert_codes, const void *expert_scales, const void *x,
