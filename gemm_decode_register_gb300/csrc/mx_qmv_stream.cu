@@ -9,13 +9,15 @@
 // registers on them, and each copy instruction moves 512 contiguous bytes.
 //
 // Work is cut into units (2*MC weight rows x a run of K) that each warp
-// streams back to back: the ring runs continuously across units, so short
-// units cost nothing extra and the CTAs stay balanced to within one unit.
-//   * dense: units are (tile, K chunk); the chunks of a tile are summed in a
-//     fixed order in shared memory.  When the tokens' activations do not
-//     fit in shared memory, K is also split across CTAs (windows); the
-//     windows' partial sums go to a device workspace and the last CTA of a
-//     tile group adds them in window order (deterministic).
+// streams back to back: the ring runs continuously across units.
+//   * dense: a CTA's tiles go to its warps whole and round-robin when that
+//     balances them; otherwise the CTA's stages (tile-major) are dealt out
+//     in equal contiguous runs, so a tile's K is cut only where two runs
+//     meet, and the pieces' partial sums are added in K order in shared
+//     memory.  When the tokens' activations do not fit in shared memory, K
+//     is also split across CTAs (windows); the windows' partial sums go to a
+//     device workspace and the last CTA of a tile group adds them in window
+//     order (deterministic).
 //   * MoE: units are (work group of up to MC slots routed to one expert,
 //     tile) over the whole K of that expert.
 #include <algorithm>
@@ -327,9 +329,9 @@ struct QmvSArgs {
     int G;         // CTAs per window
     int nwin;      // K windows
     int WU;        // units per window (multiple of UPS)
-    int wk;        // chunks per tile per window (a power of two)
-    int wk_log2;
-    int CU;        // units per chunk (multiple of UPS)
+    int pmax;      // partial-sum slots per tile (pieces a tile's K may be cut into)
+    int split;     // 0: whole tiles per warp; 1, 2: equal runs of stages per warp,
+                   // a piece's slot 1: (warp - the tile's first warp), 2: its stage offset
     int ntl_max;   // tiles per CTA (upper bound)
     int ks;        // staged row stride (f16 elements)
 };
@@ -346,7 +348,7 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) qmv_stream_kernel(QmvSArgs a)
     int *flag = reinterpret_cast<int *>(maxbits + 8);
     off += 80;
     float *red = reinterpret_cast<float *>(smem + off);
-    off += (((size_t)a.ntl_max * a.wk * G::RT * MC * 4) + 15) & ~(size_t)15;
+    off += (((size_t)a.ntl_max * a.pmax * G::RT * MC * 4) + 15) & ~(size_t)15;
     uint8_t *rings = smem + off;
 
     const int gb = blockIdx.x % a.G, win = blockIdx.x / a.G;
@@ -356,30 +358,65 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) qmv_stream_kernel(QmvSArgs a)
 
     const int warp = threadIdx.x >> 5;
     const int ntl = gb < a.tiles ? (a.tiles - gb + a.G - 1) / a.G : 0;
-    const int nv = ntl * a.wk;
-    const int n_my = warp < nv ? (nv - warp + QMV_WARPS - 1) / QMV_WARPS : 0;
+    // The CTA's work is its tiles' stages in tile-major order (S of them).
+    // Whole tiles go round-robin to the warps when that balances them (many
+    // tiles); otherwise each warp takes an equal contiguous run, so the warps
+    // finish together and a tile's K is cut only where runs meet (cutting
+    // rows finer measured slower).  A piece's partial sums go to a slot of
+    // its tile; the slots are added in K order.
+    const int spw = (xu1 - xu0 + G::UPS - 1) / G::UPS;  // stages per row in this window
+    const long long S = (long long)ntl * spw;
+    long long lo_w = 0, hi_w = 0;
+    int t_first = 0, n_my = 0;
+    if (a.split) {
+        lo_w = S * warp / QMV_WARPS;
+        hi_w = S * (warp + 1) / QMV_WARPS;
+        if (hi_w > lo_w) {
+            t_first = (int)(lo_w / spw);
+            n_my = (int)((hi_w - 1) / spw) - t_first + 1;
+        }
+    } else {
+        t_first = warp;
+        n_my = warp < ntl ? (ntl - warp + QMV_WARPS - 1) / QMV_WARPS : 0;
+    }
     const int RB = FMT == FMT_MXFP8 ? a.K : a.K / 2;
     const int KS = FMT == FMT_NVFP4 ? a.K / 16 : a.K / 32;
     const int tok = lane_token<MC>();
     const int xrow = tok < a.mc ? tok : -1;
 
+    // unit i of this warp: tile t, stages [lo, hi) of the CTA's sequence
+    auto unit_tile = [&](int i) { return a.split ? t_first + i : warp + QMV_WARPS * i; };
     auto next = [&](int i) {
-        const int v = warp + QMV_WARPS * i;
-        const int ti = v >> a.wk_log2, c = v & (a.wk - 1);
+        const int t = unit_tile(i);
         SUnit u;
         u.codes = a.codes;
         u.scales = a.scales;
-        u.row0 = (gb + ti * a.G) * G::RT;
-        u.ub = xu0 + c * a.CU;
-        u.ul = min(xu1, u.ub + a.CU);
-        if (u.ub > u.ul) u.ub = u.ul;
+        u.row0 = (gb + t * a.G) * G::RT;
+        if (a.split) {
+            const long long t0 = (long long)t * spw;
+            const long long lo = lo_w > t0 ? lo_w : t0, hi = hi_w < t0 + spw ? hi_w : t0 + spw;
+            u.ub = xu0 + (int)(lo - t0) * G::UPS;
+            u.ul = min(xu1, xu0 + (int)(hi - t0) * G::UPS);
+        } else {
+            u.ub = xu0;
+            u.ul = xu1;
+        }
         u.jump = MC;
         u.lim = a.N;
         return u;
     };
+    auto slot_of = [&](int i) {
+        if (!a.split) return 0;
+        const long long t0 = (long long)unit_tile(i) * spw;
+        if (lo_w <= t0) return 0;
+        if (a.split == 2) return (int)(lo_w - t0);
+        // the warp whose run holds the tile's first stage
+        const int wf = (int)((QMV_WARPS * (t0 + 1) + S - 1) / S) - 1;
+        return warp - wf;
+    };
     auto xrow_of = [&](int) { return xrow; };
     auto done = [&](int i, const float (&acc)[2][2]) {
-        const int v = warp + QMV_WARPS * i;
+        const size_t v = (size_t)unit_tile(i) * a.pmax + slot_of(i);
         float vv[2][2];
         qmv_warp_reduce<MC>(acc, vv);
 #pragma unroll
@@ -387,7 +424,7 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) qmv_stream_kernel(QmvSArgs a)
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 int r, t;
-                if (tile_out<MC>(h, c, r, t)) red[((size_t)v * G::RT + r) * MC + t] = vv[h][c];
+                if (tile_out<MC>(h, c, r, t)) red[(v * G::RT + r) * MC + t] = vv[h][c];
             }
     };
     pdl_trigger();
@@ -401,6 +438,7 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) qmv_stream_kernel(QmvSArgs a)
     pdl_wait();
     stage_x<FMT>(a.x + (size_t)a.m0 * a.K + (size_t)xu0 * 32, (size_t)a.K, len, a.mc, nullptr, xs, a.ks, sh,
                  maxbits, [&]() { st.prime(G::STAGES - 2); });
+    for (int i = threadIdx.x; i < ntl * a.pmax * G::RT * MC; i += blockDim.x) red[i] = 0.f;  // unused slots add 0
     __syncthreads();
     st.run(xrow_of, done, ring, xs, a.ks, xu0);
     __syncthreads();
@@ -414,7 +452,7 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) qmv_stream_kernel(QmvSArgs a)
         const int row = (gb + ti * a.G) * G::RT + r;
         if (row >= a.N) continue;
         float s = 0.f;
-        for (int c = 0; c < a.wk; ++c) s += red[((size_t)(ti * a.wk + c) * G::RT + r) * MC + t];
+        for (int c = 0; c < a.pmax; ++c) s += red[((size_t)(ti * a.pmax + c) * G::RT + r) * MC + t];
         s *= pow2f(sh[t]);
         if (a.nwin == 1) {
             if (FMT == FMT_NVFP4) s *= g;
@@ -504,22 +542,31 @@ static cudaError_t plan_qmv_stream(const DeviceState &ds, cudaStream_t st, const
     a.WU = WU;
     a.ntl_max = (a.tiles + a.G - 1) / a.G;
     if (nwin > 1 && ((size_t)nwin * mc * N > WS_FLOATS || a.G > WS_COUNTERS)) return cudaErrorNotSupported;
-    // chunks per tile: as fine as one stage, within the reduction budget
+    // work split: whole tiles round-robin when the busiest warp has at most
+    // 5 % more than the average; else equal runs of stages (a tile cut into
+    // at most pmax pieces when every warp's run has a stage, else one slot
+    // per stage offset)
     const int spw = (WU + G::UPS - 1) / G::UPS;  // stages per row per window
-    int wk = 1, wl = 0;
-    while ((long long)a.ntl_max * wk < 6LL * QMV_WARPS && wk * 2 <= spw && wk < 16) {
-        wk *= 2;
-        ++wl;
+    const int spw_last = (U - (nwin - 1) * WU + G::UPS - 1) / G::UPS;  // the last window may be shorter
+    const int ntl_min = a.tiles / a.G;
+    const long long s_min = (long long)ntl_min * std::min(spw, spw_last);
+    const long long busiest = (long long)((a.ntl_max + QMV_WARPS - 1) / QMV_WARPS) * QMV_WARPS;
+    if (a.ntl_max >= QMV_WARPS && busiest * 100 <= (long long)a.ntl_max * 105) {
+        a.split = 0;
+        a.pmax = 1;
+    } else if (s_min >= QMV_WARPS) {
+        a.split = 1;
+        const long long q = s_min / QMV_WARPS;  // shortest run (stages)
+        a.pmax = (int)std::min<long long>(spw, (spw + q - 1) / q + 1);
+    } else {
+        a.split = 2;
+        a.pmax = spw;
     }
-    const long long per = (long long)a.ntl_max * G::RT * MC * 4;
+    const long long per = (long long)a.ntl_max * a.pmax * G::RT * MC * 4;
     const long long red_cap = (long long)ds.max_smem_optin - rings - 128 - (long long)MC * ks * 2;
     if (per > red_cap) return cudaErrorNotSupported;
-    while (wk > 1 && per * wk > red_cap) { wk /= 2; --wl; }
-    a.wk = wk;
-    a.wk_log2 = wl;
-    a.CU = ((spw + wk - 1) / wk) * G::UPS;
     a.ks = ks;
-    const size_t red = (((size_t)a.ntl_max * wk * G::RT * MC * 4) + 15) & ~(size_t)15;
+    const size_t red = (((size_t)a.ntl_max * a.pmax * G::RT * MC * 4) + 15) & ~(size_t)15;
     const size_t smem = (size_t)MC * ks * 2 + 80 + red + rings;
     if (smem > (size_t)ds.max_smem_optin) return cudaErrorNotSupported;
     if (query) {
