@@ -446,8 +446,17 @@ struct QmmArgs {
     uint16_t *Y;
     int *err;
     int M, N, K;
+    int y32;  // Y is 32-byte aligned: the epilogue stores 32 bytes per instruction
     unsigned long long wait_ns;
 };
+
+// 32 contiguous bytes to global memory (32-byte aligned address).
+__device__ __forceinline__ void st_global_v8(void *p, const uint32_t *v)
+{
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v[0]), "r"(v[1]), "r"(v[2]),
+                 "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
 
 template <int FMT, int NACC>
 __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_constant__ CUtensorMap tmap_x,
@@ -720,9 +729,18 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_consta
                 o[i] = f32x2_to_bf16x2(lo, hi);
             }
             if (m < a.M) {  // rows past M were zero-filled by TMA
-                uint4 *dst = reinterpret_cast<uint4 *>(a.Y + (size_t)m * a.N + n0 + nc);
+                // a lane writes 64 bytes of its own row, so every store
+                // instruction touches 32 rows: the fewer instructions the
+                // better (measured: prefill up projection 1680 -> 1731 TFLOP/s)
+                uint16_t *dst = a.Y + (size_t)m * a.N + n0 + nc;
+                if (a.y32) {
+                    st_global_v8(dst, o);
+                    st_global_v8(dst + 16, o + 8);
+                } else {
+                    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                    for (int i = 0; i < 4; ++i) d4[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                }
             }
         }
     }
@@ -845,6 +863,7 @@ cudaError_t launch_qmm(const DeviceState &ds, cudaStream_t st, int fmt, const ui
     a.N = N;
     a.K = K;
     a.wait_ns = QMM_WAIT_NS;
+    a.y32 = (reinterpret_cast<uintptr_t>(Y) & 31u) == 0 ? 1 : 0;
     if (fmt == FMT_MXFP4) return run_qmm_fmt<FMT_MXFP4>(ds, st, xmap, cmap, a);
     if (fmt == FMT_MXFP8) return run_qmm_fmt<FMT_MXFP8>(ds, st, xmap, cmap, a);
     return run_qmm_fmt<FMT_NVFP4>(ds, st, xmap, cmap, a);

@@ -75,3 +75,22 @@ def test_qmm_prefill_full_size(orc, N, K, seed):
     want = orc.qmm_points(0, codes, scales, X, M, N, K, ms, ns).reshape(rows.size, N)
     check_close(Y[rows], want, f"qmm full {N}x{K}", bf16_out=True)
     assert np.all(np.isfinite(Y))
+
+
+def test_qmm_output_alignment_paths():
+    """Y 32-byte aligned (the epilogue stores 32 bytes per instruction) and
+    Y only 16-byte aligned (16-byte stores): the same bits."""
+    need_gpu()
+    import torch
+    from gemm_decode_register_gb300 import ops
+
+    fmt, M, N, K = 0, 300, 512, 256
+    codes, scales = synth.weights(fmt, N, K, 61)
+    X = dev_bf16(synth.activations(M, K, 62))
+    c, s = dev_u8(codes), dev_u8(scales)
+    y_al = ops.qmm(fmt, c, s, X, N)
+    big = torch.empty(M * N + 8, dtype=torch.bfloat16, device="cuda")
+    y_16 = big[8:].view(M, N)
+    assert y_16.data_ptr() % 32 == 16
+    ops.qmm(fmt, c, s, X, N, Y=y_16)
+    assert torch.equal(y_al.view(torch.int16), y_16.view(torch.int16))

@@ -32,6 +32,9 @@ for fmt in (0, 1, 2):
         CASES.append((fmt, M, 67, 320))        # ragged N (tiles of 2*MC rows)
     CASES += [(fmt, 1, 1000, 4096), (fmt, 4, 513, 2048), (fmt, 8, 129, 1056)]
 CASES += [(2, 1, 33, 48), (2, 4, 31, 16), (2, 3, 70, 1040)]   # NVFP4 with K % 32 == 16
+# streamed shapes whose CTAs deal equal runs of stages to their warps, cutting
+# tiles where runs meet (M=1: 13-14 tiles of 4 stages per CTA; M=2: 4-5 tiles)
+CASES += [(fmt, 1, 4096, 8192) for fmt in (0, 1, 2)] + [(fmt, 2, 3000, 4096) for fmt in (0, 2)]
 
 
 @pytest.mark.parametrize("fmt,M,N,K", CASES)
