@@ -424,7 +424,73 @@ def extras(torch, ops, synth, dev, stream, hbm, bf16_burst, bf16_sust, args):
             del c, s, X, Y
     except Exception as exc:  # reported, not hidden
         res["prefill_qmm"] = {"error": str(exc).splitlines()[0][:200]}
+    for name, fn in (("moe_prefill", extras_moe_prefill), ("crossover_upgate", extras_crossover)):
+        try:
+            res.update(fn(torch, ops, synth, dev, stream, bf16_burst, iters))
+        except Exception as exc:  # reported, not hidden
+            res[name] = {"error": str(exc).splitlines()[0][:200]}
     return res
+
+
+def extras_moe_prefill(torch, ops, synth, dev, stream, bf16_burst, iters):
+    """Expert-batched MoE prefill: 4096 tokens, top-8 of 128 experts, hidden
+    2048, expert intermediate 768 (weights 321 MB, larger than L2)."""
+    res = {}
+    F4 = synth.FMT_MXFP4
+    E, topk, H, I, T = 128, 8, 2048, 768, 4096
+    c1, s1 = synth.weights(F4, 2 * I, H, 40, E=E, exp_lo=118, exp_hi=132)
+    c2, s2 = synth.weights(F4, H, I, 41, E=E, exp_lo=118, exp_hi=132)
+    d1, e1, d2, e2 = (upload(torch, a) for a in (c1, s1, c2, s2))
+    ids = torch.from_numpy(synth.expert_ids(T, E, topk, 500)).cuda()
+    r = torch.from_numpy(synth.router_weights(T, topk, 501)).cuda()
+    x = bf16_dev(torch, synth.activations(T, H, 502)).view(T, H)
+    h = bf16_dev(torch, synth.activations(T * topk, I, 503)).view(T * topk, I)
+    out = torch.empty((T, H), dtype=torch.float32, device=dev)
+    ws = ops.moe_ffn_prefill_workspace(T, E, topk, H, I, device=dev)
+    n = max(5, iters // 10)
+    g = graph_of(torch, lambda: ops.moe_ffn_prefill(F4, d1, e1, d2, e2, x, ids, r, E, I, out=out, workspace=ws))
+    t = time_region(torch, g.replay, n, stream)
+    fl = 2.0 * T * topk * (2 * I * H + H * I)
+    res["moe_prefill_ffn_T4096"] = {"tok_s": round(T / t, 1), "us": round(t * 1e6, 1),
+                                    "tflops": round(fl / t / 1e12, 1),
+                                    "frac_bf16_burst": round(fl / t / 1e12 / bf16_burst, 4),
+                                    "path": "mx_moe_ffn_prefill: route, gather, grouped gate-up GEMM + SwiGLU, "
+                                            "grouped down GEMM, combine (5 launches)"}
+    for name, d, e, xin, idv, N, K in (("gate_up", d1, e1, x, ids, 2 * I, H),
+                                       ("down", d2, e2, h, ids.reshape(-1, 1).contiguous(), H, I)):
+        Tq, tk = idv.shape
+        y = torch.empty((Tq, tk, N), dtype=torch.bfloat16, device=dev)
+        wsq = torch.empty(ops.load().mx_moe_qmm_workspace_size(Tq, E, tk, K), dtype=torch.uint8, device=dev)
+        gq = graph_of(torch, lambda: ops.moe_qmm(F4, d, e, xin, idv, E, N, y=y, workspace=wsq))
+        tq = time_region(torch, gq.replay, n, stream)
+        flq = 2.0 * Tq * tk * N * K
+        res[f"moe_prefill_qmm_{name}"] = {"tflops": round(flq / tq / 1e12, 1), "us": round(tq * 1e6, 1),
+                                          "frac_bf16_burst": round(flq / tq / 1e12 / bf16_burst, 4),
+                                          "path": "mx_moe_qmm: route, gather, grouped GEMM (3 launches)"}
+        del y, wsq
+    return res
+
+
+def extras_crossover(torch, ops, synth, dev, stream, bf16_burst, iters):
+    """Decode GEMV against prefill GEMM as the token count grows, on the FFN
+    up/gate shape (57344 x 8192, 250 MB of weights: larger than L2)."""
+    F4 = synth.FMT_MXFP4
+    N, K = 57344, 8192
+    codes, scales = synth.weights(F4, N, K, 2, exp_lo=118, exp_hi=132)
+    c, s = upload(torch, codes), upload(torch, scales)
+    rows, first = {}, None
+    n = max(3, iters // 20)
+    for M in (1, 2, 4, 8, 16, 32, 64, 128, 256):
+        X = bf16_dev(torch, synth.activations(M, K, 400 + M)).view(M, K)
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        tv = time_region(torch, graph_of(torch, lambda: ops.qmv(F4, c, s, X, N, y=y)).replay, n, stream)
+        tm = time_region(torch, graph_of(torch, lambda: ops.qmm(F4, c, s, X, N, Y=Y)).replay, n, stream)
+        rows[str(M)] = {"qmv_us": round(tv * 1e6, 1), "qmm_us": round(tm * 1e6, 1)}
+        if first is None and tm < tv:
+            first = M
+    return {"crossover_upgate": {"rows": rows, "qmm_faster_from_M": first,
+                                 "note": "qmv: 8 tokens per pass over the weights; qmm: 256-row pair tiles"}}
 
 
 # ------------------------------------------------------------------ oracle

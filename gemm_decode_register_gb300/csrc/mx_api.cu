@@ -157,6 +157,80 @@ extern "C" int mx_qmm(int fmt, const void *codes, const void *scales, const void
     return finish(e);
 }
 
+// Expert-batched prefill: limits beyond mx_moe_qmv's.
+static constexpr long long PREFILL_MAX_SLOTS = 1ll << 24;  // T * topk
+
+static bool prefill_sizes_ok(long long T, long long E, long long topk)
+{
+    return T * topk <= PREFILL_MAX_SLOTS && E <= MOE_MAX_EXPERTS;
+}
+
+extern "C" size_t mx_moe_qmm_workspace_size(int T, int E, int topk, int K)
+{
+    if (T <= 0 || E <= 0 || topk <= 0 || K <= 0 || topk > E || !prefill_sizes_ok(T, E, topk)) return 0;
+    return moe_group_plan(T, E, topk, K, 0).bytes;
+}
+
+extern "C" int mx_moe_qmm(int fmt, const void *expert_codes, const void *expert_scales, const void *x,
+                          const int32_t *expert_ids, void *y, int T, int E, int topk, int N, int K, void *workspace,
+                          size_t workspace_bytes)
+{
+    if (!fmt_ok(fmt)) return MX_EUNSUPPORTED;
+    if (!expert_codes || !expert_scales || !x || !expert_ids || !y || !workspace) return MX_EINVAL;
+    if (T <= 0 || E <= 0 || topk <= 0 || N <= 0 || K <= 0 || topk > E || K % block_of(fmt) != 0)
+        return MX_EINVAL;
+    if (N % 256 != 0 || K % 64 != 0 || !prefill_sizes_ok(T, E, topk) || (long long)E * N > 0x7FFFFFFFll)
+        return MX_EUNSUPPORTED;
+    if (workspace_bytes < moe_group_plan(T, E, topk, K, 0).bytes) return MX_EINVAL;
+    if (!aligned16(expert_codes) || !aligned16(expert_scales) || !aligned16(x) || !aligned16(y) ||
+        (reinterpret_cast<uintptr_t>(expert_ids) & 3u) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return MX_EALIGN;
+    DeviceState *ds = device_state();
+    if (!ds) return MX_ECUDA;
+    cudaError_t e = launch_moe_qmm(*ds, t_stream, fmt, static_cast<const uint8_t *>(expert_codes),
+                                   static_cast<const uint8_t *>(expert_scales), static_cast<const uint16_t *>(x),
+                                   expert_ids, static_cast<uint16_t *>(y), T, E, topk, N, K, workspace);
+    if (e == cudaErrorInvalidValue) return MX_EUNSUPPORTED;
+    return finish(e);
+}
+
+extern "C" size_t mx_moe_ffn_prefill_workspace_size(int T, int E, int topk, int H, int I)
+{
+    if (T <= 0 || E <= 0 || topk <= 0 || H <= 0 || I <= 0 || topk > E || !prefill_sizes_ok(T, E, topk)) return 0;
+    return moe_group_plan(T, E, topk, H, I).bytes;
+}
+
+extern "C" int mx_moe_ffn_prefill(int fmt, const void *gate_up_codes, const void *gate_up_scales,
+                                  const void *down_codes, const void *down_scales, const void *x,
+                                  const int32_t *expert_ids, const float *router_weights, float *out, int T, int E,
+                                  int topk, int H, int I, void *workspace, size_t workspace_bytes)
+{
+    if (!fmt_ok(fmt)) return MX_EUNSUPPORTED;
+    if (!gate_up_codes || !gate_up_scales || !down_codes || !down_scales || !x || !expert_ids || !router_weights ||
+        !out || !workspace)
+        return MX_EINVAL;
+    if (T <= 0 || E <= 0 || topk <= 0 || H <= 0 || I <= 0 || topk > E || H % block_of(fmt) != 0 ||
+        I % block_of(fmt) != 0)
+        return MX_EINVAL;
+    if (H % 256 != 0 || I % 128 != 0 || !prefill_sizes_ok(T, E, topk) || (long long)E * 2 * I > 0x7FFFFFFFll ||
+        (long long)E * H > 0x7FFFFFFFll)
+        return MX_EUNSUPPORTED;
+    if (workspace_bytes < moe_group_plan(T, E, topk, H, I).bytes) return MX_EINVAL;
+    if (!aligned16(gate_up_codes) || !aligned16(gate_up_scales) || !aligned16(down_codes) ||
+        !aligned16(down_scales) || !aligned16(x) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(expert_ids) & 3u) || (reinterpret_cast<uintptr_t>(router_weights) & 3u) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return MX_EALIGN;
+    DeviceState *ds = device_state();
+    if (!ds) return MX_ECUDA;
+    cudaError_t e = launch_moe_ffn_prefill(
+        *ds, t_stream, fmt, static_cast<const uint8_t *>(gate_up_codes), static_cast<const uint8_t *>(gate_up_scales),
+        static_cast<const uint8_t *>(down_codes), static_cast<const uint8_t *>(down_scales),
+        static_cast<const uint16_t *>(x), expert_ids, router_weights, out, T, E, topk, H, I, workspace);
+    if (e == cudaErrorInvalidValue) return MX_EUNSUPPORTED;
+    return finish(e);
+}
+
 extern "C" int mx_dequant(int fmt, const void *codes, const void *scales, float *W, int N, int K)
 {
     if (!fmt_ok(fmt)) return MX_EUNSUPPORTED;

@@ -53,6 +53,28 @@ cudaError_t launch_moe_down_combine(const DeviceState &ds, cudaStream_t st, int 
 cudaError_t launch_qmm(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,
                        const uint8_t *scales, const uint16_t *X, uint16_t *Y, int M, int N, int K);
 
+// Grouped (expert-batched) prefill: routes on the device, gathers the
+// routed rows into expert order and runs the pair GEMM per group tile.
+// Y / h / per-slot outputs are bf16.
+cudaError_t launch_qmm_grouped(const DeviceState &ds, cudaStream_t st, int fmt, bool swiglu, const uint8_t *codes,
+                               const uint8_t *scales, const uint16_t *Xs, int rows, const int *groups,
+                               int max_groups, const int *slot_of, uint16_t *Y, int E, int N, int K);
+
+// Byte offsets of the grouped-prefill workspace (caller-owned, 256-byte aligned).
+struct MoeGroupPlan {
+    int S = 0;           // routed rows (T * topk)
+    int max_groups = 0;  // most group tiles any routing can make
+    size_t off_groups = 0, off_slot = 0, off_xs = 0, off_hs = 0, bytes = 0;
+};
+MoeGroupPlan moe_group_plan(int T, int E, int topk, int K, int I /* 0: no FFN */);
+cudaError_t launch_moe_qmm(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,
+                           const uint8_t *scales, const uint16_t *x, const int32_t *ids, uint16_t *y, int T, int E,
+                           int topk, int N, int K, void *workspace);
+cudaError_t launch_moe_ffn_prefill(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *gu_codes,
+                                   const uint8_t *gu_scales, const uint8_t *dn_codes, const uint8_t *dn_scales,
+                                   const uint16_t *x, const int32_t *ids, const float *rw, float *out, int T, int E,
+                                   int topk, int H, int I, void *workspace);
+
 // Limits checked on the host.
 constexpr int QMV_MAX_K = 1 << 20;
 constexpr int MOE_MAX_SLOTS = 1024;  // T * topk

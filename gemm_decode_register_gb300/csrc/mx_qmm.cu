@@ -441,13 +441,23 @@ __device__ __forceinline__ uint32_t scale_load(const uint8_t *p)
     return SPK == 4 ? ld_nc_u32(p) : ld_nc_u16(p);
 }
 
+// What a pair tile computes and where its rows go.
+constexpr int QMM_DENSE = 0;        // Y[M][N] = X W^T
+constexpr int QMM_GROUPED = 1;      // expert groups of sorted rows; row i of group g -> Y[slot_of[r0 + i]]
+constexpr int QMM_GROUPED_GLU = 2;  // as 1, but CTA 0 takes gate rows, CTA 1 up rows; h = SwiGLU -> H[r0 + i]
+
 struct QmmArgs {
     const uint8_t *scales;
-    uint16_t *Y;
+    uint16_t *Y;  // dense / grouped: [rows][N]; SwiGLU: h [rows][N / 2]
     int *err;
-    int M, N, K;
-    int y32;  // Y is 32-byte aligned: the epilogue stores 32 bytes per instruction
+    int M, N, K;  // grouped: N rows per expert, M unused
+    int y32;  // Y rows and base 32-byte aligned: the epilogue stores 32 bytes per instruction
     unsigned long long wait_ns;
+    // grouped modes: the routing tables (written by moe_group_route_kernel)
+    const int *groups;   // [0] = number of tiles G; from word 4 on: G x {expert, first sorted row, rows, 0}
+    const int *slot_of;  // sorted row -> slot (QMM_GROUPED)
+    int E;               // experts
+    int ntile;           // column tiles per group tile
 };
 
 // 32 contiguous bytes to global memory (32-byte aligned address).
@@ -458,11 +468,12 @@ __device__ __forceinline__ void st_global_v8(void *p, const uint32_t *v)
                  : "memory");
 }
 
-template <int FMT, int NACC>
+template <int FMT, int NACC, int MODE>
 __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_constant__ CUtensorMap tmap_x,
                                                              const __grid_constant__ CUtensorMap tmap_c, QmmArgs a)
 {
     using QG = QmmGeo<FMT, NACC>;
+    static_assert(MODE == QMM_DENSE || NACC == 1, "grouped tiles are 256 rows");
     constexpr int SX = QG::SX, SD = QG::SD, SC = QG::SC, SPK = QG::SPK;
     constexpr uint32_t SIG_BYTES = 8 * 16;  // one 16-byte signal per decoder warp of CTA 1
     extern __shared__ uint8_t smem_raw[];
@@ -489,10 +500,34 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_consta
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
     const int cid = (int)cluster_id_x();
-    const int m_tiles = (a.M + QG::BM - 1) / QG::BM;
-    const int m0 = (cid % m_tiles) * QG::BM;
-    const int n0 = (cid / m_tiles) * QMM_BN;
     const int KB = a.K / QMM_BK;
+    // m0: first X row of the tile; n0: first output column; wrow: first of
+    // this CTA's 128 weight rows (over all experts); rows: valid tile rows
+    int m0, n0, wrow, rows, expert = 0;
+    if constexpr (MODE == QMM_DENSE) {
+        const int m_tiles = (a.M + QG::BM - 1) / QG::BM;
+        m0 = (cid % m_tiles) * QG::BM;
+        n0 = (cid / m_tiles) * QMM_BN;
+        wrow = n0 + 128 * (int)rank;
+        rows = a.M - m0;
+    } else {
+        // the routing tables come from the previous kernel; a grid sized for
+        // the most tiles any routing can make leaves the spare pairs idle
+        pdl_wait();
+        const int g = cid / a.ntile, nt = cid - g * a.ntile;
+        if (g >= __ldcg(a.groups)) return;  // both CTAs of the pair see the same g
+        const int4 t = __ldcg(reinterpret_cast<const int4 *>(a.groups + 4) + g);
+        expert = t.x;
+        m0 = t.y;
+        rows = t.z;
+        if constexpr (MODE == QMM_GROUPED) {
+            n0 = nt * QMM_BN;
+            wrow = expert * a.N + n0 + 128 * (int)rank;
+        } else {
+            n0 = nt * 128;  // h columns; gate rows n0.. (CTA 0), up rows N/2 + n0.. (CTA 1)
+            wrow = expert * a.N + (int)rank * (a.N / 2) + n0;
+        }
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < SX; ++s) {
@@ -529,7 +564,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_consta
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     pdl_trigger();
-    pdl_wait();  // X and Y may be used by the neighbouring kernels
+    if constexpr (MODE == QMM_DENSE) pdl_wait();  // X and Y may be used by the neighbouring kernels
 
     if (warp == 10) {
         // ---------------- X producer: both CTAs' slabs complete on CTA 0's
@@ -555,7 +590,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_consta
         // (whole warp, QMM_SPF k-blocks in flight).  The scales come through
         // shared memory so that the decoders hold no global loads in flight.
         const size_t srow_bytes = (size_t)KB * SPK;
-        const uint8_t *sbase = a.scales + (size_t)(n0 + 128 * (int)rank + lane) * srow_bytes;
+        const uint8_t *sbase = a.scales + (size_t)(wrow + lane) * srow_bytes;
         uint32_t pv[QMM_SPF][4];
 #pragma unroll
         for (int j = 0; j < QMM_SPF; ++j)
@@ -578,8 +613,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_consta
                 }
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&full_c[s], QG::C_BYTES);
-                    tma_load_2d(cring + s * QG::C_BYTES, &tmap_c, kb * QG::CODE_ROW, n0 + 128 * (int)rank,
-                                &full_c[s]);
+                    tma_load_2d(cring + s * QG::C_BYTES, &tmap_c, kb * QG::CODE_ROW, wrow, &full_c[s]);
                 }
                 uint8_t *sc = sring + s * QG::SC_BYTES;
 #pragma unroll
@@ -707,39 +741,85 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_consta
         const int quarter = warp & 3;   // TMEM lanes 32*quarter .. +31
         const int group = (warp - 2) >> 2;  // which half of the accumulator columns
         float g = 1.0f;
-        if (FMT == FMT_NVFP4) g = load_f32_unaligned(a.scales + (size_t)a.N * (a.K / 16));
-        for (int c = group * NACC * 128; c < (group + 1) * NACC * 128; c += 32) {
-            const int h = c / QMM_BN, nc = c % QMM_BN;
-            const int m = m0 + 256 * h + 128 * (int)rank + 32 * quarter + lane;
-            uint32_t v[32];
-            if (ok) {
-                tmem_ld32(tmem + (uint32_t)c + ((uint32_t)(quarter * 32) << 16), v);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = 0x7FC00000u;
-            }
-            uint32_t o[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float lo = __uint_as_float(v[2 * i]), hi = __uint_as_float(v[2 * i + 1]);
-                if (FMT == FMT_NVFP4) {
-                    lo = __fmul_rn(lo, g);
-                    hi = __fmul_rn(hi, g);
-                }
-                o[i] = f32x2_to_bf16x2(lo, hi);
-            }
-            if (m < a.M) {  // rows past M were zero-filled by TMA
-                // a lane writes 64 bytes of its own row, so every store
-                // instruction touches 32 rows: the fewer instructions the
-                // better (measured: prefill up projection 1680 -> 1731 TFLOP/s)
-                uint16_t *dst = a.Y + (size_t)m * a.N + n0 + nc;
-                if (a.y32) {
-                    st_global_v8(dst, o);
-                    st_global_v8(dst + 16, o + 8);
+        if (FMT == FMT_NVFP4) {
+            const size_t blocks = (size_t)(MODE == QMM_DENSE ? 1 : a.E) * a.N * (a.K / 16);
+            g = load_f32_unaligned(a.scales + blocks + 4 * (size_t)expert);
+        }
+        if constexpr (MODE == QMM_GROUPED_GLU) {
+            // columns c (gate) and 128 + c (up) of a row hold the same h column
+            const int i = 128 * (int)rank + 32 * quarter + lane;  // tile row
+            const int hw = a.N / 2;
+            for (int c = 64 * group; c < 64 * group + 64; c += 32) {
+                uint32_t vg[32], vu[32];
+                if (ok) {
+                    tmem_ld32(tmem + (uint32_t)c + ((uint32_t)(quarter * 32) << 16), vg);
+                    tmem_ld32(tmem + (uint32_t)(128 + c) + ((uint32_t)(quarter * 32) << 16), vu);
                 } else {
-                    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) d4[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                    for (int j = 0; j < 32; ++j) vg[j] = vu[j] = 0x7FC00000u;
+                }
+                uint32_t o[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    float g0 = __uint_as_float(vg[2 * j]), g1 = __uint_as_float(vg[2 * j + 1]);
+                    float u0 = __uint_as_float(vu[2 * j]), u1 = __uint_as_float(vu[2 * j + 1]);
+                    if (FMT == FMT_NVFP4) {
+                        g0 = __fmul_rn(g0, g);
+                        g1 = __fmul_rn(g1, g);
+                        u0 = __fmul_rn(u0, g);
+                        u1 = __fmul_rn(u1, g);
+                    }
+                    o[j] = swiglu_bf16(g0, u0) | (swiglu_bf16(g1, u1) << 16);
+                }
+                if (i < rows) {
+                    uint16_t *dst = a.Y + (size_t)(m0 + i) * hw + n0 + c;
+                    if (a.y32) {
+                        st_global_v8(dst, o);
+                        st_global_v8(dst + 16, o + 8);
+                    } else {
+                        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            d4[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+                    }
+                }
+            }
+        } else {
+            for (int c = group * NACC * 128; c < (group + 1) * NACC * 128; c += 32) {
+                const int h = c / QMM_BN, nc = c % QMM_BN;
+                const int i = 256 * h + 128 * (int)rank + 32 * quarter + lane;  // tile row
+                uint32_t v[32];
+                if (ok) {
+                    tmem_ld32(tmem + (uint32_t)c + ((uint32_t)(quarter * 32) << 16), v);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = 0x7FC00000u;
+                }
+                uint32_t o[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    float lo = __uint_as_float(v[2 * j]), hi = __uint_as_float(v[2 * j + 1]);
+                    if (FMT == FMT_NVFP4) {
+                        lo = __fmul_rn(lo, g);
+                        hi = __fmul_rn(hi, g);
+                    }
+                    o[j] = f32x2_to_bf16x2(lo, hi);
+                }
+                if (i < rows) {  // dense: rows past M were zero-filled by TMA
+                    // a lane writes 64 bytes of its own row, so every store
+                    // instruction touches 32 rows: the fewer instructions the
+                    // better (measured: prefill up projection 1680 -> 1731 TFLOP/s)
+                    const size_t yrow = MODE == QMM_DENSE ? (size_t)(m0 + i) : (size_t)__ldcg(a.slot_of + m0 + i);
+                    uint16_t *dst = a.Y + yrow * a.N + n0 + nc;
+                    if (a.y32) {
+                        st_global_v8(dst, o);
+                        st_global_v8(dst + 16, o + 8);
+                    } else {
+                        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            d4[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+                    }
                 }
             }
         }
@@ -776,20 +856,19 @@ static EncodeTiledFn encode_fn()
     return fn;
 }
 
-template <int FMT, int NACC>
+template <int FMT, int NACC, int MODE>
 static cudaError_t run_qmm(const DeviceState &ds, cudaStream_t st, const CUtensorMap &xmap, const CUtensorMap &cmap,
-                           const QmmArgs &a)
+                           const QmmArgs &a, int pairs)
 {
     using QG = QmmGeo<FMT, NACC>;
     if (QG::SMEM > ds.max_smem_optin) return cudaErrorInvalidValue;
     static int configured_dev[64] = {0};
     if (ds.device < 64 && !configured_dev[ds.device]) {
-        cudaError_t e =
-            cudaFuncSetAttribute(qmm_kernel<FMT, NACC>, cudaFuncAttributeMaxDynamicSharedMemorySize, QG::SMEM);
+        cudaError_t e = cudaFuncSetAttribute(qmm_kernel<FMT, NACC, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             QG::SMEM);
         if (e != cudaSuccess) return e;
         configured_dev[ds.device] = 1;
     }
-    const int pairs = ((a.M + QG::BM - 1) / QG::BM) * (a.N / QMM_BN);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * pairs);
     cfg.blockDim = dim3(QMM_THREADS);
@@ -804,7 +883,7 @@ static cudaError_t run_qmm(const DeviceState &ds, cudaStream_t st, const CUtenso
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, qmm_kernel<FMT, NACC>, xmap, cmap, a);
+    return cudaLaunchKernelEx(&cfg, qmm_kernel<FMT, NACC, MODE>, xmap, cmap, a);
 }
 
 // Pair tiles of 512 rows halve each SM's decode and shared-memory writes per
@@ -826,18 +905,21 @@ template <int FMT>
 static cudaError_t run_qmm_fmt(const DeviceState &ds, cudaStream_t st, const CUtensorMap &xmap,
                                const CUtensorMap &cmap, const QmmArgs &a)
 {
-    return qmm_nacc(ds, a.M, a.N) == 2 ? run_qmm<FMT, 2>(ds, st, xmap, cmap, a) : run_qmm<FMT, 1>(ds, st, xmap, cmap, a);
+    const int n_tiles = a.N / QMM_BN;
+    if (qmm_nacc(ds, a.M, a.N) == 2)
+        return run_qmm<FMT, 2, QMM_DENSE>(ds, st, xmap, cmap, a, ((a.M + 511) / 512) * n_tiles);
+    return run_qmm<FMT, 1, QMM_DENSE>(ds, st, xmap, cmap, a, ((a.M + 255) / 256) * n_tiles);
 }
 
-cudaError_t launch_qmm(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,
-                       const uint8_t *scales, const uint16_t *X, uint16_t *Y, int M, int N, int K)
+// X: [rows][K] bf16, boxes of 64 x 128 rows, 128-byte swizzle; rows past
+// `rows` read as zero.  Codes: [wrows][row bytes], boxes of one k-block's
+// bytes x 128 rows.
+static cudaError_t encode_maps(int fmt, const uint16_t *X, long long rows, const uint8_t *codes, long long wrows,
+                               int K, CUtensorMap &xmap, CUtensorMap &cmap)
 {
-    if (N % QMM_BN != 0 || K % QMM_BK != 0) return cudaErrorInvalidValue;
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
-    // X: [M][K] bf16, boxes of 64 x 128 rows, 128-byte swizzle; rows past M read as zero
-    CUtensorMap xmap;
-    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
     const cuuint32_t box[2] = {(cuuint32_t)QMM_BK, 128u};
     const cuuint32_t estr[2] = {1u, 1u};
@@ -845,16 +927,57 @@ cudaError_t launch_qmm(const DeviceState &ds, cudaStream_t st, int fmt, const ui
                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    // packed codes: [N][row bytes], boxes of one k-block's bytes x 128 rows
     const cuuint64_t row_bytes = fmt == FMT_MXFP8 ? (cuuint64_t)K : (cuuint64_t)K / 2;
-    CUtensorMap cmap;
-    const cuuint64_t cdims[2] = {row_bytes, (cuuint64_t)N};
+    const cuuint64_t cdims[2] = {row_bytes, (cuuint64_t)wrows};
     const cuuint64_t cstrides[1] = {row_bytes};
     const cuuint32_t cbox[2] = {fmt == FMT_MXFP8 ? (cuuint32_t)QMM_BK : (cuuint32_t)QMM_BK / 2, 128u};
     r = enc(&cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(codes), cdims, cstrides, cbox, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t launch_qmm_grouped(const DeviceState &ds, cudaStream_t st, int fmt, bool swiglu, const uint8_t *codes,
+                               const uint8_t *scales, const uint16_t *Xs, int rows, const int *groups,
+                               int max_groups, const int *slot_of, uint16_t *Y, int E, int N, int K)
+{
+    if (K % QMM_BK != 0 || (swiglu ? (N % 256) : (N % QMM_BN)) != 0) return cudaErrorInvalidValue;
+    if (max_groups <= 0) return cudaSuccess;
+    CUtensorMap xmap, cmap;
+    cudaError_t e = encode_maps(fmt, Xs, rows, codes, (long long)E * N, K, xmap, cmap);
+    if (e != cudaSuccess) return e;
+    QmmArgs a;
+    a.scales = scales;
+    a.Y = Y;
+    a.err = ds.err;
+    a.M = rows;
+    a.N = N;
+    a.K = K;
+    a.wait_ns = QMM_WAIT_NS;
+    const int yw = swiglu ? N / 2 : N;  // output row width
+    a.y32 = ((reinterpret_cast<uintptr_t>(Y) & 31u) == 0 && yw % 16 == 0) ? 1 : 0;
+    a.groups = groups;
+    a.slot_of = slot_of;
+    a.E = E;
+    a.ntile = swiglu ? (N / 2) / 128 : N / QMM_BN;
+    const int pairs = max_groups * a.ntile;
+    if (swiglu) {
+        if (fmt == FMT_MXFP4) return run_qmm<FMT_MXFP4, 1, QMM_GROUPED_GLU>(ds, st, xmap, cmap, a, pairs);
+        if (fmt == FMT_MXFP8) return run_qmm<FMT_MXFP8, 1, QMM_GROUPED_GLU>(ds, st, xmap, cmap, a, pairs);
+        return run_qmm<FMT_NVFP4, 1, QMM_GROUPED_GLU>(ds, st, xmap, cmap, a, pairs);
+    }
+    if (fmt == FMT_MXFP4) return run_qmm<FMT_MXFP4, 1, QMM_GROUPED>(ds, st, xmap, cmap, a, pairs);
+    if (fmt == FMT_MXFP8) return run_qmm<FMT_MXFP8, 1, QMM_GROUPED>(ds, st, xmap, cmap, a, pairs);
+    return run_qmm<FMT_NVFP4, 1, QMM_GROUPED>(ds, st, xmap, cmap, a, pairs);
+}
+
+cudaError_t launch_qmm(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,
+                       const uint8_t *scales, const uint16_t *X, uint16_t *Y, int M, int N, int K)
+{
+    if (N % QMM_BN != 0 || K % QMM_BK != 0) return cudaErrorInvalidValue;
+    CUtensorMap xmap, cmap;
+    cudaError_t e = encode_maps(fmt, X, M, codes, N, K, xmap, cmap);
+    if (e != cudaSuccess) return e;
     QmmArgs a;
     a.scales = scales;
     a.Y = Y;
@@ -864,6 +987,10 @@ cudaError_t launch_qmm(const DeviceState &ds, cudaStream_t st, int fmt, const ui
     a.K = K;
     a.wait_ns = QMM_WAIT_NS;
     a.y32 = (reinterpret_cast<uintptr_t>(Y) & 31u) == 0 ? 1 : 0;
+    a.groups = nullptr;
+    a.slot_of = nullptr;
+    a.E = 1;
+    a.ntile = 0;
     if (fmt == FMT_MXFP4) return run_qmm_fmt<FMT_MXFP4>(ds, st, xmap, cmap, a);
     if (fmt == FMT_MXFP8) return run_qmm_fmt<FMT_MXFP8>(ds, st, xmap, cmap, a);
     return run_qmm_fmt<FMT_NVFP4>(ds, st, xmap, cmap, a);

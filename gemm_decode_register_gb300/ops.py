@@ -44,7 +44,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                "(run __graft_entry__.build() or python -m "
                                "gemm_decode_register_gb300.build)")
         lib = ctypes.CDLL(p)
-        P, I = ctypes.c_void_p, ctypes.c_int
+        P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
         sig = {
             "mx_qmv": [I, P, P, P, P, I, I, I],
             "mx_qmv_noalloc": [I, P, P, P, P, I, I, I],
@@ -57,11 +57,18 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "mx_swiglu": [P, P, I, I],
             "mx_moe_combine": [P, P, P, I, I, I],
             "mx_device_error": [],
+            "mx_moe_qmm": [I, P, P, P, P, P, I, I, I, I, I, P, Z],
+            "mx_moe_ffn_prefill": [I, P, P, P, P, P, P, P, P, I, I, I, I, I, P, Z],
         }
         for name, args in sig.items():
             f = getattr(lib, name)
             f.argtypes = args
             f.restype = I
+        for name, args in {"mx_moe_qmm_workspace_size": [I, I, I, I],
+                           "mx_moe_ffn_prefill_workspace_size": [I, I, I, I, I]}.items():
+            f = getattr(lib, name)
+            f.argtypes = args
+            f.restype = Z
         lib.mx_strerror.argtypes = [I]
         lib.mx_strerror.restype = ctypes.c_char_p
         _lib = lib
@@ -72,7 +79,7 @@ def header_symbols() -> list[str]:
     """Names of the functions include/mx.h declares."""
     with open(HEADER) as f:
         text = f.read()
-    return re.findall(r"^\s*(?:const\s+char\s*\*|int)\s*(mx_\w+)\s*\(", text, flags=re.M)
+    return re.findall(r"^\s*(?:const\s+char\s*\*|int|size_t)\s*(mx_\w+)\s*\(", text, flags=re.M)
 
 
 def _check(fn: str, status: int) -> None:
@@ -166,6 +173,52 @@ def qmm(fmt: int, codes: torch.Tensor, scales: torch.Tensor, X: torch.Tensor, N:
     _stream()
     _check("mx_qmm", load().mx_qmm(fmt, _ptr(codes), _ptr(scales), _ptr(X), _ptr(Y), M, N, K))
     return Y
+
+
+def _workspace(nbytes: int, ws: torch.Tensor | None, device) -> torch.Tensor:
+    if nbytes == 0:
+        raise ValueError("sizes outside the library's limits")
+    if ws is None:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    return ws
+
+
+def moe_qmm(fmt: int, codes: torch.Tensor, scales: torch.Tensor, x: torch.Tensor, expert_ids: torch.Tensor,
+            E: int, N: int, y: torch.Tensor | None = None, workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """y[t][j] bf16 = W_{expert_ids[t][j]} x[t] for many tokens (grouped tensor-core GEMM)."""
+    T, K = x.shape
+    topk = expert_ids.shape[1]
+    if y is None:
+        y = torch.empty((T, topk, N), dtype=torch.bfloat16, device=x.device)
+    lib = load()
+    ws = _workspace(lib.mx_moe_qmm_workspace_size(T, E, topk, K), workspace, x.device)
+    _stream()
+    _check("mx_moe_qmm", lib.mx_moe_qmm(fmt, _ptr(codes), _ptr(scales), _ptr(x), _ptr(expert_ids), _ptr(y),
+                                        T, E, topk, N, K, _ptr(ws), ws.numel()))
+    return y
+
+
+def moe_ffn_prefill_workspace(T: int, E: int, topk: int, H: int, I: int, device="cuda") -> torch.Tensor:
+    return _workspace(load().mx_moe_ffn_prefill_workspace_size(T, E, topk, H, I), None, device)
+
+
+def moe_ffn_prefill(fmt: int, gu_codes: torch.Tensor, gu_scales: torch.Tensor, dn_codes: torch.Tensor,
+                    dn_scales: torch.Tensor, x: torch.Tensor, expert_ids: torch.Tensor,
+                    router_weights: torch.Tensor, E: int, I: int, out: torch.Tensor | None = None,
+                    workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """out[t] fp32 = sum_j r[t][j] down_e(SwiGLU(gate_up_e x[t])) over many tokens."""
+    T, H = x.shape
+    topk = expert_ids.shape[1]
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.float32, device=x.device)
+    lib = load()
+    ws = _workspace(lib.mx_moe_ffn_prefill_workspace_size(T, E, topk, H, I), workspace, x.device)
+    _stream()
+    _check("mx_moe_ffn_prefill", lib.mx_moe_ffn_prefill(fmt, _ptr(gu_codes), _ptr(gu_scales), _ptr(dn_codes),
+                                                        _ptr(dn_scales), _ptr(x), _ptr(expert_ids),
+                                                        _ptr(router_weights), _ptr(out), T, E, topk, H, I,
+                                                        _ptr(ws), ws.numel()))
+    return out
 
 
 def dequant(fmt: int, codes: torch.Tensor, scales: torch.Tensor, N: int, K: int,

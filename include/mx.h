@@ -51,6 +51,7 @@
 #ifndef MX_H
 #define MX_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -149,6 +150,48 @@ int mx_moe_down_combine(int fmt, const void *expert_codes, const void *expert_sc
  * the epilogue. */
 int mx_qmm(int fmt, const void *codes, const void *scales, const void *X, void *Y, int M, int N,
            int K);
+
+/* Expert-batched MoE prefill (grouped GEMM): the mx_moe_qmv operation for
+ * many tokens, on the tensor cores.
+ *   y[t][j][n] = bf16_rne( sum_k x[t][k] * W_e[n][k] ),  e = expert_ids[t][j],
+ * x bf16 [T][K], y bf16 [T][topk][N], expert stacks as in mx_moe_qmv.  The
+ * pages read only the experts a token is routed to (talk slide 4) and name
+ * MoE prefill as the weak spot once dense prefill runs on the matrix units
+ * (release post, section "Bandwidth utilisation per model"); here the
+ * (token, slot) rows are grouped by expert on the device, gathered into
+ * expert order and multiplied 256 rows at a time as in mx_qmm, so each
+ * expert's weights are decoded once per 256 routed rows.  Launches: routing
+ * (one block), the gather, the grouped GEMM.
+ * workspace: caller-owned device memory of at least
+ * mx_moe_qmm_workspace_size(T, E, topk, K) bytes, 256-byte aligned (else
+ * MX_EINVAL / MX_EALIGN); the call overwrites it, so calls sharing one
+ * workspace must not overlap.  N a multiple of 256 and K of 64, T*topk <=
+ * 2^24, E <= 4096, E*N < 2^31 (else MX_EUNSUPPORTED).  An id outside [0, E)
+ * sets MX_DEVERR_BAD_EXPERT and fills that slot's N outputs with NaN.
+ * codes, scales, x, y 16-byte aligned; ids 4-byte aligned.  For a down
+ * projection pass T' = T*topk rows, topk = 1. */
+size_t mx_moe_qmm_workspace_size(int T, int E, int topk, int K);
+int mx_moe_qmm(int fmt, const void *expert_codes, const void *expert_scales, const void *x,
+               const int32_t *expert_ids, void *y, int T, int E, int topk, int N, int K, void *workspace,
+               size_t workspace_bytes);
+
+/* Expert-batched MoE FFN prefill, one call:
+ *   h[t][j]  = bf16_rne( silu(W_gu,e[0:I] x[t]) * (W_gu,e[I:2I] x[t]) )   (as mx_moe_gate_up_swiglu)
+ *   yd[t][j] = bf16_rne( W_dn,e h[t][j] )
+ *   out[t][n] = sum_j r[t][j] * yd[t][j][n]  (fp32 fused multiply-adds in slot order)
+ * e = expert_ids[t][j]; gate-up stacks [E][2I][H], down stacks [E][H][I];
+ * x bf16 [T][H]; r fp32 [T][topk]; out fp32 [T][H].  Launches: routing,
+ * gather, grouped gate-up GEMM with the SwiGLU in its epilogue (CTA pairs
+ * whose two halves hold gate row i and up row I + i), grouped down GEMM,
+ * combine.  workspace: at least mx_moe_ffn_prefill_workspace_size(T, E,
+ * topk, H, I) bytes, 256-byte aligned.  H a multiple of 256, I of 128; other
+ * limits as mx_moe_qmm.  A bad id sets MX_DEVERR_BAD_EXPERT and makes that
+ * token's outputs NaN.  Pointers 16-byte aligned; ids and r 4-byte. */
+size_t mx_moe_ffn_prefill_workspace_size(int T, int E, int topk, int H, int I);
+int mx_moe_ffn_prefill(int fmt, const void *gate_up_codes, const void *gate_up_scales, const void *down_codes,
+                       const void *down_scales, const void *x, const int32_t *expert_ids,
+                       const float *router_weights, float *out, int T, int E, int topk, int H, int I,
+                       void *workspace, size_t workspace_bytes);
 
 /* ---- support calls (not on the pages; part of this library's contract) */
 
