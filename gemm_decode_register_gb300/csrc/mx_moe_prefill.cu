@@ -13,7 +13,7 @@
 //
 // Launches (all with programmatic dependent launch; each waits for the one
 // before it before touching the workspace):
-//   moe_group_route_kernel   one block: per-expert counts, exclusive scans,
+//   moe_group_route_*        one block: per-expert counts, exclusive scans,
 //                            the group tile table, sorted row -> slot
 //   gather_rows_kernel       X rows into expert order (bf16, 16-byte copies)
 //   qmm_kernel (grouped)     per group tile and column tile; output rows
@@ -53,43 +53,16 @@ MoeGroupPlan moe_group_plan(int T, int E, int topk, int K, int I)
     return p;
 }
 
-// One block.  Slots with an expert id outside [0, E) are left out of every
-// group; they set DEVERR_BAD_EXPERT and, when ynan is given, their output row
-// of ynan_w bf16 values is written as NaN.
-__global__ void __launch_bounds__(ROUTE_THREADS) moe_group_route_kernel(const int32_t *__restrict__ ids, int S, int E,
-                                                                        int *__restrict__ groups,
-                                                                        int *__restrict__ slot_of, uint16_t *ynan,
-                                                                        int ynan_w, int *err)
+// Exclusive scans of the per-expert row counts cnt[] and tile counts
+// (ceil(cnt / 256)) into pos[] and tile0[], the group tile table, and the
+// totals in groups[0] (tiles) and groups[1] (rows).  Thread tid owns experts
+// [tid * per, tid * per + per).  Ends with the block synchronised.
+__device__ void route_scan_tiles(const int *cnt, int *pos, int *tile0, int E, int *groups)
 {
-    extern __shared__ int route_smem[];
-    int *cnt = route_smem;           // [E] rows per expert
-    int *pos = route_smem + E;       // [E] first sorted row, then the placement cursor
-    int *tile0 = route_smem + 2 * E; // [E] first group tile
     __shared__ int wsum_r[32], wsum_t[32];
-    __shared__ int bad;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    pdl_trigger();
-    pdl_wait();  // the ids may come from the previous kernel; the tables may still be read by it
-    for (int e = tid; e < E; e += ROUTE_THREADS) cnt[e] = 0;
-    if (tid == 0) bad = 0;
-    __syncthreads();
-    for (int s = tid; s < S; s += ROUTE_THREADS) {
-        const int e = ids[s];
-        if ((unsigned)e < (unsigned)E) {
-            atomicAdd(&cnt[e], 1);
-        } else {
-            bad = 1;
-            if (ynan) {
-                uint4 *row = reinterpret_cast<uint4 *>(ynan + (size_t)s * ynan_w);
-                for (int c = 0; c < ynan_w / 8; ++c) row[c] = make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u);
-            }
-        }
-    }
-    __syncthreads();
-    // exclusive scans of the row counts and of the tile counts: thread tid
-    // owns experts [tid * per, tid * per + per)
     const int per = (E + ROUTE_THREADS - 1) / ROUTE_THREADS;
-    const int e0 = tid * per, e1 = min(e0 + per, E);
+    const int e0 = min(tid * per, E), e1 = min(e0 + per, E);
     int rsum = 0, tsum = 0;
     for (int e = e0; e < e1; ++e) {
         rsum += cnt[e];
@@ -143,11 +116,121 @@ __global__ void __launch_bounds__(ROUTE_THREADS) moe_group_route_kernel(const in
             tiles[tile0[e] + i] = make_int4(e, pos[e] + i * GROUP_ROWS, min(GROUP_ROWS, n - i * GROUP_ROWS), 0);
     }
     __syncthreads();
-    // placement; the order of an expert's rows is unspecified (each output
-    // row depends on its own X row only, so it does not change the result)
+}
+
+__device__ __forceinline__ void nan_row(uint16_t *ynan, int s, int w)
+{
+    uint4 *row = reinterpret_cast<uint4 *>(ynan + (size_t)s * w);
+    for (int c = 0; c < w / 8; ++c) row[c] = make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u);
+}
+
+// One block, any E <= 4096.  Slots with an expert id outside [0, E) are left
+// out of every group; they set DEVERR_BAD_EXPERT and, when ynan is given,
+// their output row of ynan_w bf16 values is written as NaN.  An expert's
+// rows are placed in no particular order (each output row depends on its
+// own X row only, so the order does not change the result).
+__global__ void __launch_bounds__(ROUTE_THREADS) moe_group_route_kernel(const int32_t *__restrict__ ids, int S, int E,
+                                                                        int *__restrict__ groups,
+                                                                        int *__restrict__ slot_of, uint16_t *ynan,
+                                                                        int ynan_w, int *err)
+{
+    extern __shared__ int route_smem[];
+    int *cnt = route_smem;            // [E] rows per expert
+    int *pos = route_smem + E;        // [E] first sorted row, then the placement cursor
+    int *tile0 = route_smem + 2 * E;  // [E] first group tile
+    __shared__ int bad;
+    const int tid = threadIdx.x;
+    pdl_trigger();
+    pdl_wait();  // the ids may come from the previous kernel; the tables may still be read by it
+    for (int e = tid; e < E; e += ROUTE_THREADS) cnt[e] = 0;
+    if (tid == 0) bad = 0;
+    __syncthreads();
+    for (int s = tid; s < S; s += ROUTE_THREADS) {
+        const int e = ids[s];
+        if ((unsigned)e < (unsigned)E) {
+            atomicAdd(&cnt[e], 1);
+        } else {
+            bad = 1;
+            if (ynan) nan_row(ynan, s, ynan_w);
+        }
+    }
+    __syncthreads();
+    route_scan_tiles(cnt, pos, tile0, E, groups);
     for (int s = tid; s < S; s += ROUTE_THREADS) {
         const int e = ids[s];
         if ((unsigned)e < (unsigned)E) slot_of[atomicAdd(&pos[e], 1)] = s;
+    }
+    if (tid == 0 && bad) set_device_error(err, DEVERR_BAD_EXPERT);
+}
+
+// One block, E <= ROUTE_SMALL_E: warp w takes a contiguous run of slots and
+// keeps its own per-expert counts, so atomics only ever contend within a
+// warp; the warps' counts, scanned per expert, give each warp a contiguous
+// range of every expert's rows to fill.
+constexpr int ROUTE_SMALL_E = 256;
+constexpr int ROUTE_BATCHES = 8;
+
+__global__ void __launch_bounds__(ROUTE_THREADS) moe_group_route_small_kernel(const int32_t *__restrict__ ids, int S,
+                                                                              int E, int *__restrict__ groups,
+                                                                              int *__restrict__ slot_of,
+                                                                              uint16_t *ynan, int ynan_w, int *err)
+{
+    constexpr int NW = ROUTE_THREADS / 32;
+    __shared__ int hist[NW][ROUTE_SMALL_E];  // per warp: count, then its next row within the expert
+    __shared__ int cnt[ROUTE_SMALL_E], pos[ROUTE_SMALL_E], tile0[ROUTE_SMALL_E];
+    __shared__ int bad;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int run = (S + NW - 1) / NW;
+    const int s0 = min(warp * run, S), s1 = min(s0 + run, S);
+    pdl_trigger();
+    pdl_wait();
+    for (int i = tid; i < NW * ROUTE_SMALL_E; i += ROUTE_THREADS) (&hist[0][0])[i] = 0;
+    if (tid == 0) bad = 0;
+    __syncthreads();
+    // ids are read ROUTE_BATCHES batches of 32 at a time, all loads in flight
+    // before the first is used
+    for (int b0 = s0; b0 < s1; b0 += 32 * ROUTE_BATCHES) {
+        int key[ROUTE_BATCHES];
+#pragma unroll
+        for (int i = 0; i < ROUTE_BATCHES; ++i) {
+            const int s = b0 + 32 * i + lane;
+            key[i] = s < s1 ? ids[s] : 0;
+        }
+#pragma unroll
+        for (int i = 0; i < ROUTE_BATCHES; ++i) {
+            const int s = b0 + 32 * i + lane;
+            if (s >= s1) continue;
+            if ((unsigned)key[i] < (unsigned)E) {
+                atomicAdd(&hist[warp][key[i]], 1);
+            } else {
+                bad = 1;
+                if (ynan) nan_row(ynan, s, ynan_w);
+            }
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += ROUTE_THREADS) {
+        int off = 0;
+        for (int w = 0; w < NW; ++w) {
+            const int c = hist[w][e];
+            hist[w][e] = off;
+            off += c;
+        }
+        cnt[e] = off;
+    }
+    __syncthreads();
+    route_scan_tiles(cnt, pos, tile0, E, groups);
+    for (int b0 = s0; b0 < s1; b0 += 32 * ROUTE_BATCHES) {
+        int key[ROUTE_BATCHES];
+#pragma unroll
+        for (int i = 0; i < ROUTE_BATCHES; ++i) {
+            const int s = b0 + 32 * i + lane;
+            key[i] = s < s1 ? ids[s] : -1;
+        }
+#pragma unroll
+        for (int i = 0; i < ROUTE_BATCHES; ++i)
+            if ((unsigned)key[i] < (unsigned)E)
+                slot_of[pos[key[i]] + atomicAdd(&hist[warp][key[i]], 1)] = b0 + 32 * i + lane;
     }
     if (tid == 0 && bad) set_device_error(err, DEVERR_BAD_EXPERT);
 }
@@ -220,8 +303,11 @@ static cudaError_t route_and_gather(const DeviceState &ds, cudaStream_t st, cons
         if (e != cudaSuccess) return e;
         configured_dev[ds.device] = 1;
     }
-    cudaError_t e = launch_k(moe_group_route_kernel, dim3(1), dim3(ROUTE_THREADS), (size_t)3 * E * sizeof(int), st,
-                             ids, p.S, E, groups, slot_of, ynan, ynan_w, ds.err);
+    cudaError_t e = E <= ROUTE_SMALL_E
+                        ? launch_k(moe_group_route_small_kernel, dim3(1), dim3(ROUTE_THREADS), 0, st, ids, p.S, E,
+                                   groups, slot_of, ynan, ynan_w, ds.err)
+                        : launch_k(moe_group_route_kernel, dim3(1), dim3(ROUTE_THREADS), (size_t)3 * E * sizeof(int),
+                                   st, ids, p.S, E, groups, slot_of, ynan, ynan_w, ds.err);
     if (e != cudaSuccess) return e;
     int blocks = (p.S + 7) / 8;  // 8 warps (rows) per block
     const int cap = ds.num_sms * 8;

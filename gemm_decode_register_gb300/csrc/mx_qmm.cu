@@ -17,20 +17,23 @@
 // Per CTA, K streams in 64-wide k-blocks through three rings of shared
 // memory (X slabs, decoded weights, packed codes with their scales):
 //
-//   warp 10     X: NACC 128 x 64 bf16 slabs per k-block by TMA (128-byte
-//               swizzle); both CTAs' slabs complete on CTA 0's barrier
 //   warp 0      codes of the CTA's 128 weight rows by TMA, and their block
 //               scales through registers into shared memory
 //   warp 1      CTA 0: one thread issues the pair's MMAs (NACC accumulators
 //               of 256 columns sharing the decoded weights) and commits each
 //               k-block to the empty barriers of both CTAs
-//   warps 2-9   decoders: two threads per weight row, 32 elements each; they
-//               decode the codes exactly to bf16 (code * scale has at most 6
-//               significant bits) into the 128-byte-swizzled K-major layout
-//               TMA produces; CTA 0's warps then arrive on CTA 0's barrier,
-//               CTA 1's signal it with a 16-byte bulk copy that completes
-//               there.  Then the epilogue: tcgen05.ld of the CTA's
-//               accumulator rows, NVFP4 tensor scale, round to bf16, store.
+//   warps 2-    decoders, in groups of 8 warps (one group for 512-row tiles,
+//               two taking alternate k-blocks for 256-row tiles, whose MMAs
+//               are twice as fast per k-block): two threads per weight row,
+//               32 elements each; they decode the codes exactly to bf16
+//               (code * scale has at most 6 significant bits) into the
+//               128-byte-swizzled K-major layout TMA produces; CTA 0's warps
+//               then arrive on CTA 0's barrier, CTA 1's signal it with a
+//               16-byte bulk copy that completes there.  Then the epilogue:
+//               tcgen05.ld of the CTA's accumulator rows, NVFP4 tensor
+//               scale, round to bf16, store.
+//   last warp   X: NACC 128 x 64 bf16 slabs per k-block by TMA (128-byte
+//               swizzle); both CTAs' slabs complete on CTA 0's barrier
 //
 // Every mbarrier wait is bounded (about two seconds of %globaltimer); a wait
 // that gives up sets MX_DEVERR_TIMEOUT in the device error word, the CTA
@@ -45,8 +48,6 @@ namespace mx {
 
 constexpr int QMM_BN = 256;                    // UMMA N: 128 weight rows from each CTA
 constexpr int QMM_BK = 64;                     // bf16 elements per 128-byte swizzle row
-constexpr int QMM_THREADS = 352;               // 11 warps
-constexpr int QMM_SPF = 4;                     // k-blocks of block scales the producer keeps in flight
 constexpr int QMM_X_BYTES = 128 * QMM_BK * 2;  // a CTA's 128 rows of one 256-row X slab
 constexpr int QMM_W_BYTES = 128 * QMM_BK * 2;  // a CTA's 128 decoded weight rows
 constexpr int QMM_SMEM_LIMIT = 232448;         // 227 KB of dynamic shared memory per CTA
@@ -66,11 +67,18 @@ struct QmmGeo {
     static constexpr int SPK = FMT == FMT_NVFP4 ? 4 : 2;  // scale bytes per row per k-block
     static constexpr int SC_BYTES = 128 * SPK;
     static constexpr int X_STAGE = NACC * QMM_X_BYTES;
-    static constexpr int SX = NACC == 2 ? 4 : 6;
-    static constexpr int SD = NACC == 2 ? 5 : 6;
+    static constexpr int SX = NACC == 2 ? 4 : 8;  // 256-row tiles: X slabs land late under load, go deeper
+    static constexpr int SD = NACC == 2 ? 5 : 4;
+    static constexpr int SC_MAX = 4;  // codes ring depth cap
+    // decoder groups: with 256-row tiles one group of 8 warps decoding a
+    // k-block at a time cannot keep up with the MMAs (its warps are latency
+    // bound), so two groups take alternate k-blocks
+    static constexpr int NG = NACC == 1 ? 2 : 1;
+    static constexpr int THREADS = 96 + 256 * NG;  // codes producer, MMA, X producer, decoders
+    static constexpr int SPF = 4;     // k-blocks of block scales the producer keeps in flight
     static constexpr int RESERVED = 1024 /*align*/ + 128 /*signal landing*/ + 512 /*barriers*/;
     static constexpr int C_FIT = (QMM_SMEM_LIMIT - RESERVED - SX * X_STAGE - SD * QMM_W_BYTES) / (C_BYTES + SC_BYTES);
-    static constexpr int SC = C_FIT > 4 ? 4 : C_FIT;
+    static constexpr int SC = C_FIT > SC_MAX ? SC_MAX : C_FIT;
     // layout: [X ring][D ring][codes ring][scales ring][signal landing][barriers]
     static constexpr int OFF_D = SX * X_STAGE;
     static constexpr int OFF_C = OFF_D + SD * QMM_W_BYTES;
@@ -81,6 +89,9 @@ struct QmmGeo {
     static constexpr int TMEM_COLS = 256 * NACC;
     static_assert(OFF_C % 1024 == 0 && OFF_S % 128 == 0 && OFF_SIG % 128 == 0, "ring alignment");
     static_assert(SC >= 2, "codes ring too shallow");
+    // each ring slot is always used by the same decoder group (so a group
+    // never waits on a phase two completions ahead of the barrier)
+    static_assert(SC % NG == 0 && SD % NG == 0, "ring depth and decoder groups");
     static_assert((2 * SX + 2 * SC + 3 * SD + 1) * 8 + 16 <= 512, "barrier area");
     static_assert(SMEM <= QMM_SMEM_LIMIT, "shared memory");
 };
@@ -165,13 +176,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
-// Cluster-scope acquire: phases may be completed by the peer CTA's threads
-// or by the pair's MMA commits.
+// Wait on a phase with the default (CTA-scope acquire) semantics.  Every
+// cross-CTA hand-over completes through the asynchronous proxy (TMA and bulk
+// copies completing transactions on the barrier, tcgen05.commit arrivals), so
+// a CTA-scope acquire is what the consumer needs; a cluster-scope acquire
+// cost measurably more per wait on the MMA thread's critical path.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
                  "selp.u32 %0, 1, 0, p;\n\t}"
                  : "=r"(ok)
                  : "r"(smem_u32(bar)), "r"(parity)
@@ -460,6 +474,19 @@ struct QmmArgs {
     int ntile;           // column tiles per group tile
 };
 
+// silu(g) * u rounded to bf16 for the prefill SwiGLU epilogue: the same
+// formula as swiglu_bf16 (sigmoid from e^-|g|, so nothing overflows) with the
+// fast exponent and division intrinsics; the epilogue of a 256-row tile
+// evaluates it 32768 times per CTA after the last MMA, where the exactly
+// rounded division dominated the tile's tail.  The result differs from
+// swiglu_bf16's by at most one bf16 unit, and only near rounding boundaries.
+__device__ __forceinline__ uint32_t swiglu_bf16_fast(float g, float u)
+{
+    const float e = __expf(-fabsf(g));
+    const float sig = __fdividef(g >= 0.0f ? 1.0f : e, 1.0f + e);
+    return f32x2_to_bf16x2(g * sig * u, 0.0f) & 0xFFFFu;
+}
+
 // 32 contiguous bytes to global memory (32-byte aligned address).
 __device__ __forceinline__ void st_global_v8(void *p, const uint32_t *v)
 {
@@ -469,7 +496,7 @@ __device__ __forceinline__ void st_global_v8(void *p, const uint32_t *v)
 }
 
 template <int FMT, int NACC, int MODE>
-__global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_constant__ CUtensorMap tmap_x,
+__global__ void __launch_bounds__(QmmGeo<FMT, NACC>::THREADS, 1) qmm_kernel(const __grid_constant__ CUtensorMap tmap_x,
                                                              const __grid_constant__ CUtensorMap tmap_c, QmmArgs a)
 {
     using QG = QmmGeo<FMT, NACC>;
@@ -566,7 +593,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_consta
     pdl_trigger();
     if constexpr (MODE == QMM_DENSE) pdl_wait();  // X and Y may be used by the neighbouring kernels
 
-    if (warp == 10) {
+    if (warp == 2 + 8 * QG::NG) {
         // ---------------- X producer: both CTAs' slabs complete on CTA 0's
         // barrier, each CTA adding one arrival and its own bytes
         if (lane == 0) {
@@ -587,21 +614,21 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_consta
         }
     } else if (warp == 0) {
         // ---------------- codes producer: codes by TMA (lane 0), block scales
-        // (whole warp, QMM_SPF k-blocks in flight).  The scales come through
+        // (whole warp, QG::SPF k-blocks in flight).  The scales come through
         // shared memory so that the decoders hold no global loads in flight.
         const size_t srow_bytes = (size_t)KB * SPK;
         const uint8_t *sbase = a.scales + (size_t)(wrow + lane) * srow_bytes;
-        uint32_t pv[QMM_SPF][4];
+        uint32_t pv[QG::SPF][4];
 #pragma unroll
-        for (int j = 0; j < QMM_SPF; ++j)
+        for (int j = 0; j < QG::SPF; ++j)
 #pragma unroll
             for (int i = 0; i < 4; ++i)
                 if (j < KB) pv[j][i] = scale_load<SPK>(sbase + (size_t)(32 * i) * srow_bytes + SPK * j);
         int issued = 0;
         bool go = true;
-        for (int kb0 = 0; kb0 < KB && go; kb0 += QMM_SPF) {
+        for (int kb0 = 0; kb0 < KB && go; kb0 += QG::SPF) {
 #pragma unroll
-            for (int j = 0; j < QMM_SPF; ++j) {
+            for (int j = 0; j < QG::SPF; ++j) {
                 const int kb = kb0 + j;
                 if (kb >= KB) break;
                 const int s = kb % SC;
@@ -624,10 +651,10 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_consta
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&full_c[s]);
                 issued = kb + 1;
-                if (kb + QMM_SPF < KB)
+                if (kb + QG::SPF < KB)
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                        pv[j][i] = scale_load<SPK>(sbase + (size_t)(32 * i) * srow_bytes + SPK * (kb + QMM_SPF));
+                        pv[j][i] = scale_load<SPK>(sbase + (size_t)(32 * i) * srow_bytes + SPK * (kb + QG::SPF));
             }
         }
         // drain: every issued codes TMA must land before the CTA may exit
@@ -665,14 +692,16 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_consta
             *x_taken = taken;
         }
     } else {
-        // ---------------- decoders (warps 2..9): thread d decodes half (d & 1)
-        // of weight row n0 + 128 rank + (d >> 1).  CTA 0's decoders arrive on
-        // their own barrier; CTA 1's signal CTA 0 with a 16-byte bulk copy.
-        const int d = threadIdx.x - 64;
+        // ---------------- decoders (warps 2 ..): group grp (8 warps) takes
+        // k-blocks grp, grp + NG, ...; its thread d decodes half (d & 1) of
+        // weight row wrow + (d >> 1).  CTA 0's decoders arrive on their own
+        // barrier; CTA 1's signal CTA 0 with a 16-byte bulk copy.
+        const int dw = warp - 2, grp = dw >> 3, dl = dw & 7;
+        const int d = 32 * dl + lane;
         const int row = d >> 1, half = d & 1;
-        const uint32_t sig0 = map_to_cta(smem_u32(sig + 16 * (warp - 2)), 0);
+        const uint32_t sig0 = map_to_cta(smem_u32(sig + 16 * dl), 0);
         const uint32_t pf0 = map_to_cta(smem_u32(peer_full), 0);
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = grp; kb < KB; kb += QG::NG) {
             const int sc = kb % SC, sd = kb % SD;
             if (!mbar_wait(&full_c[sc], (kb / SC) & 1, abort_flag, a.wait_ns)) break;
             const uint8_t *cp = cring + sc * QG::C_BYTES + row * QG::CODE_ROW + half * (QG::CODE_ROW / 2);
@@ -704,14 +733,14 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_consta
             __syncwarp();
             if (lane == 0) {
                 if (rank == 0) mbar_arrive(&dec_full[sd]);
-                else bulk_signal(sig0, dslot + 16 * (warp - 2), pf0 + 8u * (uint32_t)sd);
+                else bulk_signal(sig0, dslot + 16 * dl, pf0 + 8u * (uint32_t)sd);
             }
         }
     }
 
     // ---------------- epilogue (decoder warps): TMEM -> bf16 -> Y
     bool acc_ok = true;
-    if (warp >= 2 && warp <= 9) {
+    if (warp >= 2 && warp < 2 + 8 * QG::NG) {
         // the MMAs must have finished (even on abort) before TMEM is read or freed
         acc_ok = mbar_wait(acc_full, 0, abort_flag, a.wait_ns, false);
     }
@@ -720,7 +749,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_consta
     cluster_sync_all();
     tc_fence_after();
     const int aborted = *abort_flag | ld_cluster_s32(map_to_cta(smem_u32((const void *)abort_flag), rank ^ 1u));
-    if (aborted && rank == 0 && threadIdx.x == 320) {
+    if (aborted && rank == 0 && threadIdx.x == 32 * (2 + 8 * QG::NG)) {
         // X slabs the MMAs did not take may still be landing in either CTA:
         // supply the arrival of a CTA that did not load a k-block, then wait
         // for each outstanding slot (its bytes complete on this barrier)
@@ -736,10 +765,11 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_consta
         // microseconds; give them that long before this CTA may exit
         __nanosleep(20000);
     }
-    if (warp >= 2 && warp <= 9) {
+    if (warp >= 2 && warp < 2 + 8 * QG::NG) {
         const bool ok = acc_ok && !aborted;
-        const int quarter = warp & 3;   // TMEM lanes 32*quarter .. +31
-        const int group = (warp - 2) >> 2;  // which half of the accumulator columns
+        const int quarter = warp & 3;      // TMEM lanes 32*quarter .. +31 (a warp reads its own quarter)
+        const int group = (warp - 2) >> 2;  // which of the 2 * NG column ranges
+        constexpr int NCG = 2 * QG::NG;
         float g = 1.0f;
         if (FMT == FMT_NVFP4) {
             const size_t blocks = (size_t)(MODE == QMM_DENSE ? 1 : a.E) * a.N * (a.K / 16);
@@ -749,7 +779,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_consta
             // columns c (gate) and 128 + c (up) of a row hold the same h column
             const int i = 128 * (int)rank + 32 * quarter + lane;  // tile row
             const int hw = a.N / 2;
-            for (int c = 64 * group; c < 64 * group + 64; c += 32) {
+            for (int c = group * (128 / NCG); c < (group + 1) * (128 / NCG); c += 32) {
                 uint32_t vg[32], vu[32];
                 if (ok) {
                     tmem_ld32(tmem + (uint32_t)c + ((uint32_t)(quarter * 32) << 16), vg);
@@ -769,7 +799,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_consta
                         u0 = __fmul_rn(u0, g);
                         u1 = __fmul_rn(u1, g);
                     }
-                    o[j] = swiglu_bf16(g0, u0) | (swiglu_bf16(g1, u1) << 16);
+                    o[j] = swiglu_bf16_fast(g0, u0) | (swiglu_bf16_fast(g1, u1) << 16);
                 }
                 if (i < rows) {
                     uint16_t *dst = a.Y + (size_t)(m0 + i) * hw + n0 + c;
@@ -785,7 +815,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const __grid_consta
                 }
             }
         } else {
-            for (int c = group * NACC * 128; c < (group + 1) * NACC * 128; c += 32) {
+            for (int c = group * (NACC * 256 / NCG); c < (group + 1) * (NACC * 256 / NCG); c += 32) {
                 const int h = c / QMM_BN, nc = c % QMM_BN;
                 const int i = 256 * h + 128 * (int)rank + 32 * quarter + lane;  // tile row
                 uint32_t v[32];
@@ -871,7 +901,7 @@ static cudaError_t run_qmm(const DeviceState &ds, cudaStream_t st, const CUtenso
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * pairs);
-    cfg.blockDim = dim3(QMM_THREADS);
+    cfg.blockDim = dim3(QG::THREADS);
     cfg.dynamicSmemBytes = QG::SMEM;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];

@@ -176,7 +176,8 @@ int mx_moe_qmm(int fmt, const void *expert_codes, const void *expert_scales, con
                size_t workspace_bytes);
 
 /* Expert-batched MoE FFN prefill, one call:
- *   h[t][j]  = bf16_rne( silu(W_gu,e[0:I] x[t]) * (W_gu,e[I:2I] x[t]) )   (as mx_moe_gate_up_swiglu)
+ *   h[t][j]  = bf16_rne( silu(W_gu,e[0:I] x[t]) * (W_gu,e[I:2I] x[t]) )   (as mx_moe_gate_up_swiglu,
+ *              with the fast exponent and division: within one bf16 unit of it)
  *   yd[t][j] = bf16_rne( W_dn,e h[t][j] )
  *   out[t][n] = sum_j r[t][j] * yd[t][j][n]  (fp32 fused multiply-adds in slot order)
  * e = expert_ids[t][j]; gate-up stacks [E][2I][H], down stacks [E][H][I];

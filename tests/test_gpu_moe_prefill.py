@@ -51,6 +51,22 @@ def test_moe_qmm_parity(orc, fmt, T, E, topk, N, K):
     check_close(bf16_bits_to_f64(y), want.reshape(T * topk, N), f"moe_qmm fmt{fmt} T{T}", bf16_out=True)
 
 
+def test_moe_qmm_many_experts(orc):
+    """More experts than the per-warp counting tables hold (E = 300): the
+    routing takes its shared-counter path."""
+    need_gpu()
+    fmt, T, E, topk, N, K = 0, 64, 300, 4, 256, 64
+    codes, scales = synth.weights(fmt, N, K, 60, E=E)
+    x = synth.activations(T, K, 59)
+    ids = synth.expert_ids(T, E, topk, 58)
+    ids[:20, 0] = 7  # one expert with more rows than the rest
+    ids[:20, 1:] = synth.expert_ids(20, E - 8, topk - 1, 57) + 8
+    y = bf16_host(run_moe_qmm(fmt, codes, scales, x, ids, E, N)).reshape(T * topk, N)
+    want, rc = orc.moe_qmv(fmt, codes, scales, x, ids, T, E, topk, N, K)
+    assert rc == 0
+    check_close(bf16_bits_to_f64(y), want.reshape(T * topk, N), "moe_qmm E=300", bf16_out=True)
+
+
 def test_moe_qmm_skewed_routing(orc):
     """Every slot on one expert (three group tiles), the others idle; and the
     down-projection call form (topk = 1 over T * topk rows)."""
