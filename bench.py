@@ -586,6 +586,8 @@ CASES = {
     "qmm_down": ("qmm", 0, 4096, 8192, 28672),
     "qmm_small": ("qmm", 0, 1024, 4096, 4096),
     "qmm_mid": ("qmm", 0, 2048, 8192, 4096),
+    # expert-batched MoE FFN prefill: 4096 tokens, top-8 of 128 experts, hidden 2048, I 768
+    "moe_prefill_ffn_t4096": ("moe_prefill", 0, 4096, 2048, 768),
 }
 
 
@@ -600,7 +602,19 @@ def run_case(args):
     b.build()
     kind, fmt, M, N, K = CASES[args.case]
     stream = torch.cuda.current_stream()
-    if kind == "moe_ffn":
+    if kind == "moe_prefill":
+        E, topk, H, I = 128, 8, N, K
+        c1, s1 = synth.weights(fmt, 2 * I, H, 40, E=E)
+        c2, s2 = synth.weights(fmt, H, I, 41, E=E)
+        d1, e1, d2, e2 = (upload(torch, a) for a in (c1, s1, c2, s2))
+        ids = torch.from_numpy(synth.expert_ids(M, E, topk, 5)).cuda()
+        r = torch.from_numpy(synth.router_weights(M, topk, 7)).cuda()
+        x = bf16_dev(torch, synth.activations(M, H, 6)).view(M, H)
+        out = torch.empty((M, H), dtype=torch.float32, device="cuda")
+        ws = ops.moe_ffn_prefill_workspace(M, E, topk, H, I)
+        f = lambda: ops.moe_ffn_prefill(fmt, d1, e1, d2, e2, x, ids, r, E, I, out=out, workspace=ws)  # noqa: E731
+        wb = c1.nbytes + s1.nbytes + c2.nbytes + s2.nbytes
+    elif kind == "moe_ffn":
         E, topk, H, I = 128, 8, N, K
         c1, s1 = synth.weights(fmt, 2 * I, H, 40, E=E)
         c2, s2 = synth.weights(fmt, H, I, 41, E=E)
@@ -641,6 +655,8 @@ def run_case(args):
            "weight_gbs": round(wb / t / 1e9, 1)}
     if kind == "qmm":
         out["tflops"] = round(2.0 * M * N * K / t / 1e12, 1)
+    if kind == "moe_prefill":
+        out["tflops"] = round(2.0 * M * 8 * 3 * N * K / t / 1e12, 1)
     print(json.dumps(out), flush=True)
 
 
