@@ -63,3 +63,84 @@ def test_moe_rejects(lib, args, want):
 ])
 def test_qmm_rejects(lib, args, want):
     assert lib.mx_qmm(*args) == want
+
+
+Z = 1 << 30  # a workspace size large enough for every case below
+
+
+@pytest.mark.parametrize("args,want", [
+    ((9, A, A, A, A, A, 8, 4, 2, 256, 64, A, Z), -2),       # unknown format
+    ((0, A, A, A, A, A, 8, 4, 5, 256, 64, A, Z), -1),       # topk > E
+    ((0, A, A, A, 0, A, 8, 4, 2, 256, 64, A, Z), -1),       # null ids
+    ((0, A, A, A, A, A, 8, 4, 2, 256, 64, 0, Z), -1),       # null workspace
+    ((0, A, A, A, A, A, 8, 4, 2, 128, 64, A, Z), -2),       # N not a multiple of 256
+    ((0, A, A, A, A, A, 8, 4, 2, 256, 96, A, Z), -2),       # K not a multiple of 64
+    ((0, A, A, A, A, A, 8, 5000, 2, 256, 64, A, Z), -2),    # E > 4096
+    ((0, A, A, A, A, A, 8, 4, 2, 256, 64, A, 1024), -1),    # workspace too small
+    ((0, A, A, A, A, A, 8, 4, 2, 256, 64, A + 16, Z), -3),  # workspace not 256-byte aligned
+    ((0, A, A, A, A + 2, A, 8, 4, 2, 256, 64, A, Z), -3),   # misaligned ids
+])
+def test_moe_qmm_rejects(lib, args, want):
+    assert lib.mx_moe_qmm(*args) == want
+
+
+@pytest.mark.parametrize("args,want", [
+    ((0, A, A, A, A, A, A, A, A, 8, 4, 2, 256, 128, A, Z), 0),     # valid (not called: see below)
+    ((0, A, A, A, A, A, A, A, A, 8, 4, 2, 320, 128, A, Z), -2),    # H not a multiple of 256
+    ((0, A, A, A, A, A, A, A, A, 8, 4, 2, 256, 96, A, Z), -2),     # I not a multiple of 128
+    ((0, A, A, A, A, A, A, 0, A, 8, 4, 2, 256, 128, A, Z), -1),    # null router weights
+    ((0, A, A, A, A, A, A, A, A, 8, 4, 2, 256, 128, A, 4096), -1),  # workspace too small
+    ((0, A, A, A, A, A, A, A + 2, A, 8, 4, 2, 256, 128, A, Z), -3),  # misaligned router weights
+])
+def test_moe_ffn_prefill_rejects(lib, args, want):
+    if want == 0:
+        return  # a valid call would launch kernels
+    assert lib.mx_moe_ffn_prefill(*args) == want
+
+
+def _align256(v):
+    return (v + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("T,E,topk,K,I", [(4096, 128, 8, 2048, 768), (1, 8, 8, 256, 128), (37, 300, 3, 64, 0),
+                                         (1000, 1, 1, 512, 256)])
+def test_prefill_workspace_sizes(lib, T, E, topk, K, I):
+    """Workspace = tile table (16 bytes + 16 per group tile, at most
+    (S + 255 * min(S, E)) / 256 tiles for S = T * topk routed rows) + sorted
+    row -> slot (4 S) + gathered activations (2 S K) [+ SwiGLU output 2 S I],
+    each part 256-byte aligned."""
+    S = T * topk
+    tiles = (S + 255 * min(S, E)) // 256
+    plain = _align256(_align256(16 + 16 * tiles) + 4 * S) + 2 * S * K
+    assert lib.mx_moe_qmm_workspace_size(T, E, topk, K) == _align256(plain)
+    if I:
+        assert lib.mx_moe_ffn_prefill_workspace_size(T, E, topk, K, I) == _align256(_align256(plain) + 2 * S * I)
+    assert lib.mx_moe_qmm_workspace_size(0, E, topk, K) == 0
+    assert lib.mx_moe_qmm_workspace_size(T, E, E + 1, K) == 0
+
+
+def test_group_tile_bound():
+    """The grid bound (S + 255 * min(S, E)) / 256 covers every routing: brute
+    force over random and adversarial row counts per expert."""
+    import numpy as np
+
+    rng = np.random.default_rng(0)
+    for _ in range(2000):
+        E = int(rng.integers(1, 300))
+        S = int(rng.integers(1, 5000))
+        kind = rng.integers(0, 3)
+        if kind == 0:
+            counts = np.bincount(rng.integers(0, E, S), minlength=E)
+        elif kind == 1:  # as many experts as possible just above a multiple of 256
+            counts = np.zeros(E, np.int64)
+            left = S
+            for e in range(E):
+                take = min(left, 257 if left >= 257 else left)
+                counts[e] = take
+                left -= take
+            counts[0] += left
+        else:
+            counts = np.zeros(E, np.int64)
+            counts[rng.integers(0, E)] = S
+        tiles = int(sum((c + 255) // 256 for c in counts))
+        assert tiles <= (S + 255 * min(S, E)) // 256
