@@ -1,8 +1,10 @@
 // mx_moe_prefill.cu -- expert-batched MoE prefill: the routed (token, slot)
 // rows are grouped by expert on the device, gathered into expert order and
 // run through the pair tensor-core GEMM (qmm_kernel, grouped modes) one
-// 256-row group tile at a time, so that each expert's weights are decoded
-// once per 256 routed rows instead of once per token.
+// group tile of up to 512 rows at a time (two 256-row accumulators sharing
+// each decoded weight tile; a tile of at most 256 rows runs only the first),
+// so that each expert's weights are decoded once per 512 routed rows instead
+// of once per token.
 //
 // The pages read only the experts a token is routed to (talk "High-
 // performance LLM/VLM inference on AMD Strix Halo with mlxcel engine",
@@ -32,7 +34,7 @@
 
 namespace mx {
 
-constexpr int GROUP_ROWS = 256;  // rows of a group tile (the pair MMA's M)
+constexpr int GROUP_ROWS = 512;  // rows of a group tile (two 256-row pair MMAs sharing the decoded weights)
 constexpr int ROUTE_THREADS = 1024;
 
 static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
@@ -42,7 +44,7 @@ MoeGroupPlan moe_group_plan(int T, int E, int topk, int K, int I)
     MoeGroupPlan p;
     const long long S = (long long)T * topk;
     const long long active = S < E ? S : E;
-    // sum over experts of ceil(rows_e / 256) <= (S + 255 * active experts) / 256
+    // sum over experts of ceil(rows_e / G) <= (S + (G - 1) * active experts) / G
     p.S = (int)S;
     p.max_groups = (int)((S + (long long)(GROUP_ROWS - 1) * active) / GROUP_ROWS);
     p.off_groups = 0;
@@ -54,7 +56,7 @@ MoeGroupPlan moe_group_plan(int T, int E, int topk, int K, int I)
 }
 
 // Exclusive scans of the per-expert row counts cnt[] and tile counts
-// (ceil(cnt / 256)) into pos[] and tile0[], the group tile table, and the
+// (ceil(cnt / GROUP_ROWS)) into pos[] and tile0[], the group tile table, and the
 // totals in groups[0] (tiles) and groups[1] (rows).  Thread tid owns experts
 // [tid * per, tid * per + per).  Ends with the block synchronised.
 __device__ void route_scan_tiles(const int *cnt, int *pos, int *tile0, int E, int *groups)

@@ -59,7 +59,7 @@ constexpr unsigned long long QMM_WAIT_NS = 2000000000ull;
 //   C ring (SC slots): the packed codes (TMA) and block scales of a k-block.
 // A D slot is held from its decode through the hand-over to CTA 0 until the
 // MMA finishes; a C slot only until its codes are decoded.
-template <int FMT, int NACC>
+template <int FMT, int NACC, bool GROUPED = false>
 struct QmmGeo {
     static constexpr int BM = 256 * NACC;  // output rows per pair tile
     static constexpr int CODE_ROW = FMT == FMT_MXFP8 ? QMM_BK : QMM_BK / 2;  // code bytes per row per k-block
@@ -67,13 +67,14 @@ struct QmmGeo {
     static constexpr int SPK = FMT == FMT_NVFP4 ? 4 : 2;  // scale bytes per row per k-block
     static constexpr int SC_BYTES = 128 * SPK;
     static constexpr int X_STAGE = NACC * QMM_X_BYTES;
-    static constexpr int SX = NACC == 2 ? 4 : 8;  // 256-row tiles: X slabs land late under load, go deeper
-    static constexpr int SD = NACC == 2 ? 5 : 4;
-    static constexpr int SC_MAX = 4;  // codes ring depth cap
     // decoder groups: with 256-row tiles one group of 8 warps decoding a
     // k-block at a time cannot keep up with the MMAs (its warps are latency
-    // bound), so two groups take alternate k-blocks
-    static constexpr int NG = NACC == 1 ? 2 : 1;
+    // bound), so two groups take alternate k-blocks; grouped tiles (up to 512
+    // rows, often only 256 used) take two groups as well
+    static constexpr int NG = (NACC == 1 || GROUPED) ? 2 : 1;
+    static constexpr int SX = NACC == 2 ? 4 : 8;  // 256-row tiles: X slabs land late under load, go deeper
+    static constexpr int SD = NACC == 2 ? (NG == 2 ? 4 : 5) : 4;
+    static constexpr int SC_MAX = 4;  // codes ring depth cap
     static constexpr int THREADS = 96 + 256 * NG;  // codes producer, MMA, X producer, decoders
     static constexpr int SPF = 4;     // k-blocks of block scales the producer keeps in flight
     static constexpr int RESERVED = 1024 /*align*/ + 128 /*signal landing*/ + 512 /*barriers*/;
@@ -496,11 +497,10 @@ __device__ __forceinline__ void st_global_v8(void *p, const uint32_t *v)
 }
 
 template <int FMT, int NACC, int MODE>
-__global__ void __launch_bounds__(QmmGeo<FMT, NACC>::THREADS, 1) qmm_kernel(const __grid_constant__ CUtensorMap tmap_x,
+__global__ void __launch_bounds__(QmmGeo<FMT, NACC, MODE != QMM_DENSE>::THREADS, 1) qmm_kernel(const __grid_constant__ CUtensorMap tmap_x,
                                                              const __grid_constant__ CUtensorMap tmap_c, QmmArgs a)
 {
-    using QG = QmmGeo<FMT, NACC>;
-    static_assert(MODE == QMM_DENSE || NACC == 1, "grouped tiles are 256 rows");
+    using QG = QmmGeo<FMT, NACC, MODE != QMM_DENSE>;
     constexpr int SX = QG::SX, SD = QG::SD, SC = QG::SC, SPK = QG::SPK;
     constexpr uint32_t SIG_BYTES = 8 * 16;  // one 16-byte signal per decoder warp of CTA 1
     extern __shared__ uint8_t smem_raw[];
@@ -555,6 +555,9 @@ __global__ void __launch_bounds__(QmmGeo<FMT, NACC>::THREADS, 1) qmm_kernel(cons
             wrow = expert * a.N + (int)rank * (a.N / 2) + n0;
         }
     }
+    // 256-row halves of the tile that hold rows: a grouped tile of at most 256
+    // rows skips the second half's X slabs, MMAs and epilogue
+    const int nh = (MODE == QMM_DENSE || rows > 256) ? NACC : 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < SX; ++s) {
@@ -603,11 +606,12 @@ __global__ void __launch_bounds__(QmmGeo<FMT, NACC>::THREADS, 1) qmm_kernel(cons
                 const int s = kb % SX;
                 if (kb >= SX && !mbar_wait(&empty_x[s], ((kb / SX) - 1) & 1, abort_flag, a.wait_ns)) break;
                 const uint32_t bar = fx0 + 8u * (uint32_t)s;
-                mbar_arrive_expect_tx_cluster(bar, NACC * QMM_X_BYTES);
+                mbar_arrive_expect_tx_cluster(bar, (uint32_t)(nh * QMM_X_BYTES));
 #pragma unroll
                 for (int h = 0; h < NACC; ++h)
-                    tma_load_2d_pair(xring + s * QG::X_STAGE + h * QMM_X_BYTES, &tmap_x, kb * QMM_BK,
-                                     m0 + 256 * h + 128 * (int)rank, bar);
+                    if (h < nh)
+                        tma_load_2d_pair(xring + s * QG::X_STAGE + h * QMM_X_BYTES, &tmap_x, kb * QMM_BK,
+                                         m0 + 256 * h + 128 * (int)rank, bar);
                 issued = kb + 1;
             }
             *x_issued = issued;
@@ -683,7 +687,9 @@ __global__ void __launch_bounds__(QmmGeo<FMT, NACC>::THREADS, 1) qmm_kernel(cons
                     const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
 #pragma unroll
                     for (int h = 0; h < NACC; ++h)
-                        umma2_bf16(tmem + h * QMM_BN, sw128_desc(xa + h * QMM_X_BYTES + kk * 32), bd, idesc, acc);
+                        if (h < nh)
+                            umma2_bf16(tmem + h * QMM_BN, sw128_desc(xa + h * QMM_X_BYTES + kk * 32), bd, idesc,
+                                       acc);
                 }
                 umma2_commit_both(&empty_x[sx]);
                 umma2_commit_both(&empty_d[sd]);
@@ -776,14 +782,19 @@ __global__ void __launch_bounds__(QmmGeo<FMT, NACC>::THREADS, 1) qmm_kernel(cons
             g = load_f32_unaligned(a.scales + blocks + 4 * (size_t)expert);
         }
         if constexpr (MODE == QMM_GROUPED_GLU) {
-            // columns c (gate) and 128 + c (up) of a row hold the same h column
-            const int i = 128 * (int)rank + 32 * quarter + lane;  // tile row
+            // in accumulator h, columns c (gate) and 128 + c (up) of a row hold
+            // the same h column
             const int hw = a.N / 2;
-            for (int c = group * (128 / NCG); c < (group + 1) * (128 / NCG); c += 32) {
+            constexpr int PER = NACC * 128 / NCG;
+            for (int cc = group * PER; cc < (group + 1) * PER; cc += 32) {
+                const int h = cc / 128, c = cc % 128;
+                if (h >= nh) continue;  // warp-uniform
+                const int i = 256 * h + 128 * (int)rank + 32 * quarter + lane;  // tile row
+                const uint32_t tb = tmem + (uint32_t)(h * QMM_BN) + ((uint32_t)(quarter * 32) << 16);
                 uint32_t vg[32], vu[32];
                 if (ok) {
-                    tmem_ld32(tmem + (uint32_t)c + ((uint32_t)(quarter * 32) << 16), vg);
-                    tmem_ld32(tmem + (uint32_t)(128 + c) + ((uint32_t)(quarter * 32) << 16), vu);
+                    tmem_ld32(tb + (uint32_t)c, vg);
+                    tmem_ld32(tb + (uint32_t)(128 + c), vu);
                 } else {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) vg[j] = vu[j] = 0x7FC00000u;
@@ -817,6 +828,7 @@ __global__ void __launch_bounds__(QmmGeo<FMT, NACC>::THREADS, 1) qmm_kernel(cons
         } else {
             for (int c = group * (NACC * 256 / NCG); c < (group + 1) * (NACC * 256 / NCG); c += 32) {
                 const int h = c / QMM_BN, nc = c % QMM_BN;
+                if (h >= nh) continue;  // warp-uniform
                 const int i = 256 * h + 128 * (int)rank + 32 * quarter + lane;  // tile row
                 uint32_t v[32];
                 if (ok) {
@@ -890,7 +902,7 @@ template <int FMT, int NACC, int MODE>
 static cudaError_t run_qmm(const DeviceState &ds, cudaStream_t st, const CUtensorMap &xmap, const CUtensorMap &cmap,
                            const QmmArgs &a, int pairs)
 {
-    using QG = QmmGeo<FMT, NACC>;
+    using QG = QmmGeo<FMT, NACC, MODE != QMM_DENSE>;
     if (QG::SMEM > ds.max_smem_optin) return cudaErrorInvalidValue;
     static int configured_dev[64] = {0};
     if (ds.device < 64 && !configured_dev[ds.device]) {
@@ -992,13 +1004,13 @@ cudaError_t launch_qmm_grouped(const DeviceState &ds, cudaStream_t st, int fmt, 
     a.ntile = swiglu ? (N / 2) / 128 : N / QMM_BN;
     const int pairs = max_groups * a.ntile;
     if (swiglu) {
-        if (fmt == FMT_MXFP4) return run_qmm<FMT_MXFP4, 1, QMM_GROUPED_GLU>(ds, st, xmap, cmap, a, pairs);
-        if (fmt == FMT_MXFP8) return run_qmm<FMT_MXFP8, 1, QMM_GROUPED_GLU>(ds, st, xmap, cmap, a, pairs);
-        return run_qmm<FMT_NVFP4, 1, QMM_GROUPED_GLU>(ds, st, xmap, cmap, a, pairs);
+        if (fmt == FMT_MXFP4) return run_qmm<FMT_MXFP4, 2, QMM_GROUPED_GLU>(ds, st, xmap, cmap, a, pairs);
+        if (fmt == FMT_MXFP8) return run_qmm<FMT_MXFP8, 2, QMM_GROUPED_GLU>(ds, st, xmap, cmap, a, pairs);
+        return run_qmm<FMT_NVFP4, 2, QMM_GROUPED_GLU>(ds, st, xmap, cmap, a, pairs);
     }
-    if (fmt == FMT_MXFP4) return run_qmm<FMT_MXFP4, 1, QMM_GROUPED>(ds, st, xmap, cmap, a, pairs);
-    if (fmt == FMT_MXFP8) return run_qmm<FMT_MXFP8, 1, QMM_GROUPED>(ds, st, xmap, cmap, a, pairs);
-    return run_qmm<FMT_NVFP4, 1, QMM_GROUPED>(ds, st, xmap, cmap, a, pairs);
+    if (fmt == FMT_MXFP4) return run_qmm<FMT_MXFP4, 2, QMM_GROUPED>(ds, st, xmap, cmap, a, pairs);
+    if (fmt == FMT_MXFP8) return run_qmm<FMT_MXFP8, 2, QMM_GROUPED>(ds, st, xmap, cmap, a, pairs);
+    return run_qmm<FMT_NVFP4, 2, QMM_GROUPED>(ds, st, xmap, cmap, a, pairs);
 }
 
 cudaError_t launch_qmm(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,

@@ -159,8 +159,8 @@ int mx_qmm(int fmt, const void *codes, const void *scales, const void *X, void *
  * MoE prefill as the weak spot once dense prefill runs on the matrix units
  * (release post, section "Bandwidth utilisation per model"); here the
  * (token, slot) rows are grouped by expert on the device, gathered into
- * expert order and multiplied 256 rows at a time as in mx_qmm, so each
- * expert's weights are decoded once per 256 routed rows.  Launches: routing
+ * expert order and multiplied in tiles of up to 512 rows as in mx_qmm, so
+ * each expert's weights are decoded once per 512 routed rows.  Launches: routing
  * (one block), the gather, the grouped GEMM.
  * workspace: caller-owned device memory of at least
  * mx_moe_qmm_workspace_size(T, E, topk, K) bytes, 256-byte aligned (else

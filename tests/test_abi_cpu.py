@@ -105,12 +105,12 @@ def _align256(v):
 @pytest.mark.parametrize("T,E,topk,K,I", [(4096, 128, 8, 2048, 768), (1, 8, 8, 256, 128), (37, 300, 3, 64, 0),
                                          (1000, 1, 1, 512, 256)])
 def test_prefill_workspace_sizes(lib, T, E, topk, K, I):
-    """Workspace = tile table (16 bytes + 16 per group tile, at most
-    (S + 255 * min(S, E)) / 256 tiles for S = T * topk routed rows) + sorted
-    row -> slot (4 S) + gathered activations (2 S K) [+ SwiGLU output 2 S I],
-    each part 256-byte aligned."""
+    """Workspace = tile table (16 bytes + 16 per group tile of up to 512
+    rows, at most (S + 511 * min(S, E)) / 512 tiles for S = T * topk routed
+    rows) + sorted row -> slot (4 S) + gathered activations (2 S K)
+    [+ SwiGLU output 2 S I], each part 256-byte aligned."""
     S = T * topk
-    tiles = (S + 255 * min(S, E)) // 256
+    tiles = (S + 511 * min(S, E)) // 512
     plain = _align256(_align256(16 + 16 * tiles) + 4 * S) + 2 * S * K
     assert lib.mx_moe_qmm_workspace_size(T, E, topk, K) == _align256(plain)
     if I:
@@ -119,28 +119,30 @@ def test_prefill_workspace_sizes(lib, T, E, topk, K, I):
     assert lib.mx_moe_qmm_workspace_size(T, E, E + 1, K) == 0
 
 
-def test_group_tile_bound():
-    """The grid bound (S + 255 * min(S, E)) / 256 covers every routing: brute
-    force over random and adversarial row counts per expert."""
+@pytest.mark.parametrize("G", [256, 512])
+def test_group_tile_bound(G):
+    """The grid bound (S + (G - 1) * min(S, E)) / G on the number of group
+    tiles of up to G rows covers every routing: brute force over random and
+    adversarial row counts per expert."""
     import numpy as np
 
-    rng = np.random.default_rng(0)
+    rng = np.random.default_rng(G)
     for _ in range(2000):
         E = int(rng.integers(1, 300))
         S = int(rng.integers(1, 5000))
         kind = rng.integers(0, 3)
         if kind == 0:
             counts = np.bincount(rng.integers(0, E, S), minlength=E)
-        elif kind == 1:  # as many experts as possible just above a multiple of 256
+        elif kind == 1:  # as many experts as possible just above a multiple of G
             counts = np.zeros(E, np.int64)
             left = S
             for e in range(E):
-                take = min(left, 257 if left >= 257 else left)
+                take = min(left, G + 1)
                 counts[e] = take
                 left -= take
             counts[0] += left
         else:
             counts = np.zeros(E, np.int64)
             counts[rng.integers(0, E)] = S
-        tiles = int(sum((c + 255) // 256 for c in counts))
-        assert tiles <= (S + 255 * min(S, E)) // 256
+        tiles = int(sum((c + G - 1) // G for c in counts))
+        assert tiles <= (S + (G - 1) * min(S, E)) // G

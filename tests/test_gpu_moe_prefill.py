@@ -1,5 +1,5 @@
 """Expert-batched MoE prefill on the GPU: mx_moe_qmm (routed rows grouped by
-expert, one tensor-core GEMM per 256-row group tile, outputs in slot order)
+expert, one tensor-core GEMM per group tile of up to 512 rows, outputs in slot order)
 and mx_moe_ffn_prefill (gate-up with the SwiGLU in the GEMM epilogue, down,
 router-weighted combine), against the oracle."""
 import numpy as np
@@ -34,7 +34,7 @@ for fmt in (0, 1, 2):
     CASES += [
         (fmt, 40, 6, 3, 256, 128),   # ~20 rows per expert: one partial group tile each
         (fmt, 300, 4, 2, 512, 192),  # ~150 rows per expert, two column tiles, 3 k-blocks
-        (fmt, 700, 3, 2, 256, 64),   # ~470 rows per expert: a full and a partial tile
+        (fmt, 700, 3, 2, 256, 64),   # ~470 rows per expert: one tile using both 256-row halves
         (fmt, 1, 8, 8, 256, 256),    # one token
     ]
 
@@ -68,7 +68,7 @@ def test_moe_qmm_many_experts(orc):
 
 
 def test_moe_qmm_skewed_routing(orc):
-    """Every slot on one expert (three group tiles), the others idle; and the
+    """Every slot on one expert (a 512-row and an 88-row group tile), the others idle; and the
     down-projection call form (topk = 1 over T * topk rows)."""
     need_gpu()
     fmt, T, E, N, K = 0, 600, 5, 256, 128
