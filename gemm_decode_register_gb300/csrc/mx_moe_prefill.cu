@@ -250,7 +250,8 @@ __global__ void gather_rows_kernel(const uint16_t *__restrict__ x, const int *__
         const int t = __ldcg(slot_of + p) / topk;
         const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * K);
         uint4 *dst = reinterpret_cast<uint4 *>(xs + (size_t)p * K);
-        for (int c = lane; c < vec; c += 32) dst[c] = __ldg(src + c);
+        // x may have been written by the kernel before this one: coherent (L2) loads
+        for (int c = lane; c < vec; c += 32) dst[c] = __ldcg(src + c);
     }
 }
 
