@@ -87,6 +87,8 @@ def _load(defines: tuple[str, ...] = ()) -> ctypes.CDLL:
             lib.or_swiglu_bf16.argtypes = [P, P, I64, I64]
             lib.or_moe_combine.restype = I
             lib.or_moe_combine.argtypes = [P, P, P, I64, I64, I64]
+            lib.or_quantize.restype = I
+            lib.or_quantize.argtypes = [I, P, P, P, I64, I64]
             _LIBS[defines] = lib
         return _LIBS[defines]
 
@@ -196,6 +198,20 @@ class Oracle:
         out = np.empty((T, N), dtype=np.float64)
         self.lib.or_moe_combine(yd.ctypes.data, r.ctypes.data, out.ctypes.data, T, topk, N)
         return out
+
+
+    def quantize(self, fmt, x, M, K):
+        """bf16 bits [M][K] -> (codes, scales) in the layouts the decode reads
+        (NVFP4: the fp32 tensor scale appended to the scales)."""
+        x, px = self._bf16bits(x)
+        nc = M * K if fmt == 1 else M * K // 2
+        ns = M * K // (16 if fmt == 2 else 32) + (4 if fmt == 2 else 0)
+        codes = np.zeros(nc, dtype=np.uint8)
+        scales = np.zeros(ns, dtype=np.uint8)
+        rc = self.lib.or_quantize(fmt, px, codes.ctypes.data, scales.ctypes.data, M, K)
+        if rc:
+            raise ValueError(f"or_quantize rc={rc}")
+        return codes, scales
 
 
 _DEFAULT: Oracle | None = None

@@ -338,3 +338,152 @@ int or_moe_combine(const double *yd, const float *r, double *out, int64_t T, int
     }
     return 0;
 }
+
+/* ------------------------------------------------------------- quantise */
+
+/* bf16 activations -> block-float codes and scales: the reverse of the
+ * decode above.  The pages say only that block-float quantisation runs on
+ * the GPU's hardware NVFP4 / MXFP4 converter on Blackwell (manual page
+ * "Building from source", CUDA build options, "GPU architecture
+ * auto-detection") and that FP8 block checkpoints are re-quantised to MXFP8
+ * (manual, ROCm status table).  The procedure is the plain reading of the
+ * format definitions:
+ *  - MXFP4 / MXFP8 (OCP MX v1.0 conversion): per block of 32, shared
+ *    exponent e = floor(log2(amax)) - emax_elem (emax_elem = 2 for E2M1,
+ *    8 for E4M3), clamped to [-127, 127], amax = 0 giving -127; scale byte
+ *    e + 127; each element x / 2^e rounded to nearest-even in the element
+ *    format, saturating at the largest finite value.  A block holding a NaN
+ *    or an infinity gets scale 0xFF (NaN) and zero codes.
+ *  - NVFP4: g = fp32(G / 2688) with G the largest finite |x| of the whole
+ *    tensor (g = 1 when G = 0), stored after the scales as the tensor scale;
+ *    per block of 16, s = E4M3(fp32(amax / fp32(6 g))) (nearest-even,
+ *    saturating) and each element fp32(x / fp32(s g)) rounded to E2M1 (all
+ *    codes zero when s g = 0); a block holding a NaN or an infinity gets
+ *    scale 0x7F (NaN) and zero codes.
+ *  - A zero result is stored as +0 (code 0), whatever the sign of x.
+ * The fp32 steps of NVFP4 are written as separate float operations so that
+ * each is one IEEE round-to-nearest-even operation. */
+
+/* Nearest-even code of |v| among the 8 E2M1 magnitudes, saturating at 6. */
+static unsigned e2m1_round(double a)
+{
+    unsigned best = 0;
+    double bd = INFINITY;
+    for (unsigned c = 0; c < 8; ++c) {
+        const double d = fabs(or_e2m1(c) - a);
+#ifdef OR_PLANT_Q_TIES_UP
+        if (d < bd || d == bd) {
+#else
+        if (d < bd || (d == bd && (c & 1u) == 0)) {
+#endif
+            bd = d;
+            best = c;
+        }
+    }
+    return best;
+}
+
+/* Nearest-even code of |v| among the 127 finite E4M3 magnitudes, saturating
+ * at 448. */
+static unsigned e4m3_round(double a)
+{
+    unsigned best = 0;
+    double bd = INFINITY;
+    for (unsigned c = 0; c < 0x7F; ++c) {
+        const double d = fabs(or_e4m3(c) - a);
+        if (d < bd || (d == bd && (c & 1u) == 0)) {
+            bd = d;
+            best = c;
+        }
+    }
+    return best;
+}
+
+/* Signed code: the magnitude's code with the sign bit set for negative v,
+ * except that a zero magnitude is +0. */
+static unsigned signed_code(int fmt, double v)
+{
+    const unsigned mag = fmt == OR_FMT_MXFP8 ? e4m3_round(fabs(v)) : e2m1_round(fabs(v));
+    if (mag == 0 || !(v < 0)) return mag;
+    return mag | (fmt == OR_FMT_MXFP8 ? 0x80u : 0x8u);
+}
+
+static void put_code(int fmt, uint8_t *codes, int64_t m, int64_t k, int64_t K, unsigned c)
+{
+    if (fmt == OR_FMT_MXFP8) {
+        codes[m * K + k] = (uint8_t)c;
+    } else {
+        uint8_t *b = &codes[m * (K / 2) + k / 2];
+#ifdef OR_PLANT_Q_NIBBLE_SWAP
+        if (k % 2 == 1) *b = (uint8_t)((*b & 0xF0u) | c);
+#else
+        if (k % 2 == 0) *b = (uint8_t)((*b & 0xF0u) | c);
+#endif
+        else *b = (uint8_t)((*b & 0x0Fu) | (c << 4));
+    }
+}
+
+int or_quantize(int fmt, const uint16_t *x, uint8_t *codes, uint8_t *scales, int64_t M, int64_t K)
+{
+    const int B = block_of(fmt);
+    if (M <= 0 || K <= 0 || K % B) return -1;
+    memset(codes, 0, (size_t)(fmt == OR_FMT_MXFP8 ? M * K : M * K / 2));
+    float g = 1.0f;
+    if (fmt == OR_FMT_NVFP4) {
+        double G = 0.0;
+        for (int64_t i = 0; i < M * K; ++i) {
+            const double a = fabs(or_bf16(x[i]));
+            if (isfinite(a) && a > G) G = a;
+        }
+        if (G > 0) g = (float)G / 2688.0f;  /* G is a bf16 value: exact in float */
+        memcpy(scales + M * (K / 16), &g, 4);
+    }
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t b0 = 0; b0 < K; b0 += B) {
+            double amax = 0.0;
+            int finite = 1;
+            for (int64_t k = b0; k < b0 + B; ++k) {
+                const double v = or_bf16(x[m * K + k]);
+                if (!isfinite(v)) finite = 0;
+                else if (fabs(v) > amax) amax = fabs(v);
+            }
+            uint8_t *sb = &scales[m * (K / B) + b0 / B];
+            if (!finite) {
+                *sb = fmt == OR_FMT_NVFP4 ? 0x7F : 0xFF;
+                continue;  /* codes stay zero */
+            }
+            if (fmt == OR_FMT_NVFP4) {
+                const float d = 6.0f * g;
+                const float t = (float)amax / d;
+                const unsigned s = e4m3_round(t);
+                *sb = (uint8_t)s;
+                const float den = (float)or_e4m3(s) * g;
+                if (den == 0.0f) continue;
+                for (int64_t k = b0; k < b0 + B; ++k) {
+                    const float v = (float)or_bf16(x[m * K + k]) / den;
+                    put_code(fmt, codes, m, k, K, signed_code(fmt, v));
+                }
+            } else {
+                const int emax = fmt == OR_FMT_MXFP8 ? 8 : 2;
+                int e = -127;
+                if (amax > 0) {
+                    int ex;
+                    frexp(amax, &ex);   /* amax = f * 2^ex, f in [0.5, 1): floor(log2(amax)) = ex - 1 */
+#ifdef OR_PLANT_Q_EMAX
+                    e = ex - emax;
+#else
+                    e = ex - 1 - emax;
+#endif
+                    if (e < -127) e = -127;
+                    if (e > 127) e = 127;
+                }
+                *sb = (uint8_t)(e + 127);
+                for (int64_t k = b0; k < b0 + B; ++k) {
+                    const double v = ldexp(or_bf16(x[m * K + k]), -e);  /* exact */
+                    put_code(fmt, codes, m, k, K, signed_code(fmt, v));
+                }
+            }
+        }
+    }
+    return 0;
+}

@@ -368,6 +368,178 @@ def pin_swiglu_combine(orc):
     assert np.allclose(r.sum(axis=1), 1.0, atol=1e-6)
 
 
+# ------------------------------------------------------------- quantisation
+
+E2M1_MAG = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def f32_to_bf16_exact(v: np.ndarray) -> np.ndarray:
+    """bf16 bits of fp32 values that bf16 holds exactly (asserted)."""
+    f = np.asarray(v, dtype=np.float32).reshape(-1)
+    bits = f.view(np.uint32)
+    assert np.all(bits & 0xFFFF == 0), "value not representable in bf16"
+    return (bits >> 16).astype(np.uint16)
+
+
+def canonical_zero(fmt: int, codes: np.ndarray) -> np.ndarray:
+    """Codes with -0 replaced by +0 (the quantiser stores every zero as +0)."""
+    c = np.asarray(codes, dtype=np.uint8).copy()
+    if fmt == F8:
+        c[c == 0x80] = 0
+        return c
+    lo, hi = c & 0xF, c >> 4
+    lo[lo == 8] = 0
+    hi[hi == 8] = 0
+    return (lo | (hi << 4)).astype(np.uint8)
+
+
+def pin_quantize_roundtrip(orc):
+    """Codes and scales built so that every block's largest magnitude sits in
+    the element format's top binade (MX) or is 6 times the block scale with a
+    power-of-two tensor scale (NVFP4): decoding them (independent decode) and
+    quantising the bf16 result must give the same codes and scales back."""
+    rng = np.random.default_rng(11)
+    M, K = 6, 128
+    for fmt in (F4, F8):
+        codes, scales = synth.weights(fmt, M, K, 12, exp_lo=110, exp_hi=140)
+        if fmt == F8:
+            c = codes.reshape(M, K).copy()
+            c[(c & 0x7F) == 0x7F] = 0x7E  # no NaN elements
+            top = rng.integers(0x78, 0x7F, size=(M, K // 32)) | (rng.integers(0, 2, size=(M, K // 32)) << 7)
+            c[:, rng.integers(0, 32) + 32 * np.arange(K // 32)] = top.astype(np.uint8)
+            codes = c.reshape(-1)
+        else:
+            nib = nibbles(codes, K).copy()
+            top = rng.integers(4, 8, size=(M, K // 32)) | (rng.integers(0, 2, size=(M, K // 32)) << 3)
+            nib[:, rng.integers(0, 32) + 32 * np.arange(K // 32)] = top
+            codes = (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8).reshape(-1)
+        W = independent_dequant(fmt, codes, scales, M, K)
+        c2, s2 = orc.quantize(fmt, f32_to_bf16_exact(W), M, K)
+        assert np.array_equal(s2, np.asarray(scales).reshape(-1)), f"fmt {fmt}: scales"
+        assert np.array_equal(c2, canonical_zero(fmt, codes)), f"fmt {fmt}: codes"
+    # NVFP4: tensor scale 2^-3, block scales any positive E4M3 >= 2^-6, one
+    # block at 448; every block holds a +-6
+    nb = M * K // 16
+    sc = rng.integers(0x08, 0x7F, size=nb).astype(np.uint8)
+    sc[rng.integers(0, nb)] = 0x7E
+    nib = rng.integers(0, 16, size=(M, K)).astype(np.uint8)
+    nib.reshape(-1, 16)[np.arange(nb), rng.integers(0, 16, size=nb)] = 7 | (rng.integers(0, 2, size=nb) << 3)
+    codes = (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8).reshape(-1)
+    scales = np.concatenate([sc, np.array([0.125], dtype="<f4").view(np.uint8)])
+    W = independent_dequant(NV, codes, scales, M, K)
+    c2, s2 = orc.quantize(NV, f32_to_bf16_exact(W), M, K)
+    assert np.array_equal(s2, scales), "nvfp4: scales"
+    assert np.array_equal(c2, canonical_zero(NV, codes)), "nvfp4: codes"
+
+
+def _nearest_even(mags: np.ndarray, a: float) -> int:
+    """Index of the nearest magnitude to a (ties to the even index), a beyond
+    the largest saturating to it."""
+    d = np.abs(mags - a)
+    best = np.flatnonzero(d == d.min())
+    return int(best[0] if len(best) == 1 else [i for i in best if i % 2 == 0][0])
+
+
+def pin_quantize_nearest(orc):
+    """Random activations over a wide range of magnitudes: the MX scale is
+    floor(log2(amax)) - emax + 127 (from frexp), the NVFP4 tensor and block
+    scales follow their fp32 formulas (numpy float32 steps, torch E4M3
+    rounding), and every code is the nearest-even (saturating) element."""
+    rng = np.random.default_rng(13)
+    M, K = 8, 96
+    xf = (rng.standard_normal((M, K)) * np.exp2(rng.integers(-30, 30, size=(M, 1)))).astype(np.float32)
+    x = (xf.view(np.uint32) >> 16).astype(np.uint16)  # truncation: any bf16 values will do
+    xv = bf16_to_f64(x).reshape(M, K)
+    e4m3_mags = e4m3_by_torch(np.arange(0x7F, dtype=np.uint8))
+    for fmt in (F4, F8):
+        emax = 8 if fmt == F8 else 2
+        mags = e4m3_mags if fmt == F8 else E2M1_MAG
+        codes, scales = orc.quantize(fmt, x, M, K)
+        cv = e4m3_by_torch(codes).reshape(M, K) if fmt == F8 else \
+            np.array([e2m1_by_fp16_placement(c) for c in range(16)])[nibbles(codes, K)]
+        for m in range(M):
+            for b in range(K // 32):
+                blk = xv[m, 32 * b:32 * b + 32]
+                amax = np.abs(blk).max()
+                e = math.frexp(amax)[1] - 1 - emax if amax > 0 else -127
+                e = min(max(e, -127), 127)
+                assert scales[m * (K // 32) + b] == e + 127, f"fmt {fmt}: scale of block {m},{b}"
+                for k in range(32):
+                    v = math.ldexp(blk[k], -e)
+                    want = mags[_nearest_even(mags, abs(v))]
+                    got = cv[m, 32 * b + k]
+                    assert abs(got) == want and (want == 0 or np.sign(got) == np.sign(v)), \
+                        f"fmt {fmt}: element {m},{32 * b + k}"
+    codes, scales = orc.quantize(NV, x, M, K)
+    G = np.float32(np.abs(xv).max())
+    g = G / np.float32(2688.0)
+    assert scales[M * K // 16:].view("<f4")[0] == g, "nvfp4 tensor scale"
+    import torch
+
+    cv = np.array([e2m1_by_fp16_placement(c) for c in range(16)])[nibbles(codes, K)]
+    for m in range(M):
+        for b in range(K // 16):
+            blk = xv[m, 16 * b:16 * b + 16].astype(np.float32)
+            t = np.float32(np.abs(blk).max()) / (np.float32(6.0) * g)
+            s = int(torch.tensor([float(t)], dtype=torch.float32).to(torch.float8_e4m3fn).view(torch.uint8)[0])
+            assert scales[m * (K // 16) + b] == s, f"nvfp4 block scale {m},{b}"
+            den = np.float32(e4m3_by_torch(np.array([s], np.uint8))[0]) * g
+            for k in range(16):
+                if den == 0:  # block scale rounded to zero: all codes zero
+                    assert cv[m, 16 * b + k] == 0, f"nvfp4 element {m},{b},{k}"
+                    continue
+                v = float(blk[k] / den)
+                want = E2M1_MAG[_nearest_even(E2M1_MAG, abs(v))]
+                got = cv[m, 16 * b + k]
+                assert abs(got) == want and (want == 0 or np.sign(got) == np.sign(v)), f"nvfp4 element {m},{b},{k}"
+
+
+def pin_quantize_specials(orc):
+    """Hand-derived cases (definitions above or_quantize): a block whose
+    largest |x| is 4 has scale 2^0 (E8M0 127) in MXFP4; then 0.25 -> 0 and
+    0.75 -> 1 and 2.5 -> 2 and 5 -> 4 (ties to the even code), 7.5 in a
+    block of max 7.5 saturates to 6, -0 and -0.1 are stored as +0, a NaN or
+    an infinity makes the block's scale NaN with zero codes, and an all-zero
+    block has scale byte 0 (MX) or 0 (NVFP4)."""
+    def bits(vals):
+        return (np.asarray(vals, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+    K = 32
+    row = np.zeros(K, np.float32)
+    row[:8] = [4.0, 0.25, 0.75, 2.5, 5.0 / 1.0, -5.0, -0.0, -0.1]
+    row[4] = 3.5   # tie between 3 and 4 -> 4 (code 6, even)
+    codes, scales = orc.quantize(F4, bits(row), 1, K)
+    assert scales[0] == 127
+    want = [6, 0, 2, 4, 6, 14, 0, 0]  # 4, 0, 1, 2, 4, -4, +0, +0
+    assert list(nibbles(codes, K)[0, :8]) == want
+    row2 = np.zeros(K, np.float32)
+    row2[0], row2[1] = 7.5, -7.0
+    codes, scales = orc.quantize(F4, bits(row2), 1, K)
+    assert scales[0] == 127 and list(nibbles(codes, K)[0, :2]) == [7, 15]  # saturate to +-6
+    for bad in (np.nan, np.inf, -np.inf):
+        r3 = np.ones(K, np.float32)
+        r3[5] = bad
+        for fmt, nanscale in ((F4, 0xFF), (F8, 0xFF)):
+            codes, scales = orc.quantize(fmt, bits(r3), 1, K)
+            assert scales[0] == nanscale and not codes.any()
+        codes, scales = orc.quantize(NV, bits(r3), 1, K)
+        assert scales[0] == 0x7F and scales[1] != 0x7F and not codes[:8].any()
+    z = np.zeros(K, np.float32)
+    for fmt in (F4, F8, NV):
+        codes, scales = orc.quantize(fmt, bits(z), 1, K)
+        assert not codes.any() and not scales[: K // synth.block_of(fmt)].any()
+    codes, scales = orc.quantize(NV, bits(z), 1, K)
+    assert scales[2:].view("<f4")[0] == 1.0  # no finite non-zero value: tensor scale 1
+    # MXFP8: block max 448 -> floor(log2 448) = 8 -> scale 2^0; 500 -> saturates to 448
+    r4 = np.zeros(K, np.float32)
+    r4[0], r4[1], r4[2] = 448.0, 300.0, -2.0 ** -9
+    codes, scales = orc.quantize(F8, bits(r4), 1, K)
+    assert scales[0] == 127 and list(codes[:3]) == [0x7E, 0x79, 0x81]  # 448, 288 (300 -> 288), -2^-9
+    r4[0] = 500.0
+    codes, scales = orc.quantize(F8, bits(r4), 1, K)
+    assert scales[0] == 127 and codes[0] == 0x7E
+
+
 ALL_PINS = [pin_e2m1, pin_e8m0, pin_e4m3, pin_bf16, pin_dequant, pin_qmv_bruteforce,
             pin_qmv_matmul, pin_invariants, pin_worked_examples, pin_moe, pin_points,
-            pin_swiglu_combine]
+            pin_swiglu_combine, pin_quantize_roundtrip, pin_quantize_nearest, pin_quantize_specials]
