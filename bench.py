@@ -424,7 +424,8 @@ def extras(torch, ops, synth, dev, stream, hbm, bf16_burst, bf16_sust, args):
             del c, s, X, Y
     except Exception as exc:  # reported, not hidden
         res["prefill_qmm"] = {"error": str(exc).splitlines()[0][:200]}
-    for name, fn in (("moe_prefill", extras_moe_prefill), ("crossover_upgate", extras_crossover)):
+    for name, fn in (("moe_prefill", extras_moe_prefill), ("crossover_upgate", extras_crossover),
+                     ("quantize", extras_quantize)):
         try:
             res.update(fn(torch, ops, synth, dev, stream, bf16_burst, iters))
         except Exception as exc:  # reported, not hidden
@@ -468,6 +469,26 @@ def extras_moe_prefill(torch, ops, synth, dev, stream, bf16_burst, iters):
                                           "frac_bf16_burst": round(flq / tq / 1e12 / bf16_burst, 4),
                                           "path": "mx_moe_qmm: route, gather, grouped GEMM (3 launches)"}
         del y, wsq
+    return res
+
+
+def extras_quantize(torch, ops, synth, dev, stream, bf16_burst, iters):
+    """On-device quantisation of the prefill activations (4096 x 8192 bf16,
+    67 MB in: larger than L2): bytes read and written per second."""
+    res = {}
+    M, K = 4096, 8192
+    x = bf16_dev(torch, synth.activations(M, K, 600)).view(M, K)
+    hbm = peaks()[0]
+    for fmt, name in ((synth.FMT_MXFP4, "mxfp4"), (synth.FMT_MXFP8, "mxfp8"), (synth.FMT_NVFP4, "nvfp4")):
+        codes, scales = ops.quantize(fmt, x)
+        t = time_region(torch, graph_of(torch, lambda: ops.quantize(fmt, x, codes, scales)).replay,
+                        max(10, iters // 4), stream)
+        nbytes = 2 * M * K + codes.numel() + scales.numel() + (2 * M * K if fmt == synth.FMT_NVFP4 else 0)
+        res[f"quantize_{name}"] = {"us": round(t * 1e6, 2), "gbs": round(nbytes / t / 1e9, 1),
+                                   "frac_hbm": round(nbytes / t / 1e9 / hbm, 4),
+                                   "bytes": nbytes,
+                                   "note": "x read once (NVFP4: twice, tensor maximum then blocks) + codes and "
+                                           "scales written"}
     return res
 
 

@@ -231,6 +231,24 @@ extern "C" int mx_moe_ffn_prefill(int fmt, const void *gate_up_codes, const void
     return finish(e);
 }
 
+namespace mx {
+// mx_quant.cu
+cudaError_t launch_quantize(const DeviceState &ds, cudaStream_t st, int fmt, const uint16_t *x, uint8_t *codes,
+                            uint8_t *scales, int M, int K);
+}  // namespace mx
+
+extern "C" int mx_quantize(int fmt, const void *x, void *codes, void *scales, int M, int K)
+{
+    if (!fmt_ok(fmt)) return MX_EUNSUPPORTED;
+    if (!x || !codes || !scales) return MX_EINVAL;
+    if (M <= 0 || K <= 0 || K % block_of(fmt) != 0) return MX_EINVAL;
+    if (!aligned16(x) || !aligned16(codes)) return MX_EALIGN;
+    DeviceState *ds = device_state();
+    if (!ds) return MX_ECUDA;
+    return finish(launch_quantize(*ds, t_stream, fmt, static_cast<const uint16_t *>(x), static_cast<uint8_t *>(codes),
+                                  static_cast<uint8_t *>(scales), M, K));
+}
+
 extern "C" int mx_dequant(int fmt, const void *codes, const void *scales, float *W, int N, int K)
 {
     if (!fmt_ok(fmt)) return MX_EUNSUPPORTED;

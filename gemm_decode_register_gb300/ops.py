@@ -58,6 +58,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "mx_moe_combine": [P, P, P, I, I, I],
             "mx_device_error": [],
             "mx_moe_qmm": [I, P, P, P, P, P, I, I, I, I, I, P, Z],
+            "mx_quantize": [I, P, P, P, I, I],
             "mx_moe_ffn_prefill": [I, P, P, P, P, P, P, P, P, I, I, I, I, I, P, Z],
         }
         for name, args in sig.items():
@@ -219,6 +220,21 @@ def moe_ffn_prefill(fmt: int, gu_codes: torch.Tensor, gu_scales: torch.Tensor, d
                                                         _ptr(router_weights), _ptr(out), T, E, topk, H, I,
                                                         _ptr(ws), ws.numel()))
     return out
+
+
+def quantize(fmt: int, x: torch.Tensor, codes: torch.Tensor | None = None,
+             scales: torch.Tensor | None = None) -> tuple[torch.Tensor, torch.Tensor]:
+    """bf16 x [M][K] -> (codes, scales) uint8 in the decode's layouts (NVFP4:
+    the fp32 tensor scale appended to the scales)."""
+    M, K = x.shape
+    blk = block_of(fmt)
+    if codes is None:
+        codes = torch.empty(M * K if fmt == FMT_MXFP8 else M * K // 2, dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(M * K // blk + (4 if fmt == FMT_NVFP4 else 0), dtype=torch.uint8, device=x.device)
+    _stream()
+    _check("mx_quantize", load().mx_quantize(fmt, _ptr(x), _ptr(codes), _ptr(scales), M, K))
+    return codes, scales
 
 
 def dequant(fmt: int, codes: torch.Tensor, scales: torch.Tensor, N: int, K: int,

@@ -194,6 +194,27 @@ int mx_moe_ffn_prefill(int fmt, const void *gate_up_codes, const void *gate_up_s
                        const float *router_weights, float *out, int T, int E, int topk, int H, int I,
                        void *workspace, size_t workspace_bytes);
 
+/* On-device block-float quantisation of bf16 activations, the reverse of the
+ * decode (manual page "Building from source", CUDA build options: on
+ * Blackwell, block-float quantisation runs on the hardware NVFP4 / MXFP4
+ * converter; ROCm status table: FP8 block checkpoints are re-quantised to
+ * MXFP8).  x bf16 [M][K] in; codes and scales out in the layouts above
+ * (NVFP4: the fp32 tensor scale is written after the M*K/16 scale bytes).
+ *   MXFP4 / MXFP8 (OCP MX v1.0 conversion): per 32 elements the scale is
+ *     2^e, e = floor(log2(max |x|)) - emax (2 for E2M1, 8 for E4M3), at
+ *     least -127; each element x / 2^e rounded to nearest-even in the
+ *     element format, saturating at its largest finite value.
+ *   NVFP4: g = fp32(G / 2688), G the largest finite |x| of the whole tensor
+ *     (1 when G = 0); per 16 elements s = E4M3(fp32(max |x| / fp32(6 g)))
+ *     and each element fp32(x / fp32(s g)) rounded to E2M1 (zero codes when
+ *     s g = 0).  Two launches (tensor maximum, then the blocks); the
+ *     maximum goes through a word of the library's per-device scratch, so
+ *     NVFP4 calls on different streams of one device must not overlap.
+ *   A block holding a NaN or an infinity gets a NaN scale (0xFF / 0x7F) and
+ *   zero codes; a zero result is stored as +0.
+ * K a multiple of the block (else MX_EINVAL); x and codes 16-byte aligned. */
+int mx_quantize(int fmt, const void *x, void *codes, void *scales, int M, int K);
+
 /* ---- support calls (not on the pages; part of this library's contract) */
 
 /* Stream for subsequent calls from this host thread (a cudaStream_t; NULL =

@@ -146,3 +146,17 @@ def test_group_tile_bound(G):
             counts[rng.integers(0, E)] = S
         tiles = int(sum((c + G - 1) // G for c in counts))
         assert tiles <= (S + (G - 1) * min(S, E)) // G
+
+
+@pytest.mark.parametrize("args,want", [
+    ((9, A, A, A, 4, 64), -2),       # unknown format
+    ((0, 0, A, A, 4, 64), -1),       # null x
+    ((0, A, A, 0, 4, 64), -1),       # null scales
+    ((0, A, A, A, 0, 64), -1),       # M = 0
+    ((0, A, A, A, 4, 48), -1),       # K not a multiple of 32
+    ((2, A, A, A, 4, 40), -1),       # NVFP4 K not a multiple of 16
+    ((0, A + 2, A, A, 4, 64), -3),   # misaligned x
+    ((1, A, A + 8, A, 4, 64), -3),   # misaligned codes
+])
+def test_quantize_rejects(lib, args, want):
+    assert lib.mx_quantize(*args) == want
