@@ -35,6 +35,9 @@ CASES += [(2, 1, 33, 48), (2, 4, 31, 16), (2, 3, 70, 1040)]   # NVFP4 with K % 3
 # streamed shapes whose CTAs deal equal runs of stages to their warps, cutting
 # tiles where runs meet (M=1: 13-14 tiles of 4 stages per CTA; M=2: 4-5 tiles)
 CASES += [(fmt, 1, 4096, 8192) for fmt in (0, 1, 2)] + [(fmt, 2, 3000, 4096) for fmt in (0, 2)]
+# more tokens than one pass of 8 (speculative-decode verify sizes): 2 and 3
+# passes over the weights
+CASES += [(0, 16, 300, 1024), (1, 13, 67, 320), (2, 24, 130, 512), (0, 6, 1000, 4096)]
 
 
 @pytest.mark.parametrize("fmt,M,N,K", CASES)

@@ -100,7 +100,6 @@ def test_quantized_weights_feed_qmv(orc, fmt):
     codes equal the oracle's, and the GEMV over them passes the tolerance
     gate against the oracle's GEMV over the oracle's codes."""
     need_gpu()
-    import torch
     from gemm_decode_register_gb300 import ops
     from gpu_util import check_close
 
@@ -112,4 +111,3 @@ def test_quantized_weights_feed_qmv(orc, fmt):
     x = synth.activations(M, K, 9)
     y = ops.qmv(fmt, c, s, dev_bf16(x).view(M, K), N).cpu().numpy()
     check_close(y, orc.qmv(fmt, wc, ws, x, M, N, K), f"qmv over quantised fmt{fmt}")
-    del torch
