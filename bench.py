@@ -609,6 +609,10 @@ CASES = {
     "qmm_mid": ("qmm", 0, 2048, 8192, 4096),
     # expert-batched MoE FFN prefill: 4096 tokens, top-8 of 128 experts, hidden 2048, I 768
     "moe_prefill_ffn_t4096": ("moe_prefill", 0, 4096, 2048, 768),
+    # on-device quantisation of 4096 x 8192 bf16 activations
+    "quantize_mxfp4": ("quantize", 0, 4096, 0, 8192),
+    "quantize_mxfp8": ("quantize", 1, 4096, 0, 8192),
+    "quantize_nvfp4": ("quantize", 2, 4096, 0, 8192),
 }
 
 
@@ -623,7 +627,12 @@ def run_case(args):
     b.build()
     kind, fmt, M, N, K = CASES[args.case]
     stream = torch.cuda.current_stream()
-    if kind == "moe_prefill":
+    if kind == "quantize":
+        x = bf16_dev(torch, synth.activations(M, K, 600)).view(M, K)
+        qc, qs = ops.quantize(fmt, x)
+        f = lambda: ops.quantize(fmt, x, qc, qs)  # noqa: E731
+        wb = 2 * M * K + qc.numel() + qs.numel()
+    elif kind == "moe_prefill":
         E, topk, H, I = 128, 8, N, K
         c1, s1 = synth.weights(fmt, 2 * I, H, 40, E=E)
         c2, s2 = synth.weights(fmt, H, I, 41, E=E)
