@@ -458,17 +458,17 @@ __device__ __forceinline__ uint32_t scale_load(const uint8_t *p)
 
 // What a pair tile computes and where its rows go.
 constexpr int QMM_DENSE = 0;        // Y[M][N] = X W^T
-constexpr int QMM_GROUPED = 1;      // expert groups of sorted rows; row i of group g -> Y[slot_of[r0 + i]]
+constexpr int QMM_GROUPED = 1;      // expert groups of sorted rows (up to 512); row i of group g -> Y[slot_of[r0 + i]]
 constexpr int QMM_GROUPED_GLU = 2;  // as 1, but CTA 0 takes gate rows, CTA 1 up rows; h = SwiGLU -> H[r0 + i]
 
 struct QmmArgs {
     const uint8_t *scales;
     uint16_t *Y;  // dense / grouped: [rows][N]; SwiGLU: h [rows][N / 2]
     int *err;
-    int M, N, K;  // grouped: N rows per expert, M unused
+    int M, N, K;  // grouped: N weight rows per expert, M rows of the gathered X
     int y32;  // Y rows and base 32-byte aligned: the epilogue stores 32 bytes per instruction
     unsigned long long wait_ns;
-    // grouped modes: the routing tables (written by moe_group_route_kernel)
+    // grouped modes: the routing tables (written by the moe_group_route kernels)
     const int *groups;   // [0] = number of tiles G; from word 4 on: G x {expert, first sorted row, rows, 0}
     const int *slot_of;  // sorted row -> slot (QMM_GROUPED)
     int E;               // experts
