@@ -160,3 +160,17 @@ def test_group_tile_bound(G):
 ])
 def test_quantize_rejects(lib, args, want):
     assert lib.mx_quantize(*args) == want
+
+
+def test_no_undeclared_exports(lib):
+    """Every mx_* function the library exports is declared in include/mx.h
+    (the header is the whole ABI)."""
+    import shutil
+    import subprocess
+
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    out = subprocess.run([nm, "-D", "--defined-only", b.LIB], capture_output=True, text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T mx_" in ln}
+    assert exported == set(ops.header_symbols())
