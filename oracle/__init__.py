@@ -89,6 +89,8 @@ def _load(defines: tuple[str, ...] = ()) -> ctypes.CDLL:
             lib.or_moe_combine.argtypes = [P, P, P, I64, I64, I64]
             lib.or_quantize.restype = I
             lib.or_quantize.argtypes = [I, P, P, P, I64, I64]
+            lib.or_qmm_qx.restype = I
+            lib.or_qmm_qx.argtypes = [I, P, P, P, P, P, I64, I64, I64]
             _LIBS[defines] = lib
         return _LIBS[defines]
 
@@ -212,6 +214,20 @@ class Oracle:
         if rc:
             raise ValueError(f"or_quantize rc={rc}")
         return codes, scales
+
+
+    def qmm_qx(self, fmt, codes, scales, xcodes, xscales, M, N, K) -> np.ndarray:
+        """y [M][N] fp64 = decoded activations (block-float, same format) x
+        decoded weights^T."""
+        codes, pc = self._u8(codes)
+        scales, ps = self._u8(scales)
+        xcodes, pxc = self._u8(xcodes)
+        xscales, pxs = self._u8(xscales)
+        y = np.empty((M, N), dtype=np.float64)
+        rc = self.lib.or_qmm_qx(fmt, pc, ps, pxc, pxs, y.ctypes.data, M, N, K)
+        if rc:
+            raise ValueError(f"or_qmm_qx rc={rc}")
+        return y
 
 
 _DEFAULT: Oracle | None = None

@@ -487,3 +487,40 @@ int or_quantize(int fmt, const uint16_t *x, uint8_t *codes, uint8_t *scales, int
     }
     return 0;
 }
+
+/* ------------------------------------------- product over quantised activations */
+
+/* y[m][n] = sum_k X^[m][k] * W^[n][k], fp64, increasing k, where both X^ and
+ * W^ are decoded block-float tensors of the same format (X^ from x codes
+ * [M][K(/2)] and scales [M][K/block] (+ tensor scale), W^ as in or_qmv): the
+ * reference for a matmul whose activations were quantised first (the
+ * on-device quantiser above feeding a block-scaled tensor-core product).
+ * Parity of such a kernel is judged against this, on the same quantised
+ * operands. */
+int or_qmm_qx(int fmt, const uint8_t *codes, const uint8_t *scales, const uint8_t *xcodes,
+              const uint8_t *xscales, double *y, int64_t M, int64_t N, int64_t K)
+{
+    if (M <= 0 || N <= 0 || K <= 0 || K % block_of(fmt)) return -1;
+    float *X = (float *)malloc((size_t)(M * K) * sizeof(float));
+    float *W = (float *)malloc((size_t)K * sizeof(float));
+    if (!X || !W) {
+        free(X);
+        free(W);
+        return -2;
+    }
+    const float gx = fmt == OR_FMT_NVFP4 ? tensor_scale(xscales, M, K) : 1.0f;
+    const float gw = fmt == OR_FMT_NVFP4 ? tensor_scale(scales, N, K) : 1.0f;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t k = 0; k < K; ++k) X[m * K + k] = weight(fmt, xcodes, xscales, gx, m, k, M, K);
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t k = 0; k < K; ++k) W[k] = weight(fmt, codes, scales, gw, n, k, N, K);
+        for (int64_t m = 0; m < M; ++m) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k) acc += (double)X[m * K + k] * (double)W[k];
+            y[m * N + n] = acc;
+        }
+    }
+    free(X);
+    free(W);
+    return 0;
+}

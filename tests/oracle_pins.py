@@ -540,6 +540,35 @@ def pin_quantize_specials(orc):
     assert scales[0] == 127 and codes[0] == 0x7E
 
 
+def pin_qmm_qx(orc):
+    """The product over quantised activations equals the float64 matmul of
+    the two independently decoded tensors, and swapping the roles of the
+    operands (activations as weights and back) transposes it bit for bit."""
+    M, N, K = 5, 7, 96
+    for fmt in (F4, F8, NV):
+        wc, ws = synth.weights(fmt, N, K, 21)
+        x = synth.activations(M, K, 22)
+        xc, xs = orc.quantize(fmt, x, M, K)
+        y = orc.qmm_qx(fmt, wc, ws, xc, xs, M, N, K)
+        Xd = independent_dequant(fmt, xc, xs, M, K).astype(np.float64)
+        Wd = independent_dequant(fmt, wc, ws, N, K).astype(np.float64)
+        assert np.allclose(y, Xd @ Wd.T, rtol=1e-12, atol=1e-30), f"fmt {fmt}"
+        yt = orc.qmm_qx(fmt, xc, xs, wc, ws, N, M, K)
+        assert np.array_equal(y.view(np.uint64), yt.T.copy().view(np.uint64)), f"fmt {fmt}: roles"
+    # tiny K, exact rationals: K = 32 products of decoded values summed exactly
+    fmt, M, N, K = F4, 2, 3, 32
+    wc, ws = synth.weights(fmt, N, K, 23)
+    xc, xs = orc.quantize(fmt, synth.activations(M, K, 24), M, K)
+    y = orc.qmm_qx(fmt, wc, ws, xc, xs, M, N, K)
+    Xd = independent_dequant(fmt, xc, xs, M, K)
+    Wd = independent_dequant(fmt, wc, ws, N, K)
+    for m in range(M):
+        for n in range(N):
+            exact = sum(Fraction(float(Xd[m, k])) * Fraction(float(Wd[n, k])) for k in range(K))
+            assert abs(Fraction(y[m, n]) - exact) <= abs(exact) * Fraction(1, 2 ** 50)
+
+
 ALL_PINS = [pin_e2m1, pin_e8m0, pin_e4m3, pin_bf16, pin_dequant, pin_qmv_bruteforce,
             pin_qmv_matmul, pin_invariants, pin_worked_examples, pin_moe, pin_points,
-            pin_swiglu_combine, pin_quantize_roundtrip, pin_quantize_nearest, pin_quantize_specials]
+            pin_swiglu_combine, pin_quantize_roundtrip, pin_quantize_nearest, pin_quantize_specials,
+            pin_qmm_qx]
