@@ -1,8 +1,11 @@
 // mx_api.cu -- the C ABI declared in include/mx.h: argument validation,
-// per-thread stream, per-device state and the device error word.
+// per-thread stream, per-device state, per-stream workspace slots and the
+// device error word.
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <thread>
+#include <vector>
 
 #include "../../include/mx.h"
 #include "mx_internal.h"
@@ -12,6 +15,11 @@ namespace mx {
 static thread_local cudaStream_t t_stream = nullptr;
 static std::mutex g_mu;
 static DeviceState g_dev[64];
+
+// The device error word: a module variable, so it exists (zeroed) on every
+// device the library is loaded on and needs no allocation.  [0] is the word;
+// the rest pads it to a sector of its own.
+static __device__ __align__(256) int g_err_word[64];
 
 cudaStream_t current_stream() { return t_stream; }
 
@@ -26,19 +34,92 @@ DeviceState *device_state()
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return nullptr;
     if (cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
         return nullptr;
-    void *scratch = nullptr;
-    if (cudaMalloc(&scratch, SCRATCH_BYTES) != cudaSuccess) return nullptr;
-    if (cudaMemset(scratch, 0, SCRATCH_BYTES) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
-        cudaFree(scratch);
-        return nullptr;
-    }
+    void *err = nullptr;
+    if (cudaGetSymbolAddress(&err, g_err_word) != cudaSuccess || err == nullptr) return nullptr;
     ds.num_sms = sms;
     ds.max_smem_optin = smem;
-    ds.err = static_cast<int *>(scratch);
-    ds.ws = reinterpret_cast<float *>(static_cast<char *>(scratch) + 256);
-    ds.ws_count = reinterpret_cast<int *>(ds.ws + WS_FLOATS);
+    ds.err = static_cast<int *>(err);
     ds.device = dev;
     return &ds;
+}
+
+// ---- per-stream workspace slots
+//
+// Calls whose kernels pass partial sums through global memory (mx_qmv with K
+// split across CTAs, mx_moe_down_combine, NVFP4 mx_quantize) each use the
+// slot of the stream they are issued on, so calls on different streams never
+// share one.  A slot is made on the first such call on a stream and kept
+// until the process exits.  The per-thread default stream is one stream per
+// host thread, so its slots are also keyed by the thread.
+namespace {
+
+struct StreamSlot {
+    cudaStream_t stream;
+    std::thread::id thread;  // only for cudaStreamPerThread
+    char *mem;
+};
+
+struct DeviceSlots {
+    std::vector<StreamSlot> slots;
+    cudaStream_t zero_stream = nullptr;  // private stream that clears new slots
+};
+
+DeviceSlots g_slots[64];
+
+// Restores the calling thread's stream-capture mode on scope exit.
+struct RelaxedCapture {
+    cudaStreamCaptureMode prev = cudaStreamCaptureModeRelaxed;
+    RelaxedCapture() { cudaThreadExchangeStreamCaptureMode(&prev); }
+    ~RelaxedCapture() { cudaThreadExchangeStreamCaptureMode(&prev); }
+};
+
+char *new_slot(DeviceSlots &d)
+{
+    // cudaMalloc is not a stream operation: in relaxed mode it is allowed
+    // while a stream of this thread is being captured, and the memory is not
+    // part of the graph.  The slot is cleared on a private stream and waited
+    // for here, so the clearing is neither captured nor ordered against the
+    // caller's streams.
+    RelaxedCapture relaxed;
+    if (d.zero_stream == nullptr && cudaStreamCreateWithFlags(&d.zero_stream, cudaStreamNonBlocking) != cudaSuccess)
+        return nullptr;
+    void *p = nullptr;
+    if (cudaMalloc(&p, SLOT_BYTES) != cudaSuccess) return nullptr;
+    if (cudaMemsetAsync(p, 0, SLOT_BYTES, d.zero_stream) != cudaSuccess ||
+        cudaStreamSynchronize(d.zero_stream) != cudaSuccess) {
+        cudaFree(p);
+        return nullptr;
+    }
+    return static_cast<char *>(p);
+}
+
+}  // namespace
+
+bool attach_stream_workspace(DeviceState &v, cudaStream_t st)
+{
+    if (v.device < 0 || v.device >= 64) return false;
+    const std::thread::id tid = st == cudaStreamPerThread ? std::this_thread::get_id() : std::thread::id();
+    char *mem = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        DeviceSlots &d = g_slots[v.device];
+        for (const StreamSlot &s : d.slots)
+            if (s.stream == st && s.thread == tid) {
+                mem = s.mem;
+                break;
+            }
+        if (mem == nullptr) {
+            mem = new_slot(d);
+            if (mem == nullptr) return false;
+            d.slots.push_back(StreamSlot{st, tid, mem});
+        }
+    }
+    v.amax = reinterpret_cast<unsigned *>(mem);
+    v.ws = reinterpret_cast<float *>(mem + 256);
+    v.ws_count = reinterpret_cast<int *>(v.ws + WS_FLOATS);
+    v.ws_floats = WS_FLOATS;
+    v.ws_counters = WS_COUNTERS;
+    return true;
 }
 
 }  // namespace mx
@@ -67,7 +148,13 @@ extern "C" int mx_qmv(int fmt, const void *codes, const void *scales, const void
     if (!aligned16(codes) || !aligned16(scales) || !aligned16(x) || !aligned16(y)) return MX_EALIGN;
     DeviceState *ds = device_state();
     if (!ds) return MX_ECUDA;
-    cudaError_t e = launch_qmv(*ds, t_stream, fmt, static_cast<const uint8_t *>(codes),
+    // a workspace slot only for shapes that split K across CTAs
+    DeviceState v = *ds;
+    v.ws_floats = WS_FLOATS;
+    v.ws_counters = WS_COUNTERS;
+    const QmvScratchNeed need = qmv_scratch_need(v, fmt, M, N, K);
+    if ((need.floats > 0 || need.counters > 0) && !attach_stream_workspace(v, t_stream)) return MX_ECUDA;
+    cudaError_t e = launch_qmv(v, t_stream, fmt, static_cast<const uint8_t *>(codes),
                                static_cast<const uint8_t *>(scales), static_cast<const uint16_t *>(x), y,
                                M, N, K);
     if (e == cudaErrorInvalidValue) return MX_EUNSUPPORTED;
@@ -132,7 +219,9 @@ extern "C" int mx_moe_down_combine(int fmt, const void *expert_codes, const void
         return MX_EALIGN;
     DeviceState *ds = device_state();
     if (!ds) return MX_ECUDA;
-    cudaError_t e = launch_moe_down_combine(*ds, t_stream, fmt, static_cast<const uint8_t *>(expert_codes),
+    DeviceState v = *ds;
+    if (!attach_stream_workspace(v, t_stream)) return MX_ECUDA;
+    cudaError_t e = launch_moe_down_combine(v, t_stream, fmt, static_cast<const uint8_t *>(expert_codes),
                                             static_cast<const uint8_t *>(expert_scales),
                                             static_cast<const uint16_t *>(h), expert_ids, router_weights, out, T,
                                             E, topk, N, K);
@@ -245,7 +334,9 @@ extern "C" int mx_quantize(int fmt, const void *x, void *codes, void *scales, in
     if (!aligned16(x) || !aligned16(codes)) return MX_EALIGN;
     DeviceState *ds = device_state();
     if (!ds) return MX_ECUDA;
-    return finish(launch_quantize(*ds, t_stream, fmt, static_cast<const uint16_t *>(x), static_cast<uint8_t *>(codes),
+    DeviceState v = *ds;
+    if (fmt == MX_FMT_NVFP4 && !attach_stream_workspace(v, t_stream)) return MX_ECUDA;
+    return finish(launch_quantize(v, t_stream, fmt, static_cast<const uint16_t *>(x), static_cast<uint8_t *>(codes),
                                   static_cast<uint8_t *>(scales), M, K));
 }
 
@@ -283,14 +374,23 @@ extern "C" int mx_moe_combine(const float *yd, const float *r, float *out, int T
     return finish(launch_moe_combine(*ds, t_stream, yd, r, out, T, topk, N));
 }
 
+extern "C" int mx_debug_qmm_stall(int stall, unsigned long long wait_ns)
+{
+    set_qmm_stall(stall, wait_ns);
+    return MX_OK;
+}
+
 extern "C" int mx_device_error(void)
 {
     DeviceState *ds = device_state();
     if (!ds) return MX_ECUDA;
-    if (cudaStreamSynchronize(t_stream) != cudaSuccess) return MX_ECUDA;
     int word = 0;
-    if (cudaMemcpy(&word, ds->err, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return MX_ECUDA;
-    if (word && cudaMemset(ds->err, 0, sizeof word) != cudaSuccess) return MX_ECUDA;
+    if (cudaMemcpyAsync(&word, ds->err, sizeof word, cudaMemcpyDeviceToHost, t_stream) != cudaSuccess ||
+        cudaStreamSynchronize(t_stream) != cudaSuccess)
+        return MX_ECUDA;
+    if (word && (cudaMemsetAsync(ds->err, 0, sizeof word, t_stream) != cudaSuccess ||
+                 cudaStreamSynchronize(t_stream) != cudaSuccess))
+        return MX_ECUDA;
     return word;
 }
 

@@ -7,23 +7,34 @@
 
 namespace mx {
 
-// Per-device state, created on first use of a device.
+// Per-device state, created on first use of a device, plus (in the copy a
+// call works on) the workspace slot of the calling stream.
 struct DeviceState {
     int device = -1;
     int num_sms = 0;
-    int max_smem_optin = 0;  // bytes of dynamic shared memory a block may opt into
-    int *err = nullptr;      // device error word (first int of the scratch block)
-    float *ws = nullptr;     // split-K partial sums (WS_FLOATS floats)
-    int *ws_count = nullptr; // split-K arrival counters (WS_COUNTERS ints, kept at zero between calls)
+    int max_smem_optin = 0;    // bytes of dynamic shared memory a block may opt into
+    int *err = nullptr;        // device error word (shared by every stream of the device)
+    float *ws = nullptr;       // split-K / per-slot partial sums (ws_floats floats)
+    int *ws_count = nullptr;   // arrival counters (ws_counters ints, kept at zero between calls)
+    unsigned *amax = nullptr;  // NVFP4 quantiser: the tensor maximum's bits
+    size_t ws_floats = 0;      // capacities: 0 = no workspace attached
+    int ws_counters = 0;
 };
 
-// Device scratch: error word (256 bytes), split-K partials, counters.
+// Workspace slot of one stream: NVFP4 tensor-maximum word (256 bytes), partial
+// sums, arrival counters.
 constexpr size_t WS_FLOATS = (size_t)4 << 20;  // 16 MiB
 constexpr int WS_COUNTERS = 4096;
-constexpr size_t SCRATCH_BYTES = 256 + WS_FLOATS * 4 + WS_COUNTERS * 4;
+constexpr size_t SLOT_BYTES = 256 + WS_FLOATS * 4 + WS_COUNTERS * 4;
 
 DeviceState *device_state();  // current device; nullptr on CUDA error
 cudaStream_t current_stream();
+
+// Point v's workspace at the slot of stream st (allocated, zeroed, on the
+// first call that needs one on this stream; the calling thread is switched
+// to relaxed capture mode for that, so a first call inside a stream capture
+// works too).  false on a CUDA error.
+bool attach_stream_workspace(DeviceState &v, cudaStream_t st);
 
 // Launchers: validated arguments in, a CUDA error code out.  The plain
 // launch_qmv / launch_moe_qmv pick the streaming kernels when the shape
@@ -74,6 +85,9 @@ cudaError_t launch_moe_ffn_prefill(const DeviceState &ds, cudaStream_t st, int f
                                    const uint8_t *gu_scales, const uint8_t *dn_codes, const uint8_t *dn_scales,
                                    const uint16_t *x, const int32_t *ids, const float *rw, float *out, int T, int E,
                                    int topk, int H, int I, void *workspace);
+
+// Test hook of the tensor-core kernels' bounded waits (mx_debug_qmm_stall).
+void set_qmm_stall(int stall_x, unsigned long long wait_ns);
 
 // Limits checked on the host.
 constexpr int QMV_MAX_K = 1 << 20;

@@ -1,8 +1,8 @@
 // mx_noalloc.cu -- mx_qmv_noalloc: the decode GEMV for callers that must
 // not allocate device memory.
 //
-// mx_qmv takes its split-K workspace (and error word) from a 16 MiB block it
-// cudaMalloc's on its first call on each device.  Some callers cannot allow
+// mx_qmv takes its split-K workspace from a 16 MiB slot it cudaMalloc's on
+// the first call on a stream that needs one.  Some callers cannot allow
 // that: a serving engine that has already handed the whole device pool to
 // its own allocator (a cudaMalloc there fails or breaks its accounting), or
 // a latency-critical decode loop where the implicit device synchronisation
@@ -84,9 +84,12 @@ extern "C" int mx_qmv_noalloc(int fmt, const void *codes, const void *scales, co
     ds.err = nullptr;  // the qmv kernels never write the error word
     ds.ws = reinterpret_cast<float *>(d->scratch);
     ds.ws_count = reinterpret_cast<int *>(d->scratch + NA_FLOATS * 4);
-    // the workspace this shape needs must fit the fixed array
+    ds.ws_floats = NA_FLOATS;
+    ds.ws_counters = NA_COUNTERS;
+    // A group of 8 tokens whose split-K partial sums would not fit the array
+    // runs on the direct-load kernel instead, which needs no workspace; the
+    // query reports what the groups that do use the array need.
     const QmvScratchNeed need = qmv_scratch_need(ds, fmt, M, N, K);
-    if (need.floats > NA_FLOATS || need.counters > NA_COUNTERS) return MX_EUNSUPPORTED;
     cudaStream_t st = current_stream();
     // the array keeps the last call's contents: the arrival counters must
     // start at zero (a cleared range, not an allocation)

@@ -39,6 +39,8 @@
 // that gives up sets MX_DEVERR_TIMEOUT in the device error word, the CTA
 // drains what it has in flight, both CTAs of the pair write NaN to their Y
 // rows and return.
+#include <atomic>
+
 #include <cuda.h>
 
 #include "mx_common.cuh"
@@ -52,6 +54,10 @@ constexpr int QMM_X_BYTES = 128 * QMM_BK * 2;  // a CTA's 128 rows of one 256-ro
 constexpr int QMM_W_BYTES = 128 * QMM_BK * 2;  // a CTA's 128 decoded weight rows
 constexpr int QMM_SMEM_LIMIT = 232448;         // 227 KB of dynamic shared memory per CTA
 constexpr unsigned long long QMM_WAIT_NS = 2000000000ull;
+// control words after the barriers: TMEM base, abort flag, X k-blocks loaded,
+// X k-blocks taken, decoded k-blocks taken from CTA 1, and the count of
+// signals each of up to 16 decoder warps issued
+constexpr int QMM_CTRL_WORDS = 5 + 16;
 
 // Per-format, per-tile-height geometry.  Three rings of k-blocks:
 //   X ring (SX slots): NACC slabs of 128 x 64 bf16 X rows, by TMA;
@@ -93,7 +99,7 @@ struct QmmGeo {
     // each ring slot is always used by the same decoder group (so a group
     // never waits on a phase two completions ahead of the barrier)
     static_assert(SC % NG == 0 && SD % NG == 0, "ring depth and decoder groups");
-    static_assert((2 * SX + 2 * SC + 3 * SD + 1) * 8 + 16 <= 512, "barrier area");
+    static_assert((2 * SX + 2 * SC + 3 * SD + 1) * 8 + 4 * QMM_CTRL_WORDS <= 512, "barrier area");
     static_assert(SMEM <= QMM_SMEM_LIMIT, "shared memory");
 };
 
@@ -223,6 +229,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
 {
     if (mbar_try_wait(bar, parity)) return true;
     return mbar_wait_slow(bar, parity, abort_flag, limit_ns, respect_abort);
+}
+
+// Complete `bytes` of the current phase's pending transactions without an
+// arrival (for copies that will never be issued).
+__device__ __forceinline__ void mbar_complete_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem()
@@ -376,7 +390,14 @@ __device__ __forceinline__ void qhalf_store(const uint32_t *w, uint32_t sbits, u
 {
     if constexpr (FMT == FMT_MXFP8) {
         const uint32_t e = sbits & 0xFFu;
-        if (e - 10u <= 132u) {
+        // An E4M3 NaN byte (S.1111.111) converts to an f16 NaN, which the
+        // exact move would turn into a finite bf16: a half row holding one
+        // takes the fp32 path, which keeps it NaN.  (b & 0x7F) + 1 sets bit 7
+        // of its byte only for 0x7F, and never carries into the next byte.
+        uint32_t nan_probe = 0u;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) nan_probe |= (w[c] & 0x7F7F7F7Fu) + 0x01010101u;
+        if (e - 10u <= 132u && (nan_probe & 0x80808080u) == 0u) {
             const uint32_t m = bf16x2_pow2_m15((int)e);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
@@ -467,7 +488,9 @@ struct QmmArgs {
     int *err;
     int M, N, K;  // grouped: N weight rows per expert, M rows of the gathered X
     int y32;  // Y rows and base 32-byte aligned: the epilogue stores 32 bytes per instruction
-    unsigned long long wait_ns;
+    unsigned long long wait_ns;   // limit of a pipeline wait (producer / consumer)
+    unsigned long long drain_ns;  // limit of a wait for copies already in flight
+    int stall_x;                  // test hook: issue no X loads, so the MMA issuer's first wait times out
     // grouped modes: the routing tables (written by the moe_group_route kernels)
     const int *groups;   // [0] = number of tiles G; from word 4 on: G x {expert, first sorted row, rows, 0}
     const int *slot_of;  // sorted row -> slot (QMM_GROUPED)
@@ -523,6 +546,8 @@ __global__ void __launch_bounds__(QmmGeo<FMT, NACC, MODE != QMM_DENSE>::THREADS,
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *x_issued = reinterpret_cast<volatile int *>(tmem_slot + 2);  // X k-blocks this CTA loaded
     volatile int *x_taken = reinterpret_cast<volatile int *>(tmem_slot + 3);   // (CTA 0) X k-blocks the MMAs took
+    volatile int *peer_taken = reinterpret_cast<volatile int *>(tmem_slot + 4);  // (CTA 0) k-blocks whose CTA 1 half the MMAs took
+    volatile int *sig_issued = reinterpret_cast<volatile int *>(tmem_slot + 5);  // (CTA 1) [8 NG] signals each decoder warp issued
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
@@ -577,6 +602,8 @@ __global__ void __launch_bounds__(QmmGeo<FMT, NACC, MODE != QMM_DENSE>::THREADS,
         *abort_flag = 0;
         *x_issued = 0;
         *x_taken = 0;
+        *peer_taken = 0;
+        for (int w = 0; w < 8 * QG::NG; ++w) sig_issued[w] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         // first use of each peer_full: its one arrival, and the signal bytes to wait for
         for (int s = 0; s < SD; ++s) mbar_arrive_expect_tx(&peer_full[s], SIG_BYTES);
@@ -602,7 +629,7 @@ __global__ void __launch_bounds__(QmmGeo<FMT, NACC, MODE != QMM_DENSE>::THREADS,
         if (lane == 0) {
             const uint32_t fx0 = map_to_cta(smem_u32(full_x), 0);
             int issued = 0;
-            for (int kb = 0; kb < KB; ++kb) {
+            for (int kb = 0; kb < KB && !a.stall_x; ++kb) {
                 const int s = kb % SX;
                 if (kb >= SX && !mbar_wait(&empty_x[s], ((kb / SX) - 1) & 1, abort_flag, a.wait_ns)) break;
                 const uint32_t bar = fx0 + 8u * (uint32_t)s;
@@ -664,18 +691,19 @@ __global__ void __launch_bounds__(QmmGeo<FMT, NACC, MODE != QMM_DENSE>::THREADS,
         // drain: every issued codes TMA must land before the CTA may exit
         if (lane == 0)
             for (int kb = (issued > SC ? issued - SC : 0); kb < issued; ++kb)
-                mbar_wait(&full_c[kb % SC], (kb / SC) & 1, abort_flag, a.wait_ns, false);
+                mbar_wait(&full_c[kb % SC], (kb / SC) & 1, abort_flag, a.drain_ns, false);
     } else if (warp == 1) {
         if (rank == 0 && lane == 0) {
             // ---------------- MMA issuer (CTA 0)
             constexpr uint32_t idesc = qmm_idesc();
-            int taken = 0;
+            int taken = 0, ptaken = 0;
             for (int kb = 0; kb < KB; ++kb) {
                 const int sx = kb % SX, sd = kb % SD;
                 if (!mbar_wait(&full_x[sx], (kb / SX) & 1, abort_flag, a.wait_ns)) break;
                 taken = kb + 1;
                 if (!mbar_wait(&dec_full[sd], (kb / SD) & 1, abort_flag, a.wait_ns)) break;
                 if (!mbar_wait(&peer_full[sd], (kb / SD) & 1, abort_flag, a.wait_ns)) break;
+                ptaken = kb + 1;
                 // arm the slot's next use: its arrival, and the signal bytes to wait for
                 mbar_arrive_expect_tx(&peer_full[sd], SIG_BYTES);
                 tc_fence_after();
@@ -696,6 +724,7 @@ __global__ void __launch_bounds__(QmmGeo<FMT, NACC, MODE != QMM_DENSE>::THREADS,
             }
             umma2_commit_both(acc_full);  // fires once every MMA issued so far has completed
             *x_taken = taken;
+            *peer_taken = ptaken;
         }
     } else {
         // ---------------- decoders (warps 2 ..): group grp (8 warps) takes
@@ -707,6 +736,7 @@ __global__ void __launch_bounds__(QmmGeo<FMT, NACC, MODE != QMM_DENSE>::THREADS,
         const int row = d >> 1, half = d & 1;
         const uint32_t sig0 = map_to_cta(smem_u32(sig + 16 * dl), 0);
         const uint32_t pf0 = map_to_cta(smem_u32(peer_full), 0);
+        int nsig = 0;  // (CTA 1, lane 0) signals issued
         for (int kb = grp; kb < KB; kb += QG::NG) {
             const int sc = kb % SC, sd = kb % SD;
             if (!mbar_wait(&full_c[sc], (kb / SC) & 1, abort_flag, a.wait_ns)) break;
@@ -738,17 +768,22 @@ __global__ void __launch_bounds__(QmmGeo<FMT, NACC, MODE != QMM_DENSE>::THREADS,
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                if (rank == 0) mbar_arrive(&dec_full[sd]);
-                else bulk_signal(sig0, dslot + 16 * dl, pf0 + 8u * (uint32_t)sd);
+                if (rank == 0) {
+                    mbar_arrive(&dec_full[sd]);
+                } else {
+                    bulk_signal(sig0, dslot + 16 * dl, pf0 + 8u * (uint32_t)sd);
+                    ++nsig;
+                }
             }
         }
+        if (lane == 0 && rank == 1) sig_issued[dw] = nsig;  // read by CTA 0 if the pair gives up
     }
 
     // ---------------- epilogue (decoder warps): TMEM -> bf16 -> Y
     bool acc_ok = true;
     if (warp >= 2 && warp < 2 + 8 * QG::NG) {
         // the MMAs must have finished (even on abort) before TMEM is read or freed
-        acc_ok = mbar_wait(acc_full, 0, abort_flag, a.wait_ns, false);
+        acc_ok = mbar_wait(acc_full, 0, abort_flag, a.drain_ns, false);
     }
     // every role of both CTAs is done: settle whether the pair gave up
     tc_fence_before();
@@ -765,11 +800,26 @@ __global__ void __launch_bounds__(QmmGeo<FMT, NACC, MODE != QMM_DENSE>::THREADS,
             const int s = kb % SX;
             if (kb >= i0) mbar_arrive_expect_tx_cluster(smem_u32(&full_x[s]), 0);
             if (kb >= i1) mbar_arrive_expect_tx_cluster(smem_u32(&full_x[s]), 0);
-            mbar_wait(&full_x[s], (kb / SX) & 1, abort_flag, a.wait_ns, false);
+            mbar_wait(&full_x[s], (kb / SX) & 1, abort_flag, a.drain_ns, false);
         }
-        // CTA 1's 16-byte signals issued before it stopped land within
-        // microseconds; give them that long before this CTA may exit
-        __nanosleep(20000);
+        // CTA 1's 16-byte signals of decoded k-blocks the MMAs did not take
+        // may still be landing on this CTA's peer_full barriers.  CTA 1's
+        // decoder warps published how many they issued (group g's warps
+        // signal k-blocks g, g + NG, ...).  A signal for k-block kb is only
+        // issued once the MMAs of kb - SD finished, so every outstanding one
+        // belongs to [taken, taken + SD), whose phases are armed for 8
+        // signals: complete the bytes of the signals never issued, then wait
+        // for the phase, after which none is in flight.
+        const int pt = *peer_taken;
+        for (int kb = pt; kb < pt + SD && kb < KB; ++kb) {
+            const int grp = kb % QG::NG, idx = kb / QG::NG;
+            int n = 0;
+            for (int w = 0; w < 8; ++w)
+                n += ld_cluster_s32(map_to_cta(smem_u32((const void *)(sig_issued + 8 * grp + w)), 1u)) > idx;
+            if (n == 0) continue;
+            if (n < 8) mbar_complete_tx(&peer_full[kb % SD], 16u * (uint32_t)(8 - n));
+            mbar_wait(&peer_full[kb % SD], (kb / SD) & 1, abort_flag, a.drain_ns, false);
+        }
     }
     if (warp >= 2 && warp < 2 + 8 * QG::NG) {
         const bool ok = acc_ok && !aborted;
@@ -878,6 +928,24 @@ __global__ void __launch_bounds__(QmmGeo<FMT, NACC, MODE != QMM_DENSE>::THREADS,
 }
 
 // ------------------------------------------------------------ host
+
+// Test hook state (mx_debug_qmm_stall): process-wide, read at each launch.
+static std::atomic<int> g_stall_x{0};
+static std::atomic<unsigned long long> g_wait_ns{0};
+
+void set_qmm_stall(int stall_x, unsigned long long wait_ns)
+{
+    g_stall_x.store(stall_x ? 1 : 0);
+    g_wait_ns.store(wait_ns);
+}
+
+static void qmm_wait_args(QmmArgs &a)
+{
+    const unsigned long long w = g_wait_ns.load();
+    a.wait_ns = w ? w : QMM_WAIT_NS;
+    a.drain_ns = QMM_WAIT_NS;
+    a.stall_x = g_stall_x.load();
+}
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
@@ -995,7 +1063,7 @@ cudaError_t launch_qmm_grouped(const DeviceState &ds, cudaStream_t st, int fmt, 
     a.M = rows;
     a.N = N;
     a.K = K;
-    a.wait_ns = QMM_WAIT_NS;
+    qmm_wait_args(a);
     const int yw = swiglu ? N / 2 : N;  // output row width
     a.y32 = ((reinterpret_cast<uintptr_t>(Y) & 31u) == 0 && yw % 16 == 0) ? 1 : 0;
     a.groups = groups;
@@ -1027,7 +1095,7 @@ cudaError_t launch_qmm(const DeviceState &ds, cudaStream_t st, int fmt, const ui
     a.M = M;
     a.N = N;
     a.K = K;
-    a.wait_ns = QMM_WAIT_NS;
+    qmm_wait_args(a);
     a.y32 = (reinterpret_cast<uintptr_t>(Y) & 31u) == 0 ? 1 : 0;
     a.groups = nullptr;
     a.slot_of = nullptr;

@@ -52,13 +52,28 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) qmv_kernel(QmvArgs a)
     const int xrow = tok < a.mc ? tok : -1;
     float g = 1.0f;
     if (FMT == FMT_NVFP4) g = load_f32_unaligned(a.scales + (size_t)a.N * (a.K / 16));
+    // fold factors of the lane's accumulator columns; the fold is on when a
+    // token was staged scaled up (the same decision in every CTA)
+    float f[2];
+    bool fold = false;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        const int t = acc_token<MC>(c);
+        f[c] = t < a.mc ? pow2f(sh_fold<FMT>(sh[t])) : 1.0f;
+    }
+    for (int t = 0; t < a.mc; ++t) fold |= sh_fold<FMT>(sh[t]) < 0;
 
     for (int base = blockIdx.x * WR; base < a.tiles; base += gridDim.x * WR) {
         const int tile = base + wr;
         float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-        if (tile < a.tiles)
-            qmv_tile<FMT, MC, dense_uf<FMT>()>(a.codes, a.scales, a.N, a.K, tile * RT, it0, it1, xs,
-                                                a.ks, xrow, acc);
+        if (tile < a.tiles) {
+            if (fold)
+                qmv_tile<FMT, MC, dense_uf<FMT>(), true>(a.codes, a.scales, a.N, a.K, tile * RT, it0, it1, xs,
+                                                          a.ks, xrow, acc, f);
+            else
+                qmv_tile<FMT, MC, dense_uf<FMT>()>(a.codes, a.scales, a.N, a.K, tile * RT, it0, it1, xs,
+                                                    a.ks, xrow, acc);
+        }
         float v[2][2];
         qmv_warp_reduce<MC>(acc, v);
 #pragma unroll
@@ -75,7 +90,7 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) qmv_kernel(QmvArgs a)
             if (base + w < a.tiles && row < a.N && t < a.mc) {
                 float s = 0.f;
                 for (int k = 0; k < a.wk; ++k) s += red[((w * a.wk + k) * RT + r) * MC + t];
-                s *= pow2f(sh[t]);
+                s *= pow2f(sh_final<FMT>(sh[t]));
                 if (FMT == FMT_NVFP4) s *= g;
                 a.y[(size_t)(a.m0 + t) * a.N + row] = s;
             }
@@ -186,7 +201,18 @@ __device__ __forceinline__ void moe_item(const MoeArgs &a, const uint8_t *ec, co
     const int tok = lane_token<MC>();
     const int xrow = tok < mc ? mem[tok] / a.topk : -1;
     float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-    qmv_tile<FMT, MC, MOE_UF>(ec, es, a.N, a.K, tile * RT, 0, iters, xs, a.ks, xrow, acc);
+    float f[2];
+    bool fold = false;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        const int t = acc_token<MC>(c);
+        f[c] = t < mc ? pow2f(sh_fold<FMT>(sh[mem[t] / a.topk])) : 1.0f;
+        fold |= f[c] != 1.0f;
+    }
+    if (__any_sync(0xFFFFFFFFu, fold))
+        qmv_tile<FMT, MC, MOE_UF, true>(ec, es, a.N, a.K, tile * RT, 0, iters, xs, a.ks, xrow, acc, f);
+    else
+        qmv_tile<FMT, MC, MOE_UF>(ec, es, a.N, a.K, tile * RT, 0, iters, xs, a.ks, xrow, acc);
     float v[2][2];
     qmv_warp_reduce<MC>(acc, v);
 #pragma unroll
@@ -198,7 +224,7 @@ __device__ __forceinline__ void moe_item(const MoeArgs &a, const uint8_t *ec, co
                 const int row = tile * RT + r;
                 if (row < a.N && t < mc) {
                     const int slot = mem[t];
-                    float s = v[h][c] * pow2f(sh[slot / a.topk]);
+                    float s = v[h][c] * pow2f(sh_final<FMT>(sh[slot / a.topk]));
                     if (FMT == FMT_NVFP4) s *= g;
                     a.y[(size_t)slot * a.N + row] = s;
                 }

@@ -15,8 +15,11 @@
 // multiply-accumulate runs on the tensor pipe: codes are converted by
 // cvt.rn.f16x2.e2m1x2 / .e4m3x2 straight into the A fragment of an
 // m16n8k16 f16 MMA with fp32 accumulation, and the activations, scaled per
-// token by a power of two into fp16 range (exact for bf16 inputs), form
-// the B fragment.  To keep one block scale per MMA output while loads stay
+// token by a power of two so that the largest magnitude lies in [1, 2),
+// form the B fragment (exact for elements within 2^14 of the token's
+// largest; smaller ones become f16 subnormals with an absolute error of at
+// most 2^-25 times that largest magnitude, and those below 2^-24 of it
+// flush to zero).  To keep one block scale per MMA output while loads stay
 // contiguous, the 16 A rows of an MMA are (weight row, block) pairs and the
 // 8 B columns are (token, block) pairs with the same block set:
 //
@@ -64,8 +67,13 @@ __host__ __device__ inline int stage_stride(int K)
 // shared memory.  Row r of xs holds elements [0, len) of source row src[r]
 // (or r when src is null) of x, whose rows are ld elements apart.  sh[r]
 // receives the per-row power-of-two exponent: the staged values are
-// x * 2^-sh[r] with max |.| in [1, 2) (exact: bf16 has 8 significant bits,
-// f16 11).  Elements past len up to the next 32-element unit are zero.
+// x * 2^-sh[r] with the largest finite magnitude in [1, 2).  bf16 has 8
+// significant bits and f16 11, so an element is staged exactly when it is
+// at least 2^-14 times that largest magnitude (an f16 normal); smaller ones
+// become f16 subnormals (absolute error at most 2^-25 times the largest) and
+// those below 2^-24 times it become zero.  Infinities and NaNs do not set
+// the scale and stay infinities and NaNs.  Elements past len up to the next
+// 32-element unit are zero.
 // When the rows fit in registers (<= 8 chunks of 8 elements per thread)
 // global memory is read once; otherwise twice.
 constexpr int STAGE_REG_CHUNKS = 8;
@@ -88,6 +96,14 @@ __device__ __forceinline__ void stage_store(uint16_t *xs, int ks, int r, int k0,
     }
 }
 
+// Magnitude bits of a bf16 value for the row maximum; an infinity or a NaN
+// counts as zero (it must not set the scale of the finite elements).
+__device__ __forceinline__ unsigned fin_mag(uint32_t h)
+{
+    h &= 0x7FFFu;
+    return h >= 0x7F80u ? 0u : h;
+}
+
 struct NoMid {
     __device__ void operator()() const {}
 };
@@ -106,13 +122,13 @@ __device__ void stage_x(const uint16_t *__restrict__ x, size_t ld, int len, int 
     const bool in_regs = total <= (int)blockDim.x * STAGE_REG_CHUNKS && (len % 8) == 0 && (ld % 8) == 0;
     uint4 cache[STAGE_REG_CHUNKS];
     if (!in_regs) mid();
-    // pass 1: largest magnitude per row (as bf16 bits; NaN > inf > finite)
+    // pass 1: largest finite magnitude per row (as bf16 bits)
     for (int r = 0; r < nrows && !in_regs; ++r) {
         const uint32_t *row = reinterpret_cast<const uint32_t *>(x + (size_t)(src ? src[r] : r) * ld);
         unsigned m = 0;
         for (int i = threadIdx.x; i < len / 2; i += blockDim.x) {
             uint32_t v = row[i];
-            m = max(m, max(v & 0x7FFFu, (v >> 16) & 0x7FFFu));
+            m = max(m, max(fin_mag(v), fin_mag(v >> 16)));
         }
         if (m) atomicMax(&maxbits[r], m);
     }
@@ -137,8 +153,8 @@ __device__ void stage_x(const uint16_t *__restrict__ x, size_t ld, int len, int 
                 const int r = idx / cpr, k0 = (idx - r * cpr) * 8;
                 if (k0 < len) {
                     const uint4 v = cache[j];
-                    unsigned m = max(max(v.x & 0x7FFFu, (v.x >> 16) & 0x7FFFu), max(v.y & 0x7FFFu, (v.y >> 16) & 0x7FFFu));
-                    m = max(m, max(max(v.z & 0x7FFFu, (v.z >> 16) & 0x7FFFu), max(v.w & 0x7FFFu, (v.w >> 16) & 0x7FFFu)));
+                    unsigned m = max(max(fin_mag(v.x), fin_mag(v.x >> 16)), max(fin_mag(v.y), fin_mag(v.y >> 16)));
+                    m = max(m, max(max(fin_mag(v.z), fin_mag(v.z >> 16)), max(fin_mag(v.w), fin_mag(v.w >> 16))));
                     if (m) atomicMax(&maxbits[r], m);
                 }
             }
@@ -179,6 +195,24 @@ __device__ void stage_x(const uint16_t *__restrict__ x, size_t ld, int len, int 
         }
         stage_store(xs, ks, r, k0, len, v, pow2f(-sh[r]), FMT);
     }
+}
+
+// Split of a token's power of two 2^sh: MX formats fold 2^min(sh, 0) into
+// the block scales inside the loop (see compute_unit) and multiply the
+// finished sum by 2^max(sh, 0); NVFP4 applies all of 2^sh to the finished
+// sum (an E4M3 block scale times a partial of at most 2^9 cannot leave
+// fp32's range).
+template <int FMT>
+__device__ __forceinline__ int sh_fold(int sh) { return FMT == FMT_NVFP4 ? 0 : min(sh, 0); }
+template <int FMT>
+__device__ __forceinline__ int sh_final(int sh) { return FMT == FMT_NVFP4 ? sh : max(sh, 0); }
+
+// Token (0..MC-1) of the lane's accumulator column c: the m16n8k16 D
+// fragment holds columns 2q and 2q + 1.
+template <int MC>
+__device__ __forceinline__ int acc_token(int c)
+{
+    return (2 * (threadIdx.x & 3) + c) / (8 / MC);
 }
 
 // -------------------------------------------------------------- loads
@@ -248,13 +282,39 @@ __device__ __forceinline__ void load_unit(const TileCtx &t, int u, bool ok, Ld<F
     }
 }
 
+// acc[h][c] += d (row half h, column c) times the block scale of half h
+// (times the column's fold factor).
+template <bool FOLD>
+__device__ __forceinline__ void mx_accumulate(const float (&d)[4], float s0, float s1, const float (&f)[2],
+                                              float (&acc)[2][2])
+{
+    if constexpr (FOLD) {
+        acc[0][0] = fmaf(d[0], s0 * f[0], acc[0][0]);
+        acc[0][1] = fmaf(d[1], s0 * f[1], acc[0][1]);
+        acc[1][0] = fmaf(d[2], s1 * f[0], acc[1][0]);
+        acc[1][1] = fmaf(d[3], s1 * f[1], acc[1][1]);
+    } else {
+        acc[0][0] = fmaf(d[0], s0, acc[0][0]);
+        acc[0][1] = fmaf(d[1], s0, acc[0][1]);
+        acc[1][0] = fmaf(d[2], s1, acc[1][0]);
+        acc[1][1] = fmaf(d[3], s1, acc[1][1]);
+    }
+}
+
 // One MMA group: BPM units (one per A-row block offset) -> acc[h][c].
 // ok = false: the lane's unit lies outside the work; its fragments may hold
 // stale data, so nothing is accumulated (the quad that shares the A rows
 // and B column has the same ok).
-template <int FMT>
+// FOLD (MX formats): the E8M0 block scale of accumulator column c is
+// multiplied by f[c] = 2^min(sh, 0) of that column's token first, so a block
+// partial enters the sum already in the output's scale.  A token whose
+// activations are all below 1 is staged scaled up by 2^-sh; without the
+// fold a huge block scale (E8M0 above ~245) could overflow the fp32 partial
+// that the final 2^sh would have brought back into range.  f <= 1, so the
+// folded scale never overflows (a zero partial times it stays zero).
+template <int FMT, bool FOLD = false>
 __device__ __forceinline__ void compute_unit(const Ld<FMT> &l, const uint32_t (&B)[4], float (&acc)[2][2],
-                                             bool ok = true)
+                                             bool ok = true, const float (&f)[2] = {1.f, 1.f})
 {
     const float z[4] = {0.f, 0.f, 0.f, 0.f};
     if constexpr (FMT == FMT_MXFP8) {
@@ -269,12 +329,7 @@ __device__ __forceinline__ void compute_unit(const Ld<FMT> &l, const uint32_t (&
         mma_f16_16816(d, a, B[2], B[3], d);
         float s0, s1;
         e8m0x2_to_f32(l.s, s0, s1);
-        if (ok) {
-            acc[0][0] = fmaf(d[0], s0, acc[0][0]);
-            acc[0][1] = fmaf(d[1], s0, acc[0][1]);
-            acc[1][0] = fmaf(d[2], s1, acc[1][0]);
-            acc[1][1] = fmaf(d[3], s1, acc[1][1]);
-        }
+        if (ok) mx_accumulate<FOLD>(d, s0, s1, f, acc);
     } else {
         // bytes 0,1 of a row's word feed MMA step 0 (A cols 2q.. and 2q+8..),
         // bytes 2,3 feed step 1
@@ -287,12 +342,7 @@ __device__ __forceinline__ void compute_unit(const Ld<FMT> &l, const uint32_t (&
             mma_f16_16816(d, a1, B[2], B[3], d);
             float s0, s1;
             e8m0x2_to_f32(l.s, s0, s1);
-            if (ok) {
-                acc[0][0] = fmaf(d[0], s0, acc[0][0]);
-                acc[0][1] = fmaf(d[1], s0, acc[0][1]);
-                acc[1][0] = fmaf(d[2], s1, acc[1][0]);
-                acc[1][1] = fmaf(d[3], s1, acc[1][1]);
-            }
+            if (ok) mx_accumulate<FOLD>(d, s0, s1, f, acc);
         } else {
             float d0[4], d1[4];
             mma_f16_16816(d0, a0, B[0], B[1], z);
@@ -314,11 +364,12 @@ __device__ __forceinline__ void compute_unit(const Ld<FMT> &l, const uint32_t (&
 // and accumulate the lane's fragment partial sums into acc[h][c].
 // xrow: this lane's B-column activation row in xs, or -1 for a padding
 // column.
-template <int FMT, int MC, int UF>
+// FOLD, f: see compute_unit.
+template <int FMT, int MC, int UF, bool FOLD = false>
 __device__ __forceinline__ void qmv_tile(const uint8_t *__restrict__ codes,
                                          const uint8_t *__restrict__ scales, int N, int K,
                                          int row0, int it0, int it1, const uint16_t *xs, int ks,
-                                         int xrow, float (&acc)[2][2])
+                                         int xrow, float (&acc)[2][2], const float (&f)[2] = {1.f, 1.f})
 {
     constexpr int BPM = 8 / MC;
     const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
@@ -361,7 +412,7 @@ __device__ __forceinline__ void qmv_tile(const uint8_t *__restrict__ codes,
                     const uint4 v = *reinterpret_cast<const uint4 *>(xp + (size_t)u * 32);
                     B[0] = v.x; B[1] = v.y; B[2] = v.z; B[3] = v.w;
                 }
-                compute_unit<FMT>(cur[j], B, acc);
+                compute_unit<FMT, FOLD>(cur[j], B, acc, true, f);
             }
         }
         if (more) {

@@ -176,10 +176,12 @@ __device__ __forceinline__ void copy_stage(const CopyPlan<FMT, MC> &c, const Cop
 // Decode-and-multiply one stage from shared memory into acc.
 // xrow: the lane's staged activation row (-1: padding column); xu0: the
 // first unit held by the staged activations.  FULL: every unit of the stage
-// lies inside the unit's range (no per-iteration checks).
-template <int FMT, int MC, bool FULL>
+// lies inside the unit's range (no per-iteration checks).  FOLD, f: see
+// compute_unit.
+template <int FMT, int MC, bool FULL, bool FOLD>
 __device__ __forceinline__ void compute_stage_impl(const SUnit &u, int s, const uint8_t *buf, const uint16_t *xs,
-                                                   int ks, int xu0, int xrow, float (&acc)[2][2])
+                                                   int ks, int xu0, int xrow, float (&acc)[2][2],
+                                                   const float (&f)[2])
 {
     using G = SGeo<FMT, MC>;
     const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
@@ -225,19 +227,19 @@ __device__ __forceinline__ void compute_stage_impl(const SUnit &u, int s, const 
             B[2] = v.z;
             B[3] = v.w;
         }
-        compute_unit<FMT>(l, B, acc, ok);
+        compute_unit<FMT, FOLD>(l, B, acc, ok, f);
     }
 }
 
-template <int FMT, int MC>
+template <int FMT, int MC, bool FOLD>
 __device__ __forceinline__ void compute_stage(const SUnit &u, int s, const uint8_t *buf, const uint16_t *xs,
-                                              int ks, int xu0, int xrow, float (&acc)[2][2])
+                                              int ks, int xu0, int xrow, float (&acc)[2][2], const float (&f)[2])
 {
     using G = SGeo<FMT, MC>;
     if (u.ul - (u.ub + s * G::UPS) >= G::UPS)
-        compute_stage_impl<FMT, MC, true>(u, s, buf, xs, ks, xu0, xrow, acc);
+        compute_stage_impl<FMT, MC, true, FOLD>(u, s, buf, xs, ks, xu0, xrow, acc, f);
     else
-        compute_stage_impl<FMT, MC, false>(u, s, buf, xs, ks, xu0, xrow, acc);
+        compute_stage_impl<FMT, MC, false, FOLD>(u, s, buf, xs, ks, xu0, xrow, acc, f);
 }
 
 // A warp's stream of units through its ring: copies run S-1 stages ahead
@@ -289,22 +291,25 @@ struct Streamer {
     }
 
     // xrow_of(i): the lane's activation row for unit i; done(i, acc): the
-    // lane's fragment partial sums at the end of unit i.
-    template <class XRow, class Done>
-    __device__ __forceinline__ void run(const XRow &xrow_of, const Done &done, const uint8_t *ring,
-                                        const uint16_t *xs, int ks, int xu0)
+    // lane's fragment partial sums at the end of unit i; fold_of(i, f): the
+    // fold factors of the lane's accumulator columns in unit i (FOLD only).
+    template <bool FOLD, class XRow, class Done, class Fold>
+    __device__ __forceinline__ void run(const XRow &xrow_of, const Done &done, const Fold &fold_of,
+                                        const uint8_t *ring, const uint16_t *xs, int ks, int xu0)
     {
         int slot = 0;
         for (int cu = 0; cu < n_units; ++cu) {
             const SUnit cd = next(cu);
             const int nst = unit_stages<FMT, MC>(cd);
             const int xrow = xrow_of(cu);
+            float f[2] = {1.f, 1.f};
+            if constexpr (FOLD) fold_of(cu, f);
             float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
             for (int cs = 0; cs < nst; ++cs) {
                 cp_async_wait<G::STAGES - 2>();
                 __syncwarp();
                 issue();  // refills the slot consumed one stage ago
-                compute_stage<FMT, MC>(cd, cs, ring + slot * G::STAGE_BYTES, xs, ks, xu0, xrow, acc);
+                compute_stage<FMT, MC, FOLD>(cd, cs, ring + slot * G::STAGE_BYTES, xs, ks, xu0, xrow, acc, f);
                 slot = slot + 1 == G::STAGES ? 0 : slot + 1;
             }
             done(cu, acc);
@@ -440,7 +445,25 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) qmv_stream_kernel(QmvSArgs a)
                  maxbits, [&]() { st.prime(G::STAGES - 2); });
     for (int i = threadIdx.x; i < ntl * a.pmax * G::RT * MC; i += blockDim.x) red[i] = 0.f;  // unused slots add 0
     __syncthreads();
-    st.run(xrow_of, done, ring, xs, a.ks, xu0);
+    // fold factors of the lane's accumulator columns (the same in every
+    // unit); the fold is on when a token was staged scaled up, a decision
+    // every CTA takes alike
+    float fcol[2];
+    bool fold = false;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        const int t = acc_token<MC>(c);
+        fcol[c] = t < a.mc ? pow2f(sh_fold<FMT>(sh[t])) : 1.0f;
+    }
+    for (int t = 0; t < a.mc; ++t) fold |= sh_fold<FMT>(sh[t]) < 0;
+    auto fold_of = [&](int, float (&f)[2]) {
+        f[0] = fcol[0];
+        f[1] = fcol[1];
+    };
+    if (fold)
+        st.template run<true>(xrow_of, done, fold_of, ring, xs, a.ks, xu0);
+    else
+        st.template run<false>(xrow_of, done, fold_of, ring, xs, a.ks, xu0);
     __syncthreads();
 
     float g = 1.0f;
@@ -453,7 +476,7 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) qmv_stream_kernel(QmvSArgs a)
         if (row >= a.N) continue;
         float s = 0.f;
         for (int c = 0; c < a.pmax; ++c) s += red[((size_t)(ti * a.pmax + c) * G::RT + r) * MC + t];
-        s *= pow2f(sh[t]);
+        s *= pow2f(sh_final<FMT>(sh[t]));
         if (a.nwin == 1) {
             if (FMT == FMT_NVFP4) s *= g;
             a.y[(size_t)(a.m0 + t) * a.N + row] = s;
@@ -541,7 +564,11 @@ static cudaError_t plan_qmv_stream(const DeviceState &ds, cudaStream_t st, const
     if (a.G > a.tiles) a.G = a.tiles;
     a.WU = WU;
     a.ntl_max = (a.tiles + a.G - 1) / a.G;
-    if (nwin > 1 && ((size_t)nwin * mc * N > WS_FLOATS || a.G > WS_COUNTERS)) return cudaErrorNotSupported;
+    // K windows add their partial sums through the calling stream's workspace:
+    // without one attached, or when it is too small, the chunk falls back to
+    // the direct-load kernel (which needs none)
+    if (nwin > 1 && ((size_t)nwin * mc * N > ds.ws_floats || a.G > ds.ws_counters)) return cudaErrorNotSupported;
+    if (nwin > 1 && !query && (ds.ws == nullptr || ds.ws_count == nullptr)) return cudaErrorNotSupported;
     // work split: whole tiles round-robin when the busiest warp has at most
     // 5 % more than the average; else equal runs of stages (a tile cut into
     // at most pmax pieces when every warp's run has a stage, else one slot
@@ -756,7 +783,7 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) moe_stream_kernel(MoeSArgs a)
                     const int irow = tile * MC + r;
                     if (irow < a.I && t < wg_mc[w]) {
                         const int slot = sorted[wg_first[w] + t];
-                        const float f = pow2f(sh[slot / a.topk]);
+                        const float f = pow2f(sh_final<FMT>(sh[slot / a.topk]));
                         float gv = vv[0][c] * f, uv = vv[1][c] * f;
                         if (FMT == FMT_NVFP4) {
                             gv *= g;
@@ -776,7 +803,7 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) moe_stream_kernel(MoeSArgs a)
                         const int row = tile * G::RT + r;
                         if (row < a.N && t < wg_mc[w]) {
                             const int slot = sorted[wg_first[w] + t];
-                            float s = vv[h][c] * pow2f(sh[xrow_of_slot(slot)]);
+                            float s = vv[h][c] * pow2f(sh_final<FMT>(sh[xrow_of_slot(slot)]));
                             if (FMT == FMT_NVFP4) s *= g;
                             if (MODE == MOE_PLAIN) a.y[(size_t)slot * a.N + row] = s;
                             else a.ws[(size_t)slot * a.N + row] = s;
@@ -802,7 +829,22 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) moe_stream_kernel(MoeSArgs a)
     // the rest of the weight copies are issued once the activation loads are in flight
     stage_x<FMT>(a.x, (size_t)a.K, a.K, XR, nullptr, xs, a.ks, sh, maxbits, [&]() { st.prime(G::STAGES - 2); });
     __syncthreads();
-    st.run(xrow_of, done, ring, xs, a.ks, 0);
+    // fold factors per unit (the members of its work group); the fold is on
+    // when a staged row was scaled up, a decision every CTA takes alike
+    bool fold = false;
+    for (int r = 0; r < XR; ++r) fold |= sh_fold<FMT>(sh[r]) < 0;
+    auto fold_of = [&](int i, float (&f)[2]) {
+        const int w = (gw + stride * i) / tiles;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int t = acc_token<MC>(c);
+            f[c] = t < wg_mc[w] ? pow2f(sh_fold<FMT>(sh[xrow_of_slot(sorted[wg_first[w] + t])])) : 1.0f;
+        }
+    };
+    if (fold)
+        st.template run<true>(xrow_of, done, fold_of, ring, xs, a.ks, 0);
+    else
+        st.template run<false>(xrow_of, done, fold_of, ring, xs, a.ks, 0);
 
     if constexpr (MODE == MOE_DOWN_COMBINE) {
         // Each tile gets one unit per work group.  The warp that completes a
@@ -934,7 +976,8 @@ cudaError_t launch_moe_down_combine(const DeviceState &ds, cudaStream_t st, int 
     if (!stream_ok(fmt, K)) return cudaErrorInvalidValue;
     const int MC = moe_mc_down(T);
     const int RT = 2 * MC;
-    if ((size_t)T * topk * N > WS_FLOATS || (N + RT - 1) / RT > WS_COUNTERS) return cudaErrorInvalidValue;
+    if ((size_t)T * topk * N > ds.ws_floats || (N + RT - 1) / RT > ds.ws_counters || ds.ws == nullptr)
+        return cudaErrorInvalidValue;
     MoeSArgs a = moe_args(ds, codes, scales, h, ids, T, E, topk, N, K);
     a.rw = rw;
     a.out = out;

@@ -214,8 +214,9 @@ cudaError_t launch_quantize(const DeviceState &ds, cudaStream_t st, int fmt, con
     const long long cap = (long long)ds.num_sms * 16;
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
-    unsigned *gbits = reinterpret_cast<unsigned *>(ds.err) + 1;  // a word of the error block's spare bytes
+    unsigned *gbits = ds.amax;  // the calling stream's tensor-maximum word (NVFP4 only)
     if (fmt == FMT_NVFP4) {
+        if (gbits == nullptr) return cudaErrorInvalidValue;
         cudaError_t e = cudaMemsetAsync(gbits, 0, sizeof(unsigned), st);
         if (e != cudaSuccess) return e;
         const long long n8 = (long long)M * K / 8;

@@ -57,6 +57,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "mx_swiglu": [P, P, I, I],
             "mx_moe_combine": [P, P, P, I, I, I],
             "mx_device_error": [],
+            "mx_debug_qmm_stall": [I, ctypes.c_ulonglong],
             "mx_moe_qmm": [I, P, P, P, P, P, I, I, I, I, I, P, Z],
             "mx_quantize": [I, P, P, P, I, I],
             "mx_moe_ffn_prefill": [I, P, P, P, P, P, P, P, P, I, I, I, I, I, P, Z],
@@ -263,6 +264,12 @@ def moe_combine(yd: torch.Tensor, r: torch.Tensor, out: torch.Tensor | None = No
     _stream()
     _check("mx_moe_combine", load().mx_moe_combine(_ptr(yd), _ptr(r), _ptr(out), T, topk, N))
     return out
+
+
+def debug_qmm_stall(stall: bool, wait_ns: int = 0) -> None:
+    """Test hook: make later tensor-core GEMM launches withhold their
+    activation loads so that their bounded waits time out (see mx.h)."""
+    _check("mx_debug_qmm_stall", load().mx_debug_qmm_stall(1 if stall else 0, wait_ns))
 
 
 def device_error() -> int:

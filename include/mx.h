@@ -33,14 +33,21 @@
  * kernel's, not a fixed sequential one.
  *
  * Ownership and execution: every pointer is a caller-owned DEVICE pointer
- * on the current CUDA device.  The library allocates nothing per call; on
- * first use of a device it allocates one 16 MiB scratch block that holds the
- * device error word and the split-K workspace of mx_qmv (the first call on a
- * device should therefore come before any stream capture; see
- * mx_qmv_noalloc for a variant that never allocates).  Calls are asynchronous on the stream set with
+ * on the current CUDA device.  Calls are asynchronous on the stream set with
  * mx_set_stream (per host thread; default: the legacy default stream),
- * re-entrant across host threads, and return as soon as the kernel is
- * queued.
+ * re-entrant across host threads and streams, and return as soon as the
+ * kernels are queued.  The device error word is a variable of the library
+ * image.  Calls whose kernels pass partial sums through global memory
+ * (mx_qmv when K is split across CTAs, mx_moe_down_combine, NVFP4
+ * mx_quantize) use a 16 MiB workspace slot of the stream they are issued on,
+ * so calls on different streams never share one; a stream's slot is
+ * allocated and cleared by the first such call on it (cudaMalloc, with the
+ * calling thread switched to relaxed capture mode for it, so that first call
+ * may come inside a stream capture) and kept until the process exits.  The
+ * per-thread default stream gets one slot per host thread.  A captured graph
+ * keeps using the slot of the stream it was captured on: do not replay it
+ * concurrently with itself or with calls on that stream.  mx_qmv_noalloc
+ * never allocates.
  *
  * Errors: 0 on success, otherwise a negative MX_E* code; the call then
  * launched nothing.  Faults found on the device (an expert id out of range,
@@ -130,11 +137,11 @@ int mx_moe_gate_up_swiglu(int fmt, const void *expert_codes, const void *expert_
  * [T*topk][K] (mx_moe_gate_up_swiglu's output, K = I); r fp32 [T][topk];
  * out fp32 [T][N].  Slots that share an expert are served by one pass over
  * its weights; the per-slot partial sums go through the library's device
- * workspace (T*topk*N <= 4 Mi floats), whose counters are re-armed by the
- * call itself.  A bad id sets MX_DEVERR_BAD_EXPERT and makes that token's
+ * workspace slot of the calling stream (T*topk*N <= 4 Mi floats), whose
+ * counters are re-armed by the call itself.  A bad id sets MX_DEVERR_BAD_EXPERT and makes that token's
  * outputs NaN.  K a multiple of 128; h, out, codes, scales 16-byte aligned,
- * ids and r 4-byte aligned.  Calls that use the workspace (this one and
- * mx_qmv) must not run concurrently on one device. */
+ * ids and r 4-byte aligned.  Calls on one stream run in order; calls on
+ * different streams use different workspace slots. */
 int mx_moe_down_combine(int fmt, const void *expert_codes, const void *expert_scales, const void *h,
                         const int32_t *expert_ids, const float *router_weights, float *out, int T, int E,
                         int topk, int N, int K);
@@ -208,8 +215,7 @@ int mx_moe_ffn_prefill(int fmt, const void *gate_up_codes, const void *gate_up_s
  *     (1 when G = 0); per 16 elements s = E4M3(fp32(max |x| / fp32(6 g)))
  *     and each element fp32(x / fp32(s g)) rounded to E2M1 (zero codes when
  *     s g = 0).  Two launches (tensor maximum, then the blocks); the
- *     maximum goes through a word of the library's per-device scratch, so
- *     NVFP4 calls on different streams of one device must not overlap.
+ *     maximum goes through a word of the calling stream's workspace slot.
  *   A block holding a NaN or an infinity gets a NaN scale (0xFF / 0x7F) and
  *   zero codes; a zero result is stored as +0.
  * K a multiple of the block (else MX_EINVAL); x and codes 16-byte aligned. */
@@ -238,16 +244,18 @@ int mx_swiglu(const float *gu, void *h, int Q, int I);
 int mx_moe_combine(const float *yd, const float *r, float *out, int T, int topk, int N);
 
 /* Decode GEMV for callers that cannot allocate device memory.  Same
- * operation, arguments, layouts and errors as mx_qmv, which on its first call
- * on a device cudaMalloc's a 16 MiB workspace; some callers cannot allow
+ * operation, arguments, layouts and errors as mx_qmv, which cudaMalloc's a
+ * 16 MiB workspace slot on the first call on a stream whose shape splits K
+ * across CTAs; some callers cannot allow
  * that (an engine whose own allocator already owns the whole device pool, or
  * a latency-critical decode loop that cannot take the device
  * synchronisation of a first-call allocation).  This variant allocates
  * nothing: its split-K workspace is a fixed ~1 MiB array inside the library
  * image (262,144 fp32 partial sums plus 4,096 counters), held by every GPU
- * that loads the library until the process exits.  Shapes whose workspace
- * would not fit (many tokens times large N with K split into windows)
- * return MX_EUNSUPPORTED.  The first call on a device looks up the array's
+ * that loads the library until the process exits.  A group of 8 tokens whose
+ * workspace would not fit (many tokens times large N with K split into
+ * windows) runs on the slower direct-load kernel, which needs none, so every
+ * shape mx_qmv takes is served.  The first call on a device looks up the array's
  * device address and the device attributes; make that first call before any
  * stream capture.  Every call shares the one array, so two calls that
  * overlap on the GPU (for example on two streams) race; each call clears
@@ -255,6 +263,19 @@ int mx_moe_combine(const float *yd, const float *r, float *out, int T, int topk,
  * is an interface variant of mx_qmv, not a different computation. */
 int mx_qmv_noalloc(int fmt, const void *codes, const void *scales, const void *x, float *y, int M, int N,
                    int K);
+
+/* Test hook for the bounded waits of the tensor-core kernels (mx_qmm,
+ * mx_moe_qmm, mx_moe_ffn_prefill); the pages' fault handling (talk slide 10
+ * "70 Fixes to the ROCm Fork", GPU fault handling: waits that used to block
+ * forever after a fault now give up and report it).  With stall != 0, every
+ * later launch of those kernels from this process issues none of its
+ * activation loads, so the MMA issuer's first wait can only end by timing
+ * out: the pair then writes NaN to its output tile, sets MX_DEVERR_TIMEOUT
+ * and returns with nothing in flight.  wait_ns is the limit of a pipeline
+ * wait (0: the default of 2 s); waits for copies already in flight keep the
+ * 2 s limit.  mx_debug_qmm_stall(0, 0) restores normal operation.  For
+ * tests only: not to be used while other threads launch those kernels. */
+int mx_debug_qmm_stall(int stall, unsigned long long wait_ns);
 
 /* Synchronise the calling thread's stream, then return the device error
  * word of the current device (0 = none; MX_DEVERR_* bits) and clear it.

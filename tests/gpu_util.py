@@ -76,6 +76,53 @@ def check_close(got, want, what="", bf16_out=False):
     return tot, rel_rows.max(), mx.max()
 
 
+def check_special(got, want, what="", bf16_out=False):
+    """The tolerance gate for outputs that may hold NaN or +-inf: NaN
+    positions must agree exactly with the oracle's, every infinite oracle
+    value must be matched by the same infinity (and the GPU may give an
+    infinity nowhere else), and the finite entries pass the usual gate, with
+    each row's norm taken over its finite entries."""
+    got = np.asarray(got, dtype=np.float64).reshape(want.shape[0], -1)
+    want = np.asarray(want, dtype=np.float64).reshape(want.shape[0], -1)
+    gn, wn = np.isnan(got), np.isnan(want)
+    assert np.array_equal(gn, wn), f"{what}: NaN positions differ in {int((gn != wn).sum())} entries"
+    gi, wi = np.isinf(got), np.isinf(want)
+    assert np.array_equal(gi, wi), f"{what}: infinity positions differ in {int((gi != wi).sum())} entries"
+    assert np.array_equal(got[wi], want[wi]), f"{what}: infinities of the wrong sign"
+    fin = np.isfinite(want)
+    with np.errstate(invalid="ignore"):
+        err = np.where(fin, got - want, 0.0)
+    ref = np.where(fin, want, 0.0)
+    tot_n = np.linalg.norm(ref)
+    if tot_n == 0.0:
+        assert not np.any(err), f"{what}: nonzero output where the oracle is zero"
+        return 0.0, 0.0, 0.0
+    tot = np.linalg.norm(err) / tot_n
+    rn = np.linalg.norm(ref, axis=1)
+    live = rn > 0
+    rel_rows = np.linalg.norm(err[live], axis=1) / rn[live]
+    mx = np.abs(err[live]).max(axis=1) / rn[live]
+    assert not np.any(err[~live]), f"{what}: nonzero output in a row the oracle has at zero"
+    assert tot <= REL_L2, f"{what}: relL2 {tot:.3e}"
+    row_lim = REL_L2 + (BF16_ROUNDING if bf16_out else 0.0)
+    assert rel_rows.max() <= row_lim, f"{what}: worst row relL2 {rel_rows.max():.3e}"
+    assert mx.max() <= MAX_ROWNORM, f"{what}: max |err| / row norm {mx.max():.3e}"
+    return tot, rel_rows.max(), mx.max()
+
+
+def bf16_ulp_diff(a, b):
+    """Distance in units in the last place between bf16 bit patterns: the
+    patterns are mapped to integers that increase with the value (negative
+    numbers below -0, -0 and +0 one apart), so the difference counts the
+    representable numbers between the two, across zero and signs too."""
+    def key(bits):
+        v = np.asarray(bits, dtype=np.uint16).astype(np.int64)
+        mag = v & 0x7FFF
+        return np.where(v & 0x8000, -mag - 1, mag)
+
+    return np.abs(key(a) - key(b))
+
+
 def same_values(got, want):
     """Value equality with NaN == NaN (and +0 == -0)."""
     got = np.asarray(got, dtype=np.float64)

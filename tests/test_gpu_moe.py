@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 
 from gemm_decode_register_gb300 import synth
-from gpu_util import (bf16_bits_to_f64, bf16_host, check_close, dev_bf16, dev_i32, dev_u8,
+from gpu_util import (bf16_bits_to_f64, bf16_host, bf16_ulp_diff, check_close, dev_bf16, dev_i32, dev_u8,
                       need_gpu, same_values)
 
 pytestmark = pytest.mark.gpu
@@ -129,7 +129,7 @@ def test_moe_ffn_composite(orc, T):
     h_chk = orc.swiglu_bf16(gu.cpu().numpy().astype(np.float64).reshape(T * topk, 2 * I), I)
     hb = bf16_host(h)
     big = np.abs(bf16_bits_to_f64(h_chk)) >= 2.0 ** -100
-    diff = np.abs(hb.astype(np.int32) - h_chk.astype(np.int32))[big]
+    diff = bf16_ulp_diff(hb, h_chk)[big]
     assert diff.max() <= 1
     assert np.all(np.abs(bf16_bits_to_f64(hb[~big])) < 2.0 ** -99)
 

@@ -6,7 +6,8 @@ import numpy as np
 import pytest
 
 from gemm_decode_register_gb300 import synth
-from gpu_util import bf16_bits_to_f64, bf16_host, check_close, dev_bf16, dev_i32, dev_u8, need_gpu
+from gpu_util import (bf16_bits_to_f64, bf16_host, bf16_ulp_diff, check_close, dev_bf16, dev_i32, dev_u8,
+                      need_gpu)
 
 pytestmark = pytest.mark.gpu
 
@@ -57,7 +58,7 @@ def test_gate_up_swiglu_config(orc, T):
     check_close(bf16_bits_to_f64(hb), bf16_bits_to_f64(want), f"gate-up swiglu T{T}", bf16_out=True)
     gu = ops.moe_qmv(fmt, dev_u8(codes), dev_u8(scales), dev_bf16(x), dev_i32(ids), E, 2 * I)
     h2 = bf16_host(ops.swiglu(gu, I)).reshape(T * topk, I)
-    assert np.abs(hb.astype(np.int32) - h2.astype(np.int32)).max() <= 1
+    assert bf16_ulp_diff(hb, h2).max() <= 1
 
 
 @pytest.mark.parametrize("fmt", [0, 1, 2])
