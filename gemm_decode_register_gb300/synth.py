@@ -83,6 +83,36 @@ def weights(fmt: int, N: int, K: int, seed: int, *, E: int = 1, exp_lo: int = 11
     return codes, scales
 
 
+def weights_device(fmt: int, N: int, K: int, seed: int, device, *, exp_lo: int = 118, exp_hi: int = 132):
+    """(codes, scales) as uint8 torch tensors on `device`, drawn with the
+    same distributions as weights() by a seeded generator on that device
+    (for workloads too large to draw on the host: tens of GB of weights).
+    The values differ from weights() for the same seed."""
+    import torch
+
+    if K % block_of(fmt):
+        raise ValueError("K must be a multiple of the block size")
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    u8 = dict(dtype=torch.uint8, device=device, generator=g)
+    nc = N * code_bytes_per_row(fmt, K)
+    if fmt == FMT_MXFP8:
+        # 254 finite E4M3 bytes: 0..126 and 128..254 (0x7F and 0xFF are NaN)
+        v = torch.randint(0, 254, (nc,), **u8)
+        codes = v + (v >= 127).to(torch.uint8)
+    else:
+        codes = torch.randint(0, 256, (nc,), **u8)
+    nblk = N * (K // block_of(fmt))
+    if fmt == FMT_NVFP4:
+        table = torch.from_numpy(NVFP4_SCALE_CODES).to(device)
+        idx = torch.randint(0, NVFP4_SCALE_CODES.size, (nblk,), dtype=torch.int64, device=device, generator=g)
+        tail = torch.from_numpy(np.array([NVFP4_TENSOR_SCALE], dtype="<f4").view(np.uint8)).to(device)
+        scales = torch.cat([table[idx], tail])
+    else:
+        scales = torch.randint(exp_lo, exp_hi + 1, (nblk,), **u8)
+    return codes, scales
+
+
 def activations(M: int, K: int, seed: int) -> np.ndarray:
     """bf16 bit patterns of N(0, 1) samples, [M][K] uint16."""
     import torch

@@ -14,6 +14,7 @@ pages name those formats without defining them):
 * ``dequant``  -- W[n][k] = fp32(code * block scale) (NVFP4: then x fp32 g)
 * ``qmv``      -- y[m][n] = sum_k x[m][k] * W[n][k] in fp64
 * ``qmv_rows`` -- the same on a chosen subset of weight rows
+* ``qmv_rows_mt`` -- qmv_rows cut into row ranges over several host threads
 * ``qmm_points`` -- the same on chosen (m, n) output points
 * ``moe_qmv``  -- y[t][j][n] = sum_k x[t][k] * W_{ids[t][j]}[n][k]
 * ``swiglu_bf16`` -- h = bf16_rne(silu(gate) * up) from fp64 inputs
@@ -37,7 +38,7 @@ _LOCK = threading.Lock()
 _LIBS: dict[tuple, ctypes.CDLL] = {}
 
 CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11", "-Wall", "-Wextra",
-          "-shared", "-fPIC"]
+          "-shared", "-fPIC", "-pthread"]
 
 
 def build(defines: tuple[str, ...] = (), out_dir: str | None = None) -> str:
@@ -79,6 +80,8 @@ def _load(defines: tuple[str, ...] = ()) -> ctypes.CDLL:
             lib.or_qmv.argtypes = [I, P, P, P, P, I64, I64, I64]
             lib.or_qmv_rows.restype = I
             lib.or_qmv_rows.argtypes = [I, P, P, P, P, I64, I64, I64, P, I64]
+            lib.or_qmv_rows_mt.restype = I
+            lib.or_qmv_rows_mt.argtypes = [I, P, P, P, P, I64, I64, I64, P, I64, I]
             lib.or_qmm_points.restype = I
             lib.or_qmm_points.argtypes = [I, P, P, P, I64, I64, I64, P, P, I64, P]
             lib.or_moe_qmv.restype = I
@@ -159,6 +162,20 @@ class Oracle:
                                   rows.size)
         if rc:
             raise ValueError(f"or_qmv_rows rc={rc}")
+        return y
+
+    def qmv_rows_mt(self, fmt, codes, scales, x, M, N, K, rows, nthreads) -> np.ndarray:
+        """qmv_rows with the row list cut into nthreads contiguous ranges, one
+        host thread each (bit for bit the single-threaded result)."""
+        codes, pc = self._u8(codes)
+        scales, ps = self._u8(scales)
+        x, px = self._bf16bits(x)
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        y = np.empty((M, rows.size), dtype=np.float64)
+        rc = self.lib.or_qmv_rows_mt(fmt, pc, ps, px, y.ctypes.data, M, N, K, rows.ctypes.data,
+                                     rows.size, int(nthreads))
+        if rc:
+            raise ValueError(f"or_qmv_rows_mt rc={rc}")
         return y
 
     def qmm_points(self, fmt, codes, scales, x, M, N, K, ms, ns) -> np.ndarray:

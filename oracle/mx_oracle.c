@@ -32,6 +32,7 @@
  * fast-math, so the C compiler keeps every operation as written.
  */
 #include <math.h>
+#include <pthread.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -217,17 +218,16 @@ static void dequant_row(int fmt, const uint8_t *codes, const uint8_t *scales, fl
     for (int64_t k = 0; k < K; k++) wrow[k] = weight(fmt, codes, scales, g, n, k, N, K);
 }
 
-/* y[m][r] = sum_k x[m][k] * W[rows[r]][k] for a chosen list of weight rows
- * (all rows when rows == NULL).  x is bf16 [M][K]; y is fp64 [M][nrows]. */
-int or_qmv_rows(int fmt, const uint8_t *codes, const uint8_t *scales, const uint16_t *x,
-                double *y, int64_t M, int64_t N, int64_t K, const int64_t *rows, int64_t nrows)
+/* Entries r0 .. r1-1 of the row list: y[m][r] = sum_k x[m][k] * W[rows[r]][k]
+ * (rows[r] = r when rows == NULL), y fp64 [M][nrows]. */
+static int qmv_row_range(int fmt, const uint8_t *codes, const uint8_t *scales, const uint16_t *x,
+                         double *y, int64_t M, int64_t N, int64_t K, const int64_t *rows, int64_t nrows,
+                         int64_t r0, int64_t r1)
 {
-    if (fmt < 0 || fmt > 2 || M < 0 || N < 0 || K <= 0 || K % block_of(fmt) != 0) return -1;
-    if (rows == NULL) nrows = N;
     float g = fmt == OR_FMT_NVFP4 ? tensor_scale(scales, N, K) : 1.0f;
     float *wrow = (float *)malloc((size_t)K * sizeof(float));
     if (!wrow) return -2;
-    for (int64_t r = 0; r < nrows; r++) {
+    for (int64_t r = r0; r < r1; r++) {
         int64_t n = rows ? rows[r] : r;
         if (n < 0 || n >= N) { free(wrow); return -1; }
         dequant_row(fmt, codes, scales, g, n, N, K, wrow);
@@ -235,6 +235,69 @@ int or_qmv_rows(int fmt, const uint8_t *codes, const uint8_t *scales, const uint
     }
     free(wrow);
     return 0;
+}
+
+/* y[m][r] = sum_k x[m][k] * W[rows[r]][k] for a chosen list of weight rows
+ * (all rows when rows == NULL).  x is bf16 [M][K]; y is fp64 [M][nrows]. */
+int or_qmv_rows(int fmt, const uint8_t *codes, const uint8_t *scales, const uint16_t *x,
+                double *y, int64_t M, int64_t N, int64_t K, const int64_t *rows, int64_t nrows)
+{
+    if (fmt < 0 || fmt > 2 || M < 0 || N < 0 || K <= 0 || K % block_of(fmt) != 0) return -1;
+    if (rows == NULL) nrows = N;
+    return qmv_row_range(fmt, codes, scales, x, y, M, N, K, rows, nrows, 0, nrows);
+}
+
+/* The same on several host threads: the row list is cut into nthreads
+ * contiguous ranges, each computed by the routine above (same operations in
+ * the same order per row, so the result is bit for bit that of or_qmv_rows).
+ * Used to time the oracle on every core of a host; nthreads < 1 means 1. */
+struct or_rows_job {
+    int fmt;
+    const uint8_t *codes, *scales;
+    const uint16_t *x;
+    double *y;
+    int64_t M, N, K, nrows, r0, r1;
+    const int64_t *rows;
+    int rc;
+};
+
+static void *or_rows_worker(void *arg)
+{
+    struct or_rows_job *j = (struct or_rows_job *)arg;
+    j->rc = qmv_row_range(j->fmt, j->codes, j->scales, j->x, j->y, j->M, j->N, j->K, j->rows, j->nrows, j->r0,
+                          j->r1);
+    return NULL;
+}
+
+int or_qmv_rows_mt(int fmt, const uint8_t *codes, const uint8_t *scales, const uint16_t *x, double *y,
+                   int64_t M, int64_t N, int64_t K, const int64_t *rows, int64_t nrows, int nthreads)
+{
+    if (fmt < 0 || fmt > 2 || M < 0 || N < 0 || K <= 0 || K % block_of(fmt) != 0) return -1;
+    if (rows == NULL) nrows = N;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    if (nthreads > nrows) nthreads = nrows > 0 ? (int)nrows : 1;
+    pthread_t tid[256];
+    int created[256];
+    struct or_rows_job job[256];
+    for (int t = 0; t < nthreads; t++) {
+        job[t] = (struct or_rows_job){fmt, codes, scales, x, y, M, N, K, nrows,
+                                      nrows * t / nthreads, nrows * (t + 1) / nthreads, rows, 0};
+        created[t] = 0;
+    }
+    /* range 0 runs on the calling thread; a range whose thread cannot be
+     * started runs there too */
+    for (int t = 1; t < nthreads; t++)
+        created[t] = pthread_create(&tid[t], NULL, or_rows_worker, &job[t]) == 0;
+    or_rows_worker(&job[0]);
+    for (int t = 1; t < nthreads; t++) {
+        if (created[t]) pthread_join(tid[t], NULL);
+        else or_rows_worker(&job[t]);
+    }
+    int rc = 0;
+    for (int t = 0; t < nthreads; t++)
+        if (job[t].rc != 0) rc = job[t].rc;
+    return rc;
 }
 
 /* Decode GEMV: y[m][n] = sum_k x[m][k] * W[n][k], y fp64 [M][N]. */

@@ -346,6 +346,21 @@ def pin_points(orc):
     assert np.array_equal(orc.qmm_points(fmt, codes, scales, x, M, N, K, ms, ns), y[ms, ns])
 
 
+def pin_rows_threads(orc):
+    """qmv_rows_mt (the row list cut into ranges over host threads) returns
+    the single-threaded qmv_rows result bit for bit, for thread counts that
+    do and do not divide the row count, more threads than rows, and rows in
+    any order."""
+    for fmt in (F4, F8, NV):
+        M, N, K = 3, 37, 128
+        codes, scales, x = _rand_case(fmt, M, N, K, 43 + fmt)
+        rows = np.random.default_rng(fmt).permutation(N)[:29]
+        want = orc.qmv_rows(fmt, codes, scales, x, M, N, K, rows)
+        for nt in (1, 2, 3, 7, 29, 64):
+            got = orc.qmv_rows_mt(fmt, codes, scales, x, M, N, K, rows, nt)
+            assert np.array_equal(got.view(np.uint64), want.view(np.uint64)), (fmt, nt)
+
+
 def pin_swiglu_combine(orc):
     """SwiGLU: bf16 of torch's float64 silu(gate) * up by exact rational
     rounding; combine: numpy einsum in float64."""
@@ -569,6 +584,6 @@ def pin_qmm_qx(orc):
 
 
 ALL_PINS = [pin_e2m1, pin_e8m0, pin_e4m3, pin_bf16, pin_dequant, pin_qmv_bruteforce,
-            pin_qmv_matmul, pin_invariants, pin_worked_examples, pin_moe, pin_points,
+            pin_qmv_matmul, pin_invariants, pin_worked_examples, pin_moe, pin_points, pin_rows_threads,
             pin_swiglu_combine, pin_quantize_roundtrip, pin_quantize_nearest, pin_quantize_specials,
             pin_qmm_qx]

@@ -60,20 +60,21 @@ def test_qmm_agrees_with_qmv():
     check_close(Y[:4], y.astype(np.float64), "qmm vs qmv", bf16_out=True)
 
 
-@pytest.mark.parametrize("N,K,seed", [(28672, 8192, 8), (8192, 28672, 9)])
-def test_qmm_prefill_full_size(orc, N, K, seed):
+@pytest.mark.parametrize("fmt,N,K,seed", [(0, 28672, 8192, 8), (0, 8192, 28672, 9), (2, 28672, 8192, 10)])
+def test_qmm_prefill_full_size(orc, fmt, N, K, seed):
     """M = 4096 prefill shapes, launched as the benchmark launches them;
-    three whole output rows against the oracle."""
+    three whole output rows against the oracle (NVFP4 too: its tensor scale
+    is applied only in the epilogue)."""
     need_gpu()
     M = 4096
-    codes, scales = synth.weights(0, N, K, seed, exp_lo=118, exp_hi=132)
+    codes, scales = synth.weights(fmt, N, K, seed, exp_lo=118, exp_hi=132)
     X = synth.activations(M, K, 50 + seed)
-    Y = run_qmm(0, codes, scales, X, N)
+    Y = run_qmm(fmt, codes, scales, X, N)
     rows = np.array([0, 2049, M - 1])
     ms = np.repeat(rows, N)
     ns = np.tile(np.arange(N), rows.size)
-    want = orc.qmm_points(0, codes, scales, X, M, N, K, ms, ns).reshape(rows.size, N)
-    check_close(Y[rows], want, f"qmm full {N}x{K}", bf16_out=True)
+    want = orc.qmm_points(fmt, codes, scales, X, M, N, K, ms, ns).reshape(rows.size, N)
+    check_close(Y[rows], want, f"qmm full fmt{fmt} {N}x{K}", bf16_out=True)
     assert np.all(np.isfinite(Y))
 
 
