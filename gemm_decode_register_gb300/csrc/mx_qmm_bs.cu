@@ -1,0 +1,527 @@
+// mx_qmm_bs.cu -- prefill GEMM over block-float activations and weights on
+// the block-scaled tensor cores (tcgen05.mma kind::mxf8f6f4 / mxf4 /
+// mxf4nvf4), sm_103a; and the tensor pipe's dense peak per MMA kind.
+//
+//   Y[m][n] = bf16_rne( sum_k Xq[m][k] * W[n][k] ),  fp32 accumulation,
+//
+// where Xq holds block-float activations in the weights' format (the output
+// of mx_quantize) and both operands keep their codes and block scales: the
+// tensor core multiplies the codes and applies the scales itself, so nothing
+// is decoded.  The pages quantise block-float on Blackwell with the hardware
+// NVFP4 / MXFP4 converter (manual page "Building from source", CUDA build
+// options, "GPU architecture auto-detection"); talk slide 8 sets FP4 on
+// Blackwell tensor cores against software decode elsewhere.
+//
+// One CTA owns a 128 x BN output tile (BN = 128 or 256) and streams K in
+// k-blocks of 128 bytes per row (128 MXFP8 elements, 256 MXFP4 / NVFP4):
+//   warp 0      X and W codes of a k-block by TMA (128-byte swizzle) into a
+//               ring of shared-memory stages
+//   warp 1      allocates tensor memory; one thread issues 4 MMAs per k-block
+//               (K = 32 for MXFP8, 64 for the 4-bit formats) and commits each
+//               k-block to the stage's and the scale slot's empty barriers
+//   warps 2-5   block scales: each warp loads the scale bytes of its quarter
+//               of the tile's X rows and W rows and writes them to a ring of
+//               scale slots in tensor memory (tcgen05.st); then the epilogue:
+//               tcgen05.ld of its accumulator lanes, NVFP4 tensor scales,
+//               round to bf16, store.
+// Scale layout in tensor memory: a 128-row chunk of scales covers 4 scale
+// blocks along K (one byte each in a 32-bit cell, the MMA's scale-factor ID
+// picks the byte) and takes 4 columns.  X (operand A): row r at lane r,
+// column r / 32 of the chunk (each 32-lane quarter of the tensor core reads
+// its own rows); the bytes are written to all 4 columns.  W (operand B):
+// every lane quarter reads the scales of all the tile's W rows, so row n is
+// at lane n % 32, column n / 32 of the chunk, in each of the 4 quarters
+// (measured: with W rows at lane n the products were right only where the
+// output row and column fell in the same quarter).  A 256-row W tile takes
+// two chunks in consecutive column groups.  Every wait is bounded (two seconds of
+// %globaltimer); a wait that gives up sets MX_DEVERR_TIMEOUT, the CTA drains
+// its copies in flight, writes NaN and returns.
+#include "../../include/mx.h"
+#include "mx_internal.h"
+#include "mx_tc.cuh"
+
+namespace mx {
+
+constexpr unsigned long long BS_WAIT_NS = 2000000000ull;
+constexpr int BS_KB_BYTES = 128;  // code bytes per row per k-block
+constexpr int BS_SMEM_LIMIT = 232448;
+
+// ------------------------------------------------------------ primitives
+
+__device__ __forceinline__ void umma1_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_x4(uint32_t taddr, uint32_t v)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %1, %1, %1};" ::"r"(taddr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_x4v(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v0), "r"(v1),
+                 "r"(v2), "r"(v3)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// MMA kinds: the three block-scaled ones of the formats, plus the unscaled
+// bf16 and E4M3 kinds for the peak measurement.
+enum : int { BSK_BF16 = 0, BSK_E4M3 = 1, BSK_MXF8 = 2, BSK_MXF4 = 3, BSK_NVF4 = 4 };
+
+template <int KIND>
+__device__ __forceinline__ void umma1(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                      uint32_t acc)
+{
+    if constexpr (KIND == BSK_BF16) {
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                     "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+                     "l"(a), "l"(b), "r"(idesc), "r"(acc)
+                     : "memory");
+    } else if constexpr (KIND == BSK_E4M3) {
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                     "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+                     "l"(a), "l"(b), "r"(idesc), "r"(acc)
+                     : "memory");
+    } else if constexpr (KIND == BSK_MXF8) {
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+                     "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], "
+                     "p;\n\t}" ::"r"(d),
+                     "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+                     : "memory");
+    } else if constexpr (KIND == BSK_MXF4) {
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+                     "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], "
+                     "p;\n\t}" ::"r"(d),
+                     "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+                     : "memory");
+    } else {
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+                     "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], "
+                     "p;\n\t}" ::"r"(d),
+                     "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+                     : "memory");
+    }
+}
+
+// Instruction descriptor for M = 128, N = n, K-major A and B.
+//   unscaled kinds: D format fp32 (bits 4-5 = 1), A / B formats at 7 / 10
+//     (bf16 = 1 in kind::f16; E4M3 = 0 in kind::f8f6f4)
+//   block-scaled kinds: scale-factor IDs of B (bits 4-5) and A (29-30), A / B
+//     formats (E4M3 = 0 in kind::mxf8f6f4, E2M1 = 1 in kind::mxf4 and
+//     kind::mxf4nvf4), scale type at bit 23 (1 = UE8M0, 0 = UE4M3)
+//   N / 8 at bits 17-22, M / 16 at 24-28.
+template <int KIND>
+__host__ __device__ constexpr uint32_t bs_idesc(int n, uint32_t sfa_id = 0, uint32_t sfb_id = 0)
+{
+    const uint32_t shape = ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+    if (KIND == BSK_BF16) return (1u << 4) | (1u << 7) | (1u << 10) | shape;
+    if (KIND == BSK_E4M3) return (1u << 4) | shape;
+    const uint32_t fmt = KIND == BSK_MXF8 ? 0u : 1u;
+    const uint32_t ue8m0 = KIND == BSK_NVF4 ? 0u : 1u;
+    return (sfb_id << 4) | (fmt << 7) | (fmt << 10) | (ue8m0 << 23) | shape | (sfa_id << 29);
+}
+
+// ------------------------------------------------------------ peak
+
+// One CTA per SM issues `iters` k-blocks of 4 MMAs of 128 x 256 x K on
+// shared-memory operands (zeros) into tensor memory, block scales 1.0 for the
+// scaled kinds: the dense rate of the tensor pipe for that kind.  A wait that
+// runs past 10 s sets the error word.
+template <int KIND>
+__global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int *err)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t *a = smem;              // 128 rows x 128 B
+    uint8_t *b = smem + 128 * 128;  // 256 rows x 128 B
+    uint64_t *bar = reinterpret_cast<uint64_t *>(b + 256 * 128);
+    uint32_t *slot = reinterpret_cast<uint32_t *>(bar + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(slot + 1);
+    const int warp = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < (128 + 256) * 128 / 16; i += blockDim.x)
+        reinterpret_cast<uint4 *>(smem)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(slot))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *slot;
+    if constexpr (KIND >= BSK_MXF8) {
+        // scales 1.0 in columns 256 .. 271 (each warp its lane quarter)
+        const uint32_t one = KIND == BSK_NVF4 ? 0x38383838u : 0x7F7F7F7Fu;
+        for (int c = 0; c < 16; c += 4) tmem_st_x4(tmem + ((uint32_t)(32 * warp) << 16) + 256u + (uint32_t)c, one);
+        tmem_wait_st();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (threadIdx.x == 0) {
+        constexpr uint32_t idesc = bs_idesc<KIND>(256);
+        const uint32_t sa = smem_u32(a), sb = smem_u32(b);
+        for (int i = 0; i < iters; ++i) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                umma1<KIND>(tmem, sw128_desc(sa + 32 * kk), sw128_desc(sb + 32 * kk), idesc, tmem + 256u, tmem + 260u,
+                            (i | kk) != 0);
+        }
+        umma1_commit(bar);
+        if (!mbar_wait(bar, 0, abort_flag, 10000000000ull, false)) set_device_error(err, DEVERR_TIMEOUT);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
+}
+
+// K of one MMA for each kind.
+__host__ __device__ constexpr int mma_k(int kind) { return kind == BSK_BF16 ? 16 : kind <= BSK_MXF8 ? 32 : 64; }
+
+template <int KIND>
+static cudaError_t run_peak(const DeviceState &ds, cudaStream_t st, int iters, float *ms)
+{
+    // more shared memory than two CTAs could share: one CTA (and one
+    // tensor-memory allocation) per SM
+    const size_t smem = 128 * 1024;
+    cudaError_t e = cudaFuncSetAttribute(mma_peak_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaEvent_t e0, e1;
+    if ((e = cudaEventCreate(&e0)) != cudaSuccess) return e;
+    if ((e = cudaEventCreate(&e1)) != cudaSuccess) {
+        cudaEventDestroy(e0);
+        return e;
+    }
+    e = cudaEventRecord(e0, st);
+    if (e == cudaSuccess) e = launch_k(mma_peak_kernel<KIND>, dim3(ds.num_sms), dim3(128), smem, st, iters, ds.err);
+    if (e == cudaSuccess) e = cudaEventRecord(e1, st);
+    if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(ms, e0, e1);
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    return e;
+}
+
+// ------------------------------------------------------------ GEMM
+
+template <int FMT>
+struct BsFmt {
+    static constexpr int KIND = FMT == FMT_MXFP8 ? BSK_MXF8 : FMT == FMT_MXFP4 ? BSK_MXF4 : BSK_NVF4;
+    static constexpr int KB_ELEMS = FMT == FMT_MXFP8 ? 128 : 256;  // elements per k-block
+    static constexpr int SPB = FMT == FMT_MXFP8 ? 4 : FMT == FMT_MXFP4 ? 8 : 16;  // scale bytes per row per k-block
+    static constexpr int CH = SPB / 4;                                          // 4-byte scale chunks per k-block
+};
+
+template <int FMT, int BN>
+struct BsGeo {
+    static constexpr int A_BYTES = 128 * BS_KB_BYTES;
+    static constexpr int B_BYTES = BN * BS_KB_BYTES;
+    static constexpr int STAGE = A_BYTES + B_BYTES;
+    static constexpr int S = (BS_SMEM_LIMIT - 2048) / STAGE > 6 ? 6 : (BS_SMEM_LIMIT - 2048) / STAGE;
+    static constexpr int RB = BN / 128;                          // 128-row chunks of W per tile
+    static constexpr int R = 4;                                  // scale slots in tensor memory
+    static constexpr int SLOT_COLS = 4 * BsFmt<FMT>::CH * (1 + RB);
+    static constexpr int TMEM_COLS = BN + R * SLOT_COLS <= 256 ? 256 : 512;
+    static constexpr int THREADS = 192;
+    static constexpr int SMEM = 1024 + S * STAGE + 512;
+    static_assert(BN + R * SLOT_COLS <= 512, "tensor memory");
+    static_assert(SMEM <= BS_SMEM_LIMIT, "shared memory");
+    static_assert(S >= 2, "stages");
+};
+
+struct BsArgs {
+    const uint8_t *scales;   // W block scales [N][K / block] (+ NVFP4 tensor scale)
+    const uint8_t *xscales;  // X block scales [M][K / block] (+ NVFP4 tensor scale)
+    uint16_t *Y;             // bf16 [M][N]
+    int *err;
+    int M, N, K;
+    unsigned long long wait_ns;
+};
+
+template <int FMT, int BN>
+__global__ void __launch_bounds__(192, 1) qmm_bs_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                                                        const __grid_constant__ CUtensorMap tmap_w, BsArgs a)
+{
+    using G = BsGeo<FMT, BN>;
+    using F = BsFmt<FMT>;
+    constexpr int S = G::S, R = G::R, RB = G::RB, CH = F::CH;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S * G::STAGE);
+    uint64_t *full = bars;              // [S] X and W codes of a stage landed (TMA bytes)
+    uint64_t *empty = bars + S;         // [S] the MMAs that read the stage finished
+    uint64_t *sf_full = bars + 2 * S;   // [R] the 4 scale warps wrote the slot
+    uint64_t *sf_empty = sf_full + R;   // [R] the MMAs that read the slot finished
+    uint64_t *acc_full = sf_full + 2 * R;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m_tiles = (a.M + 127) / 128;
+    const int m0 = (blockIdx.x % m_tiles) * 128, n0 = (blockIdx.x / m_tiles) * BN;
+    const int KB = a.K / F::KB_ELEMS;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int r = 0; r < R; ++r) {
+            mbar_init(&sf_full[r], 4);
+            mbar_init(&sf_empty[r], 1);
+        }
+        mbar_init(acc_full, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(G::TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t sf_col0 = (uint32_t)BN;  // scale slots follow the accumulator columns
+    pdl_trigger();
+    pdl_wait();  // the activations (and their scales) come from the previous kernel
+
+    if (warp == 0) {
+        // ---------------- codes producer
+        if (lane == 0) {
+            int issued = 0;
+            for (int kb = 0; kb < KB; ++kb) {
+                const int s = kb % S;
+                if (kb >= S && !mbar_wait(&empty[s], ((kb / S) - 1) & 1, abort_flag, a.wait_ns)) break;
+                uint8_t *st = smem + s * G::STAGE;
+                mbar_arrive_expect_tx(&full[s], (uint32_t)G::STAGE);
+                tma_load_2d(st, &tmap_x, kb * BS_KB_BYTES, m0, &full[s]);
+                tma_load_2d(st + G::A_BYTES, &tmap_w, kb * BS_KB_BYTES, n0, &full[s]);
+                issued = kb + 1;
+            }
+            // every issued load must land before the CTA may exit
+            for (int kb = (issued > S ? issued - S : 0); kb < issued; ++kb)
+                mbar_wait(&full[kb % S], (kb / S) & 1, abort_flag, BS_WAIT_NS, false);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer
+        if (lane == 0) {
+            for (int kb = 0; kb < KB; ++kb) {
+                const int s = kb % S, r = kb % R;
+                if (!mbar_wait(&full[s], (kb / S) & 1, abort_flag, a.wait_ns)) break;
+                if (!mbar_wait(&sf_full[r], (kb / R) & 1, abort_flag, a.wait_ns)) break;
+                tc_fence_after();
+                const uint32_t sa = smem_u32(smem + s * G::STAGE), sb = sa + G::A_BYTES;
+                const uint32_t sfa = tmem + sf_col0 + (uint32_t)(r * G::SLOT_COLS);
+                const uint32_t sfb = sfa + (uint32_t)(4 * CH);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    // the scale chunk and byte of MMA kk: MXFP8 one 32-element block
+                    // (chunk 0, byte kk); MXFP4 two (chunk kk / 2, bytes 2 (kk % 2)
+                    // and up); NVFP4 four 16-element blocks (chunk kk, byte 0)
+                    const int c = FMT == FMT_MXFP8 ? 0 : FMT == FMT_MXFP4 ? kk >> 1 : kk;
+                    const uint32_t id = FMT == FMT_MXFP8 ? (uint32_t)kk : FMT == FMT_MXFP4 ? 2u * (kk & 1) : 0u;
+                    const uint32_t idesc = bs_idesc<F::KIND>(BN, id, id);
+                    umma1<F::KIND>(tmem, sw128_desc(sa + 32 * kk), sw128_desc(sb + 32 * kk), idesc,
+                                   sfa + (uint32_t)(4 * c), sfb + (uint32_t)(4 * c * RB), (kb | kk) != 0);
+                }
+                umma1_commit(&empty[s]);
+                umma1_commit(&sf_empty[r]);
+            }
+            umma1_commit(acc_full);  // fires once every MMA issued so far has completed
+        }
+    } else {
+        // ---------------- scale writers (warps 2-5: lane quarter q = warp % 4)
+        const int q = warp & 3;
+        const int KS = a.K / (FMT == FMT_NVFP4 ? 16 : 32);  // scale bytes per row
+        const int xr = m0 + 32 * q + lane;
+        const uint8_t *xsp = a.xscales + (size_t)(xr < a.M ? xr : 0) * KS;
+        // W rows 128 j + 32 i + lane (i = 0..3) of the tile: the same in every warp
+        const uint8_t *wsp[RB][4];
+#pragma unroll
+        for (int j = 0; j < RB; ++j)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) wsp[j][i] = a.scales + (size_t)(n0 + 128 * j + 32 * i + lane) * KS;
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        for (int kb = 0; kb < KB; ++kb) {
+            const int r = kb % R;
+            uint32_t xv[CH], wv[RB][4][CH];
+#pragma unroll
+            for (int c = 0; c < CH; ++c) {
+                xv[c] = ld_nc_u32(xsp + kb * F::SPB + 4 * c);
+#pragma unroll
+                for (int j = 0; j < RB; ++j)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) wv[j][i][c] = ld_nc_u32(wsp[j][i] + kb * F::SPB + 4 * c);
+            }
+            int ok = 1;
+            if (lane == 0 && kb >= R) ok = mbar_wait(&sf_empty[r], ((kb / R) - 1) & 1, abort_flag, a.wait_ns);
+            if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
+            tc_fence_after();
+            const uint32_t base = tmem + lane_base + sf_col0 + (uint32_t)(r * G::SLOT_COLS);
+#pragma unroll
+            for (int c = 0; c < CH; ++c) {
+                tmem_st_x4(base + (uint32_t)(4 * c), xv[c]);
+#pragma unroll
+                for (int j = 0; j < RB; ++j)
+                    tmem_st_x4v(base + (uint32_t)(4 * CH + 4 * (c * RB + j)), wv[j][0][c], wv[j][1][c], wv[j][2][c],
+                                wv[j][3][c]);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sf_full[r]);
+        }
+    }
+
+    // ---------------- epilogue (warps 2-5)
+    if (warp >= 2) {
+        const int q = warp & 3;
+        const bool ok = mbar_wait(acc_full, 0, abort_flag, BS_WAIT_NS, false) && !*abort_flag;
+        tc_fence_after();
+        float g = 1.0f;
+        if (FMT == FMT_NVFP4) {
+            g = load_f32_unaligned(a.scales + (size_t)a.N * (a.K / 16));
+            g = __fmul_rn(g, load_f32_unaligned(a.xscales + (size_t)a.M * (a.K / 16)));
+        }
+        const int row = m0 + 32 * q + lane;
+        for (int c = 0; c < BN; c += 32) {
+            uint32_t v[32];
+            tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c, v);
+            uint32_t o[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                float lo = __uint_as_float(v[2 * j]), hi = __uint_as_float(v[2 * j + 1]);
+                if (FMT == FMT_NVFP4) {
+                    lo = __fmul_rn(lo, g);
+                    hi = __fmul_rn(hi, g);
+                }
+                o[j] = ok ? f32x2_to_bf16x2(lo, hi) : 0x7FC07FC0u;
+            }
+            if (row < a.M) {
+                uint4 *dst = reinterpret_cast<uint4 *>(a.Y + (size_t)row * a.N + n0 + c);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) dst[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag) set_device_error(a.err, DEVERR_TIMEOUT);
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(G::TMEM_COLS)
+                     : "memory");
+    }
+}
+
+// Codes as [rows][row bytes] uint8 with boxes of one k-block (128 bytes) x
+// box_rows rows, 128-byte swizzle; rows past `rows` read as zero.
+static cudaError_t encode_codes_map(const uint8_t *codes, long long rows, long long row_bytes, int box_rows,
+                                    CUtensorMap &map)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    const cuuint32_t box[2] = {(cuuint32_t)BS_KB_BYTES, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1u, 1u};
+    const CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(codes), dims, strides, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int FMT, int BN>
+static cudaError_t run_qmm_bs(const DeviceState &ds, cudaStream_t st, const uint8_t *codes, const uint8_t *scales,
+                              const uint8_t *xcodes, const uint8_t *xscales, uint16_t *Y, int M, int N, int K)
+{
+    using G = BsGeo<FMT, BN>;
+    if (G::SMEM > ds.max_smem_optin) return cudaErrorInvalidValue;
+    const long long row_bytes = FMT == FMT_MXFP8 ? K : K / 2;
+    CUtensorMap xmap, wmap;
+    cudaError_t e = encode_codes_map(xcodes, M, row_bytes, 128, xmap);
+    if (e != cudaSuccess) return e;
+    if ((e = encode_codes_map(codes, N, row_bytes, BN, wmap)) != cudaSuccess) return e;
+    static int configured_dev[64] = {0};
+    if (ds.device < 64 && !configured_dev[ds.device]) {
+        e = cudaFuncSetAttribute(qmm_bs_kernel<FMT, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM);
+        if (e != cudaSuccess) return e;
+        configured_dev[ds.device] = 1;
+    }
+    BsArgs a;
+    a.scales = scales;
+    a.xscales = xscales;
+    a.Y = Y;
+    a.err = ds.err;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.wait_ns = BS_WAIT_NS;
+    const int tiles = ((M + 127) / 128) * (N / BN);
+    return launch_k(qmm_bs_kernel<FMT, BN>, dim3(tiles), dim3(G::THREADS), (size_t)G::SMEM, st, xmap, wmap, a);
+}
+
+}  // namespace mx
+
+using namespace mx;
+
+extern "C" int mx_qmm_qx(int fmt, const void *codes, const void *scales, const void *xcodes, const void *xscales,
+                         void *Y, int M, int N, int K)
+{
+    if (fmt != MX_FMT_MXFP4 && fmt != MX_FMT_MXFP8 && fmt != MX_FMT_NVFP4) return MX_EUNSUPPORTED;
+    if (!codes || !scales || !xcodes || !xscales || !Y) return MX_EINVAL;
+    if (M <= 0 || N <= 0 || K <= 0 || K % (fmt == MX_FMT_NVFP4 ? 16 : 32) != 0) return MX_EINVAL;
+    if (N % 128 != 0 || K % (fmt == MX_FMT_MXFP8 ? 128 : 256) != 0) return MX_EUNSUPPORTED;
+    auto a16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    if (!a16(codes) || !a16(scales) || !a16(xcodes) || !a16(xscales) || !a16(Y)) return MX_EALIGN;
+    DeviceState *ds = device_state();
+    if (!ds) return MX_ECUDA;
+    cudaStream_t st = current_stream();
+    const uint8_t *c = static_cast<const uint8_t *>(codes), *s = static_cast<const uint8_t *>(scales);
+    const uint8_t *xc = static_cast<const uint8_t *>(xcodes), *xs = static_cast<const uint8_t *>(xscales);
+    uint16_t *y = static_cast<uint16_t *>(Y);
+    cudaError_t e;
+    const bool wide = N % 256 == 0;
+    if (fmt == MX_FMT_MXFP8)
+        e = wide ? run_qmm_bs<FMT_MXFP8, 256>(*ds, st, c, s, xc, xs, y, M, N, K)
+                 : run_qmm_bs<FMT_MXFP8, 128>(*ds, st, c, s, xc, xs, y, M, N, K);
+    else if (fmt == MX_FMT_MXFP4)
+        e = wide ? run_qmm_bs<FMT_MXFP4, 256>(*ds, st, c, s, xc, xs, y, M, N, K)
+                 : run_qmm_bs<FMT_MXFP4, 128>(*ds, st, c, s, xc, xs, y, M, N, K);
+    else
+        e = wide ? run_qmm_bs<FMT_NVFP4, 256>(*ds, st, c, s, xc, xs, y, M, N, K)
+                 : run_qmm_bs<FMT_NVFP4, 128>(*ds, st, c, s, xc, xs, y, M, N, K);
+    if (e == cudaErrorInvalidValue) return MX_EUNSUPPORTED;
+    return e == cudaSuccess ? MX_OK : MX_ECUDA;
+}
+
+extern "C" int mx_mma_peak(int kind, int iters, float *ms)
+{
+    if (!ms || iters <= 0 || kind < 0 || kind > 4) return MX_EINVAL;
+    DeviceState *ds = device_state();
+    if (!ds) return MX_ECUDA;
+    cudaStream_t st = current_stream();
+    cudaError_t e;
+    switch (kind) {
+    case BSK_BF16: e = run_peak<BSK_BF16>(*ds, st, iters, ms); break;
+    case BSK_E4M3: e = run_peak<BSK_E4M3>(*ds, st, iters, ms); break;
+    case BSK_MXF8: e = run_peak<BSK_MXF8>(*ds, st, iters, ms); break;
+    case BSK_MXF4: e = run_peak<BSK_MXF4>(*ds, st, iters, ms); break;
+    default: e = run_peak<BSK_NVF4>(*ds, st, iters, ms); break;
+    }
+    return e == cudaSuccess ? MX_OK : MX_ECUDA;
+}

@@ -58,6 +58,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "mx_moe_combine": [P, P, P, I, I, I],
             "mx_device_error": [],
             "mx_debug_qmm_stall": [I, ctypes.c_ulonglong],
+            "mx_qmm_qx": [I, P, P, P, P, P, I, I, I],
+            "mx_mma_peak": [I, I, P],
             "mx_moe_qmm": [I, P, P, P, P, P, I, I, I, I, I, P, Z],
             "mx_quantize": [I, P, P, P, I, I],
             "mx_moe_ffn_prefill": [I, P, P, P, P, P, P, P, P, I, I, I, I, I, P, Z],
@@ -175,6 +177,34 @@ def qmm(fmt: int, codes: torch.Tensor, scales: torch.Tensor, X: torch.Tensor, N:
     _stream()
     _check("mx_qmm", load().mx_qmm(fmt, _ptr(codes), _ptr(scales), _ptr(X), _ptr(Y), M, N, K))
     return Y
+
+
+def qmm_qx(fmt: int, codes: torch.Tensor, scales: torch.Tensor, xcodes: torch.Tensor, xscales: torch.Tensor,
+           M: int, N: int, K: int, Y: torch.Tensor | None = None) -> torch.Tensor:
+    """Y[M][N] bf16 = Xq . W^T on the block-scaled tensor cores, Xq given as
+    block-float codes and scales in the weights' format."""
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=codes.device)
+    _stream()
+    _check("mx_qmm_qx", load().mx_qmm_qx(fmt, _ptr(codes), _ptr(scales), _ptr(xcodes), _ptr(xscales), _ptr(Y),
+                                         M, N, K))
+    return Y
+
+
+MMA_KINDS = {"bf16": (0, 16), "e4m3": (1, 32), "mxfp8": (2, 32), "mxfp4": (3, 64), "nvfp4": (4, 64)}
+
+
+def mma_peak_tflops(kind: str, iters: int = 8192, reps: int = 5) -> float:
+    """Best of `reps` mx_mma_peak runs, as dense TFLOP/s of the whole GPU."""
+    code, k = MMA_KINDS[kind]
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    best = 0.0
+    ms = ctypes.c_float()
+    for _ in range(reps):
+        _stream()
+        _check("mx_mma_peak", load().mx_mma_peak(code, iters, ctypes.byref(ms)))
+        best = max(best, 2.0 * 128 * 256 * k * 4 * iters * sms / (ms.value * 1e-3) / 1e12)
+    return best
 
 
 def _workspace(nbytes: int, ws: torch.Tensor | None, device) -> torch.Tensor:

@@ -158,6 +158,26 @@ int mx_moe_down_combine(int fmt, const void *expert_codes, const void *expert_sc
 int mx_qmm(int fmt, const void *codes, const void *scales, const void *X, void *Y, int M, int N,
            int K);
 
+/* Prefill GEMM over block-float activations on the block-scaled tensor
+ * cores (manual page "Building from source", CUDA build options: on
+ * Blackwell, block-float quantisation runs on the hardware NVFP4 / MXFP4
+ * converter; talk slide 8 "ROCm on RDNA 3.5 vs. Metal vs. CUDA": FP4 on
+ * Blackwell tensor cores):
+ *   Y[m][n] = bf16_rne( sum_k Xq[m][k] * W[n][k] ),  fp32 accumulation,
+ * where Xq is the block-float activation given by xcodes / xscales in the
+ * weights' format and layout ([M][K] codes, [M][K/block] scales, NVFP4: the
+ * fp32 tensor scale after the M*K/16 scale bytes; e.g. mx_quantize's
+ * output).  Nothing is decoded: tcgen05.mma kind::mxf8f6f4 (MXFP8),
+ * kind::mxf4 (MXFP4) or kind::mxf4nvf4 with 16-element blocks (NVFP4)
+ * multiplies the codes and applies both operands' block scales; the NVFP4
+ * tensor scales multiply the fp32 sum.  NVFP4 block scales are read as
+ * unsigned E4M3 (mx_quantize never writes a negative one).  Any M >= 1; N a
+ * multiple of 128 and K of 128 (MXFP8) or 256 (MXFP4, NVFP4), else
+ * MX_EUNSUPPORTED.  All pointers 16-byte aligned.  A pipeline wait that
+ * times out sets MX_DEVERR_TIMEOUT and makes that output tile NaN. */
+int mx_qmm_qx(int fmt, const void *codes, const void *scales, const void *xcodes, const void *xscales, void *Y,
+              int M, int N, int K);
+
 /* Expert-batched MoE prefill (grouped GEMM): the mx_moe_qmv operation for
  * many tokens, on the tensor cores.
  *   y[t][j][n] = bf16_rne( sum_k x[t][k] * W_e[n][k] ),  e = expert_ids[t][j],
@@ -263,6 +283,18 @@ int mx_moe_combine(const float *yd, const float *r, float *out, int T, int topk,
  * is an interface variant of mx_qmv, not a different computation. */
 int mx_qmv_noalloc(int fmt, const void *codes, const void *scales, const void *x, float *y, int M, int N,
                    int K);
+
+/* Measurement support: the dense rate of this GPU's tensor pipe for one MMA
+ * kind, the denominator of the prefill GEMMs' roofline.  One CTA per SM
+ * issues iters x 4 tcgen05.mma of 128 x 256 x K (cta_group::1) on
+ * shared-memory operands into tensor memory; *ms receives the elapsed time
+ * (CUDA events on the calling thread's stream).  kind: 0 bf16 (kind::f16,
+ * K = 16), 1 E4M3 (kind::f8f6f4, K = 32), 2 MXFP8 (kind::mxf8f6f4
+ * block-scaled, K = 32), 3 MXFP4 (kind::mxf4, K = 64), 4 NVFP4
+ * (kind::mxf4nvf4, 16-element blocks, K = 64).  FLOPs of a call:
+ * 2 * 128 * 256 * K * 4 * iters * (number of SMs).  Synchronises the
+ * stream. */
+int mx_mma_peak(int kind, int iters, float *ms);
 
 /* Test hook for the bounded waits of the tensor-core kernels (mx_qmm,
  * mx_moe_qmm, mx_moe_ffn_prefill); the pages' fault handling (talk slide 10

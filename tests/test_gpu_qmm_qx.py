@@ -1,0 +1,87 @@
+"""Prefill GEMM over block-float activations on the block-scaled tensor cores
+(mx_qmm_qx) against the oracle's product of the two decoded block-float
+operands (or_qmm_qx), on the same quantised activations; the activations
+are quantised by the oracle here and by mx_quantize (bit-exact with it) in
+the end-to-end case.  The distance to the bf16-activation product is a
+property of quantising the activations, reported by the benchmark, not
+gated here."""
+import numpy as np
+import pytest
+
+from gemm_decode_register_gb300 import synth
+from gpu_util import bf16_bits_to_f64, bf16_host, check_close, check_special, dev_bf16, dev_u8, need_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def run_qx(fmt, codes, scales, xc, xs, M, N, K):
+    from gemm_decode_register_gb300 import ops
+
+    Y = ops.qmm_qx(fmt, dev_u8(codes), dev_u8(scales), dev_u8(xc), dev_u8(xs), M, N, K)
+    return bf16_bits_to_f64(bf16_host(Y))
+
+
+SHAPES = [(128, 128, 256), (100, 256, 512), (300, 384, 1024), (1000, 512, 2048), (257, 1280, 768)]
+
+
+@pytest.mark.parametrize("fmt", [0, 1, 2])
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_qmm_qx_parity(orc, fmt, M, N, K):
+    """128 x 128 and 128 x 256 tiles (N % 256 decides), ragged M, several
+    k-blocks; activations N(0,1) quantised by the oracle."""
+    need_gpu()
+    if K % (128 if fmt == 1 else 256):
+        pytest.skip("K not a whole number of k-blocks for this format")
+    codes, scales = synth.weights(fmt, N, K, M + N + fmt, exp_lo=118, exp_hi=132)
+    x = synth.activations(M, K, K + fmt)
+    xc, xs = orc.quantize(fmt, x, M, K)
+    got = run_qx(fmt, codes, scales, xc, xs, M, N, K)
+    want = orc.qmm_qx(fmt, codes, scales, xc, xs, M, N, K)
+    check_close(got, want, f"qmm_qx fmt{fmt} {M}x{N}x{K}", bf16_out=True)
+
+
+@pytest.mark.parametrize("fmt", [0, 1, 2])
+def test_qmm_qx_one_hot_scales(orc, fmt):
+    """Scales that single out one block: every weight block scale 2^-20
+    except one block per row at 2^0 (NVFP4: E4M3 1/512 and 1.0), so a scale
+    byte applied to the wrong row or the wrong K block moves outputs by
+    orders of magnitude."""
+    need_gpu()
+    M, N, K = 128, 256, 1024
+    codes, scales = synth.weights(fmt, N, K, 5, exp_lo=118, exp_hi=132)
+    nb = K // synth.block_of(fmt)
+    sc = scales[: N * nb].reshape(N, nb)
+    rng = np.random.default_rng(6)
+    if fmt == synth.FMT_NVFP4:
+        sc[...] = 0x08  # E4M3 2^-9 * 1: 1/512
+        sc[np.arange(N), rng.integers(0, nb, size=N)] = 0x38  # 1.0
+    else:
+        sc[...] = 107
+        sc[np.arange(N), rng.integers(0, nb, size=N)] = 127
+    x = synth.activations(M, K, 7)
+    xc, xs = orc.quantize(fmt, x, M, K)
+    got = run_qx(fmt, codes, scales, xc, xs, M, N, K)
+    want = orc.qmm_qx(fmt, codes, scales, xc, xs, M, N, K)
+    check_close(got, want, f"qmm_qx one-hot scales fmt{fmt}", bf16_out=True)
+
+
+@pytest.mark.parametrize("fmt", [0, 1, 2])
+def test_qmm_qx_after_device_quantiser(orc, fmt):
+    """mx_quantize then mx_qmm_qx, all on the device, against the oracle's
+    quantiser and product; a token holding a NaN gets NaN block scales and
+    a NaN output row."""
+    need_gpu()
+    from gemm_decode_register_gb300 import ops
+
+    M, N, K = 200, 512, 2048
+    codes, scales = synth.weights(fmt, N, K, 11, exp_lo=118, exp_hi=132)
+    x = synth.activations(M, K, 12)
+    x[3, 100] = 0x7FC0  # NaN
+    xc, xs = ops.quantize(fmt, dev_bf16(x).view(M, K))
+    Y = ops.qmm_qx(fmt, dev_u8(codes), dev_u8(scales), xc, xs, M, N, K)
+    got = bf16_bits_to_f64(bf16_host(Y))
+    oc, os_ = orc.quantize(fmt, x, M, K)
+    assert np.array_equal(xc.cpu().numpy(), oc) and np.array_equal(xs.cpu().numpy(), os_)
+    want = orc.qmm_qx(fmt, codes, scales, oc, os_, M, N, K)
+    check_special(got, want, f"quantise + qmm_qx fmt{fmt}", bf16_out=True)
+    assert np.all(np.isnan(got[3]))
