@@ -466,7 +466,7 @@ def extras(torch, ops, synth, dev, stream, hbm, bf16_burst, bf16_sust, args):
     except Exception as exc:  # reported, not hidden
         res["prefill_qmm"] = {"error": str(exc).splitlines()[0][:200]}
     for name, fn in (("moe_prefill", extras_moe_prefill), ("crossover_upgate", extras_crossover),
-                     ("quantize", extras_quantize)):
+                     ("quantize", extras_quantize), ("qmm_qx", extras_qmm_qx)):
         try:
             res.update(fn(torch, ops, synth, dev, stream, bf16_burst, iters))
         except Exception as exc:  # reported, not hidden
@@ -551,6 +551,48 @@ def extras_moe_prefill(torch, ops, synth, dev, stream, bf16_burst, iters):
                                           "frac_bf16_burst": round(flq / tq / 1e12 / bf16_burst, 4),
                                           "path": "mx_moe_qmm: route, gather, grouped GEMM (3 launches)"}
         del y, wsq
+    return res
+
+
+def extras_qmm_qx(torch, ops, synth, dev, stream, bf16_burst, iters):
+    """The tensor pipe's dense rate per MMA kind (mx_mma_peak, zero operands),
+    and the prefill GEMM over quantised activations (mx_quantize, then the
+    block-scaled mx_qmm_qx) on the 4096 x 28672 x 8192 up projection in each
+    format, next to the bf16-activation GEMM (mx_qmm) on the same weights:
+    TFLOP/s, fraction of the measured peak of the GEMM's own MMA kind, and the
+    relative L2 distance between the two products (a property of quantising
+    the activations, not an error of either kernel)."""
+    res = {}
+    peaks = {k: round(ops.mma_peak_tflops(k), 1) for k in ("bf16", "e4m3", "mxfp8", "mxfp4", "nvfp4")}
+    res["tensor_peaks_tflops"] = dict(peaks, note="mx_mma_peak: one CTA per SM issuing 128x256xK tcgen05.mma "
+                                                  "(cta_group::1) on zero operands, best of 5; clocks stay at their "
+                                                  "maximum on zero data, so real operands run somewhat lower")
+    M, N, K = 4096, 28672, 8192
+    X = bf16_dev(torch, synth.activations(M, K, 58)).view(M, K)
+    n = max(5, iters // 10)
+    for fmt, fname, kind in ((synth.FMT_MXFP4, "mxfp4", "mxfp4"), (synth.FMT_MXFP8, "mxfp8", "mxfp8"),
+                             (synth.FMT_NVFP4, "nvfp4", "nvfp4")):
+        codes, scales = synth.weights_device(fmt, N, K, 8, dev, exp_lo=118, exp_hi=132)
+        xc, xs = ops.quantize(fmt, X)
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        Yb = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        tg = time_region(torch, graph_of(torch, lambda: ops.qmm_qx(fmt, codes, scales, xc, xs, M, N, K, Y=Y)).replay,
+                         n, stream)
+        tq = time_region(torch, graph_of(torch, lambda: ops.quantize(fmt, X, xc, xs)).replay, n, stream)
+        tb = time_region(torch, graph_of(torch, lambda: ops.qmm(fmt, codes, scales, X, N, Y=Yb)).replay, n, stream)
+        ops.qmm_qx(fmt, codes, scales, xc, xs, M, N, K, Y=Y)
+        ops.qmm(fmt, codes, scales, X, N, Y=Yb)
+        dist = (torch.linalg.vector_norm((Y.float() - Yb.float())) / torch.linalg.vector_norm(Yb.float())).item()
+        fl = 2.0 * M * N * K
+        res[f"prefill_qmm_qx_{fname}_28672x8192"] = {
+            "tflops": round(fl / tg / 1e12, 1), "ms": round(tg * 1e3, 3),
+            "frac_measured_peak": round(fl / tg / 1e12 / peaks[kind], 4), "peak_kind": kind,
+            "quantize_us": round(tq * 1e6, 1), "tflops_with_quantize": round(fl / (tg + tq) / 1e12, 1),
+            "bf16_path_tflops": round(fl / tb / 1e12, 1), "bf16_path_ms": round(tb * 1e3, 3),
+            "rel_l2_vs_bf16_activations": round(dist, 4),
+            "path": "mx_quantize (X to the weights' format) + mx_qmm_qx (block-scaled tcgen05.mma), against "
+                    "mx_qmm (in-SMEM decode to bf16 + tcgen05 bf16 MMA)"}
+        del codes, scales, xc, xs, Y, Yb
     return res
 
 
@@ -710,6 +752,11 @@ CASES = {
     "qmm_down": ("qmm", 0, 4096, 8192, 28672),
     "qmm_small": ("qmm", 0, 1024, 4096, 4096),
     "qmm_mid": ("qmm", 0, 2048, 8192, 4096),
+    # block-scaled GEMM over quantised activations, 4096 x 28672 x 8192 (and a small case for captures)
+    "qmm_qx_up_mxfp4": ("qmm_qx", 0, 4096, 28672, 8192),
+    "qmm_qx_up_mxfp8": ("qmm_qx", 1, 4096, 28672, 8192),
+    "qmm_qx_up_nvfp4": ("qmm_qx", 2, 4096, 28672, 8192),
+    "qmm_qx_mid_mxfp4": ("qmm_qx", 0, 2048, 8192, 4096),
     # expert-batched MoE FFN prefill: 4096 tokens, top-8 of 128 experts, hidden 2048, I 768
     "moe_prefill_ffn_t4096": ("moe_prefill", 0, 4096, 2048, 768),
     # on-device quantisation of 4096 x 8192 bf16 activations
@@ -747,6 +794,13 @@ def run_case(args):
         ws = ops.moe_ffn_prefill_workspace(M, E, topk, H, I)
         f = lambda: ops.moe_ffn_prefill(fmt, d1, e1, d2, e2, x, ids, r, E, I, out=out, workspace=ws)  # noqa: E731
         wb = c1.nbytes + s1.nbytes + c2.nbytes + s2.nbytes
+    elif kind == "qmm_qx":
+        codes, scales = synth.weights_device(fmt, N, K, 2, "cuda")
+        X = bf16_dev(torch, synth.activations(M, K, 3)).view(M, K)
+        xc, xs = ops.quantize(fmt, X)
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        f = lambda: ops.qmm_qx(fmt, codes, scales, xc, xs, M, N, K, Y=Y)  # noqa: E731
+        wb = codes.numel() + scales.numel()
     elif kind == "moe_ffn":
         E, topk, H, I = 128, 8, N, K
         c1, s1 = synth.weights(fmt, 2 * I, H, 40, E=E)
@@ -786,7 +840,7 @@ def run_case(args):
     t = time_region(torch, g.replay, args.iters, stream)
     out = {"case": args.case, "iters": args.iters, "us": round(t * 1e6, 2),
            "weight_gbs": round(wb / t / 1e9, 1)}
-    if kind == "qmm":
+    if kind in ("qmm", "qmm_qx"):
         out["tflops"] = round(2.0 * M * N * K / t / 1e12, 1)
     if kind == "moe_prefill":
         out["tflops"] = round(2.0 * M * 8 * 3 * N * K / t / 1e12, 1)

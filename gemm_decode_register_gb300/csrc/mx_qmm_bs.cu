@@ -19,9 +19,13 @@
 //   warp 1      allocates tensor memory; one thread issues 4 MMAs per k-block
 //               (K = 32 for MXFP8, 64 for the 4-bit formats) and commits each
 //               k-block to the stage's and the scale slot's empty barriers
-//   warps 2-5   block scales: each warp loads the scale bytes of its quarter
-//               of the tile's X rows and W rows and writes them to a ring of
-//               scale slots in tensor memory (tcgen05.st); then the epilogue:
+//               and, every 16 / (scale bytes per row per k-block) k-blocks,
+//               the X and W block scales of the next k-blocks as 16 bytes per
+//               row (TMA, into a ring of scale stages)
+//   warps 2-5   block scales: each warp reads the scale bytes of its rows
+//               from a scale stage (contiguous 16-byte loads) and writes them
+//               to a ring of scale slots in tensor memory (tcgen05.st), one
+//               slot per k-block; then the epilogue:
 //               tcgen05.ld of its accumulator lanes, NVFP4 tensor scales,
 //               round to bf16, store.
 // Scale layout in tensor memory: a 128-row chunk of scales covers 4 scale
@@ -221,6 +225,7 @@ struct BsFmt {
     static constexpr int KB_ELEMS = FMT == FMT_MXFP8 ? 128 : 256;  // elements per k-block
     static constexpr int SPB = FMT == FMT_MXFP8 ? 4 : FMT == FMT_MXFP4 ? 8 : 16;  // scale bytes per row per k-block
     static constexpr int CH = SPB / 4;                                          // 4-byte scale chunks per k-block
+    static constexpr int SG = 16 / SPB;                                         // k-blocks per 16-byte scale stage
 };
 
 template <int FMT, int BN>
@@ -228,16 +233,24 @@ struct BsGeo {
     static constexpr int A_BYTES = 128 * BS_KB_BYTES;
     static constexpr int B_BYTES = BN * BS_KB_BYTES;
     static constexpr int STAGE = A_BYTES + B_BYTES;
-    static constexpr int S = (BS_SMEM_LIMIT - 2048) / STAGE > 6 ? 6 : (BS_SMEM_LIMIT - 2048) / STAGE;
+    static constexpr int ST = 4;                                 // scale stages (16 bytes per X and W row)
+    static constexpr int SC_STAGE = (128 + BN) * 16;
+    static constexpr int S_FIT = (BS_SMEM_LIMIT - 2048 - ST * SC_STAGE) / STAGE;
+    static constexpr int S = S_FIT > 6 ? 6 : S_FIT;
     static constexpr int RB = BN / 128;                          // 128-row chunks of W per tile
-    static constexpr int R = 4;                                  // scale slots in tensor memory
     static constexpr int SLOT_COLS = 4 * BsFmt<FMT>::CH * (1 + RB);
+    // scale slots in tensor memory: the writers load a k-block's scales from
+    // L2 while the MMAs work through the R - 1 slots ahead of it
+    static constexpr int R = (512 - BN) / SLOT_COLS > 8 ? 8 : (512 - BN) / SLOT_COLS;
     static constexpr int TMEM_COLS = BN + R * SLOT_COLS <= 256 ? 256 : 512;
     static constexpr int THREADS = 192;
-    static constexpr int SMEM = 1024 + S * STAGE + 512;
+    static constexpr int OFF_SC = S * STAGE;
+    static constexpr int OFF_BAR = OFF_SC + ST * SC_STAGE;
+    static constexpr int SMEM = 1024 + OFF_BAR + 512;
+    static_assert((2 * S + 2 * R + 2 * ST + 1) * 8 + 8 <= 512, "barrier area");
     static_assert(BN + R * SLOT_COLS <= 512, "tensor memory");
     static_assert(SMEM <= BS_SMEM_LIMIT, "shared memory");
-    static_assert(S >= 2, "stages");
+    static_assert(S >= 2 && R >= 2, "pipeline depth");
 };
 
 struct BsArgs {
@@ -249,21 +262,33 @@ struct BsArgs {
     unsigned long long wait_ns;
 };
 
+// Word w (0..3) of a 16-byte vector (w a compile-time constant after
+// unrolling).
+__device__ __forceinline__ uint32_t word_of(const uint4 &v, int w)
+{
+    return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
+}
+
 template <int FMT, int BN>
 __global__ void __launch_bounds__(192, 1) qmm_bs_kernel(const __grid_constant__ CUtensorMap tmap_x,
-                                                        const __grid_constant__ CUtensorMap tmap_w, BsArgs a)
+                                                        const __grid_constant__ CUtensorMap tmap_w,
+                                                        const __grid_constant__ CUtensorMap tmap_xs,
+                                                        const __grid_constant__ CUtensorMap tmap_ws, BsArgs a)
 {
     using G = BsGeo<FMT, BN>;
     using F = BsFmt<FMT>;
-    constexpr int S = G::S, R = G::R, RB = G::RB, CH = F::CH;
+    constexpr int S = G::S, R = G::R, RB = G::RB, CH = F::CH, ST = G::ST, SG = F::SG;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S * G::STAGE);
+    uint8_t *scs = smem + G::OFF_SC;    // [ST] scale stages: 128 X rows then BN W rows, 16 bytes each
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + G::OFF_BAR);
     uint64_t *full = bars;              // [S] X and W codes of a stage landed (TMA bytes)
     uint64_t *empty = bars + S;         // [S] the MMAs that read the stage finished
     uint64_t *sf_full = bars + 2 * S;   // [R] the 4 scale warps wrote the slot
     uint64_t *sf_empty = sf_full + R;   // [R] the MMAs that read the slot finished
-    uint64_t *acc_full = sf_full + 2 * R;
+    uint64_t *sc_full = sf_full + 2 * R;  // [ST] a scale stage landed (TMA bytes)
+    uint64_t *sc_empty = sc_full + ST;    // [ST] the 4 scale warps read it
+    uint64_t *acc_full = sc_full + 2 * ST;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -280,6 +305,10 @@ __global__ void __launch_bounds__(192, 1) qmm_bs_kernel(const __grid_constant__ 
         for (int r = 0; r < R; ++r) {
             mbar_init(&sf_full[r], 4);
             mbar_init(&sf_empty[r], 1);
+        }
+        for (int u = 0; u < ST; ++u) {
+            mbar_init(&sc_full[u], 1);
+            mbar_init(&sc_empty[u], 4);
         }
         mbar_init(acc_full, 1);
         *abort_flag = 0;
@@ -300,11 +329,21 @@ __global__ void __launch_bounds__(192, 1) qmm_bs_kernel(const __grid_constant__ 
     pdl_wait();  // the activations (and their scales) come from the previous kernel
 
     if (warp == 0) {
-        // ---------------- codes producer
+        // ---------------- codes and scales producer
         if (lane == 0) {
-            int issued = 0;
+            int issued = 0, sissued = 0;
             for (int kb = 0; kb < KB; ++kb) {
                 const int s = kb % S;
+                if (kb % SG == 0) {
+                    // the scale stage of k-blocks kb .. kb + SG - 1
+                    const int t = kb / SG, u = t % ST;
+                    if (t >= ST && !mbar_wait(&sc_empty[u], ((t / ST) - 1) & 1, abort_flag, a.wait_ns)) break;
+                    uint8_t *sc = scs + u * G::SC_STAGE;
+                    mbar_arrive_expect_tx(&sc_full[u], (uint32_t)G::SC_STAGE);
+                    tma_load_2d(sc, &tmap_xs, 16 * t, m0, &sc_full[u]);
+                    tma_load_2d(sc + 128 * 16, &tmap_ws, 16 * t, n0, &sc_full[u]);
+                    sissued = t + 1;
+                }
                 if (kb >= S && !mbar_wait(&empty[s], ((kb / S) - 1) & 1, abort_flag, a.wait_ns)) break;
                 uint8_t *st = smem + s * G::STAGE;
                 mbar_arrive_expect_tx(&full[s], (uint32_t)G::STAGE);
@@ -315,6 +354,8 @@ __global__ void __launch_bounds__(192, 1) qmm_bs_kernel(const __grid_constant__ 
             // every issued load must land before the CTA may exit
             for (int kb = (issued > S ? issued - S : 0); kb < issued; ++kb)
                 mbar_wait(&full[kb % S], (kb / S) & 1, abort_flag, BS_WAIT_NS, false);
+            for (int t = (sissued > ST ? sissued - ST : 0); t < sissued; ++t)
+                mbar_wait(&sc_full[t % ST], (t / ST) & 1, abort_flag, BS_WAIT_NS, false);
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer
@@ -346,44 +387,51 @@ __global__ void __launch_bounds__(192, 1) qmm_bs_kernel(const __grid_constant__ 
     } else {
         // ---------------- scale writers (warps 2-5: lane quarter q = warp % 4)
         const int q = warp & 3;
-        const int KS = a.K / (FMT == FMT_NVFP4 ? 16 : 32);  // scale bytes per row
-        const int xr = m0 + 32 * q + lane;
-        const uint8_t *xsp = a.xscales + (size_t)(xr < a.M ? xr : 0) * KS;
-        // W rows 128 j + 32 i + lane (i = 0..3) of the tile: the same in every warp
-        const uint8_t *wsp[RB][4];
-#pragma unroll
-        for (int j = 0; j < RB; ++j)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) wsp[j][i] = a.scales + (size_t)(n0 + 128 * j + 32 * i + lane) * KS;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-        for (int kb = 0; kb < KB; ++kb) {
-            const int r = kb % R;
-            uint32_t xv[CH], wv[RB][4][CH];
-#pragma unroll
-            for (int c = 0; c < CH; ++c) {
-                xv[c] = ld_nc_u32(xsp + kb * F::SPB + 4 * c);
-#pragma unroll
-                for (int j = 0; j < RB; ++j)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) wv[j][i][c] = ld_nc_u32(wsp[j][i] + kb * F::SPB + 4 * c);
-            }
+        const int nstage = (KB + SG - 1) / SG;
+        bool go = true;
+        for (int t = 0; t < nstage && go; ++t) {
+            const int u = t % ST;
             int ok = 1;
-            if (lane == 0 && kb >= R) ok = mbar_wait(&sf_empty[r], ((kb / R) - 1) & 1, abort_flag, a.wait_ns);
+            if (lane == 0) ok = mbar_wait(&sc_full[u], (t / ST) & 1, abort_flag, a.wait_ns);
             if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
-            tc_fence_after();
-            const uint32_t base = tmem + lane_base + sf_col0 + (uint32_t)(r * G::SLOT_COLS);
+            // X row 32 q + lane; W rows 128 j + 32 i + lane (the same in every warp)
+            const uint8_t *sc = scs + u * G::SC_STAGE;
+            const uint4 xv = *reinterpret_cast<const uint4 *>(sc + 16 * (32 * q + lane));
+            uint4 wv[RB][4];
 #pragma unroll
-            for (int c = 0; c < CH; ++c) {
-                tmem_st_x4(base + (uint32_t)(4 * c), xv[c]);
+            for (int j = 0; j < RB; ++j)
 #pragma unroll
-                for (int j = 0; j < RB; ++j)
-                    tmem_st_x4v(base + (uint32_t)(4 * CH + 4 * (c * RB + j)), wv[j][0][c], wv[j][1][c], wv[j][2][c],
-                                wv[j][3][c]);
-            }
-            tmem_wait_st();
-            tc_fence_before();
+                for (int i = 0; i < 4; ++i)
+                    wv[j][i] = *reinterpret_cast<const uint4 *>(sc + 16 * (128 + 128 * j + 32 * i + lane));
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sf_full[r]);
+            if (lane == 0) mbar_arrive(&sc_empty[u]);
+#pragma unroll
+            for (int jj = 0; jj < SG; ++jj) {
+                const int kb = t * SG + jj;
+                if (kb >= KB) break;
+                const int r = kb % R;
+                if (lane == 0 && kb >= R) ok = mbar_wait(&sf_empty[r], ((kb / R) - 1) & 1, abort_flag, a.wait_ns);
+                if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
+                    go = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t base = tmem + lane_base + sf_col0 + (uint32_t)(r * G::SLOT_COLS);
+#pragma unroll
+                for (int c = 0; c < CH; ++c) {
+                    const int w = jj * CH + c;  // word of the 16 bytes
+                    tmem_st_x4(base + (uint32_t)(4 * c), word_of(xv, w));
+#pragma unroll
+                    for (int j = 0; j < RB; ++j)
+                        tmem_st_x4v(base + (uint32_t)(4 * CH + 4 * (c * RB + j)), word_of(wv[j][0], w),
+                                    word_of(wv[j][1], w), word_of(wv[j][2], w), word_of(wv[j][3], w));
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sf_full[r]);
+            }
         }
     }
 
@@ -445,6 +493,23 @@ static cudaError_t encode_codes_map(const uint8_t *codes, long long rows, long l
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Block scales as [rows][scale bytes per row] uint8 with boxes of 16 bytes x
+// box_rows rows, no swizzle; rows past `rows` read as zero.
+static cudaError_t encode_scales_map(const uint8_t *scales, long long rows, long long row_bytes, int box_rows,
+                                     CUtensorMap &map)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    const cuuint32_t box[2] = {16u, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1u, 1u};
+    const CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(scales), dims, strides, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int FMT, int BN>
 static cudaError_t run_qmm_bs(const DeviceState &ds, cudaStream_t st, const uint8_t *codes, const uint8_t *scales,
                               const uint8_t *xcodes, const uint8_t *xscales, uint16_t *Y, int M, int N, int K)
@@ -452,10 +517,13 @@ static cudaError_t run_qmm_bs(const DeviceState &ds, cudaStream_t st, const uint
     using G = BsGeo<FMT, BN>;
     if (G::SMEM > ds.max_smem_optin) return cudaErrorInvalidValue;
     const long long row_bytes = FMT == FMT_MXFP8 ? K : K / 2;
-    CUtensorMap xmap, wmap;
+    const long long srow_bytes = K / (FMT == FMT_NVFP4 ? 16 : 32);
+    CUtensorMap xmap, wmap, xsmap, wsmap;
     cudaError_t e = encode_codes_map(xcodes, M, row_bytes, 128, xmap);
     if (e != cudaSuccess) return e;
     if ((e = encode_codes_map(codes, N, row_bytes, BN, wmap)) != cudaSuccess) return e;
+    if ((e = encode_scales_map(xscales, M, srow_bytes, 128, xsmap)) != cudaSuccess) return e;
+    if ((e = encode_scales_map(scales, N, srow_bytes, BN, wsmap)) != cudaSuccess) return e;
     static int configured_dev[64] = {0};
     if (ds.device < 64 && !configured_dev[ds.device]) {
         e = cudaFuncSetAttribute(qmm_bs_kernel<FMT, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM);
@@ -472,7 +540,8 @@ static cudaError_t run_qmm_bs(const DeviceState &ds, cudaStream_t st, const uint
     a.K = K;
     a.wait_ns = BS_WAIT_NS;
     const int tiles = ((M + 127) / 128) * (N / BN);
-    return launch_k(qmm_bs_kernel<FMT, BN>, dim3(tiles), dim3(G::THREADS), (size_t)G::SMEM, st, xmap, wmap, a);
+    return launch_k(qmm_bs_kernel<FMT, BN>, dim3(tiles), dim3(G::THREADS), (size_t)G::SMEM, st, xmap, wmap, xsmap,
+                    wsmap, a);
 }
 
 }  // namespace mx
@@ -485,7 +554,9 @@ extern "C" int mx_qmm_qx(int fmt, const void *codes, const void *scales, const v
     if (fmt != MX_FMT_MXFP4 && fmt != MX_FMT_MXFP8 && fmt != MX_FMT_NVFP4) return MX_EUNSUPPORTED;
     if (!codes || !scales || !xcodes || !xscales || !Y) return MX_EINVAL;
     if (M <= 0 || N <= 0 || K <= 0 || K % (fmt == MX_FMT_NVFP4 ? 16 : 32) != 0) return MX_EINVAL;
-    if (N % 128 != 0 || K % (fmt == MX_FMT_MXFP8 ? 128 : 256) != 0) return MX_EUNSUPPORTED;
+    // whole k-blocks, and scale rows whose byte stride the scale TMA can take
+    // (a multiple of 16 bytes)
+    if (N % 128 != 0 || K % (fmt == MX_FMT_NVFP4 ? 256 : 512) != 0) return MX_EUNSUPPORTED;
     auto a16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
     if (!a16(codes) || !a16(scales) || !a16(xcodes) || !a16(xscales) || !a16(Y)) return MX_EALIGN;
     DeviceState *ds = device_state();

@@ -172,8 +172,8 @@ int mx_qmm(int fmt, const void *codes, const void *scales, const void *X, void *
  * multiplies the codes and applies both operands' block scales; the NVFP4
  * tensor scales multiply the fp32 sum.  NVFP4 block scales are read as
  * unsigned E4M3 (mx_quantize never writes a negative one).  Any M >= 1; N a
- * multiple of 128 and K of 128 (MXFP8) or 256 (MXFP4, NVFP4), else
- * MX_EUNSUPPORTED.  All pointers 16-byte aligned.  A pipeline wait that
+ * multiple of 128 and K of 512 (MXFP4, MXFP8: scale rows a multiple of 16
+ * bytes) or 256 (NVFP4), else MX_EUNSUPPORTED.  All pointers 16-byte aligned.  A pipeline wait that
  * times out sets MX_DEVERR_TIMEOUT and makes that output tile NaN. */
 int mx_qmm_qx(int fmt, const void *codes, const void *scales, const void *xcodes, const void *xscales, void *Y,
               int M, int N, int K);

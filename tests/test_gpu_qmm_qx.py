@@ -21,17 +21,20 @@ def run_qx(fmt, codes, scales, xc, xs, M, N, K):
     return bf16_bits_to_f64(bf16_host(Y))
 
 
-SHAPES = [(128, 128, 256), (100, 256, 512), (300, 384, 1024), (1000, 512, 2048), (257, 1280, 768)]
+SHAPES = [(128, 128, 512), (100, 256, 512), (300, 384, 1024), (1000, 512, 2048), (257, 1280, 1536),
+          (64, 128, 256)]
 
 
 @pytest.mark.parametrize("fmt", [0, 1, 2])
 @pytest.mark.parametrize("M,N,K", SHAPES)
 def test_qmm_qx_parity(orc, fmt, M, N, K):
     """128 x 128 and 128 x 256 tiles (N % 256 decides), ragged M, several
-    k-blocks; activations N(0,1) quantised by the oracle."""
+    k-blocks and scale stages, a last scale stage that is only partly used
+    (MXFP8 K = 1536: 12 k-blocks in stages of 4; MXFP4: 6 in stages of 2);
+    activations N(0,1) quantised by the oracle."""
     need_gpu()
-    if K % (128 if fmt == 1 else 256):
-        pytest.skip("K not a whole number of k-blocks for this format")
+    if K % (256 if fmt == 2 else 512):
+        pytest.skip("K outside this format's k-block and scale-row granularity")
     codes, scales = synth.weights(fmt, N, K, M + N + fmt, exp_lo=118, exp_hi=132)
     x = synth.activations(M, K, K + fmt)
     xc, xs = orc.quantize(fmt, x, M, K)
@@ -63,6 +66,18 @@ def test_qmm_qx_one_hot_scales(orc, fmt):
     got = run_qx(fmt, codes, scales, xc, xs, M, N, K)
     want = orc.qmm_qx(fmt, codes, scales, xc, xs, M, N, K)
     check_close(got, want, f"qmm_qx one-hot scales fmt{fmt}", bf16_out=True)
+
+
+def test_qmm_qx_rejects_unsupported_k():
+    """K not a multiple of 512 (MX formats) or 256 (NVFP4): MX_EUNSUPPORTED."""
+    need_gpu()
+    from gemm_decode_register_gb300 import ops
+
+    M, N, K = 128, 128, 256
+    codes, scales = synth.weights(0, N, K, 1)
+    with pytest.raises(ops.MxError) as ei:
+        ops.qmm_qx(0, dev_u8(codes), dev_u8(scales), dev_u8(codes), dev_u8(scales), M, N, K)
+    assert ei.value.status == -2
 
 
 @pytest.mark.parametrize("fmt", [0, 1, 2])
