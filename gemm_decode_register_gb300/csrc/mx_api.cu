@@ -189,14 +189,15 @@ extern "C" int mx_moe_gate_up_swiglu(int fmt, const void *expert_codes, const vo
     if (!expert_codes || !expert_scales || !x || !expert_ids || !h) return MX_EINVAL;
     if (T <= 0 || E <= 0 || topk <= 0 || I <= 0 || K <= 0 || topk > E || K % block_of(fmt) != 0)
         return MX_EINVAL;
-    if ((long long)T * topk > MOE_MAX_SLOTS || E > MOE_MAX_EXPERTS || K > QMV_MAX_K || K % 128 != 0)
-        return MX_EUNSUPPORTED;
+    if ((long long)T * topk > MOE_MAX_SLOTS || E > MOE_MAX_EXPERTS || K > QMV_MAX_K) return MX_EUNSUPPORTED;
     if (!aligned16(expert_codes) || !aligned16(expert_scales) || !aligned16(x) || !aligned16(h) ||
         (reinterpret_cast<uintptr_t>(expert_ids) & 3u))
         return MX_EALIGN;
     DeviceState *ds = device_state();
     if (!ds) return MX_ECUDA;
-    cudaError_t e = launch_moe_gate_up_swiglu(*ds, t_stream, fmt, static_cast<const uint8_t *>(expert_codes),
+    DeviceState v = *ds;  // K not a multiple of 128: gate/up products pass through the stream's workspace
+    if (K % 128 != 0 && !attach_stream_workspace(v, t_stream)) return MX_ECUDA;
+    cudaError_t e = launch_moe_gate_up_swiglu(v, t_stream, fmt, static_cast<const uint8_t *>(expert_codes),
                                               static_cast<const uint8_t *>(expert_scales),
                                               static_cast<const uint16_t *>(x), expert_ids,
                                               static_cast<uint16_t *>(h), T, E, topk, I, K);
@@ -212,8 +213,7 @@ extern "C" int mx_moe_down_combine(int fmt, const void *expert_codes, const void
     if (!expert_codes || !expert_scales || !h || !expert_ids || !router_weights || !out) return MX_EINVAL;
     if (T <= 0 || E <= 0 || topk <= 0 || N <= 0 || K <= 0 || topk > E || K % block_of(fmt) != 0)
         return MX_EINVAL;
-    if ((long long)T * topk > MOE_MAX_SLOTS || E > MOE_MAX_EXPERTS || K > QMV_MAX_K || K % 128 != 0)
-        return MX_EUNSUPPORTED;
+    if ((long long)T * topk > MOE_MAX_SLOTS || E > MOE_MAX_EXPERTS || K > QMV_MAX_K) return MX_EUNSUPPORTED;
     if (!aligned16(expert_codes) || !aligned16(expert_scales) || !aligned16(h) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(expert_ids) & 3u) || (reinterpret_cast<uintptr_t>(router_weights) & 3u))
         return MX_EALIGN;
@@ -235,7 +235,7 @@ extern "C" int mx_qmm(int fmt, const void *codes, const void *scales, const void
     if (!fmt_ok(fmt)) return MX_EUNSUPPORTED;
     if (!codes || !scales || !X || !Y) return MX_EINVAL;
     if (M <= 0 || N <= 0 || K <= 0 || K % block_of(fmt) != 0) return MX_EINVAL;
-    if (N % 256 != 0 || K % 64 != 0) return MX_EUNSUPPORTED;
+    if (!qmm_shape_ok(fmt, K)) return MX_EUNSUPPORTED;
     if (!aligned16(codes) || !aligned16(scales) || !aligned16(X) || !aligned16(Y)) return MX_EALIGN;
     DeviceState *ds = device_state();
     if (!ds) return MX_ECUDA;
@@ -268,7 +268,7 @@ extern "C" int mx_moe_qmm(int fmt, const void *expert_codes, const void *expert_
     if (!expert_codes || !expert_scales || !x || !expert_ids || !y || !workspace) return MX_EINVAL;
     if (T <= 0 || E <= 0 || topk <= 0 || N <= 0 || K <= 0 || topk > E || K % block_of(fmt) != 0)
         return MX_EINVAL;
-    if (N % 256 != 0 || K % 64 != 0 || !prefill_sizes_ok(T, E, topk) || (long long)E * N > 0x7FFFFFFFll)
+    if (!qmm_shape_ok(fmt, K) || !prefill_sizes_ok(T, E, topk) || (long long)E * N > 0x7FFFFFFFll)
         return MX_EUNSUPPORTED;
     if (workspace_bytes < moe_group_plan(T, E, topk, K, 0).bytes) return MX_EINVAL;
     if (!aligned16(expert_codes) || !aligned16(expert_scales) || !aligned16(x) || !aligned16(y) ||
@@ -301,7 +301,8 @@ extern "C" int mx_moe_ffn_prefill(int fmt, const void *gate_up_codes, const void
     if (T <= 0 || E <= 0 || topk <= 0 || H <= 0 || I <= 0 || topk > E || H % block_of(fmt) != 0 ||
         I % block_of(fmt) != 0)
         return MX_EINVAL;
-    if (H % 256 != 0 || I % 128 != 0 || !prefill_sizes_ok(T, E, topk) || (long long)E * 2 * I > 0x7FFFFFFFll ||
+    if (!qmm_shape_ok(fmt, H) || !qmm_shape_ok(fmt, I) || !prefill_sizes_ok(T, E, topk) ||
+        (long long)E * 2 * I > 0x7FFFFFFFll ||
         (long long)E * H > 0x7FFFFFFFll)
         return MX_EUNSUPPORTED;
     if (workspace_bytes < moe_group_plan(T, E, topk, H, I).bytes) return MX_EINVAL;

@@ -64,6 +64,9 @@ cudaError_t launch_moe_down_combine(const DeviceState &ds, cudaStream_t st, int 
 cudaError_t launch_qmm(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,
                        const uint8_t *scales, const uint16_t *X, uint16_t *Y, int M, int N, int K);
 
+// K the tensor-core GEMMs take (their TMA loads need rows 16-byte apart).
+bool qmm_shape_ok(int fmt, int K);
+
 // Grouped (expert-batched) prefill: routes on the device, gathers the
 // routed rows into expert order and runs the pair GEMM per group tile.
 // Y / h / per-slot outputs are bf16.

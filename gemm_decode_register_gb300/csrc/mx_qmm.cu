@@ -251,6 +251,24 @@ __device__ __forceinline__ uint32_t scale_load(const uint8_t *p)
     return SPK == 4 ? ld_nc_u32(p) : ld_nc_u16(p);
 }
 
+// The SPK block-scale bytes of k-block kb of one weight row (`row`: its
+// scales, nsc bytes).  Bytes past the row's scales (a last k-block that K
+// only partly covers) and rows past the weights read as 1.0: their codes are
+// zero-filled by the TMA, so they add zero.  `wide`: rows are SPK-aligned,
+// so a whole k-block's scales come in one load.
+template <int SPK>
+__device__ __forceinline__ uint32_t scale_load_edge(const uint8_t *row, bool row_ok, int kb, int nsc, bool wide)
+{
+    constexpr uint32_t one = SPK == 4 ? 0x38383838u : 0x7F7Fu;  // E4M3 1.0 / E8M0 1.0
+    if (!row_ok) return one;
+    const int b0 = kb * SPK;
+    if (wide && b0 + SPK <= nsc) return scale_load<SPK>(row + b0);
+    uint32_t v = 0;
+#pragma unroll
+    for (int j = 0; j < SPK; ++j) v |= (b0 + j < nsc ? ld_nc_u8(row + b0 + j) : (one & 0xFFu)) << (8 * j);
+    return v;
+}
+
 // What a pair tile computes and where its rows go.
 constexpr int QMM_DENSE = 0;        // Y[M][N] = X W^T
 constexpr int QMM_GROUPED = 1;      // expert groups of sorted rows (up to 512); row i of group g -> Y[slot_of[r0 + i]]
@@ -261,7 +279,8 @@ struct QmmArgs {
     uint16_t *Y;  // dense / grouped: [rows][N]; SwiGLU: h [rows][N / 2]
     int *err;
     int M, N, K;  // grouped: N weight rows per expert, M rows of the gathered X
-    int y32;  // Y rows and base 32-byte aligned: the epilogue stores 32 bytes per instruction
+    int wrows;    // weight rows in the codes tensor (N, or E * N for expert stacks)
+    int ystore;   // 2: Y rows 32-byte aligned (32-byte stores); 1: 16-byte; 0: 2-byte stores
     unsigned long long wait_ns;   // limit of a pipeline wait (producer / consumer)
     unsigned long long drain_ns;  // limit of a wait for copies already in flight
     int stall_x;                  // test hook: issue no X loads, so the MMA issuer's first wait times out
@@ -285,12 +304,35 @@ __device__ __forceinline__ uint32_t swiglu_bf16_fast(float g, float u)
     return f32x2_to_bf16x2(g * sig * u, 0.0f) & 0xFFFFu;
 }
 
+// 32 bf16 outputs of one row (o: 16 bf16 pairs) at dst, of which the first
+// `valid` are stored (a last column tile that N only partly covers); ystore:
+// see QmmArgs.
+__device__ __forceinline__ void store_row32(uint16_t *dst, const uint32_t *o, int valid, int ystore);
+
 // 32 contiguous bytes to global memory (32-byte aligned address).
 __device__ __forceinline__ void st_global_v8(void *p, const uint32_t *v)
 {
     asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v[0]), "r"(v[1]), "r"(v[2]),
                  "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
                  : "memory");
+}
+
+__device__ __forceinline__ void store_row32(uint16_t *dst, const uint32_t *o, int valid, int ystore)
+{
+    if (valid >= 32 && ystore == 2) {
+        st_global_v8(dst, o);
+        st_global_v8(dst + 16, o + 8);
+    } else if (valid >= 32 && ystore == 1) {
+        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) d4[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            if (2 * j < valid) dst[2 * j] = (uint16_t)(o[j] & 0xFFFFu);
+            if (2 * j + 1 < valid) dst[2 * j + 1] = (uint16_t)(o[j] >> 16);
+        }
+    }
 }
 
 template <int FMT, int NACC, int MODE>
@@ -326,7 +368,7 @@ __global__ void __launch_bounds__(QmmGeo<FMT, NACC, MODE != QMM_DENSE>::THREADS,
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
     const int cid = (int)cluster_id_x();
-    const int KB = a.K / QMM_BK;
+    const int KB = (a.K + QMM_BK - 1) / QMM_BK;  // the last k-block may be partly past K
     // m0: first X row of the tile; n0: first output column; wrow: first of
     // this CTA's 128 weight rows (over all experts); rows: valid tile rows
     int m0, n0, wrow, rows, expert = 0;
@@ -421,14 +463,22 @@ __global__ void __launch_bounds__(QmmGeo<FMT, NACC, MODE != QMM_DENSE>::THREADS,
         // ---------------- codes producer: codes by TMA (lane 0), block scales
         // (whole warp, QG::SPF k-blocks in flight).  The scales come through
         // shared memory so that the decoders hold no global loads in flight.
-        const size_t srow_bytes = (size_t)KB * SPK;
-        const uint8_t *sbase = a.scales + (size_t)(wrow + lane) * srow_bytes;
+        const int nsc = a.K / (FMT == FMT_NVFP4 ? 16 : 32);  // scale bytes per weight row
+        const bool wide = nsc % SPK == 0;
+        const uint8_t *srow[4];
+        bool rok[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = wrow + lane + 32 * i;
+            rok[i] = r < a.wrows;
+            srow[i] = a.scales + (size_t)(rok[i] ? r : 0) * nsc;
+        }
         uint32_t pv[QG::SPF][4];
 #pragma unroll
         for (int j = 0; j < QG::SPF; ++j)
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-                if (j < KB) pv[j][i] = scale_load<SPK>(sbase + (size_t)(32 * i) * srow_bytes + SPK * j);
+                if (j < KB) pv[j][i] = scale_load_edge<SPK>(srow[i], rok[i], j, nsc, wide);
         int issued = 0;
         bool go = true;
         for (int kb0 = 0; kb0 < KB && go; kb0 += QG::SPF) {
@@ -459,7 +509,7 @@ __global__ void __launch_bounds__(QmmGeo<FMT, NACC, MODE != QMM_DENSE>::THREADS,
                 if (kb + QG::SPF < KB)
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                        pv[j][i] = scale_load<SPK>(sbase + (size_t)(32 * i) * srow_bytes + SPK * (kb + QG::SPF));
+                        pv[j][i] = scale_load_edge<SPK>(srow[i], rok[i], kb + QG::SPF, nsc, wide);
             }
         }
         // drain: every issued codes TMA must land before the CTA may exit
@@ -636,18 +686,8 @@ __global__ void __launch_bounds__(QmmGeo<FMT, NACC, MODE != QMM_DENSE>::THREADS,
                     }
                     o[j] = swiglu_bf16_fast(g0, u0) | (swiglu_bf16_fast(g1, u1) << 16);
                 }
-                if (i < rows) {
-                    uint16_t *dst = a.Y + (size_t)(m0 + i) * hw + n0 + c;
-                    if (a.y32) {
-                        st_global_v8(dst, o);
-                        st_global_v8(dst + 16, o + 8);
-                    } else {
-                        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            d4[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-                    }
-                }
+                if (i < rows && n0 + c < hw)
+                    store_row32(a.Y + (size_t)(m0 + i) * hw + n0 + c, o, hw - (n0 + c), a.ystore);
             }
         } else {
             for (int c = group * (NACC * 256 / NCG); c < (group + 1) * (NACC * 256 / NCG); c += 32) {
@@ -676,16 +716,7 @@ __global__ void __launch_bounds__(QmmGeo<FMT, NACC, MODE != QMM_DENSE>::THREADS,
                     // instruction touches 32 rows: the fewer instructions the
                     // better (measured: prefill up projection 1680 -> 1731 TFLOP/s)
                     const size_t yrow = MODE == QMM_DENSE ? (size_t)(m0 + i) : (size_t)__ldcg(a.slot_of + m0 + i);
-                    uint16_t *dst = a.Y + yrow * a.N + n0 + nc;
-                    if (a.y32) {
-                        st_global_v8(dst, o);
-                        st_global_v8(dst + 16, o + 8);
-                    } else {
-                        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            d4[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-                    }
+                    if (n0 + nc < a.N) store_row32(a.Y + yrow * a.N + n0 + nc, o, a.N - (n0 + nc), a.ystore);
                 }
             }
         }
@@ -760,8 +791,8 @@ static int qmm_nacc(const DeviceState &ds, int M, int N)
 {
     if (M <= 256) return 1;
     const long long slots = ds.num_sms / 2 > 0 ? ds.num_sms / 2 : 1;
-    const long long p1 = (long long)((M + 255) / 256) * (N / QMM_BN);
-    const long long p2 = (long long)((M + 511) / 512) * (N / QMM_BN);
+    const long long p1 = (long long)((M + 255) / 256) * ((N + QMM_BN - 1) / QMM_BN);
+    const long long p2 = (long long)((M + 511) / 512) * ((N + QMM_BN - 1) / QMM_BN);
     const long long w1 = (p1 + slots - 1) / slots, w2 = (p2 + slots - 1) / slots;
     return w2 * 120 <= w1 * 100 ? 2 : 1;
 }
@@ -770,7 +801,7 @@ template <int FMT>
 static cudaError_t run_qmm_fmt(const DeviceState &ds, cudaStream_t st, const CUtensorMap &xmap,
                                const CUtensorMap &cmap, const QmmArgs &a)
 {
-    const int n_tiles = a.N / QMM_BN;
+    const int n_tiles = (a.N + QMM_BN - 1) / QMM_BN;
     if (qmm_nacc(ds, a.M, a.N) == 2)
         return run_qmm<FMT, 2, QMM_DENSE>(ds, st, xmap, cmap, a, ((a.M + 511) / 512) * n_tiles);
     return run_qmm<FMT, 1, QMM_DENSE>(ds, st, xmap, cmap, a, ((a.M + 255) / 256) * n_tiles);
@@ -802,11 +833,27 @@ static cudaError_t encode_maps(int fmt, const uint16_t *X, long long rows, const
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Shapes the TMA loads can take: codes rows (K/2 or K bytes) and X rows (2K
+// bytes) a multiple of 16 bytes apart, i.e. K % 32 == 0 (the MX block; NVFP4
+// with K % 32 == 16 is out).
+bool qmm_shape_ok(int fmt, int K) { return K > 0 && K % 32 == 0; }
+
+// Widest epilogue store the output rows allow: 32 bytes when Y and every row
+// (width elements of bf16) are 32-byte aligned, 16 bytes when 16-byte
+// aligned, else 2-byte stores.
+static int y_store_width(const void *Y, int width)
+{
+    const uintptr_t y = reinterpret_cast<uintptr_t>(Y);
+    if ((y & 31u) == 0 && width % 16 == 0) return 2;
+    if ((y & 15u) == 0 && width % 8 == 0) return 1;
+    return 0;
+}
+
 cudaError_t launch_qmm_grouped(const DeviceState &ds, cudaStream_t st, int fmt, bool swiglu, const uint8_t *codes,
                                const uint8_t *scales, const uint16_t *Xs, int rows, const int *groups,
                                int max_groups, const int *slot_of, uint16_t *Y, int E, int N, int K)
 {
-    if (K % QMM_BK != 0 || (swiglu ? (N % 256) : (N % QMM_BN)) != 0) return cudaErrorInvalidValue;
+    if (!qmm_shape_ok(fmt, K) || (swiglu && N % 2 != 0)) return cudaErrorInvalidValue;
     if (max_groups <= 0) return cudaSuccess;
     CUtensorMap xmap, cmap;
     cudaError_t e = encode_maps(fmt, Xs, rows, codes, (long long)E * N, K, xmap, cmap);
@@ -820,11 +867,12 @@ cudaError_t launch_qmm_grouped(const DeviceState &ds, cudaStream_t st, int fmt, 
     a.K = K;
     qmm_wait_args(a);
     const int yw = swiglu ? N / 2 : N;  // output row width
-    a.y32 = ((reinterpret_cast<uintptr_t>(Y) & 31u) == 0 && yw % 16 == 0) ? 1 : 0;
+    a.wrows = E * N;
+    a.ystore = y_store_width(Y, yw);
     a.groups = groups;
     a.slot_of = slot_of;
     a.E = E;
-    a.ntile = swiglu ? (N / 2) / 128 : N / QMM_BN;
+    a.ntile = swiglu ? (N / 2 + 127) / 128 : (N + QMM_BN - 1) / QMM_BN;
     const int pairs = max_groups * a.ntile;
     if (swiglu) {
         if (fmt == FMT_MXFP4) return run_qmm<FMT_MXFP4, 2, QMM_GROUPED_GLU>(ds, st, xmap, cmap, a, pairs);
@@ -839,7 +887,7 @@ cudaError_t launch_qmm_grouped(const DeviceState &ds, cudaStream_t st, int fmt, 
 cudaError_t launch_qmm(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,
                        const uint8_t *scales, const uint16_t *X, uint16_t *Y, int M, int N, int K)
 {
-    if (N % QMM_BN != 0 || K % QMM_BK != 0) return cudaErrorInvalidValue;
+    if (!qmm_shape_ok(fmt, K)) return cudaErrorInvalidValue;
     CUtensorMap xmap, cmap;
     cudaError_t e = encode_maps(fmt, X, M, codes, N, K, xmap, cmap);
     if (e != cudaSuccess) return e;
@@ -851,7 +899,8 @@ cudaError_t launch_qmm(const DeviceState &ds, cudaStream_t st, int fmt, const ui
     a.N = N;
     a.K = K;
     qmm_wait_args(a);
-    a.y32 = (reinterpret_cast<uintptr_t>(Y) & 31u) == 0 ? 1 : 0;
+    a.wrows = N;
+    a.ystore = y_store_width(Y, N);
     a.groups = nullptr;
     a.slot_of = nullptr;
     a.E = 1;

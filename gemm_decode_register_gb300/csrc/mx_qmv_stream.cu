@@ -961,7 +961,15 @@ cudaError_t launch_moe_gate_up_swiglu(const DeviceState &ds, cudaStream_t st, in
                                       const uint8_t *scales, const uint16_t *x, const int32_t *ids, uint16_t *h,
                                       int T, int E, int topk, int I, int K)
 {
-    if (!stream_ok(fmt, K)) return cudaErrorInvalidValue;
+    if (!stream_ok(fmt, K)) {
+        // rows not 128-element aligned: the direct-load MoE kernel writes the
+        // gate and up products to the workspace, then the SwiGLU glue (the
+        // same silu and rounding) forms h
+        if ((size_t)T * topk * 2 * I > ds.ws_floats || ds.ws == nullptr) return cudaErrorInvalidValue;
+        cudaError_t e = launch_moe_qmv_direct(ds, st, fmt, codes, scales, x, ids, ds.ws, T, E, topk, 2 * I, K);
+        if (e != cudaSuccess) return e;
+        return launch_swiglu(ds, st, ds.ws, h, T * topk, I);
+    }
     MoeSArgs a = moe_args(ds, codes, scales, x, ids, T, E, topk, 2 * I, K);
     a.h = h;
     a.I = I;
@@ -973,7 +981,15 @@ cudaError_t launch_moe_down_combine(const DeviceState &ds, cudaStream_t st, int 
                                     const uint8_t *scales, const uint16_t *h, const int32_t *ids, const float *rw,
                                     float *out, int T, int E, int topk, int N, int K)
 {
-    if (!stream_ok(fmt, K)) return cudaErrorInvalidValue;
+    if (!stream_ok(fmt, K)) {
+        // rows not 128-element aligned: per-slot down products from the
+        // direct-load MoE kernel through the workspace, then the router
+        // combine (fused multiply-adds in slot order, as the fused kernel)
+        if ((size_t)T * topk * N > ds.ws_floats || ds.ws == nullptr) return cudaErrorInvalidValue;
+        cudaError_t e = launch_moe_qmv_direct(ds, st, fmt, codes, scales, h, ids, ds.ws, T * topk, E, 1, N, K);
+        if (e != cudaSuccess) return e;
+        return launch_moe_combine(ds, st, ds.ws, rw, out, T, topk, N);
+    }
     const int MC = moe_mc_down(T);
     const int RT = 2 * MC;
     if ((size_t)T * topk * N > ds.ws_floats || (N + RT - 1) / RT > ds.ws_counters || ds.ws == nullptr)

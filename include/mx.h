@@ -123,8 +123,10 @@ int mx_moe_qmv(int fmt, const void *expert_codes, const void *expert_scales, con
  * rows I..2I-1 up (NVFP4: E fp32 tensor scales after the whole
  * [E][2I][K/16] scale block).  x bf16 [T][K]; h bf16 [T][topk][I].  silu and
  * the rounding are those of mx_swiglu, so h equals mx_swiglu applied to
- * mx_moe_qmv's output with N = 2I.  K must be a multiple of 128 (else
- * MX_EUNSUPPORTED); other limits and the bad-id behaviour (h rows NaN) as in
+ * mx_moe_qmv's output with N = 2I.  When K is not a multiple of 128 the
+ * products come from the direct-load MoE kernel through the calling stream's
+ * workspace slot, then the SwiGLU glue (two launches; T*topk*2I <= 4 Mi
+ * floats).  Other limits and the bad-id behaviour (h rows NaN) as in
  * mx_moe_qmv.  codes, scales, x, h 16-byte aligned; ids 4-byte aligned. */
 int mx_moe_gate_up_swiglu(int fmt, const void *expert_codes, const void *expert_scales, const void *x,
                           const int32_t *expert_ids, void *h, int T, int E, int topk, int I, int K);
@@ -139,7 +141,9 @@ int mx_moe_gate_up_swiglu(int fmt, const void *expert_codes, const void *expert_
  * its weights; the per-slot partial sums go through the library's device
  * workspace slot of the calling stream (T*topk*N <= 4 Mi floats), whose
  * counters are re-armed by the call itself.  A bad id sets MX_DEVERR_BAD_EXPERT and makes that token's
- * outputs NaN.  K a multiple of 128; h, out, codes, scales 16-byte aligned,
+ * outputs NaN.  When K is not a multiple of 128 the per-slot products come
+ * from the direct-load MoE kernel, then the router combine (two launches).
+ * h, out, codes, scales 16-byte aligned,
  * ids and r 4-byte aligned.  Calls on one stream run in order; calls on
  * different streams use different workspace slots. */
 int mx_moe_down_combine(int fmt, const void *expert_codes, const void *expert_scales, const void *h,
@@ -152,9 +156,10 @@ int mx_moe_down_combine(int fmt, const void *expert_codes, const void *expert_sc
  *   Y[m][n] = bf16_rne( sum_k X[m][k] * W[n][k] ),  fp32 accumulation.
  * X bf16 [M][K], Y bf16 [M][N].  The weight tile is decoded exactly to bf16
  * in shared memory and multiplied by tcgen05 tensor-core MMA with the
- * accumulator in tensor memory.  Any M >= 1; N must be a multiple of 256
- * and K of 64 (else MX_EUNSUPPORTED); the NVFP4 tensor scale is applied in
- * the epilogue. */
+ * accumulator in tensor memory.  Any M >= 1 and N >= 1 (a last column tile
+ * that N only partly covers is masked); K a multiple of 32 (the TMA loads
+ * need code rows a multiple of 16 bytes apart: NVFP4 with K % 32 == 16 gives
+ * MX_EUNSUPPORTED); the NVFP4 tensor scale is applied in the epilogue. */
 int mx_qmm(int fmt, const void *codes, const void *scales, const void *X, void *Y, int M, int N,
            int K);
 
@@ -192,8 +197,8 @@ int mx_qmm_qx(int fmt, const void *codes, const void *scales, const void *xcodes
  * workspace: caller-owned device memory of at least
  * mx_moe_qmm_workspace_size(T, E, topk, K) bytes, 256-byte aligned (else
  * MX_EINVAL / MX_EALIGN); the call overwrites it, so calls sharing one
- * workspace must not overlap.  N a multiple of 256 and K of 64, T*topk <=
- * 2^24, E <= 4096, E*N < 2^31 (else MX_EUNSUPPORTED).  An id outside [0, E)
+ * workspace must not overlap.  Any N; K a multiple of 32 (as mx_qmm), T*topk
+ * <= 2^24, E <= 4096, E*N < 2^31 (else MX_EUNSUPPORTED).  An id outside [0, E)
  * sets MX_DEVERR_BAD_EXPERT and fills that slot's N outputs with NaN.
  * codes, scales, x, y 16-byte aligned; ids 4-byte aligned.  For a down
  * projection pass T' = T*topk rows, topk = 1. */
@@ -212,8 +217,8 @@ int mx_moe_qmm(int fmt, const void *expert_codes, const void *expert_scales, con
  * gather, grouped gate-up GEMM with the SwiGLU in its epilogue (CTA pairs
  * whose two halves hold gate row i and up row I + i), grouped down GEMM,
  * combine.  workspace: at least mx_moe_ffn_prefill_workspace_size(T, E,
- * topk, H, I) bytes, 256-byte aligned.  H a multiple of 256, I of 128; other
- * limits as mx_moe_qmm.  A bad id sets MX_DEVERR_BAD_EXPERT and makes that
+ * topk, H, I) bytes, 256-byte aligned.  H and I multiples of 32 (each is the
+ * K of one of the GEMMs); other limits as mx_moe_qmm.  A bad id sets MX_DEVERR_BAD_EXPERT and makes that
  * token's outputs NaN.  Pointers 16-byte aligned; ids and r 4-byte. */
 size_t mx_moe_ffn_prefill_workspace_size(int T, int E, int topk, int H, int I);
 int mx_moe_ffn_prefill(int fmt, const void *gate_up_codes, const void *gate_up_scales, const void *down_codes,

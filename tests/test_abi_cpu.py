@@ -57,8 +57,8 @@ def test_moe_rejects(lib, args, want):
 
 
 @pytest.mark.parametrize("args,want", [
-    ((0, A, A, A, A, 128, 200, 64), -2),   # N not a multiple of 256
-    ((0, A, A, A, A, 128, 256, 96), -2),   # K not a multiple of 64
+    ((2, A, A, A, A, 128, 200, 48), -2),   # NVFP4 K % 32 == 16: code rows not 16 bytes apart for the TMA
+    ((0, A, A, A, A, 128, 256, 80), -1),   # K not a multiple of the block
     ((0, A, A, A, 0, 128, 256, 64), -1),   # null Y
 ])
 def test_qmm_rejects(lib, args, want):
@@ -73,8 +73,7 @@ Z = 1 << 30  # a workspace size large enough for every case below
     ((0, A, A, A, A, A, 8, 4, 5, 256, 64, A, Z), -1),       # topk > E
     ((0, A, A, A, 0, A, 8, 4, 2, 256, 64, A, Z), -1),       # null ids
     ((0, A, A, A, A, A, 8, 4, 2, 256, 64, 0, Z), -1),       # null workspace
-    ((0, A, A, A, A, A, 8, 4, 2, 128, 64, A, Z), -2),       # N not a multiple of 256
-    ((0, A, A, A, A, A, 8, 4, 2, 256, 96, A, Z), -2),       # K not a multiple of 64
+    ((2, A, A, A, A, A, 8, 4, 2, 200, 48, A, Z), -2),       # NVFP4 K % 32 == 16
     ((0, A, A, A, A, A, 8, 5000, 2, 256, 64, A, Z), -2),    # E > 4096
     ((0, A, A, A, A, A, 8, 4, 2, 256, 64, A, 1024), -1),    # workspace too small
     ((0, A, A, A, A, A, 8, 4, 2, 256, 64, A + 16, Z), -3),  # workspace not 256-byte aligned
@@ -86,8 +85,8 @@ def test_moe_qmm_rejects(lib, args, want):
 
 @pytest.mark.parametrize("args,want", [
     ((0, A, A, A, A, A, A, A, A, 8, 4, 2, 256, 128, A, Z), 0),     # valid (not called: see below)
-    ((0, A, A, A, A, A, A, A, A, 8, 4, 2, 320, 128, A, Z), -2),    # H not a multiple of 256
-    ((0, A, A, A, A, A, A, A, A, 8, 4, 2, 256, 96, A, Z), -2),     # I not a multiple of 128
+    ((2, A, A, A, A, A, A, A, A, 8, 4, 2, 48, 128, A, Z), -2),     # NVFP4 H % 32 == 16 (the gate-up GEMM's K)
+    ((2, A, A, A, A, A, A, A, A, 8, 4, 2, 256, 80, A, Z), -2),     # NVFP4 I % 32 == 16 (the down GEMM's K)
     ((0, A, A, A, A, A, A, 0, A, 8, 4, 2, 256, 128, A, Z), -1),    # null router weights
     ((0, A, A, A, A, A, A, A, A, 8, 4, 2, 256, 128, A, 4096), -1),  # workspace too small
     ((0, A, A, A, A, A, A, A + 2, A, 8, 4, 2, 256, 128, A, Z), -3),  # misaligned router weights

@@ -184,15 +184,21 @@ def test_fused_bad_expert_ids(orc):
     assert np.all(np.isnan(out))
 
 
-def test_fused_rejects_unsupported_k():
-    """K not a multiple of 128 has no fused kernel: MX_EUNSUPPORTED."""
+@pytest.mark.parametrize("fmt,K", [(0, 96), (1, 160), (2, 48), (2, 336)])
+def test_fused_k_not_multiple_of_128(orc, fmt, K):
+    """Rows that are not 128-element aligned: the direct-load MoE kernel
+    through the workspace, then the glue (SwiGLU; router combine), against
+    the oracle chain."""
     need_gpu()
-    from gemm_decode_register_gb300 import ops
-
-    fmt, T, E, topk, I, K = 0, 1, 4, 2, 16, 96
-    c1, s1 = synth.weights(fmt, 2 * I, K, 47, E=E)
+    T, E, topk, I, N = 3, 6, 2, 40, 72
+    c1, s1 = synth.weights(fmt, 2 * I, K, 47 + K, E=E)
     x = synth.activations(T, K, 48)
     ids = synth.expert_ids(T, E, topk, 49)
-    with pytest.raises(ops.MxError) as ei:
-        fused_gate_up(fmt, c1, s1, x, ids, E, I)
-    assert ei.value.status == -2
+    hb = bf16_host(fused_gate_up(fmt, c1, s1, x, ids, E, I)).reshape(T * topk, I)
+    want = oracle_h(orc, fmt, c1, s1, x, ids, T, E, topk, I, K)
+    check_close(bf16_bits_to_f64(hb), bf16_bits_to_f64(want), f"gate-up K{K} fmt{fmt}", bf16_out=True)
+    c2, s2 = synth.weights(fmt, N, K, 50 + K, E=E)
+    h = synth.activations(T * topk, K, 51)
+    r = synth.router_weights(T, topk, 52)
+    out = fused_down(fmt, c2, s2, h, ids, r, E, N).cpu().numpy()
+    check_close(out, oracle_out(orc, fmt, c2, s2, h, ids, r, T, E, topk, N, K), f"down-combine K{K} fmt{fmt}")

@@ -36,6 +36,9 @@ for fmt in (0, 1, 2):
         (fmt, 300, 4, 2, 512, 192),  # ~150 rows per expert, two column tiles, 3 k-blocks
         (fmt, 700, 3, 2, 256, 64),   # ~470 rows per expert: one tile using both 256-row halves
         (fmt, 1, 8, 8, 256, 256),    # one token
+        (fmt, 90, 5, 2, 200, 96),    # ragged: a partly covered column tile, a last k-block K only partly covers
+        (fmt, 60, 3, 2, 1000, 160),  # ragged N (rows 16 bytes apart) and K
+        (fmt, 30, 2, 1, 1, 32),      # one output column, one half k-block
     ]
 
 
@@ -125,7 +128,8 @@ def test_moe_qmm_bad_ids(orc):
 
 def test_moe_qmm_workspace_checks():
     """A workspace below mx_moe_qmm_workspace_size is MX_EINVAL, one that is
-    not 256-byte aligned MX_EALIGN; N not a multiple of 256 MX_EUNSUPPORTED."""
+    not 256-byte aligned MX_EALIGN; NVFP4 with K % 32 == 16 (code rows the
+    TMA cannot take) MX_EUNSUPPORTED."""
     torch = need_gpu()
     from gemm_decode_register_gb300 import ops
 
@@ -143,9 +147,9 @@ def test_moe_qmm_workspace_checks():
     with pytest.raises(ops.MxError) as ei:
         run_moe_qmm(fmt, codes, scales, x, ids, E, N, workspace=big[16:])
     assert ei.value.status == -3
-    c2, s2 = synth.weights(fmt, 128, K, 71, E=E)
+    c2, s2 = synth.weights(2, 128, 48, 71, E=E)
     with pytest.raises(ops.MxError) as ei:
-        run_moe_qmm(fmt, c2, s2, x, ids, E, 128)
+        run_moe_qmm(2, c2, s2, synth.activations(T, 48, 72), ids, E, 128)
     assert ei.value.status == -2
 
 
@@ -170,6 +174,9 @@ def test_moe_qmm_full_size_sampled(orc, N, K, T, topk, seed):
 
 
 FFN_CASES = [(fmt, 50, 6, 3, 256, 128) for fmt in (0, 1, 2)] + [(0, 300, 5, 4, 512, 256)]
+# ragged: H and I not multiples of the tiles (a partly used gate/up column
+# tile, last k-blocks that H and I only partly cover)
+FFN_CASES += [(fmt, 40, 4, 2, 160, 96) for fmt in (0, 1, 2)] + [(0, 30, 3, 2, 96, 224)]
 
 
 @pytest.mark.parametrize("fmt,T,E,topk,H,I", FFN_CASES)

@@ -32,6 +32,33 @@ def test_qmm_parity(orc, fmt, M, N, K):
 
 
 @pytest.mark.parametrize("fmt", [0, 1, 2])
+@pytest.mark.parametrize("M,N,K", [(300, 1, 64), (256, 255, 96), (100, 257, 160), (513, 1000, 224),
+                                   (64, 300, 32), (1000, 9828, 96)])
+def test_qmm_ragged(orc, fmt, M, N, K):
+    """N not a multiple of the 256-column pair tile (a masked last tile;
+    rows 2 bytes, 8 bytes or 16 bytes apart) and K not a multiple of the
+    64-element k-block (the last k-block's codes zero-filled by the TMA, its
+    missing scales read as 1.0); 1000 x 9828 takes 512-row pair tiles."""
+    need_gpu()
+    codes, scales = synth.weights(fmt, N, K, M + N + K, exp_lo=118, exp_hi=132)
+    X = synth.activations(M, K, 7 * M + K)
+    check_close(run_qmm(fmt, codes, scales, X, N), orc.qmv(fmt, codes, scales, X, M, N, K),
+                f"qmm ragged fmt{fmt} {M}x{N}x{K}", bf16_out=True)
+
+
+def test_qmm_rejects_nvfp4_k_16_mod_32():
+    """NVFP4 rows of K = 48 elements are 24 bytes apart: the TMA loads cannot
+    take them, MX_EUNSUPPORTED."""
+    need_gpu()
+    from gemm_decode_register_gb300 import ops
+
+    codes, scales = synth.weights(2, 256, 48, 1)
+    with pytest.raises(ops.MxError) as ei:
+        ops.qmm(2, dev_u8(codes), dev_u8(scales), dev_bf16(synth.activations(8, 48, 2)), 256)
+    assert ei.value.status == -2
+
+
+@pytest.mark.parametrize("fmt", [0, 1, 2])
 def test_qmm_onehot_rows_exact(orc, fmt):
     """Row m of X is e_{k_m}: Y[m] must be bf16(W[:, k_m]) exactly (every
     decoded weight has at most 6 significant bits, one nonzero product per
