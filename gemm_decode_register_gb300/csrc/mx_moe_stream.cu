@@ -116,11 +116,44 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) moe_stream_kernel(MoeSArgs a)
     auto done = [&](int i, const float (&acc)[2][2]) {
         const int item = gw + stride * i;
         const int w = item / tiles, tile = item - w * tiles;
-        float vv[2][2];
-        qmv_warp_reduce<MC>(acc, vv);
         float g = 1.0f;
         if (FMT == FMT_NVFP4)
             g = load_f32_unaligned(a.scales + (size_t)a.E * R * KS + 4 * (size_t)wg_e[w]);
+        if constexpr (G::PAIR) {
+            // every lane holds tile row r for token t (MC = 4: no lanes to add)
+            static_assert(MC == 4, "paired MoE tiles of 4 slots");
+            float v;
+            int r, t;
+            pair_reduce<MC>(acc, v, r, t);
+            if constexpr (MODE == MOE_GATE_UP_SWIGLU) {
+                // gate row i (tile row r < MC) is paired with up row I + i
+                // (tile row MC + r), two lane groups further
+                const float up = __shfl_down_sync(0xFFFFFFFFu, v, 16);
+                const int irow = tile * MC + r;
+                if (r < MC && irow < a.I && t < wg_mc[w]) {
+                    const int slot = sorted[wg_first[w] + t];
+                    const float fs = pow2f(sh_final<FMT>(sh[slot / a.topk]));
+                    float gv = v * fs, uv = up * fs;
+                    if (FMT == FMT_NVFP4) {
+                        gv *= g;
+                        uv *= g;
+                    }
+                    a.h[(size_t)slot * a.I + irow] = (uint16_t)swiglu_bf16(gv, uv);
+                }
+            } else {
+                const int row = tile * G::RT + r;
+                if (row < a.N && t < wg_mc[w]) {
+                    const int slot = sorted[wg_first[w] + t];
+                    float sv = v * pow2f(sh_final<FMT>(sh[xrow_of_slot(slot)]));
+                    if (FMT == FMT_NVFP4) sv *= g;
+                    if (MODE == MOE_PLAIN) a.y[(size_t)slot * a.N + row] = sv;
+                    else a.ws[(size_t)slot * a.N + row] = sv;
+                }
+            }
+            return;
+        }
+        float vv[2][2];
+        qmv_warp_reduce<MC>(acc, vv);
         if constexpr (MODE == MOE_GATE_UP_SWIGLU) {
             // the lane holding gate row i of a token also holds its up row
 #pragma unroll

@@ -117,15 +117,21 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) qmv_stream_kernel(QmvSArgs a)
     auto xrow_of = [&](int) { return xrow; };
     auto done = [&](int i, const float (&acc)[2][2]) {
         const size_t v = (size_t)unit_tile(i) * a.pmax + slot_of(i);
-        float vv[2][2];
-        qmv_warp_reduce<MC>(acc, vv);
+        if constexpr (G::PAIR) {
+            float x;
+            int r, t;
+            if (pair_reduce<MC>(acc, x, r, t)) red[(v * G::RT + r) * MC + t] = x;
+        } else {
+            float vv[2][2];
+            qmv_warp_reduce<MC>(acc, vv);
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+            for (int h = 0; h < 2; ++h)
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                int r, t;
-                if (tile_out<MC>(h, c, r, t)) red[(v * G::RT + r) * MC + t] = vv[h][c];
-            }
+                for (int c = 0; c < 2; ++c) {
+                    int r, t;
+                    if (tile_out<MC>(h, c, r, t)) red[(v * G::RT + r) * MC + t] = vv[h][c];
+                }
+        }
     };
     pdl_trigger();
     uint8_t *ring = rings + (size_t)warp * G::STAGES * G::STAGE_BYTES;

@@ -49,10 +49,24 @@ struct SGeo {
     static constexpr int IPS = FMT == FMT_MXFP8 ? 4 : 8;          // MMA iterations per stage
     static constexpr int UPS = IPS * BPM;                          // units per row per stage
     static constexpr int CB = UPS * UCB;                           // code bytes per row per stage
-    static constexpr int RS = CB + (FMT == FMT_MXFP8 ? 256 : 128) / MC;  // padded row stride
     static constexpr int SPU = FMT == FMT_NVFP4 ? 2 : 1;           // scale bytes per unit
     static constexpr int SB = UPS * SPU;                           // scale bytes per row per stage
-    static constexpr int CODE_BYTES = RT * RS;
+    // Paired units (MC <= 4): lane group g decodes, for tile row g / HB, the
+    // units 2j and 2j + 1 (j = g % HB) of each MMA iteration as A rows g and
+    // g + 8; the two block scales are adjacent bytes and only the two
+    // accumulators of matching blocks are kept.  MC = 8 (one unit per MMA
+    // iteration and row) keeps A rows g and g + 8 as tile rows g and 8 + g.
+    static constexpr bool PAIR = MC <= 4;
+    static constexpr int HB = PAIR ? BPM / 2 : 1;                 // lane groups per tile row
+    // Shared-memory offset of tile row r: rows are CB bytes plus a pad whose
+    // size spreads the 8 lane groups' loads of one iteration over the banks.
+    __host__ __device__ static constexpr int row_base(int r)
+    {
+        return !PAIR ? r * (CB + (FMT == FMT_MXFP8 ? 256 : 128) / MC)
+               : FMT == FMT_MXFP8 ? r * (CB + 32)
+                                  : r * CB + 16 * ((r & 1) + (r >> 1) * 2 * HB);
+    }
+    static constexpr int CODE_BYTES = (row_base(RT - 1) + CB + 15) / 16 * 16;
     static constexpr int STAGE_BYTES = CODE_BYTES + RT * SB;
     // ring depth: one stage in decode, the rest in flight (short tiles leave
     // room in shared memory for a deeper ring)
@@ -101,7 +115,7 @@ struct CopyPlan {
 template <int FMT, int MC>
 struct CopyLane {
     using G = SGeo<FMT, MC>;
-    int row[CopyPlan<FMT, MC>::NP], off[CopyPlan<FMT, MC>::NP];
+    int row[CopyPlan<FMT, MC>::NP], off[CopyPlan<FMT, MC>::NP], dst[CopyPlan<FMT, MC>::NP];
     int srow[CopyPlan<FMT, MC>::NW], soff[CopyPlan<FMT, MC>::NW];
     __device__ __forceinline__ CopyLane()
     {
@@ -111,6 +125,7 @@ struct CopyLane {
             const int p = lane + 32 * j;
             row[j] = p / (G::CB / 16);
             off[j] = (p % (G::CB / 16)) * 16;
+            dst[j] = G::row_base(row[j]) + off[j];
         }
 #pragma unroll
         for (int j = 0; j < CopyPlan<FMT, MC>::NW; ++j) {
@@ -156,10 +171,101 @@ __device__ __forceinline__ void copy_stage(const CopyPlan<FMT, MC> &c, const Cop
     const int cs = s * G::CB, ss = s * G::SB;
 #pragma unroll
     for (int j = 0; j < c.NP; ++j)
-        if (cs < c.left[j]) cp_async16(dst + cl.row[j] * G::RS + cl.off[j], c.src[j] + cs);
+        if (cs < c.left[j]) cp_async16(dst + cl.dst[j], c.src[j] + cs);
 #pragma unroll
     for (int j = 0; j < c.NW; ++j)
         if (ss < c.sleft[j]) cp_async4(dst + G::CODE_BYTES + cl.srow[j] * G::SB + cl.soff[j], c.ssrc[j] + ss);
+}
+
+// One MMA group of the paired-unit layout: A row g holds unit 2j and A row
+// g + 8 unit 2j + 1 of the same weight row (l.s: their scales, low byte
+// first; NVFP4: two bytes each).  Only the products of matching blocks are
+// accumulated: acc[0][0] (unit 2j, B column 2q) and acc[1][1] (unit 2j + 1,
+// B column 2q + 1); on lanes with q % HB == j both belong to token q / HB.
+// ok = false: the lane's units lie outside the work (nothing accumulated).
+// FOLD, f: as compute_unit (f[0] = f[1] here: one token per lane).
+template <int FMT, bool FOLD>
+__device__ __forceinline__ void compute_pair(const Ld<FMT> &l, const uint32_t (&B)[4], float (&acc)[2][2], bool ok,
+                                             const float (&f)[2])
+{
+    const float z[4] = {0.f, 0.f, 0.f, 0.f};
+    if constexpr (FMT == FMT_MXFP8) {
+        float d[4];
+        uint32_t a[4];
+        e4m3x4_to_f16x2(l.c[0].x, a[0], a[2]);
+        e4m3x4_to_f16x2(l.c[1].x, a[1], a[3]);
+        mma_f16_16816(d, a, B[0], B[1], z);
+        e4m3x4_to_f16x2(l.c[0].y, a[0], a[2]);
+        e4m3x4_to_f16x2(l.c[1].y, a[1], a[3]);
+        mma_f16_16816(d, a, B[2], B[3], d);
+        float s0, s1;
+        e8m0x2_to_f32(l.s, s0, s1);
+        if (ok) {
+            acc[0][0] = fmaf(d[0], FOLD ? s0 * f[0] : s0, acc[0][0]);
+            acc[1][1] = fmaf(d[3], FOLD ? s1 * f[1] : s1, acc[1][1]);
+        }
+    } else {
+        uint32_t a0[4], a1[4];
+        e2m1x8_to_f16x2(l.c[0], a0[0], a0[2], a1[0], a1[2]);
+        e2m1x8_to_f16x2(l.c[1], a0[1], a0[3], a1[1], a1[3]);
+        if constexpr (FMT == FMT_MXFP4) {
+            float d[4];
+            mma_f16_16816(d, a0, B[0], B[1], z);
+            mma_f16_16816(d, a1, B[2], B[3], d);
+            float s0, s1;
+            e8m0x2_to_f32(l.s, s0, s1);
+            if (ok) {
+                acc[0][0] = fmaf(d[0], FOLD ? s0 * f[0] : s0, acc[0][0]);
+                acc[1][1] = fmaf(d[3], FOLD ? s1 * f[1] : s1, acc[1][1]);
+            }
+        } else {
+            // MMA step s covers 16-element block s of each unit
+            float d0[4], d1[4];
+            mma_f16_16816(d0, a0, B[0], B[1], z);
+            mma_f16_16816(d1, a1, B[2], B[3], z);
+            const uint32_t f0 = e4m3x2_to_f16x2(l.s[0]), f1 = e4m3x2_to_f16x2(l.s[1]);
+            if (ok) {
+                acc[0][0] = fmaf(d1[0], f16_hi_to_f32(f0), fmaf(d0[0], f16_lo_to_f32(f0), acc[0][0]));
+                acc[1][1] = fmaf(d1[3], f16_hi_to_f32(f1), fmaf(d0[3], f16_lo_to_f32(f1), acc[1][1]));
+            }
+        }
+    }
+}
+
+// End of a tile in the paired-unit layout: adds each tile row's HB lane
+// groups (the lanes with q % HB == j hold a (row, token) pair's two
+// accumulators, the others none).  Returns true on the lane left holding
+// tile row r and token t, with the sum in v.
+template <int MC>
+__device__ __forceinline__ bool pair_reduce(const float (&acc)[2][2], float &v, int &r, int &t)
+{
+    constexpr int HB = 4 / MC;
+    const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+    float x = q % HB == g % HB ? acc[0][0] + acc[1][1] : 0.f;
+    if constexpr (MC == 1) {
+        // lanes 16r + 5j (j = 0..3) hold row r
+        x += __shfl_xor_sync(0xFFFFFFFFu, x, 8);
+        x += __shfl_xor_sync(0xFFFFFFFFu, x, 4);
+        x += __shfl_xor_sync(0xFFFFFFFFu, x, 2);
+        x += __shfl_xor_sync(0xFFFFFFFFu, x, 1);
+        r = g >> 2;
+        t = 0;
+        v = x;
+        return (lane & 15) == 0;
+    } else if constexpr (MC == 2) {
+        // lanes 8r + 2t and 8r + 2t + 5 hold (row r, token t)
+        x += __shfl_xor_sync(0xFFFFFFFFu, x, 1);
+        x += __shfl_xor_sync(0xFFFFFFFFu, x, 4);
+        r = g >> 1;
+        t = q >> 1;
+        v = x;
+        return (lane & 5) == 0;
+    } else {
+        r = g;
+        t = q;
+        v = x;
+        return true;
+    }
 }
 
 // Decode-and-multiply one stage from shared memory into acc.
@@ -175,14 +281,57 @@ __device__ __forceinline__ void compute_stage_impl(const SUnit &u, int s, const 
     using G = SGeo<FMT, MC>;
     const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
     const int b = g % G::BPM;
-    const int r0 = g / G::BPM, r1 = MC + g / G::BPM;
     const int u0 = u.ub + s * G::UPS;
     const int lane_off = FMT == FMT_MXFP8 ? 8 * q : (FMT == FMT_NVFP4 ? 2 * q : 4 * q);
-    const uint8_t *a0 = buf + r0 * G::RS + b * G::UCB + lane_off;
-    const uint8_t *a1 = buf + r1 * G::RS + b * G::UCB + lane_off;
+    const uint16_t *xp = xrow >= 0 ? xs + (size_t)xrow * ks + 8 * q + (size_t)(u0 + b - xu0) * 32 : nullptr;
+    if constexpr (G::PAIR) {
+        const int rr = g / G::HB, j = g % G::HB;  // tile row; its units 2j, 2j + 1 of each iteration
+        const uint8_t *a0 = buf + G::row_base(rr) + 2 * j * G::UCB + lane_off;
+        const uint8_t *sp = buf + G::CODE_BYTES + rr * G::SB + 2 * j * G::SPU;
+#pragma unroll
+        for (int it = 0; it < G::IPS; ++it) {
+            const int rel = it * G::BPM;
+            bool ok_a = true, ok_b = true;
+            if constexpr (!FULL) {
+                if (rel >= u.ul - u0) break;  // warp-uniform end of the unit
+                ok_a = u0 + rel + 2 * j < u.ul;
+                ok_b = u0 + rel + b < u.ul;
+            }
+            Ld<FMT> l;
+            if constexpr (FMT == FMT_MXFP4) {
+                l.c[0] = *reinterpret_cast<const uint32_t *>(a0 + rel * 16);
+                l.c[1] = *reinterpret_cast<const uint32_t *>(a0 + rel * 16 + 16);
+                l.s = *reinterpret_cast<const uint16_t *>(sp + rel);
+            } else if constexpr (FMT == FMT_MXFP8) {
+                l.c[0] = *reinterpret_cast<const uint2 *>(a0 + rel * 32);
+                l.c[1] = *reinterpret_cast<const uint2 *>(a0 + rel * 32 + 32);
+                l.s = *reinterpret_cast<const uint16_t *>(sp + rel);
+            } else {
+                l.c[0] = __byte_perm(*reinterpret_cast<const uint16_t *>(a0 + rel * 16),
+                                     *reinterpret_cast<const uint16_t *>(a0 + rel * 16 + 8), 0x5410);
+                l.c[1] = __byte_perm(*reinterpret_cast<const uint16_t *>(a0 + rel * 16 + 16),
+                                     *reinterpret_cast<const uint16_t *>(a0 + rel * 16 + 24), 0x5410);
+                const uint32_t w = *reinterpret_cast<const uint32_t *>(sp + rel * 2);
+                l.s[0] = w & 0xFFFFu;
+                l.s[1] = w >> 16;
+            }
+            uint32_t B[4] = {0u, 0u, 0u, 0u};
+            if (xp && ok_b) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(xp + (size_t)rel * 32);
+                B[0] = v.x;
+                B[1] = v.y;
+                B[2] = v.z;
+                B[3] = v.w;
+            }
+            compute_pair<FMT, FOLD>(l, B, acc, ok_a, f);
+        }
+        return;
+    }
+    const int r0 = g / G::BPM, r1 = MC + g / G::BPM;
+    const uint8_t *a0 = buf + G::row_base(r0) + b * G::UCB + lane_off;
+    const uint8_t *a1 = buf + G::row_base(r1) + b * G::UCB + lane_off;
     const uint8_t *s0 = buf + G::CODE_BYTES + r0 * G::SB + b * G::SPU;
     const uint8_t *s1 = buf + G::CODE_BYTES + r1 * G::SB + b * G::SPU;
-    const uint16_t *xp = xrow >= 0 ? xs + (size_t)xrow * ks + 8 * q + (size_t)(u0 + b - xu0) * 32 : nullptr;
 #pragma unroll
     for (int it = 0; it < G::IPS; ++it) {
         const int rel = it * G::BPM;
