@@ -84,15 +84,19 @@ __device__ __forceinline__ void stage_store(uint16_t *xs, int ks, int r, int k0,
     // elements k0 .. k0+7 of row r (k0 a multiple of 8), zero past len
     const int u = k0 >> 5, p0 = k0 & 31;
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t out[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int p = p0 + 2 * j;
-        int slot = p;
-        if (fmt == FMT_NVFP4) slot = 8 * ((p & 15) >> 2) + 4 * (p >> 4) + (p & 3);
-        uint32_t out = 0u;
-        if (k0 + 2 * j < len)
-            out = f32x2_to_f16x2(bf16_to_f32(w[j] & 0xFFFFu) * f, bf16_to_f32(w[j] >> 16) * f);
-        *reinterpret_cast<uint32_t *>(xs + (size_t)r * ks + u * 32 + slot) = out;
+    for (int j = 0; j < 4; ++j)
+        out[j] = k0 + 2 * j < len ? f32x2_to_f16x2(bf16_to_f32(w[j] & 0xFFFFu) * f, bf16_to_f32(w[j] >> 16) * f)
+                                  : 0u;
+    uint16_t *row = xs + (size_t)r * ks + u * 32;
+    if (fmt == FMT_NVFP4) {
+        // slots of elements p0, p0+2 are adjacent, and those of p0+4, p0+6
+        const int s0 = 8 * ((p0 & 15) >> 2) + 4 * (p0 >> 4);
+        *reinterpret_cast<uint2 *>(row + s0) = make_uint2(out[0], out[1]);
+        *reinterpret_cast<uint2 *>(row + s0 + 8) = make_uint2(out[2], out[3]);
+    } else {
+        *reinterpret_cast<uint4 *>(row + p0) = make_uint4(out[0], out[1], out[2], out[3]);
     }
 }
 
