@@ -180,6 +180,19 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Ask L2 for the 128-byte lines of [p, p + bytes), the block's threads taking
+// every blockDim-th line.  A prefetch moves nothing into the SM and has no
+// effect on what later loads return (L2 is where the previous kernel's
+// writes land), so it may be issued before griddepcontrol.wait: data that
+// the previous kernel has not touched then starts its way from HBM ahead of
+// the weight stream instead of queueing behind it.
+__device__ __forceinline__ void prefetch_l2(const void *p, size_t bytes)
+{
+    const char *c = static_cast<const char *>(p);
+    for (size_t o = (size_t)threadIdx.x * 128; o < bytes; o += (size_t)blockDim.x * 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(c + o));
+}
+
 // ---------------------------------------------------------- activation
 
 // SwiGLU of one (gate, up) pair rounded to bf16 (bits in the low half):

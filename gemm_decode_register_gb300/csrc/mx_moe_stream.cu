@@ -35,10 +35,10 @@ __host__ __device__ inline int moe_xrows(int T, int topk)
     return MODE == MOE_DOWN_COMBINE ? T * topk : T;
 }
 
-template <int FMT, int MC, int MODE>
+// S: ring depth of each warp (stages).
+template <int FMT, int MC, int MODE, int S>
 __global__ void __launch_bounds__(QMV_THREADS, 1) moe_stream_kernel(MoeSArgs a)
 {
-    constexpr int S = SGeo<FMT, MC>::STAGES;
     using G = SGeo<FMT, MC>;
     extern __shared__ __align__(16) uint8_t smem[];
     const int P = a.T * a.topk;
@@ -61,8 +61,10 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) moe_stream_kernel(MoeSArgs a)
     // The routing and the routed experts' weights do not depend on the
     // previous kernel (no kernel of this library writes expert ids; the
     // caller's ids are complete when the call is issued): the grouping and
-    // the first weight copies overlap its tail.  Activations and outputs wait.
+    // the whole ring's weight copies overlap its tail.  Activations and
+    // outputs wait (their L2 prefetch is issued first).
     pdl_trigger();
+    prefetch_l2(a.x, (size_t)XR * a.K * 2);  // the activation rows, ahead of the weight stream
     RouteSmem rs{cnt, wgs, pos, sorted, wg_e, wg_first, wg_mc, tmp};
     const int nwg = moe_route(a.ids, P, a.E, MC, rs);
     if (MODE == MOE_DOWN_COMBINE && nwg == 0) {
@@ -194,7 +196,7 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) moe_stream_kernel(MoeSArgs a)
     };
     uint8_t *ring = rings + (size_t)warp * S * G::STAGE_BYTES;
     Streamer<FMT, MC, decltype(next), S> st(next, n_my, ring, R, RB, KS);
-    st.prime(1);
+    st.prime(S - 1);
     pdl_wait();
     for (int p = blockIdx.x; p < P; p += gridDim.x) {
         const int e = a.ids[p];
@@ -206,8 +208,7 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) moe_stream_kernel(MoeSArgs a)
                 for (int i = threadIdx.x; i < a.I; i += blockDim.x) a.h[(size_t)p * a.I + i] = 0x7FC0u;
         }
     }
-    // the rest of the weight copies are issued once the activation loads are in flight
-    stage_x<FMT>(a.x, (size_t)a.K, a.K, XR, nullptr, xs, a.ks, sh, maxbits, [&]() { st.prime(S - 2); });
+    stage_x<FMT>(a.x, (size_t)a.K, a.K, XR, nullptr, xs, a.ks, sh, maxbits);
     __syncthreads();
     // fold factors per unit (the members of its work group); the fold is on
     // when a staged row was scaled up, a decision every CTA takes alike
@@ -255,6 +256,24 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) moe_stream_kernel(MoeSArgs a)
     }
 }
 
+template <int FMT, int MC, int MODE, int S>
+static cudaError_t launch_moe_stream(const DeviceState &ds, cudaStream_t st, const MoeSArgs &a, size_t smem)
+{
+    static int configured_dev[64] = {0};
+    if (ds.device < 64 && !configured_dev[ds.device]) {
+        cudaError_t e = cudaFuncSetAttribute(moe_stream_kernel<FMT, MC, MODE, S>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, ds.max_smem_optin);
+        if (e != cudaSuccess) return e;
+        configured_dev[ds.device] = 1;
+    }
+    return launch_k(moe_stream_kernel<FMT, MC, MODE, S>, dim3(ds.num_sms), dim3(QMV_THREADS), smem, st, a);
+}
+
+// Work groups of 4 slots stream an expert's rows in units of a few stages
+// (K of a few thousand): a ring of MOE_DEEP stages holds a whole unit in
+// flight when shared memory allows, else the default depth.
+constexpr int MOE_DEEP = 5;
+
 template <int FMT, int MC, int MODE>
 static cudaError_t run_moe_stream(const DeviceState &ds, cudaStream_t st, const MoeSArgs &a)
 {
@@ -262,16 +281,14 @@ static cudaError_t run_moe_stream(const DeviceState &ds, cudaStream_t st, const 
     const int P = a.T * a.topk;
     const int XR = moe_xrows<MODE>(a.T, a.topk);
     const size_t head = (((size_t)(3 * a.E + 4 * P + 40 + 2 * XR) * 4) + 15) & ~(size_t)15;
-    const size_t smem = head + (size_t)XR * a.ks * 2 + (size_t)QMV_WARPS * G::STAGES * G::STAGE_BYTES;
-    if (smem > (size_t)ds.max_smem_optin) return cudaErrorNotSupported;
-    static int configured_dev[64] = {0};
-    if (ds.device < 64 && !configured_dev[ds.device]) {
-        cudaError_t e = cudaFuncSetAttribute(moe_stream_kernel<FMT, MC, MODE>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, ds.max_smem_optin);
-        if (e != cudaSuccess) return e;
-        configured_dev[ds.device] = 1;
+    const size_t base = head + (size_t)XR * a.ks * 2;
+    if constexpr (MC == 4) {
+        const size_t deep = base + (size_t)QMV_WARPS * MOE_DEEP * G::STAGE_BYTES;
+        if (deep <= (size_t)ds.max_smem_optin) return launch_moe_stream<FMT, MC, MODE, MOE_DEEP>(ds, st, a, deep);
     }
-    return launch_k(moe_stream_kernel<FMT, MC, MODE>, dim3(ds.num_sms), dim3(QMV_THREADS), smem, st, a);
+    const size_t smem = base + (size_t)QMV_WARPS * G::STAGES * G::STAGE_BYTES;
+    if (smem > (size_t)ds.max_smem_optin) return cudaErrorNotSupported;
+    return launch_moe_stream<FMT, MC, MODE, G::STAGES>(ds, st, a, smem);
 }
 
 // Work groups of 4 or 8 slots (see moe_mc).
