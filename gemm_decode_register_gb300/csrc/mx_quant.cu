@@ -86,35 +86,150 @@ __device__ __forceinline__ uint32_t bf16_amax(const uint32_t (&w)[N], bool &nonf
     return m;
 }
 
-// G: the largest finite |x| over the tensor, as fp32 bits, by atomicMax into
-// *gbits (zeroed by the host before the launch).
-__global__ void quant_amax_kernel(const uint16_t *__restrict__ x, long long n8, unsigned *gbits)
+// Largest finite magnitude bits of the bf16 pairs of a 16-byte vector.
+__device__ __forceinline__ uint32_t vec_fin_amax(const uint4 &v)
 {
-    pdl_trigger();
-    pdl_wait();
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t m = 0;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8;
-         i += (long long)gridDim.x * blockDim.x) {
-        const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(x) + i);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint32_t lo = w[j] & 0x7FFFu, hi = (w[j] >> 16) & 0x7FFFu;
-            if (lo < 0x7F80u) m = max(m, lo);
-            if (hi < 0x7F80u) m = max(m, hi);
-        }
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t lo = w[j] & 0x7FFFu, hi = (w[j] >> 16) & 0x7FFFu;
+        if (lo < 0x7F80u) m = max(m, lo);
+        if (hi < 0x7F80u) m = max(m, hi);
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-    if ((threadIdx.x & 31) == 0 && m) atomicMax(gbits, m << 16);
+    return m;
 }
 
+constexpr int AMAX_THREADS = 256;
+constexpr int AMAX_UNROLL = 4;  // independent 16-byte loads in flight per thread
+
+// G: the largest finite |x| over the tensor, as fp32 bits, by atomicMax into
+// *gbits (zeroed by the host before the launch): each block reduces its
+// share in registers and shared memory and adds one atomic.
+__global__ void __launch_bounds__(AMAX_THREADS) quant_amax_kernel(const uint16_t *__restrict__ x, long long n8,
+                                                                  unsigned *gbits)
+{
+    __shared__ uint32_t wmax[AMAX_THREADS / 32];
+    pdl_trigger();
+    pdl_wait();
+    const uint4 *v = reinterpret_cast<const uint4 *>(x);
+    const long long stride = (long long)gridDim.x * AMAX_THREADS;
+    long long i = blockIdx.x * (long long)AMAX_THREADS + threadIdx.x;
+    uint32_t m = 0;
+    for (; i + (AMAX_UNROLL - 1) * stride < n8; i += AMAX_UNROLL * stride) {
+        uint4 r[AMAX_UNROLL];
+#pragma unroll
+        for (int u = 0; u < AMAX_UNROLL; ++u) r[u] = __ldcg(v + i + u * stride);  // kept in L2 for the block pass
+#pragma unroll
+        for (int u = 0; u < AMAX_UNROLL; ++u) m = max(m, vec_fin_amax(r[u]));
+    }
+    for (; i < n8; i += stride) m = max(m, vec_fin_amax(__ldcg(v + i)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        m = threadIdx.x < AMAX_THREADS / 32 ? wmax[threadIdx.x] : 0u;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        if (threadIdx.x == 0 && m) atomicMax(gbits, m << 16);
+    }
+}
+
+// Eight quotients x_i / den to E2M1 codes, identical to converting the
+// correctly rounded fp32 quotients.  The products q_i = x_i * rcp(den) (rcp
+// correctly rounded) lie within 2^-22 |q_i| of the rounded quotients (two
+// roundings of at most 2^-24 each); q_i (1 - 2^-21) and q_i (1 + 2^-21),
+// themselves rounded, bracket that interval, and since the conversion to
+// E2M1 is monotone, equal codes at both ends fix the code of the rounded
+// quotient.  Otherwise a quotient lies near a rounding boundary of E2M1 and
+// the eight are divided after all; so are they when rcp(den) overflows (den
+// below 2^-128: a tensor whose largest magnitude is below about 2^-117).
+__device__ __forceinline__ uint32_t e2m1x8_of_quotients(const float (&x)[8], float den, float rcp)
+{
+    float q[8], lo[8], hi[8];
+    if (!(rcp <= 3.4028234663852886e38f)) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(x[i], den);
+        return f32x8_to_e2m1x8(q);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        q[i] = __fmul_rn(x[i], rcp);
+        lo[i] = __fmul_rn(q[i], 1.0f - 0x1p-21f);
+        hi[i] = __fmul_rn(q[i], 1.0f + 0x1p-21f);
+    }
+    const uint32_t c = f32x8_to_e2m1x8(q);
+    if (f32x8_to_e2m1x8(lo) == c && f32x8_to_e2m1x8(hi) == c) return c;
+    float d[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) d[i] = __fdiv_rn(x[i], den);
+    return f32x8_to_e2m1x8(d);
+}
+
+// One block's codes (NC 32-bit words) and scale byte from its W bf16 pairs.
+template <int FMT, int W, int NC>
+__device__ __forceinline__ uint32_t quant_block(const uint32_t (&w)[W], float g, float d6, uint32_t (&c)[NC])
+{
+#pragma unroll
+    for (int i = 0; i < NC; ++i) c[i] = 0;
+    bool nonfinite;
+    const uint32_t amax = bf16_amax(w, nonfinite);
+    if (nonfinite) return FMT == FMT_NVFP4 ? 0x7Fu : 0xFFu;
+    if constexpr (FMT == FMT_NVFP4) {
+        const float t = __fdiv_rn(__uint_as_float(amax << 16), d6);
+        const uint32_t sbyte = f32x4_to_e4m3x4(t, 0.0f, 0.0f, 0.0f) & 0xFFu;
+        const float den = __fmul_rn(f16_lo_to_f32(e4m3x2_to_f16x2(sbyte)), g);  // s exactly, times g
+        if (den != 0.0f) {
+            const float rcp = __frcp_rn(den);
+#pragma unroll
+            for (int i = 0; i < NC; ++i) {
+                float v[8];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    v[2 * j] = bf16_lo(w[4 * i + j]);
+                    v[2 * j + 1] = bf16_hi(w[4 * i + j]);
+                }
+                c[i] = e2m1x8_plus_zero(e2m1x8_of_quotients(v, den, rcp));
+            }
+        }
+        return sbyte;
+    } else {
+        constexpr int EMAX = FMT == FMT_MXFP8 ? 8 : 2;
+        const int E = (int)(amax >> 7);  // bf16 exponent field of amax
+        const int e = E == 0 ? -127 : max(E - 127 - EMAX, -127);
+        const float mul = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e, a normal fp32
+        if constexpr (FMT == FMT_MXFP8) {
+#pragma unroll
+            for (int i = 0; i < NC; ++i)
+                c[i] = e4m3x4_plus_zero(f32x4_to_e4m3x4(bf16_lo(w[2 * i]) * mul, bf16_hi(w[2 * i]) * mul,
+                                                        bf16_lo(w[2 * i + 1]) * mul, bf16_hi(w[2 * i + 1]) * mul));
+        } else {
+#pragma unroll
+            for (int i = 0; i < NC; ++i) {
+                float v[8];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    v[2 * j] = bf16_lo(w[4 * i + j]) * mul;  // exact
+                    v[2 * j + 1] = bf16_hi(w[4 * i + j]) * mul;
+                }
+                c[i] = e2m1x8_plus_zero(f32x8_to_e2m1x8(v));
+            }
+        }
+        return (uint32_t)(e + 127);
+    }
+}
+
+// Each thread takes P consecutive blocks per step (P = 2 for NVFP4, so that
+// every thread, as for the MX formats, reads 64 contiguous bytes per step).
 template <int FMT>
 __global__ void quantize_kernel(const uint16_t *__restrict__ x, uint8_t *__restrict__ codes,
                                 uint8_t *__restrict__ scales, long long nblocks, const unsigned *gbits)
 {
-    constexpr int B = FMT == FMT_NVFP4 ? 16 : 32;  // elements per block
-    constexpr int W = B / 2;                          // bf16 pairs per block
+    constexpr int B = FMT == FMT_NVFP4 ? 16 : 32;          // elements per block
+    constexpr int W = B / 2;                                 // bf16 pairs per block
+    constexpr int NC = FMT == FMT_MXFP8 ? B / 4 : B / 8;     // 32-bit code words per block
+    constexpr int P = FMT == FMT_NVFP4 ? 2 : 1;              // blocks per thread and step
     pdl_trigger();
     pdl_wait();
     float g = 1.0f, d6 = 6.0f;
@@ -131,76 +246,41 @@ __global__ void quantize_kernel(const uint16_t *__restrict__ x, uint8_t *__restr
             p[3] = (uint8_t)(gb >> 24);
         }
     }
-    for (long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x; b < nblocks;
-         b += (long long)gridDim.x * blockDim.x) {
-        uint32_t w[W];
-        const uint4 *src = reinterpret_cast<const uint4 *>(x + b * B);
+    const long long nsteps = (nblocks + P - 1) / P;
+    for (long long st = blockIdx.x * (long long)blockDim.x + threadIdx.x; st < nsteps;
+         st += (long long)gridDim.x * blockDim.x) {
+        const long long b0 = st * P;
+        const int nb = nblocks - b0 < P ? (int)(nblocks - b0) : P;
+        uint32_t w[P][W];
 #pragma unroll
-        for (int i = 0; i < W / 4; ++i) {
-            const uint4 v = __ldcg(src + i);
-            w[4 * i] = v.x;
-            w[4 * i + 1] = v.y;
-            w[4 * i + 2] = v.z;
-            w[4 * i + 3] = v.w;
-        }
-        bool nonfinite;
-        const uint32_t amax = bf16_amax(w, nonfinite);
-        constexpr int NC = FMT == FMT_MXFP8 ? B / 4 : B / 8;  // 32-bit code words per block
-        uint32_t c[NC];
+        for (int p = 0; p < P; ++p) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(x + (b0 + p) * B);
 #pragma unroll
-        for (int i = 0; i < NC; ++i) c[i] = 0;
-        uint32_t sbyte;
-        if (nonfinite) {
-            sbyte = FMT == FMT_NVFP4 ? 0x7Fu : 0xFFu;
-        } else if constexpr (FMT == FMT_NVFP4) {
-            const float t = __fdiv_rn(__uint_as_float(amax << 16), d6);
-            sbyte = f32x4_to_e4m3x4(t, 0.0f, 0.0f, 0.0f) & 0xFFu;
-            const float den = __fmul_rn(f16_lo_to_f32(e4m3x2_to_f16x2(sbyte)), g);  // s exactly, times g
-            if (den != 0.0f) {
-#pragma unroll
-                for (int i = 0; i < NC; ++i) {
-                    float v[8];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        v[2 * j] = __fdiv_rn(bf16_lo(w[4 * i + j]), den);
-                        v[2 * j + 1] = __fdiv_rn(bf16_hi(w[4 * i + j]), den);
-                    }
-                    c[i] = e2m1x8_plus_zero(f32x8_to_e2m1x8(v));
-                }
-            }
-        } else {
-            constexpr int EMAX = FMT == FMT_MXFP8 ? 8 : 2;
-            const int E = (int)(amax >> 7);  // bf16 exponent field of amax
-            const int e = E == 0 ? -127 : max(E - 127 - EMAX, -127);
-            sbyte = (uint32_t)(e + 127);
-            const float mul = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e, a normal fp32
-            if constexpr (FMT == FMT_MXFP8) {
-#pragma unroll
-                for (int i = 0; i < NC; ++i)
-                    c[i] = e4m3x4_plus_zero(f32x4_to_e4m3x4(bf16_lo(w[2 * i]) * mul, bf16_hi(w[2 * i]) * mul,
-                                                            bf16_lo(w[2 * i + 1]) * mul, bf16_hi(w[2 * i + 1]) * mul));
-            } else {
-#pragma unroll
-                for (int i = 0; i < NC; ++i) {
-                    float v[8];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        v[2 * j] = bf16_lo(w[4 * i + j]) * mul;  // exact
-                        v[2 * j + 1] = bf16_hi(w[4 * i + j]) * mul;
-                    }
-                    c[i] = e2m1x8_plus_zero(f32x8_to_e2m1x8(v));
-                }
+            for (int i = 0; i < W / 4; ++i) {
+                const uint4 v = p < nb ? __ldcs(src + i) : make_uint4(0u, 0u, 0u, 0u);
+                w[p][4 * i] = v.x;
+                w[p][4 * i + 1] = v.y;
+                w[p][4 * i + 2] = v.z;
+                w[p][4 * i + 3] = v.w;
             }
         }
-        scales[b] = (uint8_t)sbyte;
+        uint32_t c[P][NC], sb[P];
+#pragma unroll
+        for (int p = 0; p < P; ++p) sb[p] = quant_block<FMT, W, NC>(w[p], g, d6, c[p]);
         if constexpr (FMT == FMT_MXFP8) {
-            uint4 *dst = reinterpret_cast<uint4 *>(codes + b * 32);
-            dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
-            dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
+            scales[b0] = (uint8_t)sb[0];
+            uint4 *dst = reinterpret_cast<uint4 *>(codes + b0 * 32);
+            dst[0] = make_uint4(c[0][0], c[0][1], c[0][2], c[0][3]);
+            dst[1] = make_uint4(c[0][4], c[0][5], c[0][6], c[0][7]);
         } else if constexpr (FMT == FMT_MXFP4) {
-            *reinterpret_cast<uint4 *>(codes + b * 16) = make_uint4(c[0], c[1], c[2], c[3]);
+            scales[b0] = (uint8_t)sb[0];
+            *reinterpret_cast<uint4 *>(codes + b0 * 16) = make_uint4(c[0][0], c[0][1], c[0][2], c[0][3]);
+        } else if (nb == 2) {
+            *reinterpret_cast<uint16_t *>(scales + b0) = (uint16_t)(sb[0] | (sb[1] << 8));
+            *reinterpret_cast<uint4 *>(codes + b0 * 8) = make_uint4(c[0][0], c[0][1], c[1][0], c[1][1]);
         } else {
-            *reinterpret_cast<uint2 *>(codes + b * 8) = make_uint2(c[0], c[1]);
+            scales[b0] = (uint8_t)sb[0];
+            *reinterpret_cast<uint2 *>(codes + b0 * 8) = make_uint2(c[0][0], c[0][1]);
         }
     }
 }
@@ -210,7 +290,8 @@ cudaError_t launch_quantize(const DeviceState &ds, cudaStream_t st, int fmt, con
 {
     const int B = fmt == FMT_NVFP4 ? 16 : 32;
     const long long nblocks = (long long)M * (K / B);
-    long long grid = (nblocks + 255) / 256;
+    const long long steps = fmt == FMT_NVFP4 ? (nblocks + 1) / 2 : nblocks;  // see quantize_kernel
+    long long grid = (steps + 255) / 256;
     const long long cap = (long long)ds.num_sms * 16;
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
@@ -220,10 +301,11 @@ cudaError_t launch_quantize(const DeviceState &ds, cudaStream_t st, int fmt, con
         cudaError_t e = cudaMemsetAsync(gbits, 0, sizeof(unsigned), st);
         if (e != cudaSuccess) return e;
         const long long n8 = (long long)M * K / 8;
-        long long g2 = (n8 + 255) / 256;
-        if (g2 > cap) g2 = cap;
+        long long g2 = (n8 + AMAX_THREADS * AMAX_UNROLL - 1) / (AMAX_THREADS * AMAX_UNROLL);
+        const long long cap2 = (long long)ds.num_sms * (2048 / AMAX_THREADS);  // one wave
+        if (g2 > cap2) g2 = cap2;
         if (g2 < 1) g2 = 1;
-        e = launch_k(quant_amax_kernel, dim3((unsigned)g2), dim3(256), 0, st, x, n8, gbits);
+        e = launch_k(quant_amax_kernel, dim3((unsigned)g2), dim3(AMAX_THREADS), 0, st, x, n8, gbits);
         if (e != cudaSuccess) return e;
         return launch_k(quantize_kernel<FMT_NVFP4>, dim3((unsigned)grid), dim3(256), 0, st, x, codes, scales,
                         nblocks, (const unsigned *)gbits);

@@ -111,3 +111,52 @@ def test_quantized_weights_feed_qmv(orc, fmt):
     x = synth.activations(M, K, 9)
     y = ops.qmv(fmt, c, s, dev_bf16(x).view(M, K), N).cpu().numpy()
     check_close(y, orc.qmv(fmt, wc, ws, x, M, N, K), f"qmv over quantised fmt{fmt}")
+
+
+def _bf16_up(bits, n):
+    """bf16 bit patterns n steps away from zero (positive finite values)."""
+    return (bits.astype(np.int64) + n).astype(np.uint16)
+
+
+def test_quantize_nvfp4_rounding_boundaries(orc):
+    """NVFP4 quotients x / (s g) that land exactly on E2M1 rounding midpoints
+    (ties to even) and one bf16 step either side of them: the tensor maximum
+    G = 2688 * 2^3 makes g = 8, each block's maximum 6 * g * 2^j makes
+    s = 2^j, so x = m * s * g is a bf16 value with an exact quotient m.  Also
+    a tensor whose maximum is below 2^-117, where 1 / (s g) overflows fp32.
+    Codes and scales bit for bit against the oracle."""
+    need_gpu()
+    K = 64
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32)
+    rows = []
+    for j in range(-3, 4):
+        d = np.float32(8.0 * 2.0 ** j)
+        r = np.zeros(K, np.float32)
+        for b in range(K // 16):  # every 16-element block: its maximum first, then the midpoints
+            blk = np.concatenate([[6.0 * d], mids * d, -mids * d, [0.0]]).astype(np.float32)
+            r[16 * b: 16 * b + 16] = blk[:16]
+        rows.append(r)
+    x = bf16_of(np.stack(rows))
+    # neighbours: every midpoint element moved one bf16 step up, and one down
+    up = x.copy()
+    dn = x.copy()
+    for t in range(x.shape[0]):
+        for b in range(K // 16):
+            sl = slice(16 * b + 1, 16 * b + 15)
+            up[t, sl] = _bf16_up(x[t, sl], 1)
+            dn[t, sl] = _bf16_up(x[t, sl], -1)
+    g_row = np.zeros((1, K), np.uint16)
+    g_row[0, 0] = bf16_of(np.array([[2688.0 * 8.0]], np.float32))[0, 0]  # the tensor maximum G
+    x = np.concatenate([x, up, dn, g_row])
+    M = x.shape[0]
+    c, s = gpu_quantize(2, x, M, K)
+    wc, ws = orc.quantize(2, x, M, K)
+    assert np.array_equal(s, ws), f"scales differ at {np.flatnonzero(s != ws)[:8]}"
+    assert np.array_equal(c, wc), f"codes differ at {np.flatnonzero(c != wc)[:8]}"
+    # a tiny tensor: s g below 2^-128
+    rng = np.random.default_rng(3)
+    t = (rng.standard_normal((4, K)) * 2.0 ** -125).astype(np.float32)
+    xt = bf16_of(t)
+    c, s = gpu_quantize(2, xt, 4, K)
+    wc, ws = orc.quantize(2, xt, 4, K)
+    assert np.array_equal(s, ws) and np.array_equal(c, wc)
