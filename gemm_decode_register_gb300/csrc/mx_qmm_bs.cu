@@ -243,11 +243,13 @@ struct BsGeo {
     // L2 while the MMAs work through the R - 1 slots ahead of it
     static constexpr int R = (512 - BN) / SLOT_COLS > 8 ? 8 : (512 - BN) / SLOT_COLS;
     static constexpr int TMEM_COLS = BN + R * SLOT_COLS <= 256 ? 256 : 512;
-    static constexpr int THREADS = 192;
+    // warps: 0 TMA, 1 MMA, 2-5 scale writers, 6-13 epilogue; at most four
+    // warps per scheduler, so 128 registers a thread fit each one's file
+    static constexpr int THREADS = 448;
     static constexpr int OFF_SC = S * STAGE;
     static constexpr int OFF_BAR = OFF_SC + ST * SC_STAGE;
     static constexpr int SMEM = 1024 + OFF_BAR + 512;
-    static_assert((2 * S + 2 * R + 2 * ST + 1) * 8 + 8 <= 512, "barrier area");
+    static_assert((2 * S + 2 * R + 2 * ST + 2) * 8 + 8 <= 512, "barrier area");
     static_assert(BN + R * SLOT_COLS <= 512, "tensor memory");
     static_assert(SMEM <= BS_SMEM_LIMIT, "shared memory");
     static_assert(S >= 2 && R >= 2, "pipeline depth");
@@ -270,7 +272,7 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v, int w)
 }
 
 template <int FMT, int BN>
-__global__ void __launch_bounds__(192, 1) qmm_bs_kernel(const __grid_constant__ CUtensorMap tmap_x,
+__global__ void __maxnreg__(128) qmm_bs_kernel(const __grid_constant__ CUtensorMap tmap_x,
                                                         const __grid_constant__ CUtensorMap tmap_w,
                                                         const __grid_constant__ CUtensorMap tmap_xs,
                                                         const __grid_constant__ CUtensorMap tmap_ws, BsArgs a)
@@ -288,14 +290,21 @@ __global__ void __launch_bounds__(192, 1) qmm_bs_kernel(const __grid_constant__ 
     uint64_t *sf_empty = sf_full + R;   // [R] the MMAs that read the slot finished
     uint64_t *sc_full = sf_full + 2 * R;  // [ST] a scale stage landed (TMA bytes)
     uint64_t *sc_empty = sc_full + ST;    // [ST] the 4 scale warps read it
-    uint64_t *acc_full = sc_full + 2 * ST;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 1);
+    uint64_t *acc_full = sc_full + 2 * ST;  // the MMAs of a tile completed
+    uint64_t *acc_empty = acc_full + 1;     // the 8 epilogue warps read the accumulator
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m_tiles = (a.M + 127) / 128;
-    const int m0 = (blockIdx.x % m_tiles) * 128, n0 = (blockIdx.x / m_tiles) * BN;
+    const int tiles = m_tiles * (a.N / BN);
     const int KB = a.K / F::KB_ELEMS;
+    const int nsc = (KB + SG - 1) / SG;  // scale stages per tile
+    // this CTA's tiles: blockIdx.x, blockIdx.x + gridDim.x, ... (consecutive
+    // tiles share a W column block, read by neighbouring CTAs at once)
+    const int my_tiles = (int)blockIdx.x < tiles ? (tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    auto tile_m0 = [&](int i) { return ((int)blockIdx.x + i * (int)gridDim.x) % m_tiles * 128; };
+    auto tile_n0 = [&](int i) { return ((int)blockIdx.x + i * (int)gridDim.x) / m_tiles * BN; };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -311,6 +320,7 @@ __global__ void __launch_bounds__(192, 1) qmm_bs_kernel(const __grid_constant__ 
             mbar_init(&sc_empty[u], 4);
         }
         mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 8);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -329,140 +339,183 @@ __global__ void __launch_bounds__(192, 1) qmm_bs_kernel(const __grid_constant__ 
     pdl_wait();  // the activations (and their scales) come from the previous kernel
 
     if (warp == 0) {
-        // ---------------- codes and scales producer
+        // ---------------- codes and scales producer, across the CTA's tiles
         if (lane == 0) {
-            int issued = 0, sissued = 0;
-            for (int kb = 0; kb < KB; ++kb) {
-                const int s = kb % S;
-                if (kb % SG == 0) {
-                    // the scale stage of k-blocks kb .. kb + SG - 1
-                    const int t = kb / SG, u = t % ST;
-                    if (t >= ST && !mbar_wait(&sc_empty[u], ((t / ST) - 1) & 1, abort_flag, a.wait_ns)) break;
-                    uint8_t *sc = scs + u * G::SC_STAGE;
-                    mbar_arrive_expect_tx(&sc_full[u], (uint32_t)G::SC_STAGE);
-                    tma_load_2d(sc, &tmap_xs, 16 * t, m0, &sc_full[u]);
-                    tma_load_2d(sc + 128 * 16, &tmap_ws, 16 * t, n0, &sc_full[u]);
-                    sissued = t + 1;
+            int issued = 0, sissued = 0;  // k-blocks and scale stages issued, counted over tiles
+            bool go = true;
+            for (int i = 0; i < my_tiles && go; ++i) {
+                const int m0 = tile_m0(i), n0 = tile_n0(i);
+                for (int kb = 0; kb < KB; ++kb) {
+                    const int g = i * KB + kb, s = g % S;
+                    if (kb % SG == 0) {
+                        // the scale stage of k-blocks kb .. kb + SG - 1
+                        const int t = i * nsc + kb / SG, u = t % ST;
+                        if (t >= ST && !mbar_wait(&sc_empty[u], ((t / ST) - 1) & 1, abort_flag, a.wait_ns)) {
+                            go = false;
+                            break;
+                        }
+                        uint8_t *sc = scs + u * G::SC_STAGE;
+                        mbar_arrive_expect_tx(&sc_full[u], (uint32_t)G::SC_STAGE);
+                        tma_load_2d(sc, &tmap_xs, 16 * (kb / SG), m0, &sc_full[u]);
+                        tma_load_2d(sc + 128 * 16, &tmap_ws, 16 * (kb / SG), n0, &sc_full[u]);
+                        sissued = t + 1;
+                    }
+                    if (g >= S && !mbar_wait(&empty[s], ((g / S) - 1) & 1, abort_flag, a.wait_ns)) {
+                        go = false;
+                        break;
+                    }
+                    uint8_t *st = smem + s * G::STAGE;
+                    mbar_arrive_expect_tx(&full[s], (uint32_t)G::STAGE);
+                    tma_load_2d(st, &tmap_x, kb * BS_KB_BYTES, m0, &full[s]);
+                    tma_load_2d(st + G::A_BYTES, &tmap_w, kb * BS_KB_BYTES, n0, &full[s]);
+                    issued = g + 1;
                 }
-                if (kb >= S && !mbar_wait(&empty[s], ((kb / S) - 1) & 1, abort_flag, a.wait_ns)) break;
-                uint8_t *st = smem + s * G::STAGE;
-                mbar_arrive_expect_tx(&full[s], (uint32_t)G::STAGE);
-                tma_load_2d(st, &tmap_x, kb * BS_KB_BYTES, m0, &full[s]);
-                tma_load_2d(st + G::A_BYTES, &tmap_w, kb * BS_KB_BYTES, n0, &full[s]);
-                issued = kb + 1;
             }
             // every issued load must land before the CTA may exit
-            for (int kb = (issued > S ? issued - S : 0); kb < issued; ++kb)
-                mbar_wait(&full[kb % S], (kb / S) & 1, abort_flag, BS_WAIT_NS, false);
+            for (int g = (issued > S ? issued - S : 0); g < issued; ++g)
+                mbar_wait(&full[g % S], (g / S) & 1, abort_flag, BS_WAIT_NS, false);
             for (int t = (sissued > ST ? sissued - ST : 0); t < sissued; ++t)
                 mbar_wait(&sc_full[t % ST], (t / ST) & 1, abort_flag, BS_WAIT_NS, false);
         }
     } else if (warp == 1) {
-        // ---------------- MMA issuer
+        // ---------------- MMA issuer: a tile's k-blocks into the accumulator once
+        // the epilogue has read the previous tile out of it
         if (lane == 0) {
-            for (int kb = 0; kb < KB; ++kb) {
-                const int s = kb % S, r = kb % R;
-                if (!mbar_wait(&full[s], (kb / S) & 1, abort_flag, a.wait_ns)) break;
-                if (!mbar_wait(&sf_full[r], (kb / R) & 1, abort_flag, a.wait_ns)) break;
-                tc_fence_after();
-                const uint32_t sa = smem_u32(smem + s * G::STAGE), sb = sa + G::A_BYTES;
-                const uint32_t sfa = tmem + sf_col0 + (uint32_t)(r * G::SLOT_COLS);
-                const uint32_t sfb = sfa + (uint32_t)(4 * CH);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    // the scale chunk and byte of MMA kk: MXFP8 one 32-element block
-                    // (chunk 0, byte kk); MXFP4 two (chunk kk / 2, bytes 2 (kk % 2)
-                    // and up); NVFP4 four 16-element blocks (chunk kk, byte 0)
-                    const int c = FMT == FMT_MXFP8 ? 0 : FMT == FMT_MXFP4 ? kk >> 1 : kk;
-                    const uint32_t id = FMT == FMT_MXFP8 ? (uint32_t)kk : FMT == FMT_MXFP4 ? 2u * (kk & 1) : 0u;
-                    const uint32_t idesc = bs_idesc<F::KIND>(BN, id, id);
-                    umma1<F::KIND>(tmem, sw128_desc(sa + 32 * kk), sw128_desc(sb + 32 * kk), idesc,
-                                   sfa + (uint32_t)(4 * c), sfb + (uint32_t)(4 * c * RB), (kb | kk) != 0);
+            bool go = true;
+            for (int i = 0; i < my_tiles && go; ++i) {
+                if (i > 0 && !mbar_wait(acc_empty, (i - 1) & 1, abort_flag, a.wait_ns)) {
+                    go = false;
+                    break;
                 }
-                umma1_commit(&empty[s]);
-                umma1_commit(&sf_empty[r]);
+                for (int kb = 0; kb < KB; ++kb) {
+                    const int g = i * KB + kb, s = g % S, r = g % R;
+                    if (!mbar_wait(&full[s], (g / S) & 1, abort_flag, a.wait_ns) ||
+                        !mbar_wait(&sf_full[r], (g / R) & 1, abort_flag, a.wait_ns)) {
+                        go = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + s * G::STAGE), sb = sa + G::A_BYTES;
+                    const uint32_t sfa = tmem + sf_col0 + (uint32_t)(r * G::SLOT_COLS);
+                    const uint32_t sfb = sfa + (uint32_t)(4 * CH);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        // the scale chunk and byte of MMA kk: MXFP8 one 32-element block
+                        // (chunk 0, byte kk); MXFP4 two (chunk kk / 2, bytes 2 (kk % 2)
+                        // and up); NVFP4 four 16-element blocks (chunk kk, byte 0)
+                        const int c = FMT == FMT_MXFP8 ? 0 : FMT == FMT_MXFP4 ? kk >> 1 : kk;
+                        const uint32_t id = FMT == FMT_MXFP8 ? (uint32_t)kk : FMT == FMT_MXFP4 ? 2u * (kk & 1) : 0u;
+                        const uint32_t idesc = bs_idesc<F::KIND>(BN, id, id);
+                        umma1<F::KIND>(tmem, sw128_desc(sa + 32 * kk), sw128_desc(sb + 32 * kk), idesc,
+                                       sfa + (uint32_t)(4 * c), sfb + (uint32_t)(4 * c * RB), (kb | kk) != 0);
+                    }
+                    umma1_commit(&empty[s]);
+                    umma1_commit(&sf_empty[r]);
+                }
+                if (go) umma1_commit(acc_full);  // fires once the tile's MMAs have completed
             }
-            umma1_commit(acc_full);  // fires once every MMA issued so far has completed
+            // after giving up: let the epilogue see the MMAs issued so far
+            // complete (it writes NaN) before the tensor memory is released
+            if (!go) umma1_commit(acc_full);
         }
-    } else {
+    } else if (warp < 6) {
         // ---------------- scale writers (warps 2-5: lane quarter q = warp % 4)
         const int q = warp & 3;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-        const int nstage = (KB + SG - 1) / SG;
         bool go = true;
-        for (int t = 0; t < nstage && go; ++t) {
-            const int u = t % ST;
-            int ok = 1;
-            if (lane == 0) ok = mbar_wait(&sc_full[u], (t / ST) & 1, abort_flag, a.wait_ns);
-            if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
-            // X row 32 q + lane; W rows 128 j + 32 i + lane (the same in every warp)
-            const uint8_t *sc = scs + u * G::SC_STAGE;
-            const uint4 xv = *reinterpret_cast<const uint4 *>(sc + 16 * (32 * q + lane));
-            uint4 wv[RB][4];
-#pragma unroll
-            for (int j = 0; j < RB; ++j)
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    wv[j][i] = *reinterpret_cast<const uint4 *>(sc + 16 * (128 + 128 * j + 32 * i + lane));
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sc_empty[u]);
-#pragma unroll
-            for (int jj = 0; jj < SG; ++jj) {
-                const int kb = t * SG + jj;
-                if (kb >= KB) break;
-                const int r = kb % R;
-                if (lane == 0 && kb >= R) ok = mbar_wait(&sf_empty[r], ((kb / R) - 1) & 1, abort_flag, a.wait_ns);
+        for (int i = 0; i < my_tiles && go; ++i) {
+            for (int tl = 0; tl < nsc && go; ++tl) {
+                const int t = i * nsc + tl, u = t % ST;
+                int ok = 1;
+                if (lane == 0) ok = mbar_wait(&sc_full[u], (t / ST) & 1, abort_flag, a.wait_ns);
                 if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
                     go = false;
                     break;
                 }
-                tc_fence_after();
-                const uint32_t base = tmem + lane_base + sf_col0 + (uint32_t)(r * G::SLOT_COLS);
+                // X row 32 q + lane; W rows 128 j + 32 i + lane (the same in every warp)
+                const uint8_t *sc = scs + u * G::SC_STAGE;
+                const uint4 xv = *reinterpret_cast<const uint4 *>(sc + 16 * (32 * q + lane));
+                uint4 wv[RB][4];
 #pragma unroll
-                for (int c = 0; c < CH; ++c) {
-                    const int w = jj * CH + c;  // word of the 16 bytes
-                    tmem_st_x4(base + (uint32_t)(4 * c), word_of(xv, w));
+                for (int j = 0; j < RB; ++j)
 #pragma unroll
-                    for (int j = 0; j < RB; ++j)
-                        tmem_st_x4v(base + (uint32_t)(4 * CH + 4 * (c * RB + j)), word_of(wv[j][0], w),
-                                    word_of(wv[j][1], w), word_of(wv[j][2], w), word_of(wv[j][3], w));
-                }
-                tmem_wait_st();
-                tc_fence_before();
+                    for (int ii = 0; ii < 4; ++ii)
+                        wv[j][ii] = *reinterpret_cast<const uint4 *>(sc + 16 * (128 + 128 * j + 32 * ii + lane));
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&sf_full[r]);
+                if (lane == 0) mbar_arrive(&sc_empty[u]);
+#pragma unroll
+                for (int jj = 0; jj < SG; ++jj) {
+                    const int kb = tl * SG + jj;
+                    if (kb >= KB) break;
+                    const int g = i * KB + kb, r = g % R;
+                    if (lane == 0 && g >= R) ok = mbar_wait(&sf_empty[r], ((g / R) - 1) & 1, abort_flag, a.wait_ns);
+                    if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
+                        go = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t base = tmem + lane_base + sf_col0 + (uint32_t)(r * G::SLOT_COLS);
+#pragma unroll
+                    for (int c = 0; c < CH; ++c) {
+                        const int w = jj * CH + c;  // word of the 16 bytes
+                        tmem_st_x4(base + (uint32_t)(4 * c), word_of(xv, w));
+#pragma unroll
+                        for (int j = 0; j < RB; ++j)
+                            tmem_st_x4v(base + (uint32_t)(4 * CH + 4 * (c * RB + j)), word_of(wv[j][0], w),
+                                        word_of(wv[j][1], w), word_of(wv[j][2], w), word_of(wv[j][3], w));
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sf_full[r]);
+                }
             }
         }
-    }
-
-    // ---------------- epilogue (warps 2-5)
-    if (warp >= 2) {
-        const int q = warp & 3;
-        const bool ok = mbar_wait(acc_full, 0, abort_flag, BS_WAIT_NS, false) && !*abort_flag;
-        tc_fence_after();
+    } else {
+        // ---------------- epilogue (warps 6-13: lane quarter q = warp % 4,
+        // column half h): the warp's half tile row is read out of tensor
+        // memory into registers (bf16) and the accumulator handed back
+        // before the stores, so the next tile's MMAs overlap them
+        const int q = warp & 3, h = (warp - 6) >> 2;
+        constexpr int HC = BN / 2;  // columns per warp
         float g = 1.0f;
         if (FMT == FMT_NVFP4) {
             g = load_f32_unaligned(a.scales + (size_t)a.N * (a.K / 16));
             g = __fmul_rn(g, load_f32_unaligned(a.xscales + (size_t)a.M * (a.K / 16)));
         }
-        const int row = m0 + 32 * q + lane;
-        for (int c = 0; c < BN; c += 32) {
-            uint32_t v[32];
-            tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c, v);
-            uint32_t o[16];
+        bool live = true;
+        for (int i = 0; i < my_tiles; ++i) {
+            const int row = tile_m0(i) + 32 * q + lane, n0 = tile_n0(i) + h * HC;
+            if (live) live = mbar_wait(acc_full, i & 1, abort_flag, BS_WAIT_NS, false) && !*abort_flag;
+            uint32_t o[HC / 2];
+            if (live) {
+                tc_fence_after();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                float lo = __uint_as_float(v[2 * j]), hi = __uint_as_float(v[2 * j + 1]);
-                if (FMT == FMT_NVFP4) {
-                    lo = __fmul_rn(lo, g);
-                    hi = __fmul_rn(hi, g);
+                for (int c = 0; c < HC / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(h * HC + 32 * c), v);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        float lo = __uint_as_float(v[2 * j]), hi = __uint_as_float(v[2 * j + 1]);
+                        if (FMT == FMT_NVFP4) {
+                            lo = __fmul_rn(lo, g);
+                            hi = __fmul_rn(hi, g);
+                        }
+                        o[16 * c + j] = f32x2_to_bf16x2(lo, hi);
+                    }
                 }
-                o[j] = ok ? f32x2_to_bf16x2(lo, hi) : 0x7FC07FC0u;
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty);
+            } else {
+#pragma unroll
+                for (int j = 0; j < HC / 2; ++j) o[j] = 0x7FC07FC0u;  // a call that gave up writes NaN
             }
             if (row < a.M) {
-                uint4 *dst = reinterpret_cast<uint4 *>(a.Y + (size_t)row * a.N + n0 + c);
+                uint4 *dst = reinterpret_cast<uint4 *>(a.Y + (size_t)row * a.N + n0);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) dst[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+                for (int j = 0; j < HC / 8; ++j)
+                    dst[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
             }
         }
     }
@@ -539,8 +592,10 @@ static cudaError_t run_qmm_bs(const DeviceState &ds, cudaStream_t st, const uint
     a.N = N;
     a.K = K;
     a.wait_ns = BS_WAIT_NS;
+    // persistent CTAs, one per SM, each taking every num_sms-th tile
     const int tiles = ((M + 127) / 128) * (N / BN);
-    return launch_k(qmm_bs_kernel<FMT, BN>, dim3(tiles), dim3(G::THREADS), (size_t)G::SMEM, st, xmap, wmap, xsmap,
+    const int ctas = tiles < ds.num_sms ? tiles : ds.num_sms;
+    return launch_k(qmm_bs_kernel<FMT, BN>, dim3(ctas), dim3(G::THREADS), (size_t)G::SMEM, st, xmap, wmap, xsmap,
                     wsmap, a);
 }
 
