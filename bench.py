@@ -55,7 +55,8 @@ def peaks():
 
 
 QMV_SOURCES = ["gemm_decode_register_gb300/csrc/mx_qmv_stream.cu", "gemm_decode_register_gb300/csrc/mx_qmv_core.cuh",
-               "gemm_decode_register_gb300/csrc/mx_common.cuh", "gemm_decode_register_gb300/csrc/mx_internal.h"]
+               "gemm_decode_register_gb300/csrc/mx_common.cuh", "gemm_decode_register_gb300/csrc/mx_internal.h",
+               "gemm_decode_register_gb300/csrc/mx_stream.cuh"]
 TRAFFIC_PROFILE = "profiles/qmv_decode_layer_traffic.md"
 
 
