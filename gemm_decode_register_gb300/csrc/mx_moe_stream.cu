@@ -27,6 +27,8 @@ struct MoeSArgs {
     int T, E, topk, N, K;
     int I;              // gate-up: intermediate size (N = 2 I weight rows per expert)
     int ks;
+    int lc;             // down-combine: partials summed in shared memory (1) or through ws (0)
+    int ntile_max;      // down-combine, lc: row tiles per CTA at most
 };
 
 template <int MODE>
@@ -83,15 +85,36 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) moe_stream_kernel(MoeSArgs a)
     const int items = nwg * tiles;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gw = blockIdx.x * QMV_WARPS + warp, stride = gridDim.x * QMV_WARPS;
-    const int n_my = gw < items ? (items - gw + stride - 1) / stride : 0;
+    // Work items (work group w, row tile): dealt over every warp of the grid;
+    // or, with the CTA-local combine of the down projection, every group of
+    // this CTA's tiles (blockIdx.x, + gridDim.x, ...) over this CTA's warps,
+    // so that a tile's partial sums meet in shared memory.
+    const bool lc = MODE == MOE_DOWN_COMBINE && a.lc;
+    const int ntile_c = (int)blockIdx.x < tiles ? (tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int n_local = ntile_c * nwg;
+    const int n_my = lc ? (warp < n_local ? (n_local - warp + QMV_WARPS - 1) / QMV_WARPS : 0)
+                        : (gw < items ? (items - gw + stride - 1) / stride : 0);
+    auto item_at = [&](int i, int &w, int &tile, int &ti) {
+        if (lc) {
+            const int j = warp + QMV_WARPS * i;
+            ti = j / nwg;
+            w = j - ti * nwg;
+            tile = (int)blockIdx.x + ti * (int)gridDim.x;
+        } else {
+            const int item = gw + stride * i;
+            w = item / tiles;
+            tile = item - w * tiles;
+            ti = 0;
+        }
+    };
     const int RB = FMT == FMT_MXFP8 ? a.K : a.K / 2;
     const int KS = FMT == FMT_NVFP4 ? a.K / 16 : a.K / 32;
     const int U = (a.K + 31) / 32;
     const int tok = lane_token<MC>();
 
     auto next = [&](int i) {
-        const int item = gw + stride * i;
-        const int w = item / tiles, tile = item - w * tiles;
+        int w, tile, ti;
+        item_at(i, w, tile, ti);
         const int e = wg_e[w];
         SUnit u;
         u.codes = a.codes + (size_t)e * R * RB;
@@ -112,12 +135,14 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) moe_stream_kernel(MoeSArgs a)
     // staged activation row of a work-group member
     auto xrow_of_slot = [&](int slot) { return MODE == MOE_DOWN_COMBINE ? slot : slot / a.topk; };
     auto xrow_of = [&](int i) {
-        const int w = (gw + stride * i) / tiles;
+        int w, tile, ti;
+        item_at(i, w, tile, ti);
         return tok < wg_mc[w] ? xrow_of_slot(sorted[wg_first[w] + tok]) : -1;
     };
+    float *part = reinterpret_cast<float *>(rings + (size_t)QMV_WARPS * S * G::STAGE_BYTES);  // lc: [ntile][P][RT]
     auto done = [&](int i, const float (&acc)[2][2]) {
-        const int item = gw + stride * i;
-        const int w = item / tiles, tile = item - w * tiles;
+        int w, tile, ti;
+        item_at(i, w, tile, ti);
         float g = 1.0f;
         if (FMT == FMT_NVFP4)
             g = load_f32_unaligned(a.scales + (size_t)a.E * R * KS + 4 * (size_t)wg_e[w]);
@@ -149,6 +174,7 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) moe_stream_kernel(MoeSArgs a)
                     float sv = v * pow2f(sh_final<FMT>(sh[xrow_of_slot(slot)]));
                     if (FMT == FMT_NVFP4) sv *= g;
                     if (MODE == MOE_PLAIN) a.y[(size_t)slot * a.N + row] = sv;
+                    else if (lc) part[((size_t)ti * P + slot) * G::RT + r] = sv;
                     else a.ws[(size_t)slot * a.N + row] = sv;
                 }
             }
@@ -188,6 +214,7 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) moe_stream_kernel(MoeSArgs a)
                             float s = vv[h][c] * pow2f(sh_final<FMT>(sh[xrow_of_slot(slot)]));
                             if (FMT == FMT_NVFP4) s *= g;
                             if (MODE == MOE_PLAIN) a.y[(size_t)slot * a.N + row] = s;
+                            else if (lc) part[((size_t)ti * P + slot) * G::RT + r] = s;
                             else a.ws[(size_t)slot * a.N + row] = s;
                         }
                     }
@@ -215,7 +242,8 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) moe_stream_kernel(MoeSArgs a)
     bool fold = false;
     for (int r = 0; r < XR; ++r) fold |= sh_fold<FMT>(sh[r]) < 0;
     auto fold_of = [&](int i, float (&f)[2]) {
-        const int w = (gw + stride * i) / tiles;
+        int w, tile, ti;
+        item_at(i, w, tile, ti);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
             const int t = acc_token<MC>(c);
@@ -227,7 +255,25 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) moe_stream_kernel(MoeSArgs a)
     else
         st.template run<false>(xrow_of, done, fold_of, ring, xs, a.ks, 0);
 
-    if constexpr (MODE == MOE_DOWN_COMBINE) {
+    if (MODE == MOE_DOWN_COMBINE && lc) {
+        // The CTA's tiles: each slot's partials sit in shared memory; sum them
+        // in slot order, weighted by the router (a slot routed nowhere is NaN).
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < ntile_c * a.T * G::RT; idx += blockDim.x) {
+            const int ti = idx / (a.T * G::RT), rem = idx - ti * (a.T * G::RT);
+            const int t = rem / G::RT, r = rem - t * G::RT;
+            const int row = ((int)blockIdx.x + ti * (int)gridDim.x) * G::RT + r;
+            if (row >= a.N) continue;
+            float s = 0.f;
+            for (int j = 0; j < a.topk; ++j) {
+                const int p = t * a.topk + j;
+                const int e = a.ids[p];
+                const float v = (e >= 0 && e < a.E) ? part[((size_t)ti * P + p) * G::RT + r] : __int_as_float(0x7FC00000);
+                s = fmaf(a.rw[p], v, s);
+            }
+            a.out[(size_t)t * a.N + row] = s;
+        }
+    } else if constexpr (MODE == MOE_DOWN_COMBINE) {
         // Each tile gets one unit per work group.  The warp that completes a
         // tile's last unit sums the slots' partials in slot order, weighted
         // by the router, and re-arms the tile's counter.
@@ -275,19 +321,30 @@ static cudaError_t launch_moe_stream(const DeviceState &ds, cudaStream_t st, con
 constexpr int MOE_DEEP = 5;
 
 template <int FMT, int MC, int MODE>
-static cudaError_t run_moe_stream(const DeviceState &ds, cudaStream_t st, const MoeSArgs &a)
+static cudaError_t run_moe_stream(const DeviceState &ds, cudaStream_t st, const MoeSArgs &a0)
 {
     using G = SGeo<FMT, MC>;
+    MoeSArgs a = a0;
     const int P = a.T * a.topk;
     const int XR = moe_xrows<MODE>(a.T, a.topk);
     const size_t head = (((size_t)(3 * a.E + 4 * P + 40 + 2 * XR) * 4) + 15) & ~(size_t)15;
     const size_t base = head + (size_t)XR * a.ks * 2;
-    if constexpr (MC == 4) {
-        const size_t deep = base + (size_t)QMV_WARPS * MOE_DEEP * G::STAGE_BYTES;
-        if (deep <= (size_t)ds.max_smem_optin) return launch_moe_stream<FMT, MC, MODE, MOE_DEEP>(ds, st, a, deep);
+    const size_t lim = (size_t)ds.max_smem_optin;
+    // down projection: the CTA-local combine when its partials fit next to the ring
+    size_t part = 0;
+    if (MODE == MOE_DOWN_COMBINE) {
+        const int tiles = (a.N + G::RT - 1) / G::RT;
+        a.ntile_max = (tiles + ds.num_sms - 1) / ds.num_sms;
+        part = (((size_t)a.ntile_max * P * G::RT * 4) + 15) & ~(size_t)15;
+        a.lc = base + (size_t)QMV_WARPS * G::STAGES * G::STAGE_BYTES + part <= lim;
+        if (!a.lc) part = 0;
     }
-    const size_t smem = base + (size_t)QMV_WARPS * G::STAGES * G::STAGE_BYTES;
-    if (smem > (size_t)ds.max_smem_optin) return cudaErrorNotSupported;
+    if constexpr (MC == 4) {
+        const size_t deep = base + (size_t)QMV_WARPS * MOE_DEEP * G::STAGE_BYTES + part;
+        if (deep <= lim) return launch_moe_stream<FMT, MC, MODE, MOE_DEEP>(ds, st, a, deep);
+    }
+    const size_t smem = base + (size_t)QMV_WARPS * G::STAGES * G::STAGE_BYTES + part;
+    if (smem > lim) return cudaErrorNotSupported;
     return launch_moe_stream<FMT, MC, MODE, G::STAGES>(ds, st, a, smem);
 }
 
