@@ -138,9 +138,11 @@ int mx_moe_gate_up_swiglu(int fmt, const void *expert_codes, const void *expert_
  * multiply-adds (as mx_moe_combine).  Expert weights [N][K]; h bf16
  * [T*topk][K] (mx_moe_gate_up_swiglu's output, K = I); r fp32 [T][topk];
  * out fp32 [T][N].  Slots that share an expert are served by one pass over
- * its weights; the per-slot partial sums go through the library's device
- * workspace slot of the calling stream (T*topk*N <= 4 Mi floats), whose
- * counters are re-armed by the call itself.  A bad id sets MX_DEVERR_BAD_EXPERT and makes that token's
+ * its weights; the per-slot partial sums of a row tile meet in the shared
+ * memory of the CTA that takes all of that tile's work groups when they fit
+ * there, else they go through the library's device workspace slot of the
+ * calling stream (T*topk*N <= 4 Mi floats, counters re-armed by the call
+ * itself); either way the sum runs in slot order.  A bad id sets MX_DEVERR_BAD_EXPERT and makes that token's
  * outputs NaN.  When K is not a multiple of 128 the per-slot products come
  * from the direct-load MoE kernel, then the router combine (two launches).
  * h, out, codes, scales 16-byte aligned,
