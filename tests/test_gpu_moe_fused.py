@@ -113,6 +113,28 @@ def test_down_combine_ragged(orc, fmt, T, E, topk, N, K):
     check_close(out, want, f"down combine fmt{fmt}")
 
 
+def test_down_combine_workspace_path(orc):
+    """Row tiles whose partial sums do not fit in a CTA's shared memory next
+    to its ring (8 tokens x top-8, 57344 rows: 24 tiles of 16 rows per CTA)
+    take the device-workspace combine instead of the CTA-local one; the sum
+    is the same slot-order one."""
+    need_gpu()
+    fmt, E, topk, T, N, K = 0, 8, 8, 8, 57344, 128
+    codes, scales = synth.weights(fmt, N, K, 41, E=E)
+    h = synth.activations(T * topk, K, 42)
+    ids = synth.expert_ids(T, E, topk, 43)
+    r = synth.router_weights(T, topk, 44)
+    out = fused_down(fmt, codes, scales, h, ids, r, E, N).cpu().numpy()
+    # the oracle on 512 sampled rows (tile edges, the last tile, random rows) of every expert
+    rng = np.random.default_rng(45)
+    rows = np.unique(np.concatenate([np.arange(0, 40), np.arange(N - 40, N), rng.integers(0, N, 432)]))
+    rb, sb = K // 2, K // 32
+    sub_c = codes.reshape(E, N, rb)[:, rows].reshape(-1)
+    sub_s = scales.reshape(E, N, sb)[:, rows].reshape(-1)
+    want = oracle_out(orc, fmt, sub_c, sub_s, h, ids, r, T, E, topk, rows.size, K)
+    check_close(out[:, rows], want, "down combine through the workspace")
+
+
 def test_down_combine_deterministic():
     """The partial sums are combined in slot order by whichever warp closes a
     tile: repeated calls give the same bits."""
@@ -202,3 +224,4 @@ def test_fused_k_not_multiple_of_128(orc, fmt, K):
     r = synth.router_weights(T, topk, 52)
     out = fused_down(fmt, c2, s2, h, ids, r, E, N).cpu().numpy()
     check_close(out, oracle_out(orc, fmt, c2, s2, h, ids, r, T, E, topk, N, K), f"down-combine K{K} fmt{fmt}")
+
