@@ -74,22 +74,27 @@ __host__ __device__ inline int stage_stride(int K)
 // those below 2^-24 times it become zero.  Infinities and NaNs do not set
 // the scale and stay infinities and NaNs.  Elements past len up to the next
 // 32-element unit are zero.
+// len and ld are multiples of 8 and x is 16-byte aligned (K is a multiple
+// of the block), so every 8-element chunk is one aligned 16-byte load that
+// lies wholly inside or wholly past len.
 // When the rows fit in registers (<= 8 chunks of 8 elements per thread)
-// global memory is read once; otherwise twice.
+// global memory is read once and the chunks stay in registers; otherwise the
+// raw bf16 chunks are parked in xs and converted there in place.
 constexpr int STAGE_REG_CHUNKS = 8;
 
-__device__ __forceinline__ void stage_store(uint16_t *xs, int ks, int r, int k0, int len, uint4 v, float f,
-                                            int fmt)
+// Elements k0 .. k0+7 (k0 a multiple of 8) of staged row `row` (xs + r*ks),
+// scaled by f and rounded to f16; zero when the chunk lies past len.
+__device__ __forceinline__ void stage_store(uint16_t *row, int k0, int len, uint4 v, float f, int fmt)
 {
-    // elements k0 .. k0+7 of row r (k0 a multiple of 8), zero past len
-    const int u = k0 >> 5, p0 = k0 & 31;
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t out[4];
+    const int p0 = k0 & 31;
+    uint32_t out[4] = {0u, 0u, 0u, 0u};
+    if (k0 < len) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-        out[j] = k0 + 2 * j < len ? f32x2_to_f16x2(bf16_to_f32(w[j] & 0xFFFFu) * f, bf16_to_f32(w[j] >> 16) * f)
-                                  : 0u;
-    uint16_t *row = xs + (size_t)r * ks + u * 32;
+        for (int j = 0; j < 4; ++j)
+            out[j] = f32x2_to_f16x2(__uint_as_float(w[j] << 16) * f, __uint_as_float(w[j] & 0xFFFF0000u) * f);
+    }
+    row += k0 - p0;
     if (fmt == FMT_NVFP4) {
         // slots of elements p0, p0+2 are adjacent, and those of p0+4, p0+6
         const int s0 = 8 * ((p0 & 15) >> 2) + 4 * (p0 >> 4);
@@ -108,9 +113,78 @@ __device__ __forceinline__ unsigned fin_mag(uint32_t h)
     return h >= 0x7F80u ? 0u : h;
 }
 
+// Running per-half maximum of bf16 magnitudes: |m| = max(|m|, |w|) in each
+// half (the sign bits are meaningless; mask them off at the end).  A NaN
+// operand loses to the other one, so NaNs never enter; an infinity does.
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t m, uint32_t w)
+{
+    uint32_t d;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(m), "r"(w));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t absmax_chunk(uint32_t m, uint4 v)
+{
+    return absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(m, v.x), v.y), v.z), v.w);
+}
+
+// Largest finite magnitude (bf16 bits) of the 8 elements of a chunk,
+// element by element (the path taken when an infinity was seen).
+__device__ __forceinline__ unsigned chunk_mag_exact(uint4 v)
+{
+    unsigned m = max(max(fin_mag(v.x), fin_mag(v.x >> 16)), max(fin_mag(v.y), fin_mag(v.y >> 16)));
+    return max(m, max(max(fin_mag(v.z), fin_mag(v.z >> 16)), max(fin_mag(v.w), fin_mag(v.w >> 16))));
+}
+
 struct NoMid {
     __device__ void operator()() const {}
 };
+
+// Per-row maxima (bf16 magnitude bits) -> power-of-two exponents sh[r].
+__device__ __forceinline__ void stage_shifts(int nrows, int *sh, const unsigned *maxbits)
+{
+    for (int r = threadIdx.x; r < nrows; r += blockDim.x) {
+        unsigned mb = maxbits[r];
+        int ef = (int)(mb >> 7);
+        int s = 0;
+        if (mb != 0u && ef != 255) s = ef == 0 ? -126 : ef - 127;
+        sh[r] = s;
+    }
+}
+
+// Thread layout of the staging: a pass covers RP rows (a power of two up to
+// 16) with TPR = blockDim / RP threads per row (whole warps; blockDim a power
+// of two); thread (tr, tc) takes chunks tc, tc + TPR, ... of row tr + p * RP
+// in pass p.  A thread's j-th chunk is step q = j % NQ of pass p = j / NQ.
+// Shifts only: a division costs a long dependent chain at kernel start.
+struct StageMap {
+    int rp, tpr, tr, tc, npass, nq;
+    __device__ __forceinline__ StageMap(int nrows, int cpr)
+    {
+        const int lrp = nrows <= 1 ? 0 : nrows <= 2 ? 1 : nrows <= 4 ? 2 : nrows <= 8 ? 3 : 4;
+        const int ltpr = (31 - __clz((int)blockDim.x)) - lrp;
+        rp = 1 << lrp;
+        tpr = 1 << ltpr;
+        tr = (int)threadIdx.x >> ltpr;
+        tc = (int)threadIdx.x & (tpr - 1);
+        npass = (nrows + rp - 1) >> lrp;
+        nq = (cpr + tpr - 1) >> ltpr;
+    }
+};
+
+// The max of a pass: lanes hold their own finite maxima (a lane that saw an
+// infinity contributes 0 here and publishes its chunks exactly later), the
+// warp (one row) reduces them and lane 0 publishes.
+__device__ __forceinline__ void publish_pass(uint32_t m2, int r, int nrows, unsigned *maxbits, bool &bad)
+{
+    unsigned m = max(m2 & 0x7FFFu, (m2 >> 16) & 0x7FFFu);
+    if (m >= 0x7F80u) {
+        bad = true;
+        m = 0u;
+    }
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if ((threadIdx.x & 31) == 0 && m != 0u && r < nrows) atomicMax(&maxbits[r], m);
+}
 
 // mid() runs once the activation loads are in flight and before they are
 // used: a caller issues its weight copies there, so that the activations do
@@ -121,83 +195,126 @@ __device__ void stage_x(const uint16_t *__restrict__ x, size_t ld, int len, int 
 {
     for (int r = threadIdx.x; r < nrows; r += blockDim.x) maxbits[r] = 0u;
     __syncthreads();
-    const int cpr = (len + 31) / 32 * 4;  // 8-element chunks per row (whole units)
-    const int total = nrows * cpr;
-    const bool in_regs = total <= (int)blockDim.x * STAGE_REG_CHUNKS && (len % 8) == 0 && (ld % 8) == 0;
-    uint4 cache[STAGE_REG_CHUNKS];
-    if (!in_regs) mid();
-    // pass 1: largest finite magnitude per row (as bf16 bits)
-    for (int r = 0; r < nrows && !in_regs; ++r) {
-        const uint32_t *row = reinterpret_cast<const uint32_t *>(x + (size_t)(src ? src[r] : r) * ld);
-        unsigned m = 0;
-        for (int i = threadIdx.x; i < len / 2; i += blockDim.x) {
-            uint32_t v = row[i];
-            m = max(m, max(fin_mag(v), fin_mag(v >> 16)));
-        }
-        if (m) atomicMax(&maxbits[r], m);
-    }
-    if (in_regs) {
-        // one read: each thread caches its chunks, then reduces per row
+    // 8-element chunks per row (whole units; one all-zero chunk when len is 0)
+    const int cpr = len > 0 ? (len + 31) / 32 * 4 : 1;
+    const StageMap mp(nrows, cpr);
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    auto load = [&](int r, int c) {
+        if (r >= nrows || c * 8 >= len) return zero;
+        return *reinterpret_cast<const uint4 *>(x + (size_t)(src ? src[r] : r) * ld + c * 8);
+    };
+    bool bad = false;
+    if (mp.npass * mp.nq <= STAGE_REG_CHUNKS) {
+        uint4 cache[STAGE_REG_CHUNKS];
+        {
+            int p = 0, q = 0;
 #pragma unroll
-        for (int j = 0; j < STAGE_REG_CHUNKS; ++j) {
-            const int idx = threadIdx.x + j * blockDim.x;
-            cache[j] = make_uint4(0u, 0u, 0u, 0u);
-            if (idx < total) {
-                const int r = idx / cpr, k0 = (idx - r * cpr) * 8;
-                if (k0 < len) cache[j] = *reinterpret_cast<const uint4 *>(x + (size_t)(src ? src[r] : r) * ld + k0);
-            }
-        }
-        mid();
-        // shared atomics on one word from a warp are combined in hardware:
-        // per-chunk atomics measure faster here than a warp reduction first
-#pragma unroll
-        for (int j = 0; j < STAGE_REG_CHUNKS; ++j) {
-            const int idx = threadIdx.x + j * blockDim.x;
-            if (idx < total) {
-                const int r = idx / cpr, k0 = (idx - r * cpr) * 8;
-                if (k0 < len) {
-                    const uint4 v = cache[j];
-                    unsigned m = max(max(fin_mag(v.x), fin_mag(v.x >> 16)), max(fin_mag(v.y), fin_mag(v.y >> 16)));
-                    m = max(m, max(max(fin_mag(v.z), fin_mag(v.z >> 16)), max(fin_mag(v.w), fin_mag(v.w >> 16))));
-                    if (m) atomicMax(&maxbits[r], m);
+            for (int j = 0; j < STAGE_REG_CHUNKS; ++j) {
+                cache[j] = p < mp.npass ? load(mp.tr + p * mp.rp, mp.tc + q * mp.tpr) : zero;
+                if (++q == mp.nq) {
+                    q = 0;
+                    ++p;
                 }
             }
         }
-    }
-    __syncthreads();
-    for (int r = threadIdx.x; r < nrows; r += blockDim.x) {
-        unsigned mb = maxbits[r];
-        int ef = (int)(mb >> 7);
-        int s = 0;
-        if (mb != 0u && ef != 255) s = ef == 0 ? -126 : ef - 127;
-        sh[r] = s;
-    }
-    __syncthreads();
-    if (in_regs) {
+        mid();
+        {
+            int p = 0, q = 0;
+            uint32_t m2 = 0u;
+#pragma unroll
+            for (int j = 0; j < STAGE_REG_CHUNKS; ++j) {
+                m2 = absmax_chunk(m2, cache[j]);
+                if (++q == mp.nq) {
+                    publish_pass(m2, mp.tr + p * mp.rp, nrows, maxbits, bad);
+                    m2 = 0u;
+                    q = 0;
+                    ++p;
+                }
+            }
+        }
+        if (bad) {
+            int p = 0, q = 0;
+#pragma unroll
+            for (int j = 0; j < STAGE_REG_CHUNKS; ++j) {
+                const int r = mp.tr + p * mp.rp;
+                const unsigned m = chunk_mag_exact(cache[j]);
+                if (p < mp.npass && r < nrows && m != 0u) atomicMax(&maxbits[r], m);
+                if (++q == mp.nq) {
+                    q = 0;
+                    ++p;
+                }
+            }
+        }
+        __syncthreads();
+        stage_shifts(nrows, sh, maxbits);
+        __syncthreads();
+        int p = 0, q = 0;
+        float f = 1.0f;
 #pragma unroll
         for (int j = 0; j < STAGE_REG_CHUNKS; ++j) {
-            const int idx = threadIdx.x + j * blockDim.x;
-            if (idx < total) {
-                const int r = idx / cpr, k0 = (idx - r * cpr) * 8;
-                stage_store(xs, ks, r, k0, len, cache[j], pow2f(-sh[r]), FMT);
+            const int r = mp.tr + p * mp.rp, c = mp.tc + q * mp.tpr;
+            if (q == 0 && p < mp.npass && r < nrows) f = pow2f(-sh[r]);
+            if (p < mp.npass && r < nrows && c < cpr) stage_store(xs + (size_t)r * ks, c * 8, len, cache[j], f, FMT);
+            if (++q == mp.nq) {
+                q = 0;
+                ++p;
             }
         }
         return;
     }
-    // pass 2: convert and permute (zero past len)
-    for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
-        const int r = idx / cpr, k0 = (idx - r * cpr) * 8;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        const uint16_t *row = x + (size_t)(src ? src[r] : r) * ld;
-        if (k0 + 8 <= len && (ld % 8) == 0) {
-            v = *reinterpret_cast<const uint4 *>(row + k0);
-        } else {
-            uint32_t w[4] = {0u, 0u, 0u, 0u};
-            for (int j = 0; j < 4; ++j)
-                if (k0 + 2 * j < len) w[j] = *reinterpret_cast<const uint32_t *>(row + k0 + 2 * j);
-            v = make_uint4(w[0], w[1], w[2], w[3]);
+    mid();
+    // pass 1: raw bf16 chunks into xs (element k of row r at xs[r*ks + k])
+    // and the maxima, eight loads in flight per thread
+    for (int p = 0; p < mp.npass; ++p) {
+        const int r = mp.tr + p * mp.rp;
+        uint32_t m2 = 0u;
+        for (int q0 = 0; q0 < mp.nq; q0 += STAGE_REG_CHUNKS) {
+            uint4 cache[STAGE_REG_CHUNKS];
+#pragma unroll
+            for (int j = 0; j < STAGE_REG_CHUNKS; ++j) {
+                const int c = mp.tc + (q0 + j) * mp.tpr;
+                cache[j] = c < cpr ? load(r, c) : zero;
+            }
+#pragma unroll
+            for (int j = 0; j < STAGE_REG_CHUNKS; ++j) {
+                const int c = mp.tc + (q0 + j) * mp.tpr;
+                m2 = absmax_chunk(m2, cache[j]);
+                if (r < nrows && c < cpr) *reinterpret_cast<uint4 *>(xs + (size_t)r * ks + c * 8) = cache[j];
+            }
         }
-        stage_store(xs, ks, r, k0, len, v, pow2f(-sh[r]), FMT);
+        bool bad_p = false;
+        publish_pass(m2, r, nrows, maxbits, bad_p);
+        if (bad_p) {
+            bad = true;
+            for (int c = mp.tc; c < cpr && r < nrows; c += mp.tpr) {
+                const unsigned m = chunk_mag_exact(*reinterpret_cast<const uint4 *>(xs + (size_t)r * ks + c * 8));
+                if (m != 0u) atomicMax(&maxbits[r], m);
+            }
+        }
+    }
+    __syncthreads();
+    stage_shifts(nrows, sh, maxbits);
+    __syncthreads();
+    // pass 2: convert in place.  MX layouts keep every element where it is
+    // (a thread rewrites its own chunks); NVFP4 permutes within a 32-element
+    // unit, so a thread takes whole units (reads all four chunks first).
+    for (int p = 0; p < mp.npass; ++p) {
+        const int r = mp.tr + p * mp.rp;
+        if (r >= nrows) continue;
+        uint16_t *row = xs + (size_t)r * ks;
+        const float f = pow2f(-sh[r]);
+        if (FMT != FMT_NVFP4) {
+            for (int c = mp.tc; c < cpr; c += mp.tpr)
+                stage_store(row, c * 8, len, *reinterpret_cast<const uint4 *>(row + c * 8), f, FMT);
+        } else {
+            for (int u = mp.tc; u < cpr / 4; u += mp.tpr) {
+                uint4 v[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) v[q] = *reinterpret_cast<const uint4 *>(row + u * 32 + 8 * q);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) stage_store(row, u * 32 + 8 * q, len, v[q], f, FMT);
+            }
+        }
     }
 }
 

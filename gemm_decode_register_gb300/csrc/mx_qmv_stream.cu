@@ -26,7 +26,8 @@ struct QmvSArgs {
     int N, K;
     int m0, mc;
     int tiles;     // ceil(N / RT)
-    int G;         // CTAs per window
+    int G;         // CTAs per window (grid: G x nwin)
+    int tq, tr;    // tiles / G, tiles % G
     int nwin;      // K windows
     int WU;        // units per window (multiple of UPS)
     int pmax;      // partial-sum slots per tile (pieces a tile's K may be cut into)
@@ -51,29 +52,32 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) qmv_stream_kernel(QmvSArgs a)
     off += (((size_t)a.ntl_max * a.pmax * G::RT * MC * 4) + 15) & ~(size_t)15;
     uint8_t *rings = smem + off;
 
-    const int gb = blockIdx.x % a.G, win = blockIdx.x / a.G;
+    // (The set-up below avoids integer division where it can: at kernel
+    // start a division is a long dependent chain on the critical path.)
+    const int gb = blockIdx.x, win = blockIdx.y;
     const int U = (a.K + 31) / 32;
     const int xu0 = win * a.WU, xu1 = min(U, xu0 + a.WU);
     const int len = min(a.K - xu0 * 32, (xu1 - xu0) * 32);
 
     const int warp = threadIdx.x >> 5;
-    const int ntl = gb < a.tiles ? (a.tiles - gb + a.G - 1) / a.G : 0;
+    const int ntl = gb < a.tiles ? a.tq + (gb < a.tr ? 1 : 0) : 0;
     // The CTA's work is its tiles' stages in tile-major order (S of them).
     // Whole tiles go round-robin to the warps when that balances them (many
     // tiles); otherwise each warp takes an equal contiguous run, so the warps
     // finish together and a tile's K is cut only where runs meet (cutting
     // rows finer measured slower).  A piece's partial sums go to a slot of
     // its tile; the slots are added in K order.
+    // (32-bit counts: the planner keeps ntl * spw far below 2^27.)
     const int spw = (xu1 - xu0 + G::UPS - 1) / G::UPS;  // stages per row in this window
-    const long long S = (long long)ntl * spw;
-    long long lo_w = 0, hi_w = 0;
+    const int S = ntl * spw;
+    int lo_w = 0, hi_w = 0;
     int t_first = 0, n_my = 0;
     if (a.split) {
         lo_w = S * warp / QMV_WARPS;
         hi_w = S * (warp + 1) / QMV_WARPS;
         if (hi_w > lo_w) {
-            t_first = (int)(lo_w / spw);
-            n_my = (int)((hi_w - 1) / spw) - t_first + 1;
+            t_first = lo_w / spw;
+            n_my = (hi_w - 1) / spw - t_first + 1;
         }
     } else {
         t_first = warp;
@@ -93,10 +97,10 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) qmv_stream_kernel(QmvSArgs a)
         u.scales = a.scales;
         u.row0 = (gb + t * a.G) * G::RT;
         if (a.split) {
-            const long long t0 = (long long)t * spw;
-            const long long lo = lo_w > t0 ? lo_w : t0, hi = hi_w < t0 + spw ? hi_w : t0 + spw;
-            u.ub = xu0 + (int)(lo - t0) * G::UPS;
-            u.ul = min(xu1, xu0 + (int)(hi - t0) * G::UPS);
+            const int t0 = t * spw;
+            const int lo = lo_w > t0 ? lo_w : t0, hi = hi_w < t0 + spw ? hi_w : t0 + spw;
+            u.ub = xu0 + (lo - t0) * G::UPS;
+            u.ul = min(xu1, xu0 + (hi - t0) * G::UPS);
         } else {
             u.ub = xu0;
             u.ul = xu1;
@@ -107,11 +111,11 @@ __global__ void __launch_bounds__(QMV_THREADS, 1) qmv_stream_kernel(QmvSArgs a)
     };
     auto slot_of = [&](int i) {
         if (!a.split) return 0;
-        const long long t0 = (long long)unit_tile(i) * spw;
+        const int t0 = unit_tile(i) * spw;
         if (lo_w <= t0) return 0;
-        if (a.split == 2) return (int)(lo_w - t0);
+        if (a.split == 2) return lo_w - t0;
         // the warp whose run holds the tile's first stage
-        const int wf = (int)((QMV_WARPS * (t0 + 1) + S - 1) / S) - 1;
+        const int wf = (QMV_WARPS * (t0 + 1) + S - 1) / S - 1;
         return warp - wf;
     };
     auto xrow_of = [&](int) { return xrow; };
@@ -216,7 +220,7 @@ static cudaError_t run_qmv_stream(const DeviceState &ds, cudaStream_t st, QmvSAr
         if (e != cudaSuccess) return e;
         configured_dev[ds.device] = 1;
     }
-    return launch_k(qmv_stream_kernel<FMT, MC>, dim3(a.G * a.nwin), dim3(QMV_THREADS), smem, st, a);
+    return launch_k(qmv_stream_kernel<FMT, MC>, dim3(a.G, a.nwin), dim3(QMV_THREADS), smem, st, a);
 }
 
 // Plan and launch one token chunk; returns cudaErrorNotSupported when the
@@ -263,6 +267,8 @@ static cudaError_t plan_qmv_stream(const DeviceState &ds, cudaStream_t st, const
     a.nwin = nwin;
     a.G = nwin == 1 ? ds.num_sms : (ds.num_sms / nwin > 0 ? ds.num_sms / nwin : 1);
     if (a.G > a.tiles) a.G = a.tiles;
+    a.tq = a.tiles / a.G;
+    a.tr = a.tiles % a.G;
     a.WU = WU;
     a.ntl_max = (a.tiles + a.G - 1) / a.G;
     // K windows add their partial sums through the calling stream's workspace:
@@ -290,6 +296,7 @@ static cudaError_t plan_qmv_stream(const DeviceState &ds, cudaStream_t st, const
         a.split = 2;
         a.pmax = spw;
     }
+    if ((long long)a.ntl_max * spw * QMV_WARPS >= (1LL << 27)) return cudaErrorNotSupported;  // 32-bit counts
     const long long per = (long long)a.ntl_max * a.pmax * G::RT * MC * 4;
     const long long red_cap = (long long)ds.max_smem_optin - rings - 128 - (long long)MC * ks * 2;
     if (per > red_cap) return cudaErrorNotSupported;
