@@ -140,16 +140,11 @@ struct NoMid {
     __device__ void operator()() const {}
 };
 
-// Per-row maxima (bf16 magnitude bits) -> power-of-two exponents sh[r].
-__device__ __forceinline__ void stage_shifts(int nrows, int *sh, const unsigned *maxbits)
+// Power-of-two exponent of a row from its maximum (bf16 magnitude bits).
+__device__ __forceinline__ int stage_shift(unsigned mb)
 {
-    for (int r = threadIdx.x; r < nrows; r += blockDim.x) {
-        unsigned mb = maxbits[r];
-        int ef = (int)(mb >> 7);
-        int s = 0;
-        if (mb != 0u && ef != 255) s = ef == 0 ? -126 : ef - 127;
-        sh[r] = s;
-    }
+    const int ef = (int)(mb >> 7);
+    return (mb == 0u || ef == 255) ? 0 : (ef == 0 ? -126 : ef - 127);
 }
 
 // Thread layout of the staging: a pass covers RP rows (a power of two up to
@@ -204,13 +199,14 @@ __device__ void stage_x(const uint16_t *__restrict__ x, size_t ld, int len, int 
         return *reinterpret_cast<const uint4 *>(x + (size_t)(src ? src[r] : r) * ld + c * 8);
     };
     bool bad = false;
-    if (mp.npass * mp.nq <= STAGE_REG_CHUNKS) {
+    const int nj = mp.npass * mp.nq;  // chunks per thread
+    if (nj <= STAGE_REG_CHUNKS) {
         uint4 cache[STAGE_REG_CHUNKS];
         {
             int p = 0, q = 0;
 #pragma unroll
             for (int j = 0; j < STAGE_REG_CHUNKS; ++j) {
-                cache[j] = p < mp.npass ? load(mp.tr + p * mp.rp, mp.tc + q * mp.tpr) : zero;
+                cache[j] = j < nj ? load(mp.tr + p * mp.rp, mp.tc + q * mp.tpr) : zero;
                 if (++q == mp.nq) {
                     q = 0;
                     ++p;
@@ -223,6 +219,7 @@ __device__ void stage_x(const uint16_t *__restrict__ x, size_t ld, int len, int 
             uint32_t m2 = 0u;
 #pragma unroll
             for (int j = 0; j < STAGE_REG_CHUNKS; ++j) {
+                if (j >= nj) break;
                 m2 = absmax_chunk(m2, cache[j]);
                 if (++q == mp.nq) {
                     publish_pass(m2, mp.tr + p * mp.rp, nrows, maxbits, bad);
@@ -236,9 +233,10 @@ __device__ void stage_x(const uint16_t *__restrict__ x, size_t ld, int len, int 
             int p = 0, q = 0;
 #pragma unroll
             for (int j = 0; j < STAGE_REG_CHUNKS; ++j) {
+                if (j >= nj) break;
                 const int r = mp.tr + p * mp.rp;
                 const unsigned m = chunk_mag_exact(cache[j]);
-                if (p < mp.npass && r < nrows && m != 0u) atomicMax(&maxbits[r], m);
+                if (r < nrows && m != 0u) atomicMax(&maxbits[r], m);
                 if (++q == mp.nq) {
                     q = 0;
                     ++p;
@@ -246,15 +244,20 @@ __device__ void stage_x(const uint16_t *__restrict__ x, size_t ld, int len, int 
             }
         }
         __syncthreads();
-        stage_shifts(nrows, sh, maxbits);
-        __syncthreads();
+        // every thread derives its row's exponent (the row's first thread
+        // records it); the caller synchronises before sh is read
         int p = 0, q = 0;
         float f = 1.0f;
 #pragma unroll
         for (int j = 0; j < STAGE_REG_CHUNKS; ++j) {
+            if (j >= nj) break;
             const int r = mp.tr + p * mp.rp, c = mp.tc + q * mp.tpr;
-            if (q == 0 && p < mp.npass && r < nrows) f = pow2f(-sh[r]);
-            if (p < mp.npass && r < nrows && c < cpr) stage_store(xs + (size_t)r * ks, c * 8, len, cache[j], f, FMT);
+            if (q == 0 && r < nrows) {
+                const int e = stage_shift(maxbits[r]);
+                if (mp.tc == 0) sh[r] = e;
+                f = pow2f(-e);
+            }
+            if (r < nrows && c < cpr) stage_store(xs + (size_t)r * ks, c * 8, len, cache[j], f, FMT);
             if (++q == mp.nq) {
                 q = 0;
                 ++p;
@@ -293,8 +296,6 @@ __device__ void stage_x(const uint16_t *__restrict__ x, size_t ld, int len, int 
         }
     }
     __syncthreads();
-    stage_shifts(nrows, sh, maxbits);
-    __syncthreads();
     // pass 2: convert in place.  MX layouts keep every element where it is
     // (a thread rewrites its own chunks); NVFP4 permutes within a 32-element
     // unit, so a thread takes whole units (reads all four chunks first).
@@ -302,7 +303,9 @@ __device__ void stage_x(const uint16_t *__restrict__ x, size_t ld, int len, int 
         const int r = mp.tr + p * mp.rp;
         if (r >= nrows) continue;
         uint16_t *row = xs + (size_t)r * ks;
-        const float f = pow2f(-sh[r]);
+        const int e = stage_shift(maxbits[r]);
+        if (mp.tc == 0) sh[r] = e;
+        const float f = pow2f(-e);
         if (FMT != FMT_NVFP4) {
             for (int c = mp.tc; c < cpr; c += mp.tpr)
                 stage_store(row, c * 8, len, *reinterpret_cast<const uint4 *>(row + c * 8), f, FMT);
