@@ -252,6 +252,29 @@ static cudaError_t plan_qmv_stream(const DeviceState &ds, cudaStream_t st, const
         if (nwin > 64) return cudaErrorNotSupported;
     }
     nwin = (U + WU - 1) / WU;
+    if (nwin > 1) {
+        // Windows are needed anyway: among a few more of them take the count
+        // whose busiest CTA has the fewest stages (the windows' CTAs and the
+        // tiles per CTA change with it; ties keep fewer windows).
+        auto busiest = [&](int wu) {
+            const int nw = (U + wu - 1) / wu;
+            const int g = std::max(1, std::min(ds.num_sms / nw, tiles));
+            return (long long)((tiles + g - 1) / g) * ((wu + G::UPS - 1) / G::UPS);
+        };
+        long long best = busiest(WU);
+        for (int n = nwin + 1; n <= nwin + 2 && n <= 64; ++n) {
+            int wu = (U + n - 1) / n;
+            wu = (wu + G::UPS - 1) / G::UPS * G::UPS;
+            const long long b = busiest(wu);
+            if (b < best) {
+                best = b;
+                WU = wu;
+            }
+        }
+        ks = WU * 32;
+        if ((ks / 32) % 2 == 0) ks += 32;
+        nwin = (U + WU - 1) / WU;
+    }
     QmvSArgs a;
     a.codes = codes;
     a.scales = scales;
