@@ -137,34 +137,31 @@ __global__ void __launch_bounds__(AMAX_THREADS) quant_amax_kernel(const uint16_t
 }
 
 // Eight quotients x_i / den to E2M1 codes, identical to converting the
-// correctly rounded fp32 quotients.  The products q_i = x_i * rcp(den) (rcp
-// correctly rounded) lie within 2^-22 |q_i| of the rounded quotients (two
-// roundings of at most 2^-24 each); q_i (1 - 2^-21) and q_i (1 + 2^-21),
-// themselves rounded, bracket that interval, and since the conversion to
-// E2M1 is monotone, equal codes at both ends fix the code of the rounded
-// quotient.  Otherwise a quotient lies near a rounding boundary of E2M1 and
-// the eight are divided after all; so are they when rcp(den) overflows (den
-// below 2^-128: a tensor whose largest magnitude is below about 2^-117).
-__device__ __forceinline__ uint32_t e2m1x8_of_quotients(const float (&x)[8], float den, float rcp)
+// correctly rounded fp32 quotients Q_i.  With r = rcp(den) correctly rounded,
+// rl = r (1 - 2^-21) and rh = r (1 + 2^-21) (both rounded), the products
+// x_i rl and x_i rh (rounded) lie on either side of Q_i: each differs from
+// x_i / den by the factor 1 -/+ 2^-21 and four roundings of at most 2^-24, and
+// Q_i from x_i / den by one.  E2M1 conversion is monotone, so equal codes at
+// both ends are the code of Q_i (the code of the plain product is not needed).
+// Otherwise (rare: a quotient near a rounding boundary of E2M1, or rh beyond
+// the fp32 range) the eight are divided after all; so are they when r
+// overflows (den below 2^-128: a tensor whose largest magnitude is below
+// about 2^-117).
+__device__ __forceinline__ uint32_t e2m1x8_of_quotients(const float (&x)[8], float den, float rl, float rh)
 {
-    float q[8], lo[8], hi[8];
-    if (!(rcp <= 3.4028234663852886e38f)) {
+    float lo[8], hi[8];
+    if (rl <= 3.4028234663852886e38f) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(x[i], den);
-        return f32x8_to_e2m1x8(q);
+        for (int i = 0; i < 8; ++i) {
+            lo[i] = __fmul_rn(x[i], rl);
+            hi[i] = __fmul_rn(x[i], rh);
+        }
+        const uint32_t c = f32x8_to_e2m1x8(lo);
+        if (f32x8_to_e2m1x8(hi) == c) return c;
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        q[i] = __fmul_rn(x[i], rcp);
-        lo[i] = __fmul_rn(q[i], 1.0f - 0x1p-21f);
-        hi[i] = __fmul_rn(q[i], 1.0f + 0x1p-21f);
-    }
-    const uint32_t c = f32x8_to_e2m1x8(q);
-    if (f32x8_to_e2m1x8(lo) == c && f32x8_to_e2m1x8(hi) == c) return c;
-    float d[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) d[i] = __fdiv_rn(x[i], den);
-    return f32x8_to_e2m1x8(d);
+    for (int i = 0; i < 8; ++i) lo[i] = __fdiv_rn(x[i], den);
+    return f32x8_to_e2m1x8(lo);
 }
 
 // One block's codes (NC 32-bit words) and scale byte from its W bf16 pairs.
@@ -182,6 +179,7 @@ __device__ __forceinline__ uint32_t quant_block(const uint32_t (&w)[W], float g,
         const float den = __fmul_rn(f16_lo_to_f32(e4m3x2_to_f16x2(sbyte)), g);  // s exactly, times g
         if (den != 0.0f) {
             const float rcp = __frcp_rn(den);
+            const float rl = __fmul_rn(rcp, 1.0f - 0x1p-21f), rh = __fmul_rn(rcp, 1.0f + 0x1p-21f);
 #pragma unroll
             for (int i = 0; i < NC; ++i) {
                 float v[8];
@@ -190,7 +188,7 @@ __device__ __forceinline__ uint32_t quant_block(const uint32_t (&w)[W], float g,
                     v[2 * j] = bf16_lo(w[4 * i + j]);
                     v[2 * j + 1] = bf16_hi(w[4 * i + j]);
                 }
-                c[i] = e2m1x8_plus_zero(e2m1x8_of_quotients(v, den, rcp));
+                c[i] = e2m1x8_plus_zero(e2m1x8_of_quotients(v, den, rl, rh));
             }
         }
         return sbyte;
