@@ -376,6 +376,25 @@ def extras(torch, ops, synth, dev, stream, hbm, bf16_burst, bf16_sust, args):
                                    "us": round(t * 1e6, 2), "tok_s": round(M / t, 1)}
     del mats
 
+    # each projection alone: a graph over distinct weight copies (more than 4x L2 in all), per launch
+    L2 = 129 * 2 ** 20
+    for name, N, K, seed in DENSE:
+        wbytes = N * K // 2 + N * K // 32
+        copies = max(2, -(-4 * L2 // wbytes))
+        ws = [synth.weights_device(F4, N, K, 1000 * seed + i, dev) for i in range(copies)]
+        for M in (1, 4):
+            x = bf16_dev(torch, synth.activations(M, K, 400 + seed)).view(M, K)
+            y = torch.empty((M, N), dtype=torch.float32, device=dev)
+
+            def fp(ws=ws, x=x, y=y, N=N):
+                for c, s in ws:
+                    ops.qmv(F4, c, s, x, N, y=y)
+            g = graph_of(torch, fp)
+            t = time_region(torch, g.replay, max(5, iters // 4), stream) / copies
+            res[f"projection_{name}_M{M}"] = {"us": round(t * 1e6, 2), "gbs": round(wbytes / t / 1e9, 1),
+                                             "frac_hbm": round(wbytes / t / 1e9 / hbm, 4), "copies": copies}
+        del ws
+
     # format sweep on the FFN up/gate shape
     N, K = 57344, 8192
     for fmt, fname, seed in ((F4, "mxfp4", 2), (F8, "mxfp8", 6), (NV, "nvfp4", 7)):
