@@ -253,23 +253,23 @@ static cudaError_t plan_qmv_stream(const DeviceState &ds, cudaStream_t st, const
     }
     nwin = (U + WU - 1) / WU;
     if (nwin > 1) {
-        // Windows are needed anyway: among a few more of them take the count
-        // whose busiest CTA has the fewest stages (the windows' CTAs and the
-        // tiles per CTA change with it; ties keep fewer windows).
+        // Windows are needed anyway: one more of them is worth it when that
+        // lets the activation staging keep a thread's chunks in registers (at
+        // most 8 chunks of 8 elements per thread: rows padded to a power of
+        // two share the 512 threads) and its busiest CTA has no more stages
+        // (measured: 4 tokens, K = 28672, 3 -> 4 windows 29.3 -> 27.5 us; 8
+        // tokens, 6 -> 7 windows with one stage more, 47.3 -> 50.5 us).
+        const int rp = mc <= 1 ? 1 : mc <= 2 ? 2 : mc <= 4 ? 4 : mc <= 8 ? 8 : 16;
+        auto in_regs = [&](int wu) { return (long long)wu * rp * 4 <= (long long)QMV_THREADS * STAGE_REG_CHUNKS; };
         auto busiest = [&](int wu) {
             const int nw = (U + wu - 1) / wu;
             const int g = std::max(1, std::min(ds.num_sms / nw, tiles));
             return (long long)((tiles + g - 1) / g) * ((wu + G::UPS - 1) / G::UPS);
         };
-        long long best = busiest(WU);
-        for (int n = nwin + 1; n <= nwin + 2 && n <= 64; ++n) {
-            int wu = (U + n - 1) / n;
+        if (!in_regs(WU) && nwin < 64) {
+            int wu = (U + nwin) / (nwin + 1);
             wu = (wu + G::UPS - 1) / G::UPS * G::UPS;
-            const long long b = busiest(wu);
-            if (b < best) {
-                best = b;
-                WU = wu;
-            }
+            if (in_regs(wu) && busiest(wu) <= busiest(WU)) WU = wu;
         }
         ks = WU * 32;
         if ((ks / 32) % 2 == 0) ks += 32;
