@@ -189,6 +189,23 @@ def test_qmv_extremes(orc, fmt, wk, xk, M, N, K):
     check_special(y, want, f"qmv fmt{fmt} {wk} {xk} {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("fmt", [F4, F8, NV])
+@pytest.mark.parametrize("xk", ["nonfinite", "outlier", "wide"])
+def test_qmv_extremes_staged_in_shared_memory(orc, fmt, xk):
+    """Activations with an infinity and a NaN, an outlier or a wide range
+    through the staging path that parks raw chunks in shared memory (4 rows
+    of K = 10240): the row maxima ignore the non-finite elements there too."""
+    need_gpu()
+    from gemm_decode_register_gb300 import ops
+
+    M, N, K = 4, 96, 10240
+    codes, scales = _weights_for(fmt, None, N, K, 5 * N + fmt)
+    x = special_x(xk, M, K, 77 + fmt)
+    y = ops.qmv(fmt, dev_u8(codes), dev_u8(scales), dev_bf16(x).view(M, K), N).cpu().numpy()
+    want = orc.qmv(fmt, codes, scales, x, M, N, K)
+    check_special(y, want, f"qmv fmt{fmt} {xk} {M}x{N}x{K} (staging in shared memory)")
+
+
 # ------------------------------------------------------------------ MoE
 
 @pytest.mark.parametrize("fmt,wk,xk", ALL_CASES, ids=IDS)

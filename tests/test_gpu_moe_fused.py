@@ -113,6 +113,22 @@ def test_down_combine_ragged(orc, fmt, T, E, topk, N, K):
     check_close(out, want, f"down combine fmt{fmt}")
 
 
+@pytest.mark.parametrize("fmt", [0, 1, 2])
+def test_down_combine_rows_in_passes(orc, fmt):
+    """48 activation rows (12 tokens x top-4) of K = 768: the staging covers
+    them in three passes of 16 rows with 32 threads per row, nine chunks per
+    thread, so through shared memory."""
+    need_gpu()
+    T, E, topk, N, K = 12, 6, 4, 72, 768
+    codes, scales = synth.weights(fmt, N, K, 51 + fmt, E=E)
+    h = synth.activations(T * topk, K, 52)
+    ids = synth.expert_ids(T, E, topk, 53)
+    r = synth.router_weights(T, topk, 54)
+    out = fused_down(fmt, codes, scales, h, ids, r, E, N).cpu().numpy()
+    want = oracle_out(orc, fmt, codes, scales, h, ids, r, T, E, topk, N, K)
+    check_close(out, want, f"down combine fmt{fmt} (rows in passes)")
+
+
 def test_down_combine_workspace_path(orc):
     """Row tiles whose partial sums do not fit in a CTA's shared memory next
     to its ring (8 tokens x top-8, 57344 rows: 24 tiles of 16 rows per CTA)

@@ -40,6 +40,23 @@ CASES += [(fmt, 1, 4096, 8192) for fmt in (0, 1, 2)] + [(fmt, 2, 3000, 4096) for
 CASES += [(0, 16, 300, 1024), (1, 13, 67, 320), (2, 24, 130, 512), (0, 6, 1000, 4096)]
 
 
+# activations staged through shared memory: more than 8 chunks of 8
+# elements per thread (3-4 rows share 512 threads as 4 rows of 128 threads;
+# K = 10240 is 1280 chunks per row, one K window), so the raw bf16 chunks are
+# parked in the staging buffer and converted there in place (NVFP4: whole
+# units, its permuted layout)
+STAGED_IN_SMEM = [(fmt, M, 150, 10240) for fmt in (0, 1, 2) for M in (3, 4)]
+
+
+@pytest.mark.parametrize("fmt,M,N,K", STAGED_IN_SMEM)
+def test_qmv_staging_in_shared_memory(orc, fmt, M, N, K):
+    need_gpu()
+    codes, scales = synth.weights(fmt, N, K, 30 + M, exp_lo=118, exp_hi=132)
+    x = synth.activations(M, K, 40 + M)
+    check_close(run_qmv(fmt, codes, scales, x, N), orc.qmv(fmt, codes, scales, x, M, N, K),
+                f"fmt{fmt} M{M} N{N} K{K} (staging in shared memory)")
+
+
 @pytest.mark.parametrize("fmt,M,N,K", CASES)
 def test_qmv_parity(orc, fmt, M, N, K):
     need_gpu()
