@@ -583,10 +583,14 @@ def extras_qmm_qx(torch, ops, synth, dev, stream, bf16_burst, iters):
     relative L2 distance between the two products (a property of quantising
     the activations, not an error of either kernel)."""
     res = {}
-    peaks = {k: round(ops.mma_peak_tflops(k), 1) for k in ("bf16", "e4m3", "mxfp8", "mxfp4", "nvfp4")}
+    kinds = ("bf16", "e4m3", "mxfp8", "mxfp4", "nvfp4")
+    peaks = {k: round(ops.mma_peak_tflops(k), 1) for k in kinds}
+    filled = {k: round(ops.mma_peak_tflops(k, filled=True), 1) for k in kinds}
     res["tensor_peaks_tflops"] = dict(peaks, note="mx_mma_peak: one CTA per SM issuing 128x256xK tcgen05.mma "
-                                                  "(cta_group::1) on zero operands, best of 5; clocks stay at their "
-                                                  "maximum on zero data, so real operands run somewhat lower")
+                                                  "(cta_group::1) on zero operands, best of 5")
+    res["tensor_peaks_filled_tflops"] = dict(filled, note="the same on random finite operands (unit block "
+                                                          "scales), the same shared-memory tiles every MMA: the "
+                                                          "data does not slow the tensor pipe")
     M, N, K = 4096, 28672, 8192
     X = bf16_dev(torch, synth.activations(M, K, 58)).view(M, K)
     n = max(5, iters // 10)
@@ -607,6 +611,7 @@ def extras_qmm_qx(torch, ops, synth, dev, stream, bf16_burst, iters):
         res[f"prefill_qmm_qx_{fname}_28672x8192"] = {
             "tflops": round(fl / tg / 1e12, 1), "ms": round(tg * 1e3, 3),
             "frac_measured_peak": round(fl / tg / 1e12 / peaks[kind], 4), "peak_kind": kind,
+            "frac_filled_peak": round(fl / tg / 1e12 / filled[kind], 4),
             "quantize_us": round(tq * 1e6, 1), "tflops_with_quantize": round(fl / (tg + tq) / 1e12, 1),
             "bf16_path_tflops": round(fl / tb / 1e12, 1), "bf16_path_ms": round(tb * 1e3, 3),
             "rel_l2_vs_bf16_activations": round(dist, 4),

@@ -136,7 +136,7 @@ __host__ __device__ constexpr uint32_t bs_idesc(int n, uint32_t sfa_id = 0, uint
 // scaled kinds: the dense rate of the tensor pipe for that kind.  A wait that
 // runs past 10 s sets the error word.
 template <int KIND>
-__global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int *err)
+__global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int fill, int *err)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -146,8 +146,23 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int *err)
     uint32_t *slot = reinterpret_cast<uint32_t *>(bar + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(slot + 1);
     const int warp = threadIdx.x >> 5;
-    for (int i = threadIdx.x; i < (128 + 256) * 128 / 16; i += blockDim.x)
-        reinterpret_cast<uint4 *>(smem)[i] = make_uint4(0u, 0u, 0u, 0u);
+    // operands: zeros, or (fill) hashed bits kept finite for the kind (bf16
+    // magnitudes below 1, E4M3 without its NaN code and the sign, any FP4 code)
+    const uint32_t keep = KIND == BSK_BF16 ? 0x3F7F3F7Fu : (KIND <= BSK_MXF8 ? 0x77777777u : 0xFFFFFFFFu);
+    for (int i = threadIdx.x; i < (128 + 256) * 128 / 16; i += blockDim.x) {
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        if (fill) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t h = (uint32_t)(4 * i + j) * 0x9E3779B1u + 0x7F4A7C15u;
+                h ^= h >> 15;
+                h *= 0x2C1B3C6Du;
+                h ^= h >> 12;
+                w[j] = h & keep;
+            }
+        }
+        reinterpret_cast<uint4 *>(smem)[i] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
     fence_proxy_async_smem();
     if (threadIdx.x == 0) {
         mbar_init(bar, 1);
@@ -194,7 +209,7 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int *err)
 __host__ __device__ constexpr int mma_k(int kind) { return kind == BSK_BF16 ? 16 : kind <= BSK_MXF8 ? 32 : 64; }
 
 template <int KIND>
-static cudaError_t run_peak(const DeviceState &ds, cudaStream_t st, int iters, float *ms)
+static cudaError_t run_peak(const DeviceState &ds, cudaStream_t st, int iters, int fill, float *ms)
 {
     // more shared memory than two CTAs could share: one CTA (and one
     // tensor-memory allocation) per SM
@@ -208,7 +223,7 @@ static cudaError_t run_peak(const DeviceState &ds, cudaStream_t st, int iters, f
         return e;
     }
     e = cudaEventRecord(e0, st);
-    if (e == cudaSuccess) e = launch_k(mma_peak_kernel<KIND>, dim3(ds.num_sms), dim3(128), smem, st, iters, ds.err);
+    if (e == cudaSuccess) e = launch_k(mma_peak_kernel<KIND>, dim3(ds.num_sms), dim3(128), smem, st, iters, fill, ds.err);
     if (e == cudaSuccess) e = cudaEventRecord(e1, st);
     if (e == cudaSuccess) e = cudaEventSynchronize(e1);
     if (e == cudaSuccess) e = cudaEventElapsedTime(ms, e0, e1);
@@ -637,17 +652,20 @@ extern "C" int mx_qmm_qx(int fmt, const void *codes, const void *scales, const v
 
 extern "C" int mx_mma_peak(int kind, int iters, float *ms)
 {
-    if (!ms || iters <= 0 || kind < 0 || kind > 4) return MX_EINVAL;
+    const int fill = (kind >> 8) & 1;  // MX_PEAK_FILLED: random finite operands
+    if ((kind & ~0x100) < 0 || (kind & ~0x100) > 4) return MX_EINVAL;
+    kind &= 0xFF;
+    if (!ms || iters <= 0) return MX_EINVAL;
     DeviceState *ds = device_state();
     if (!ds) return MX_ECUDA;
     cudaStream_t st = current_stream();
     cudaError_t e;
     switch (kind) {
-    case BSK_BF16: e = run_peak<BSK_BF16>(*ds, st, iters, ms); break;
-    case BSK_E4M3: e = run_peak<BSK_E4M3>(*ds, st, iters, ms); break;
-    case BSK_MXF8: e = run_peak<BSK_MXF8>(*ds, st, iters, ms); break;
-    case BSK_MXF4: e = run_peak<BSK_MXF4>(*ds, st, iters, ms); break;
-    default: e = run_peak<BSK_NVF4>(*ds, st, iters, ms); break;
+    case BSK_BF16: e = run_peak<BSK_BF16>(*ds, st, iters, fill, ms); break;
+    case BSK_E4M3: e = run_peak<BSK_E4M3>(*ds, st, iters, fill, ms); break;
+    case BSK_MXF8: e = run_peak<BSK_MXF8>(*ds, st, iters, fill, ms); break;
+    case BSK_MXF4: e = run_peak<BSK_MXF4>(*ds, st, iters, fill, ms); break;
+    default: e = run_peak<BSK_NVF4>(*ds, st, iters, fill, ms); break;
     }
     return e == cudaSuccess ? MX_OK : MX_ECUDA;
 }

@@ -298,9 +298,12 @@ int mx_qmv_noalloc(int fmt, const void *codes, const void *scales, const void *x
  * (CUDA events on the calling thread's stream).  kind: 0 bf16 (kind::f16,
  * K = 16), 1 E4M3 (kind::f8f6f4, K = 32), 2 MXFP8 (kind::mxf8f6f4
  * block-scaled, K = 32), 3 MXFP4 (kind::mxf4, K = 64), 4 NVFP4
- * (kind::mxf4nvf4, 16-element blocks, K = 64).  FLOPs of a call:
- * 2 * 128 * 256 * K * 4 * iters * (number of SMs).  Synchronises the
- * stream. */
+ * (kind::mxf4nvf4, 16-element blocks, K = 64); the operands are zeros,
+ * or, with MX_PEAK_FILLED added to kind, hashed bits kept finite (bf16 below
+ * 1 in magnitude, E4M3 without the NaN code, any FP4 code) with unit block
+ * scales.  FLOPs of a call: 2 * 128 * 256 * K * 4 * iters * (number of SMs).
+ * MX_EINVAL for another kind.  Synchronises the stream. */
+#define MX_PEAK_FILLED 0x100
 int mx_mma_peak(int kind, int iters, float *ms);
 
 /* Test hook for the bounded waits of the tensor-core kernels (mx_qmm,
