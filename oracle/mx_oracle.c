@@ -558,7 +558,7 @@ int or_quantize(int fmt, const uint16_t *x, uint8_t *codes, uint8_t *scales, int
  * [M][K(/2)] and scales [M][K/block] (+ tensor scale), W^ as in or_qmv): the
  * reference for a matmul whose activations were quantised first (the
  * on-device quantiser above feeding a block-scaled tensor-core product).
- * Parity of such a kernel is judged against this, on the same quantised
+ * Parity of such a kernel is checked against this, on the same quantised
  * operands. */
 int or_qmm_qx(int fmt, const uint8_t *codes, const uint8_t *scales, const uint8_t *xcodes,
               const uint8_t *xscales, double *y, int64_t M, int64_t N, int64_t K)
