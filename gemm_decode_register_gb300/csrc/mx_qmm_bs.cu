@@ -653,9 +653,8 @@ extern "C" int mx_qmm_qx(int fmt, const void *codes, const void *scales, const v
 extern "C" int mx_mma_peak(int kind, int iters, float *ms)
 {
     const int fill = (kind >> 8) & 1;  // MX_PEAK_FILLED: random finite operands
-    if ((kind & ~0x100) < 0 || (kind & ~0x100) > 4) return MX_EINVAL;
-    kind &= 0xFF;
-    if (!ms || iters <= 0) return MX_EINVAL;
+    kind &= ~0x100;
+    if (kind < 0 || kind > 4 || !ms || iters <= 0) return MX_EINVAL;
     DeviceState *ds = device_state();
     if (!ds) return MX_ECUDA;
     cudaStream_t st = current_stream();

@@ -161,6 +161,24 @@ def test_quantize_rejects(lib, args, want):
     assert lib.mx_quantize(*args) == want
 
 
+@pytest.mark.parametrize("kind", [-1, 5, 0x105, 0x200, 0x300])
+def test_mma_peak_rejects_unknown_kinds(lib, kind):
+    """kind: 0..4, optionally plus MX_PEAK_FILLED (0x100); anything else is
+    MX_EINVAL, checked before the device is touched."""
+    import ctypes
+
+    ms = ctypes.c_float()
+    assert lib.mx_mma_peak(kind, 8, ctypes.byref(ms)) == -1
+
+
+def test_mma_peak_rejects_bad_arguments(lib):
+    import ctypes
+
+    ms = ctypes.c_float()
+    assert lib.mx_mma_peak(0x103, 0, ctypes.byref(ms)) == -1
+    assert lib.mx_mma_peak(3, 8, None) == -1
+
+
 def test_no_undeclared_exports(lib):
     """Every mx_* function the library exports is declared in include/mx.h
     (the header is the whole ABI)."""

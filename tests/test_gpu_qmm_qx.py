@@ -100,3 +100,19 @@ def test_qmm_qx_after_device_quantiser(orc, fmt):
     want = orc.qmm_qx(fmt, codes, scales, oc, os_, M, N, K)
     check_special(got, want, f"quantise + qmm_qx fmt{fmt}", bf16_out=True)
     assert np.all(np.isnan(got[3]))
+
+
+@pytest.mark.parametrize("kind", ["bf16", "mxfp8", "mxfp4", "nvfp4"])
+def test_mma_peak_zero_and_filled_operands(kind):
+    """The tensor-pipe microbenchmark runs on zero and on random finite
+    operands (MX_PEAK_FILLED) without a device error, at rates within a
+    factor of two of each other and of the kind's nominal ratio to bf16."""
+    need_gpu()
+    from gemm_decode_register_gb300 import ops
+
+    ops.device_error()  # clear
+    z = ops.mma_peak_tflops(kind, iters=512, reps=2)
+    f = ops.mma_peak_tflops(kind, iters=512, reps=2, filled=True)
+    assert ops.device_error() == 0
+    assert z > 0 and f > 0
+    assert 0.5 < f / z < 2.0
