@@ -106,7 +106,7 @@ def test_qmm_qx_after_device_quantiser(orc, fmt):
 def test_mma_peak_zero_and_filled_operands(kind):
     """The tensor-pipe microbenchmark runs on zero and on random finite
     operands (MX_PEAK_FILLED) without a device error, at rates within a
-    factor of two of each other and of the kind's nominal ratio to bf16."""
+    factor of two of each other."""
     need_gpu()
     from gemm_decode_register_gb300 import ops
 
