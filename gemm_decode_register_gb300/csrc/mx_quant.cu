@@ -71,18 +71,18 @@ __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // Largest |bits| of the bf16 pairs in w[0..n) (bf16 magnitudes compare as
-// integers) and whether any of them is an infinity or a NaN.
+// integers) and whether any of them is an infinity or a NaN.  One packed
+// maximum of magnitudes per pair: a NaN operand makes that half NaN (the
+// .NaN form) and an infinity is the largest magnitude, so the result is
+// 0x7F80 or above exactly when the block holds either.
 template <int N>
 __device__ __forceinline__ uint32_t bf16_amax(const uint32_t (&w)[N], bool &nonfinite)
 {
-    uint32_t m = 0;
-    nonfinite = false;
+    uint32_t m2 = 0u;
 #pragma unroll
-    for (int i = 0; i < N; ++i) {
-        const uint32_t lo = w[i] & 0x7FFFu, hi = (w[i] >> 16) & 0x7FFFu;
-        nonfinite |= lo >= 0x7F80u || hi >= 0x7F80u;
-        m = max(m, max(lo, hi));
-    }
+    for (int i = 0; i < N; ++i) asm("max.NaN.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m2) : "r"(w[i]));
+    const uint32_t m = max(m2 & 0x7FFFu, (m2 >> 16) & 0x7FFFu);
+    nonfinite = m >= 0x7F80u;
     return m;
 }
 
