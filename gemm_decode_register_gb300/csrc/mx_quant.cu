@@ -86,16 +86,28 @@ __device__ __forceinline__ uint32_t bf16_amax(const uint32_t (&w)[N], bool &nonf
     return m;
 }
 
-// Largest finite magnitude bits of the bf16 pairs of a 16-byte vector.
+// Largest finite magnitude bits of the bf16 pairs of a 16-byte vector: a
+// packed maximum of magnitudes (NaNs lose to the other operand), redone
+// element by element when an infinity (or an all-NaN pair) came out on top.
 __device__ __forceinline__ uint32_t vec_fin_amax(const uint4 &v)
 {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t m = 0;
+    uint32_t m2;
+    asm("{\n\t.reg .b32 t, u;\n\t"
+        "max.xorsign.abs.bf16x2 t, %1, %2;\n\t"
+        "max.xorsign.abs.bf16x2 u, %3, %4;\n\t"
+        "max.xorsign.abs.bf16x2 %0, t, u;\n\t}"
+        : "=r"(m2)
+        : "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
+    uint32_t m = max(m2 & 0x7FFFu, (m2 >> 16) & 0x7FFFu);
+    if (m >= 0x7F80u) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        m = 0;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const uint32_t lo = w[j] & 0x7FFFu, hi = (w[j] >> 16) & 0x7FFFu;
-        if (lo < 0x7F80u) m = max(m, lo);
-        if (hi < 0x7F80u) m = max(m, hi);
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t lo = w[j] & 0x7FFFu, hi = (w[j] >> 16) & 0x7FFFu;
+            if (lo < 0x7F80u) m = max(m, lo);
+            if (hi < 0x7F80u) m = max(m, hi);
+        }
     }
     return m;
 }
