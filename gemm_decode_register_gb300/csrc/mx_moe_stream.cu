@@ -317,8 +317,11 @@ static cudaError_t launch_moe_stream(const DeviceState &ds, cudaStream_t st, con
 
 // Work groups of 4 slots stream an expert's rows in units of a few stages
 // (K of a few thousand): a ring of MOE_DEEP stages holds a whole unit in
-// flight when shared memory allows, else the default depth.
+// flight when shared memory allows, else the default depth; groups of 8
+// slots (16-row stages) take one stage more than the default when it fits
+// (4 tokens, down projection: layer 31.6 -> 31.2 us).
 constexpr int MOE_DEEP = 5;
+constexpr int MOE_DEEP8 = 4;
 
 template <int FMT, int MC, int MODE>
 static cudaError_t run_moe_stream(const DeviceState &ds, cudaStream_t st, const MoeSArgs &a0)
@@ -339,10 +342,9 @@ static cudaError_t run_moe_stream(const DeviceState &ds, cudaStream_t st, const 
         a.lc = base + (size_t)QMV_WARPS * G::STAGES * G::STAGE_BYTES + part <= lim;
         if (!a.lc) part = 0;
     }
-    if constexpr (MC == 4) {
-        const size_t deep = base + (size_t)QMV_WARPS * MOE_DEEP * G::STAGE_BYTES + part;
-        if (deep <= lim) return launch_moe_stream<FMT, MC, MODE, MOE_DEEP>(ds, st, a, deep);
-    }
+    constexpr int DEEP = MC == 4 ? MOE_DEEP : MOE_DEEP8;
+    const size_t deep = base + (size_t)QMV_WARPS * DEEP * G::STAGE_BYTES + part;
+    if (deep <= lim) return launch_moe_stream<FMT, MC, MODE, DEEP>(ds, st, a, deep);
     const size_t smem = base + (size_t)QMV_WARPS * G::STAGES * G::STAGE_BYTES + part;
     if (smem > lim) return cudaErrorNotSupported;
     return launch_moe_stream<FMT, MC, MODE, G::STAGES>(ds, st, a, smem);
