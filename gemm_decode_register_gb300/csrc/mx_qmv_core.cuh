@@ -148,9 +148,10 @@ __device__ __forceinline__ int stage_shift(unsigned mb)
 }
 
 // Thread layout of the staging: a pass covers RP rows (a power of two up to
-// 16) with TPR = blockDim / RP threads per row (whole warps; blockDim a power
-// of two); thread (tr, tc) takes chunks tc, tc + TPR, ... of row tr + p * RP
-// in pass p.  A thread's j-th chunk is step q = j % NQ of pass p = j / NQ.
+// 16) with TPR = blockDim / RP threads per row (whole warps: blockDim is a
+// power of two of at least 512, QMV_THREADS in every caller, so that the warp
+// reduction of a row's maximum never mixes rows); thread (tr, tc) takes
+// chunks tc, tc + TPR, ... of row tr + p * RP in pass p.  A thread's j-th chunk is step q = j % NQ of pass p = j / NQ.
 // Shifts only: a division costs a long dependent chain at kernel start.
 struct StageMap {
     int rp, tpr, tr, tc, npass, nq;
