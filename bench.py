@@ -591,6 +591,14 @@ def extras_qmm_qx(torch, ops, synth, dev, stream, bf16_burst, iters):
     res["tensor_peaks_filled_tflops"] = dict(filled, note="the same on random finite operands (unit block "
                                                           "scales), the same shared-memory tiles every MMA: the "
                                                           "data does not slow the tensor pipe")
+    probes = {}
+    for k in ("mxfp8", "mxfp4"):
+        for name, fl in (("rotate", ops.PEAK_ROTATE), ("rotate_smem_stores", ops.PEAK_ROTATE | ops.PEAK_SMEM_STORES),
+                         ("rotate_tmem_stores", ops.PEAK_ROTATE | ops.PEAK_TMEM_STORES)):
+            probes[f"{k}_{name}"] = round(ops.mma_peak_tflops(k, reps=3, filled=True, flags=fl), 1)
+    res["tensor_peak_probes_tflops"] = dict(probes, note="random operands; MMAs rotating through 4 (3) stages of "
+                                                         "48 KB; meanwhile 3 warps store 16-byte vectors into "
+                                                         "shared memory, or into tensor memory, at full rate")
     M, N, K = 4096, 28672, 8192
     X = bf16_dev(torch, synth.activations(M, K, 58)).view(M, K)
     n = max(5, iters // 10)

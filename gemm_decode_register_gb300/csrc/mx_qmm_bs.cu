@@ -131,10 +131,19 @@ __host__ __device__ constexpr uint32_t bs_idesc(int n, uint32_t sfa_id = 0, uint
 
 // ------------------------------------------------------------ peak
 
+// Operand stages of the microbenchmark: A 128 rows x 128 B, then B 256 rows
+// x 128 B (48 KB); four of them.
+constexpr int PEAK_STAGE = (128 + 256) * 128;
+constexpr int PEAK_STAGES = 4;
+
 // One CTA per SM issues `iters` k-blocks of 4 MMAs of 128 x 256 x K on
-// shared-memory operands (zeros) into tensor memory, block scales 1.0 for the
-// scaled kinds: the dense rate of the tensor pipe for that kind.  A wait that
-// runs past 10 s sets the error word.
+// shared-memory operands into tensor memory, block scales 1.0 for the scaled
+// kinds: the dense rate of the tensor pipe for that kind.  Mode bits `fill`
+// (the kind's bits 8-11, see mx_mma_peak): 1 random finite operands instead
+// of zeros; 2 the MMAs rotate through the stages (3 when 4 is set) instead of
+// using one; 4 warps 1-3 meanwhile store 16-byte vectors into the fourth
+// stage at full rate; 8 they store into unused tensor-memory columns
+// instead.  A wait that runs past 10 s sets the error word.
 template <int KIND>
 __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int fill, int *err)
 {
@@ -142,16 +151,16 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int fill, i
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t *a = smem;              // 128 rows x 128 B
     uint8_t *b = smem + 128 * 128;  // 256 rows x 128 B
-    uint64_t *bar = reinterpret_cast<uint64_t *>(b + 256 * 128);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + PEAK_STAGES * PEAK_STAGE);
     uint32_t *slot = reinterpret_cast<uint32_t *>(bar + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(slot + 1);
     const int warp = threadIdx.x >> 5;
     // operands: zeros, or (fill) hashed bits kept finite for the kind (bf16
     // magnitudes below 1, E4M3 without its NaN code and the sign, any FP4 code)
     const uint32_t keep = KIND == BSK_BF16 ? 0x3F7F3F7Fu : (KIND <= BSK_MXF8 ? 0x77777777u : 0xFFFFFFFFu);
-    for (int i = threadIdx.x; i < (128 + 256) * 128 / 16; i += blockDim.x) {
+    for (int i = threadIdx.x; i < PEAK_STAGES * PEAK_STAGE / 16; i += blockDim.x) {
         uint32_t w[4] = {0u, 0u, 0u, 0u};
-        if (fill) {
+        if (fill & 1) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 uint32_t h = (uint32_t)(4 * i + j) * 0x9E3779B1u + 0x7F4A7C15u;
@@ -187,10 +196,27 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int fill, i
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (warp >= 1 && (fill & 12)) {
+        // traffic beside the MMAs: shared-memory stores into the last stage,
+        // or tensor-memory stores into columns 264-503 (the warp's lanes)
+        const uint32_t lane = threadIdx.x & 31;
+        if (fill & 4) {
+            uint4 *dst = reinterpret_cast<uint4 *>(smem + (PEAK_STAGES - 1) * PEAK_STAGE);
+            for (int i = 0; i < iters * 32; ++i)
+                dst[(i * 96 + (warp - 1) * 32 + (int)lane) % (PEAK_STAGE / 16)] = make_uint4((uint32_t)i, lane, 0u, 0u);
+        } else {
+            for (int i = 0; i < iters * 16; ++i)
+                tmem_st_x4(tmem + ((uint32_t)(32 * warp) << 16) + 264u + (uint32_t)((i * 4) % 240), (uint32_t)i);
+            tmem_wait_st();
+        }
+    }
     if (threadIdx.x == 0) {
         constexpr uint32_t idesc = bs_idesc<KIND>(256);
-        const uint32_t sa = smem_u32(a), sb = smem_u32(b);
+        const uint32_t sa0 = smem_u32(a), sb0 = smem_u32(b);
+        const int nst = (fill & 2) ? ((fill & 4) ? PEAK_STAGES - 1 : PEAK_STAGES) : 1;
         for (int i = 0; i < iters; ++i) {
+            const uint32_t so = (uint32_t)(i % nst) * (uint32_t)PEAK_STAGE;
+            const uint32_t sa = sa0 + so, sb = sb0 + so;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
                 umma1<KIND>(tmem, sw128_desc(sa + 32 * kk), sw128_desc(sb + 32 * kk), idesc, tmem + 256u, tmem + 260u,
@@ -213,7 +239,7 @@ static cudaError_t run_peak(const DeviceState &ds, cudaStream_t st, int iters, i
 {
     // more shared memory than two CTAs could share: one CTA (and one
     // tensor-memory allocation) per SM
-    const size_t smem = 128 * 1024;
+    const size_t smem = PEAK_STAGES * PEAK_STAGE + 2048;
     cudaError_t e = cudaFuncSetAttribute(mma_peak_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaEvent_t e0, e1;
@@ -652,8 +678,8 @@ extern "C" int mx_qmm_qx(int fmt, const void *codes, const void *scales, const v
 
 extern "C" int mx_mma_peak(int kind, int iters, float *ms)
 {
-    const int fill = (kind >> 8) & 1;  // MX_PEAK_FILLED: random finite operands
-    kind &= ~0x100;
+    const int fill = (kind >> 8) & 15;  // MX_PEAK_FILLED / _ROTATE / _SMEM_STORES / _TMEM_STORES
+    kind &= ~0xF00;
     if (kind < 0 || kind > 4 || !ms || iters <= 0) return MX_EINVAL;
     DeviceState *ds = device_state();
     if (!ds) return MX_ECUDA;

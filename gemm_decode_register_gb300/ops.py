@@ -194,12 +194,17 @@ def qmm_qx(fmt: int, codes: torch.Tensor, scales: torch.Tensor, xcodes: torch.Te
 MMA_KINDS = {"bf16": (0, 16), "e4m3": (1, 32), "mxfp8": (2, 32), "mxfp4": (3, 64), "nvfp4": (4, 64)}
 
 
-def mma_peak_tflops(kind: str, iters: int = 8192, reps: int = 5, filled: bool = False) -> float:
+PEAK_FILLED, PEAK_ROTATE, PEAK_SMEM_STORES, PEAK_TMEM_STORES = 0x100, 0x200, 0x400, 0x800
+
+
+def mma_peak_tflops(kind: str, iters: int = 8192, reps: int = 5, filled: bool = False, flags: int = 0) -> float:
     """Best of `reps` mx_mma_peak runs, as dense TFLOP/s of the whole GPU
-    (filled: random finite operands instead of zeros)."""
+    (filled: random finite operands instead of zeros; flags: the other
+    MX_PEAK_* bits)."""
     code, k = MMA_KINDS[kind]
+    code |= flags
     if filled:
-        code |= 0x100  # MX_PEAK_FILLED
+        code |= PEAK_FILLED
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     best = 0.0
     ms = ctypes.c_float()

@@ -301,9 +301,17 @@ int mx_qmv_noalloc(int fmt, const void *codes, const void *scales, const void *x
  * (kind::mxf4nvf4, 16-element blocks, K = 64); the operands are zeros,
  * or, with MX_PEAK_FILLED added to kind, hashed bits kept finite (bf16 below
  * 1 in magnitude, E4M3 without the NaN code, any FP4 code) with unit block
- * scales.  FLOPs of a call: 2 * 128 * 256 * K * 4 * iters * (number of SMs).
- * MX_EINVAL for another kind.  Synchronises the stream. */
+ * scales.  Added flags probe what a GEMM's pipeline adds: MX_PEAK_ROTATE
+ * rotates the MMAs through four 48 KB operand stages (three with
+ * MX_PEAK_SMEM_STORES); MX_PEAK_SMEM_STORES has three other warps store
+ * 16-byte vectors into the fourth stage at full rate meanwhile, and
+ * MX_PEAK_TMEM_STORES has them store into unused tensor-memory columns
+ * instead.  FLOPs of a call: 2 * 128 * 256 * K * 4 * iters * (number of
+ * SMs).  MX_EINVAL for another kind.  Synchronises the stream. */
 #define MX_PEAK_FILLED 0x100
+#define MX_PEAK_ROTATE 0x200
+#define MX_PEAK_SMEM_STORES 0x400
+#define MX_PEAK_TMEM_STORES 0x800
 int mx_mma_peak(int kind, int iters, float *ms);
 
 /* Test hook for the bounded waits of the tensor-core kernels (mx_qmm,

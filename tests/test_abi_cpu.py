@@ -161,10 +161,10 @@ def test_quantize_rejects(lib, args, want):
     assert lib.mx_quantize(*args) == want
 
 
-@pytest.mark.parametrize("kind", [-1, 5, 0x105, 0x200, 0x300])
+@pytest.mark.parametrize("kind", [-1, 5, 0x105, 0xF05, 0x1000, 0x2003])
 def test_mma_peak_rejects_unknown_kinds(lib, kind):
-    """kind: 0..4, optionally plus MX_PEAK_FILLED (0x100); anything else is
-    MX_EINVAL, checked before the device is touched."""
+    """kind: 0..4, optionally plus the MX_PEAK_* flags (0x100-0x800);
+    anything else is MX_EINVAL, checked before the device is touched."""
     import ctypes
 
     ms = ctypes.c_float()

@@ -116,3 +116,16 @@ def test_mma_peak_zero_and_filled_operands(kind):
     assert ops.device_error() == 0
     assert z > 0 and f > 0
     assert 0.5 < f / z < 2.0
+
+
+@pytest.mark.parametrize("flags", [0x200, 0x300, 0x700, 0xB00])
+def test_mma_peak_probe_modes(flags):
+    """The microbenchmark's probes of a GEMM pipeline (rotating operand
+    stages, other warps storing into shared or tensor memory meanwhile) run
+    without a device error."""
+    need_gpu()
+    from gemm_decode_register_gb300 import ops
+
+    ops.device_error()  # clear
+    assert ops.mma_peak_tflops("mxfp4", iters=512, reps=1, flags=flags) > 0
+    assert ops.device_error() == 0
