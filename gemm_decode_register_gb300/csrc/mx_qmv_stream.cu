@@ -287,42 +287,54 @@ static cudaError_t plan_qmv_stream(const DeviceState &ds, cudaStream_t st, const
     a.m0 = m0;
     a.mc = mc;
     a.tiles = (N + G::RT - 1) / G::RT;
-    a.nwin = nwin;
-    a.G = nwin == 1 ? ds.num_sms : (ds.num_sms / nwin > 0 ? ds.num_sms / nwin : 1);
-    if (a.G > a.tiles) a.G = a.tiles;
-    a.tq = a.tiles / a.G;
-    a.tr = a.tiles % a.G;
-    a.WU = WU;
-    a.ntl_max = (a.tiles + a.G - 1) / a.G;
-    // K windows add their partial sums through the calling stream's workspace:
-    // without one attached, or when it is too small, the chunk falls back to
-    // the direct-load kernel (which needs none)
-    if (nwin > 1 && ((size_t)nwin * mc * N > ds.ws_floats || a.G > ds.ws_counters)) return cudaErrorNotSupported;
-    if (nwin > 1 && !query && (ds.ws == nullptr || ds.ws_count == nullptr)) return cudaErrorNotSupported;
-    // work split: whole tiles round-robin when the busiest warp has at most
-    // 5 % more than the average; else equal runs of stages (a tile cut into
-    // at most pmax pieces when every warp's run has a stage, else one slot
-    // per stage offset)
-    const int spw = (WU + G::UPS - 1) / G::UPS;  // stages per row per window
-    const int spw_last = (U - (nwin - 1) * WU + G::UPS - 1) / G::UPS;  // the last window may be shorter
-    const int ntl_min = a.tiles / a.G;
-    const long long s_min = (long long)ntl_min * std::min(spw, spw_last);
-    const long long busiest = (long long)((a.ntl_max + QMV_WARPS - 1) / QMV_WARPS) * QMV_WARPS;
-    if (a.ntl_max >= QMV_WARPS && busiest * 100 <= (long long)a.ntl_max * 105) {
-        a.split = 0;
-        a.pmax = 1;
-    } else if (s_min >= QMV_WARPS) {
-        a.split = 1;
-        const long long q = s_min / QMV_WARPS;  // shortest run (stages)
-        a.pmax = (int)std::min<long long>(spw, (spw + q - 1) / q + 1);
-    } else {
-        a.split = 2;
-        a.pmax = spw;
+    // The partial-sum slots of a CTA's tile pieces must fit beside its staged
+    // activations: when they do not (few tiles per CTA cut into many pieces
+    // over a long window), one more window shrinks the staging and is tried.
+    for (int attempt = 0;; ++attempt) {
+        a.nwin = nwin;
+        a.G = nwin == 1 ? ds.num_sms : (ds.num_sms / nwin > 0 ? ds.num_sms / nwin : 1);
+        if (a.G > a.tiles) a.G = a.tiles;
+        a.tq = a.tiles / a.G;
+        a.tr = a.tiles % a.G;
+        a.WU = WU;
+        a.ntl_max = (a.tiles + a.G - 1) / a.G;
+        // K windows add their partial sums through the calling stream's
+        // workspace: without one attached, or when it is too small, the chunk
+        // falls back to the direct-load kernel (which needs none)
+        if (nwin > 1 && ((size_t)nwin * mc * N > ds.ws_floats || a.G > ds.ws_counters))
+            return cudaErrorNotSupported;
+        if (nwin > 1 && !query && (ds.ws == nullptr || ds.ws_count == nullptr)) return cudaErrorNotSupported;
+        // work split: whole tiles round-robin when the busiest warp has at
+        // most 5 % more than the average; else equal runs of stages (a tile
+        // cut into at most pmax pieces when every warp's run has a stage, else
+        // one slot per stage offset)
+        const int spw = (WU + G::UPS - 1) / G::UPS;                     // stages per row per window
+        const int spw_last = (U - (nwin - 1) * WU + G::UPS - 1) / G::UPS;  // the last window may be shorter
+        const int ntl_min = a.tiles / a.G;
+        const long long s_min = (long long)ntl_min * std::min(spw, spw_last);
+        const long long busiest = (long long)((a.ntl_max + QMV_WARPS - 1) / QMV_WARPS) * QMV_WARPS;
+        if (a.ntl_max >= QMV_WARPS && busiest * 100 <= (long long)a.ntl_max * 105) {
+            a.split = 0;
+            a.pmax = 1;
+        } else if (s_min >= QMV_WARPS) {
+            a.split = 1;
+            const long long q = s_min / QMV_WARPS;  // shortest run (stages)
+            a.pmax = (int)std::min<long long>(spw, (spw + q - 1) / q + 1);
+        } else {
+            a.split = 2;
+            a.pmax = spw;
+        }
+        if ((long long)a.ntl_max * spw * QMV_WARPS >= (1LL << 27)) return cudaErrorNotSupported;  // 32-bit counts
+        const long long per = (long long)a.ntl_max * a.pmax * G::RT * MC * 4;
+        const long long red_cap = (long long)ds.max_smem_optin - rings - 128 - (long long)MC * ks * 2;
+        if (per <= red_cap) break;
+        if (nwin >= 64 || attempt >= 16) return cudaErrorNotSupported;
+        WU = (U + nwin) / (nwin + 1);
+        WU = (WU + G::UPS - 1) / G::UPS * G::UPS;
+        ks = WU * 32;
+        if ((ks / 32) % 2 == 0) ks += 32;
+        nwin = (U + WU - 1) / WU;
     }
-    if ((long long)a.ntl_max * spw * QMV_WARPS >= (1LL << 27)) return cudaErrorNotSupported;  // 32-bit counts
-    const long long per = (long long)a.ntl_max * a.pmax * G::RT * MC * 4;
-    const long long red_cap = (long long)ds.max_smem_optin - rings - 128 - (long long)MC * ks * 2;
-    if (per > red_cap) return cudaErrorNotSupported;
     a.ks = ks;
     const size_t red = (((size_t)a.ntl_max * a.pmax * G::RT * MC * 4) + 15) & ~(size_t)15;
     const size_t smem = (size_t)MC * ks * 2 + 80 + red + rings;

@@ -57,6 +57,17 @@ def test_qmv_staging_in_shared_memory(orc, fmt, M, N, K):
                 f"fmt{fmt} M{M} N{N} K{K} (staging in shared memory)")
 
 
+# long rows: the tokens' activations span tens of K windows (a 2-D grid of
+# tile groups x windows, partial sums through the workspace)
+@pytest.mark.parametrize("fmt,M,N,K", [(0, 8, 40, 262144), (2, 3, 70, 131072)])
+def test_qmv_many_k_windows(orc, fmt, M, N, K):
+    need_gpu()
+    codes, scales = synth.weights(fmt, N, K, 60 + M, exp_lo=118, exp_hi=132)
+    x = synth.activations(M, K, 70 + M)
+    check_close(run_qmv(fmt, codes, scales, x, N), orc.qmv(fmt, codes, scales, x, M, N, K),
+                f"fmt{fmt} M{M} N{N} K{K} (many K windows)")
+
+
 @pytest.mark.parametrize("fmt,M,N,K", CASES)
 def test_qmv_parity(orc, fmt, M, N, K):
     need_gpu()
