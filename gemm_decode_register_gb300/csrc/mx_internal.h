@@ -44,6 +44,8 @@ cudaError_t launch_qmv(const DeviceState &ds, cudaStream_t st, int fmt, const ui
 cudaError_t launch_moe_qmv(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,
                            const uint8_t *scales, const uint16_t *x, const int32_t *ids, float *y,
                            int T, int E, int topk, int N, int K);
+// Whether the direct-load kernel can stage a token's row of K elements.
+bool qmv_direct_fits(const DeviceState &ds, int K);
 cudaError_t launch_qmv_direct(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,
                               const uint8_t *scales, const uint16_t *x, float *y, int M, int N, int K);
 cudaError_t launch_moe_qmv_direct(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,

@@ -130,15 +130,22 @@ static cudaError_t qmv_dispatch(const DeviceState &ds, cudaStream_t st, QmvArgs 
 
 static int round_mc(int m) { return m <= 1 ? 1 : m <= 2 ? 2 : m <= 4 ? 4 : 8; }
 
+// shared memory of a pass of mc tokens: staged rows and the warps' partials
+static size_t qmv_direct_bytes(int K, int mc)
+{
+    return (size_t)mc * stage_stride(K) * 2 + QMV_WARPS * 2 * mc * mc * 4 + 64;
+}
+
+bool qmv_direct_fits(const DeviceState &ds, int K) { return qmv_direct_bytes(K, 1) <= (size_t)ds.max_smem_optin; }
+
 cudaError_t launch_qmv_direct(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,
                        const uint8_t *scales, const uint16_t *x, float *y, int M, int N, int K)
 {
     const int ks = stage_stride(K);
     // tokens per pass: up to 8, bounded by shared memory
-    auto bytes = [&](int mc) { return (size_t)mc * ks * 2 + QMV_WARPS * 2 * mc * mc * 4 + 64; };
     int cap = 8;
-    while (cap > 1 && bytes(cap) > (size_t)ds.max_smem_optin) cap >>= 1;
-    if (bytes(1) > (size_t)ds.max_smem_optin) return cudaErrorInvalidValue;
+    while (cap > 1 && qmv_direct_bytes(K, cap) > (size_t)ds.max_smem_optin) cap >>= 1;
+    if (!qmv_direct_fits(ds, K)) return cudaErrorInvalidValue;
     for (int m0 = 0; m0 < M; m0 += cap) {
         const int mc = M - m0 < cap ? M - m0 : cap;
         const int MC = round_mc(mc);

@@ -13,6 +13,8 @@
 namespace mx {
 
 constexpr int ST_RED_BUDGET = 24 * 1024;
+// K windows at most (rows up to 2^20 elements at 8 tokens per pass need ~160)
+constexpr int ST_MAX_WINDOWS = 1024;
 
 // ------------------------------------------------------------------ dense
 
@@ -249,7 +251,7 @@ static cudaError_t plan_qmv_stream(const DeviceState &ds, cudaStream_t st, const
         ks = WU * 32;
         if ((ks / 32) % 2 == 0) ks += 32;
         if ((long long)MC * ks * 2 <= avail) break;
-        if (nwin > 64) return cudaErrorNotSupported;
+        if (nwin > ST_MAX_WINDOWS) return cudaErrorNotSupported;
     }
     nwin = (U + WU - 1) / WU;
     if (nwin > 1) {
@@ -266,7 +268,7 @@ static cudaError_t plan_qmv_stream(const DeviceState &ds, cudaStream_t st, const
             const int g = std::max(1, std::min(ds.num_sms / nw, tiles));
             return (long long)((tiles + g - 1) / g) * ((wu + G::UPS - 1) / G::UPS);
         };
-        if (!in_regs(WU) && nwin < 64) {
+        if (!in_regs(WU) && nwin < ST_MAX_WINDOWS) {
             int wu = (U + nwin) / (nwin + 1);
             wu = (wu + G::UPS - 1) / G::UPS * G::UPS;
             if (in_regs(wu) && busiest(wu) <= busiest(WU)) WU = wu;
@@ -328,7 +330,7 @@ static cudaError_t plan_qmv_stream(const DeviceState &ds, cudaStream_t st, const
         const long long per = (long long)a.ntl_max * a.pmax * G::RT * MC * 4;
         const long long red_cap = (long long)ds.max_smem_optin - rings - 128 - (long long)MC * ks * 2;
         if (per <= red_cap) break;
-        if (nwin >= 64 || attempt >= 16) return cudaErrorNotSupported;
+        if (nwin >= ST_MAX_WINDOWS || attempt >= 16) return cudaErrorNotSupported;
         WU = (U + nwin) / (nwin + 1);
         WU = (WU + G::UPS - 1) / G::UPS * G::UPS;
         ks = WU * 32;
@@ -362,18 +364,43 @@ static cudaError_t qmv_stream_chunk(const DeviceState &ds, cudaStream_t st, cons
     }
 }
 
+// One group of up to 8 tokens: the streaming kernel, else the direct-load
+// kernel (one pass over the weights, no workspace), else - for rows too long
+// for the direct kernel's staging, whose K windows' partial sums exceed the
+// workspace - the two halves of the group on their own (fewer tokens per
+// pass need less workspace).  With a query, nothing is launched and the
+// workspace the launches would use is merged into *query.
+static cudaError_t qmv_group(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,
+                             const uint8_t *scales, const uint16_t *x, float *y, int m0, int mc, int N, int K,
+                             QmvScratchNeed *query)
+{
+    QmvScratchNeed q;
+    QmvScratchNeed *qp = query ? &q : nullptr;
+    cudaError_t e;
+    if (fmt == FMT_MXFP4) e = qmv_stream_chunk<FMT_MXFP4>(ds, st, codes, scales, x, y, m0, mc, N, K, qp);
+    else if (fmt == FMT_MXFP8) e = qmv_stream_chunk<FMT_MXFP8>(ds, st, codes, scales, x, y, m0, mc, N, K, qp);
+    else e = qmv_stream_chunk<FMT_NVFP4>(ds, st, codes, scales, x, y, m0, mc, N, K, qp);
+    if (e == cudaSuccess && query) {
+        if (q.floats > query->floats) query->floats = q.floats;
+        if (q.counters > query->counters) query->counters = q.counters;
+    }
+    if (e != cudaErrorNotSupported) return e;
+    if (qmv_direct_fits(ds, K))
+        return query ? cudaSuccess
+                     : launch_qmv_direct(ds, st, fmt, codes, scales, x + (size_t)m0 * K, y + (size_t)m0 * N, mc, N, K);
+    if (mc == 1) return cudaErrorInvalidValue;
+    const int h = mc / 2;
+    e = qmv_group(ds, st, fmt, codes, scales, x, y, m0, h, N, K, query);
+    if (e != cudaSuccess) return e;
+    return qmv_group(ds, st, fmt, codes, scales, x, y, m0 + h, mc - h, N, K, query);
+}
+
 cudaError_t launch_qmv(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,
                        const uint8_t *scales, const uint16_t *x, float *y, int M, int N, int K)
 {
     if (!stream_ok(fmt, K)) return launch_qmv_direct(ds, st, fmt, codes, scales, x, y, M, N, K);
     for (int m0 = 0; m0 < M; m0 += 8) {
-        const int mc = M - m0 < 8 ? M - m0 : 8;
-        cudaError_t e;
-        if (fmt == FMT_MXFP4) e = qmv_stream_chunk<FMT_MXFP4>(ds, st, codes, scales, x, y, m0, mc, N, K);
-        else if (fmt == FMT_MXFP8) e = qmv_stream_chunk<FMT_MXFP8>(ds, st, codes, scales, x, y, m0, mc, N, K);
-        else e = qmv_stream_chunk<FMT_NVFP4>(ds, st, codes, scales, x, y, m0, mc, N, K);
-        if (e == cudaErrorNotSupported)
-            e = launch_qmv_direct(ds, st, fmt, codes, scales, x + (size_t)m0 * K, y + (size_t)m0 * N, mc, N, K);
+        const cudaError_t e = qmv_group(ds, st, fmt, codes, scales, x, y, m0, M - m0 < 8 ? M - m0 : 8, N, K, nullptr);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -383,17 +410,8 @@ QmvScratchNeed qmv_scratch_need(const DeviceState &ds, int fmt, int M, int N, in
 {
     QmvScratchNeed need;
     if (!stream_ok(fmt, K)) return need;  // the direct-load kernels use no workspace
-    for (int m0 = 0; m0 < M; m0 += 8) {
-        const int mc = M - m0 < 8 ? M - m0 : 8;
-        QmvScratchNeed q;
-        cudaError_t e;
-        if (fmt == FMT_MXFP4) e = qmv_stream_chunk<FMT_MXFP4>(ds, nullptr, nullptr, nullptr, nullptr, nullptr, m0, mc, N, K, &q);
-        else if (fmt == FMT_MXFP8) e = qmv_stream_chunk<FMT_MXFP8>(ds, nullptr, nullptr, nullptr, nullptr, nullptr, m0, mc, N, K, &q);
-        else e = qmv_stream_chunk<FMT_NVFP4>(ds, nullptr, nullptr, nullptr, nullptr, nullptr, m0, mc, N, K, &q);
-        if (e != cudaSuccess) continue;  // that chunk falls back to the direct-load kernel
-        if (q.floats > need.floats) need.floats = q.floats;
-        if (q.counters > need.counters) need.counters = q.counters;
-    }
+    for (int m0 = 0; m0 < M; m0 += 8)
+        qmv_group(ds, nullptr, fmt, nullptr, nullptr, nullptr, nullptr, m0, M - m0 < 8 ? M - m0 : 8, N, K, &need);
     return need;
 }
 

@@ -85,7 +85,9 @@ enum mx_status {
  * of dense decode GPU time):
  *   y[m][n] = sum_k x[m][k] * W[n][k],   m < M, n < N.
  * x bf16 [M][K], y fp32 [M][N].  Any M >= 1 is accepted; the weight is
- * streamed once per group of up to 8 tokens.  K must be a multiple of 32
+ * streamed once per group of up to 8 tokens (groups of rows longer than
+ * about 10^5 elements whose K windows' partial sums exceed the stream's
+ * workspace run as smaller groups).  K must be a multiple of 32
  * (MXFP4, MXFP8) or 16 (NVFP4); K <= 2^20.  codes, scales, x, y 16-byte
  * aligned. */
 int mx_qmv(int fmt, const void *codes, const void *scales, const void *x, float *y, int M, int N,
@@ -281,8 +283,9 @@ int mx_moe_combine(const float *yd, const float *r, float *out, int T, int topk,
  * image (262,144 fp32 partial sums plus 4,096 counters), held by every GPU
  * that loads the library until the process exits.  A group of 8 tokens whose
  * workspace would not fit (many tokens times large N with K split into
- * windows) runs on the slower direct-load kernel, which needs none, so every
- * shape mx_qmv takes is served.  The first call on a device looks up the array's
+ * windows) runs on the slower direct-load kernel, which needs none, or, when
+ * its rows are too long for that kernel's staging, as two smaller groups
+ * (each needing less workspace), so every shape mx_qmv takes is served.  The first call on a device looks up the array's
  * device address and the device attributes; make that first call before any
  * stream capture.  Every call shares the one array, so two calls that
  * overlap on the GPU (for example on two streams) race; each call clears

@@ -59,13 +59,38 @@ def test_qmv_staging_in_shared_memory(orc, fmt, M, N, K):
 
 # long rows: the tokens' activations span tens of K windows (a 2-D grid of
 # tile groups x windows, partial sums through the workspace)
-@pytest.mark.parametrize("fmt,M,N,K", [(0, 8, 40, 262144), (2, 3, 70, 131072)])
+@pytest.mark.parametrize("fmt,M,N,K", [(0, 8, 40, 262144), (2, 3, 70, 131072), (0, 8, 16, 1 << 20), (1, 4, 16, 1 << 20),
+                                       (2, 2, 24, 1 << 20), (0, 1, 24, 1 << 20)])
 def test_qmv_many_k_windows(orc, fmt, M, N, K):
     need_gpu()
     codes, scales = synth.weights(fmt, N, K, 60 + M, exp_lo=118, exp_hi=132)
     x = synth.activations(M, K, 70 + M)
     check_close(run_qmv(fmt, codes, scales, x, N), orc.qmv(fmt, codes, scales, x, M, N, K),
                 f"fmt{fmt} M{M} N{N} K{K} (many K windows)")
+
+
+def test_qmv_windows_beyond_the_workspace(orc):
+    """8 tokens of rows of 2^20 elements and 3456 weight rows (1.8 GB of
+    codes, drawn on the device): the K windows' partial sums of one group
+    exceed the stream's 16 MiB workspace and the row is too long for the
+    direct-load kernel, so the group runs as two groups of 4; checked on 64
+    sampled weight rows."""
+    need_gpu()
+    import torch
+    from gemm_decode_register_gb300 import ops
+
+    fmt, M, N, K = 0, 8, 3456, 1 << 20
+    dev = torch.device("cuda")
+    c, sc = synth.weights_device(fmt, N, K, 77, dev, exp_lo=118, exp_hi=132)
+    x = synth.activations(M, K, 78)
+    y = ops.qmv(fmt, c, sc, dev_bf16(x).view(M, K), N).cpu().numpy()
+    rng = np.random.default_rng(79)
+    rows = np.unique(np.concatenate([np.arange(16), np.arange(N - 16, N), rng.integers(0, N, 32)]))
+    sub_c = c.view(N, K // 2)[torch.from_numpy(rows).cuda()].cpu().numpy().reshape(-1)
+    sub_s = sc.view(N, K // 32)[torch.from_numpy(rows).cuda()].cpu().numpy().reshape(-1)
+    want = orc.qmv(fmt, sub_c, sub_s, x, M, rows.size, K)
+    check_close(y[:, rows], want, "8 x 3456 x 2^20 (groups split for the workspace)")
+    del c, sc
 
 
 @pytest.mark.parametrize("fmt,M,N,K", CASES)
