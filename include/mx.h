@@ -102,7 +102,10 @@ int mx_qmv(int fmt, const void *codes, const void *scales, const void *x, float 
  * above); x bf16 [T][K]; expert_ids int32 [T][topk]; y fp32 [T][topk][N].
  * Slots that share an expert are served by one pass over that expert's
  * weights.  The routing is read on the device (no host copy).  T*topk <=
- * 1024, E <= 4096.  The ids are read as soon as the kernel starts, before it
+ * 1024, E <= 4096; the T rows of x (padded bf16) and the routing tables
+ * must fit one CTA's shared memory (about 110,000 elements of K for one
+ * token, proportionally fewer for more), else MX_EUNSUPPORTED; the same
+ * bound holds for the fused MoE calls with their staged rows.  The ids are read as soon as the kernel starts, before it
  * waits for the preceding kernel on the stream (the routed experts' weights
  * start streaming under that kernel's tail): they must be complete when the
  * call is issued, i.e. not written by a kernel that lets its dependents start
