@@ -413,46 +413,46 @@ cudaError_t launch_moe_gate_up_swiglu(const DeviceState &ds, cudaStream_t st, in
                                       const uint8_t *scales, const uint16_t *x, const int32_t *ids, uint16_t *h,
                                       int T, int E, int topk, int I, int K)
 {
-    if (!stream_ok(fmt, K)) {
-        // rows not 128-element aligned: the direct-load MoE kernel writes the
-        // gate and up products to the workspace, then the SwiGLU glue (the
-        // same silu and rounding) forms h
-        if ((size_t)T * topk * 2 * I > ds.ws_floats || ds.ws == nullptr) return cudaErrorInvalidValue;
-        cudaError_t e = launch_moe_qmv_direct(ds, st, fmt, codes, scales, x, ids, ds.ws, T, E, topk, 2 * I, K);
-        if (e != cudaSuccess) return e;
-        return launch_swiglu(ds, st, ds.ws, h, T * topk, I);
+    if (stream_ok(fmt, K)) {
+        MoeSArgs a = moe_args(ds, codes, scales, x, ids, T, E, topk, 2 * I, K);
+        a.h = h;
+        a.I = I;
+        const cudaError_t e = moe_stream_fmt<MOE_GATE_UP_SWIGLU>(ds, st, fmt, a, moe_mc(T));
+        if (e != cudaErrorNotSupported) return e;
     }
-    MoeSArgs a = moe_args(ds, codes, scales, x, ids, T, E, topk, 2 * I, K);
-    a.h = h;
-    a.I = I;
-    const cudaError_t e = moe_stream_fmt<MOE_GATE_UP_SWIGLU>(ds, st, fmt, a, moe_mc(T));
-    return e == cudaErrorNotSupported ? cudaErrorInvalidValue : e;
+    // rows not 128-element aligned, or too long to stage beside the ring: the
+    // direct-load MoE kernel writes the gate and up products to the
+    // workspace, then the SwiGLU glue (the same silu and rounding) forms h
+    if ((size_t)T * topk * 2 * I > ds.ws_floats || ds.ws == nullptr) return cudaErrorInvalidValue;
+    cudaError_t e = launch_moe_qmv_direct(ds, st, fmt, codes, scales, x, ids, ds.ws, T, E, topk, 2 * I, K);
+    if (e != cudaSuccess) return e;
+    return launch_swiglu(ds, st, ds.ws, h, T * topk, I);
 }
 
 cudaError_t launch_moe_down_combine(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,
                                     const uint8_t *scales, const uint16_t *h, const int32_t *ids, const float *rw,
                                     float *out, int T, int E, int topk, int N, int K)
 {
-    if (!stream_ok(fmt, K)) {
-        // rows not 128-element aligned: per-slot down products from the
-        // direct-load MoE kernel through the workspace, then the router
-        // combine (fused multiply-adds in slot order, as the fused kernel)
-        if ((size_t)T * topk * N > ds.ws_floats || ds.ws == nullptr) return cudaErrorInvalidValue;
-        cudaError_t e = launch_moe_qmv_direct(ds, st, fmt, codes, scales, h, ids, ds.ws, T * topk, E, 1, N, K);
-        if (e != cudaSuccess) return e;
-        return launch_moe_combine(ds, st, ds.ws, rw, out, T, topk, N);
+    if ((size_t)T * topk * N > ds.ws_floats || ds.ws == nullptr) return cudaErrorInvalidValue;
+    if (stream_ok(fmt, K)) {
+        const int MC = moe_mc_down(T);
+        const int RT = 2 * MC;
+        if ((N + RT - 1) / RT > ds.ws_counters) return cudaErrorInvalidValue;
+        MoeSArgs a = moe_args(ds, codes, scales, h, ids, T, E, topk, N, K);
+        a.rw = rw;
+        a.out = out;
+        a.ws = ds.ws;
+        a.ws_count = ds.ws_count;
+        const cudaError_t e = moe_stream_fmt<MOE_DOWN_COMBINE>(ds, st, fmt, a, MC);
+        if (e != cudaErrorNotSupported) return e;
     }
-    const int MC = moe_mc_down(T);
-    const int RT = 2 * MC;
-    if ((size_t)T * topk * N > ds.ws_floats || (N + RT - 1) / RT > ds.ws_counters || ds.ws == nullptr)
-        return cudaErrorInvalidValue;
-    MoeSArgs a = moe_args(ds, codes, scales, h, ids, T, E, topk, N, K);
-    a.rw = rw;
-    a.out = out;
-    a.ws = ds.ws;
-    a.ws_count = ds.ws_count;
-    const cudaError_t e = moe_stream_fmt<MOE_DOWN_COMBINE>(ds, st, fmt, a, MC);
-    return e == cudaErrorNotSupported ? cudaErrorInvalidValue : e;
+    // rows not 128-element aligned, or too long to stage beside the ring:
+    // per-slot down products from the direct-load MoE kernel through the
+    // workspace, then the router combine (fused multiply-adds in slot order,
+    // as the fused kernel)
+    cudaError_t e = launch_moe_qmv_direct(ds, st, fmt, codes, scales, h, ids, ds.ws, T * topk, E, 1, N, K);
+    if (e != cudaSuccess) return e;
+    return launch_moe_combine(ds, st, ds.ws, rw, out, T, topk, N);
 }
 
 }  // namespace mx

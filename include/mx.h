@@ -104,8 +104,11 @@ int mx_qmv(int fmt, const void *codes, const void *scales, const void *x, float 
  * weights.  The routing is read on the device (no host copy).  T*topk <=
  * 1024, E <= 4096; the T rows of x (padded bf16) and the routing tables
  * must fit one CTA's shared memory (about 110,000 elements of K for one
- * token, proportionally fewer for more), else MX_EUNSUPPORTED; the same
- * bound holds for the fused MoE calls with their staged rows.  The ids are read as soon as the kernel starts, before it
+ * token, proportionally fewer for more), else MX_EUNSUPPORTED.  The fused
+ * MoE calls have the same bound on their staged rows (x's T rows for
+ * mx_moe_gate_up_swiglu, h's T*topk rows for mx_moe_down_combine); rows too
+ * long for their streaming kernels run through the direct-load kernel and
+ * the workspace instead.  The ids are read as soon as the kernel starts, before it
  * waits for the preceding kernel on the stream (the routed experts' weights
  * start streaming under that kernel's tail): they must be complete when the
  * call is issued, i.e. not written by a kernel that lets its dependents start

@@ -241,3 +241,36 @@ def test_fused_k_not_multiple_of_128(orc, fmt, K):
     out = fused_down(fmt, c2, s2, h, ids, r, E, N).cpu().numpy()
     check_close(out, oracle_out(orc, fmt, c2, s2, h, ids, r, T, E, topk, N, K), f"down-combine K{K} fmt{fmt}")
 
+
+
+@pytest.mark.parametrize("fmt", [0, 1, 2])
+@pytest.mark.parametrize("T,K", [(1, 65536), (2, 49152)])
+def test_gate_up_swiglu_rows_beyond_the_ring(orc, fmt, T, K):
+    """Rows of x too long to stage beside the streaming kernel's weight ring
+    (65536 elements of one token, 49152 of two: more than 227 KB together)
+    run through the direct-load kernel and the SwiGLU glue; h is the same
+    bf16 rounding of the same products."""
+    need_gpu()
+    E, topk, I = 4, 2, 40
+    codes, scales = synth.weights(fmt, 2 * I, K, 61 + fmt, E=E)
+    x = synth.activations(T, K, 62 + T)
+    ids = synth.expert_ids(T, E, topk, 63 + T)
+    hb = bf16_host(fused_gate_up(fmt, codes, scales, x, ids, E, I)).reshape(T * topk, I)
+    want = oracle_h(orc, fmt, codes, scales, x, ids, T, E, topk, I, K)
+    check_close(bf16_bits_to_f64(hb), bf16_bits_to_f64(want), f"gate-up fmt{fmt} K{K}", bf16_out=True)
+
+
+@pytest.mark.parametrize("fmt", [0, 1, 2])
+def test_down_combine_rows_beyond_the_ring(orc, fmt):
+    """Four rows of h (2 tokens x top-2) of 16384 elements do not fit beside
+    the streaming kernel's ring: per-slot products from the direct-load
+    kernel, then the slot-order router combine."""
+    need_gpu()
+    T, E, topk, N, K = 2, 5, 2, 37, 16384
+    codes, scales = synth.weights(fmt, N, K, 71 + fmt, E=E)
+    h = synth.activations(T * topk, K, 72)
+    ids = synth.expert_ids(T, E, topk, 73)
+    r = synth.router_weights(T, topk, 74)
+    out = fused_down(fmt, codes, scales, h, ids, r, E, N).cpu().numpy()
+    want = oracle_out(orc, fmt, codes, scales, h, ids, r, T, E, topk, N, K)
+    check_close(out, want, f"down combine fmt{fmt} K{K}")
