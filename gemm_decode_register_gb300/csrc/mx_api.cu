@@ -195,8 +195,8 @@ extern "C" int mx_moe_gate_up_swiglu(int fmt, const void *expert_codes, const vo
         return MX_EALIGN;
     DeviceState *ds = device_state();
     if (!ds) return MX_ECUDA;
-    DeviceState v = *ds;  // K not a multiple of 128: gate/up products pass through the stream's workspace
-    if (K % 128 != 0 && !attach_stream_workspace(v, t_stream)) return MX_ECUDA;
+    DeviceState v = *ds;  // rows the streaming kernel cannot take: gate/up products pass through the workspace
+    if (!attach_stream_workspace(v, t_stream)) return MX_ECUDA;
     cudaError_t e = launch_moe_gate_up_swiglu(v, t_stream, fmt, static_cast<const uint8_t *>(expert_codes),
                                               static_cast<const uint8_t *>(expert_scales),
                                               static_cast<const uint16_t *>(x), expert_ids,

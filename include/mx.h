@@ -38,8 +38,8 @@
  * re-entrant across host threads and streams, and return as soon as the
  * kernels are queued.  The device error word is a variable of the library
  * image.  Calls whose kernels pass partial sums through global memory
- * (mx_qmv when K is split across CTAs, mx_moe_down_combine, NVFP4
- * mx_quantize) use a 16 MiB workspace slot of the stream they are issued on,
+ * (mx_qmv when K is split across CTAs, mx_moe_gate_up_swiglu for rows the
+ * streaming kernel cannot take, mx_moe_down_combine, NVFP4 mx_quantize) use a 16 MiB workspace slot of the stream they are issued on,
  * so calls on different streams never share one; a stream's slot is
  * allocated and cleared by the first such call on it (cudaMalloc, with the
  * calling thread switched to relaxed capture mode for it, so that first call
