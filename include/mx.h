@@ -131,10 +131,11 @@ int mx_moe_qmv(int fmt, const void *expert_codes, const void *expert_scales, con
  * rows I..2I-1 up (NVFP4: E fp32 tensor scales after the whole
  * [E][2I][K/16] scale block).  x bf16 [T][K]; h bf16 [T][topk][I].  silu and
  * the rounding are those of mx_swiglu, so h equals mx_swiglu applied to
- * mx_moe_qmv's output with N = 2I.  When K is not a multiple of 128 the
- * products come from the direct-load MoE kernel through the calling stream's
- * workspace slot, then the SwiGLU glue (two launches; T*topk*2I <= 4 Mi
- * floats).  Other limits and the bad-id behaviour (h rows NaN) as in
+ * mx_moe_qmv's output with N = 2I.  When K is not a multiple of 128, or
+ * the staged rows of x do not fit beside the streaming kernel's weight ring,
+ * the products come from the direct-load MoE kernel through the calling
+ * stream's workspace slot, then the SwiGLU glue (two launches; T*topk*2I <=
+ * 4 Mi floats).  Other limits and the bad-id behaviour (h rows NaN) as in
  * mx_moe_qmv.  codes, scales, x, h 16-byte aligned; ids 4-byte aligned. */
 int mx_moe_gate_up_swiglu(int fmt, const void *expert_codes, const void *expert_scales, const void *x,
                           const int32_t *expert_ids, void *h, int T, int E, int topk, int I, int K);
@@ -151,8 +152,10 @@ int mx_moe_gate_up_swiglu(int fmt, const void *expert_codes, const void *expert_
  * there, else they go through the library's device workspace slot of the
  * calling stream (T*topk*N <= 4 Mi floats, counters re-armed by the call
  * itself); either way the sum runs in slot order.  A bad id sets MX_DEVERR_BAD_EXPERT and makes that token's
- * outputs NaN.  When K is not a multiple of 128 the per-slot products come
- * from the direct-load MoE kernel, then the router combine (two launches).
+ * outputs NaN.  When K is not a multiple of 128, or the staged rows of h do
+ * not fit beside the streaming kernel's weight ring, the per-slot products
+ * come from the direct-load MoE kernel, then the router combine (two
+ * launches).
  * h, out, codes, scales 16-byte aligned,
  * ids and r 4-byte aligned.  Calls on one stream run in order; calls on
  * different streams use different workspace slots. */
