@@ -557,8 +557,8 @@ def extras_moe_prefill(torch, ops, synth, dev, stream, bf16_burst, iters):
     res["moe_prefill_ffn_T4096"] = {"tok_s": round(T / t, 1), "us": round(t * 1e6, 1),
                                     "tflops": round(fl / t / 1e12, 1),
                                     "frac_bf16_burst": round(fl / t / 1e12 / bf16_burst, 4),
-                                    "path": "mx_moe_ffn_prefill: route, gather, grouped gate-up GEMM + SwiGLU, "
-                                            "grouped down GEMM, combine (5 launches)"}
+                                    "path": "mx_moe_ffn_prefill: routing (count, scan, place + gather), grouped "
+                                            "gate-up GEMM + SwiGLU, grouped down GEMM, combine (6 launches)"}
     for name, d, e, xin, idv, N, K in (("gate_up", d1, e1, x, ids, 2 * I, H),
                                        ("down", d2, e2, h, ids.reshape(-1, 1).contiguous(), H, I)):
         Tq, tk = idv.shape
@@ -569,7 +569,8 @@ def extras_moe_prefill(torch, ops, synth, dev, stream, bf16_burst, iters):
         flq = 2.0 * Tq * tk * N * K
         res[f"moe_prefill_qmm_{name}"] = {"tflops": round(flq / tq / 1e12, 1), "us": round(tq * 1e6, 1),
                                           "frac_bf16_burst": round(flq / tq / 1e12 / bf16_burst, 4),
-                                          "path": "mx_moe_qmm: route, gather, grouped GEMM (3 launches)"}
+                                          "path": "mx_moe_qmm: count, scan, place + gather, grouped GEMM "
+                                                  "(4 launches)"}
         del y, wsq
     return res
 

@@ -14,10 +14,19 @@
 // pass over its block-float weights.
 //
 // Launches (all with programmatic dependent launch; each waits for the one
-// before it before touching the workspace):
-//   moe_group_route_*        one block: per-expert counts, exclusive scans,
+// before it before touching the workspace).  Up to 256 experts:
+//   moe_count_kernel         per chunk of 128 slots: its rows per expert
+//   moe_scan_kernel          one block: per expert, the exclusive prefix of
+//                            the chunks' counts; exclusive scans over the
+//                            experts, the group tile table
+//   moe_place_gather_kernel  per chunk: each slot's sorted row (its chunk's
+//                            first row of the expert plus a cursor), and the
+//                            chunk's X rows copied into expert order
+// More experts:
+//   moe_group_route_kernel   one block: per-expert counts, exclusive scans,
 //                            the group tile table, sorted row -> slot
 //   gather_rows_kernel       X rows into expert order (bf16, 16-byte copies)
+// Then:
 //   qmm_kernel (grouped)     per group tile and column tile; output rows
 //                            scattered back to slot order, or (SwiGLU mode)
 //                            h in expert order
@@ -29,6 +38,9 @@
 //   xs       2 * S * K bytes: gathered activations (the FFN's down
 //            projection writes its per-slot outputs here afterwards)
 //   hs       2 * S * I bytes (FFN only): SwiGLU output in expert order
+//   blk      (up to 256 experts) 4 * E * (CP + 1) bytes: per expert, the
+//            chunks' counts, then their first sorted rows (row stride CP,
+//            the chunk count rounded up to 128), and pos[E]
 #include "mx_common.cuh"
 #include "mx_internal.h"
 
@@ -36,6 +48,13 @@ namespace mx {
 
 constexpr int GROUP_ROWS = 512;  // rows of a group tile (two 256-row pair MMAs sharing the decoded weights)
 constexpr int ROUTE_THREADS = 1024;
+constexpr int ROUTE_SMALL_E = 256;   // experts the multi-block routing takes
+constexpr int ROUTE_CHUNK = 128;     // slots per counting / placing block
+constexpr int GATHER_THREADS = 512;   // threads of a placing block (one warp per copied row)
+
+// Chunks of ROUTE_CHUNK slots, and the row stride of their count table.
+static int route_chunks(long long S) { return (int)((S + ROUTE_CHUNK - 1) / ROUTE_CHUNK); }
+static int route_stride(int C) { return (C + 127) / 128 * 128; }
 
 static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
@@ -51,7 +70,9 @@ MoeGroupPlan moe_group_plan(int T, int E, int topk, int K, int I)
     p.off_slot = align256(16 + 16 * (size_t)p.max_groups);
     p.off_xs = align256(p.off_slot + 4 * (size_t)S);
     p.off_hs = align256(p.off_xs + 2 * (size_t)S * K);
-    p.bytes = I > 0 ? align256(p.off_hs + 2 * (size_t)S * I) : p.off_hs;
+    p.off_blk = I > 0 ? align256(p.off_hs + 2 * (size_t)S * I) : p.off_hs;
+    const size_t blk = E <= ROUTE_SMALL_E ? 4 * (size_t)E * (route_stride(route_chunks(S)) + 1) : 0;
+    p.bytes = align256(p.off_blk + blk);
     return p;
 }
 
@@ -165,76 +186,146 @@ __global__ void __launch_bounds__(ROUTE_THREADS) moe_group_route_kernel(const in
     if (tid == 0 && bad) set_device_error(err, DEVERR_BAD_EXPERT);
 }
 
-// One block, E <= ROUTE_SMALL_E: warp w takes a contiguous run of slots and
-// keeps its own per-expert counts, so atomics only ever contend within a
-// warp; the warps' counts, scanned per expert, give each warp a contiguous
-// range of every expert's rows to fill.
-constexpr int ROUTE_SMALL_E = 256;
-constexpr int ROUTE_BATCHES = 8;
-
-__global__ void __launch_bounds__(ROUTE_THREADS) moe_group_route_small_kernel(const int32_t *__restrict__ ids, int S,
-                                                                              int E, int *__restrict__ groups,
-                                                                              int *__restrict__ slot_of,
-                                                                              uint16_t *ynan, int ynan_w, int *err)
+// Rows per expert of chunk blockIdx.x (ROUTE_CHUNK slots, one per thread)
+// into blk[e][chunk] (row stride CP).  Slots with an expert id outside
+// [0, E) count nowhere; they set DEVERR_BAD_EXPERT and, when ynan is given,
+// their output row of ynan_w bf16 values is written as NaN.
+__global__ void __launch_bounds__(ROUTE_CHUNK) moe_count_kernel(const int32_t *__restrict__ ids, int S, int E, int CP,
+                                                                int *__restrict__ blk, uint16_t *ynan, int ynan_w,
+                                                                int *err)
 {
-    constexpr int NW = ROUTE_THREADS / 32;
-    __shared__ int hist[NW][ROUTE_SMALL_E];  // per warp: count, then its next row within the expert
+    __shared__ int hist[ROUTE_SMALL_E];
+    const int tid = threadIdx.x, c = blockIdx.x;
+    const int s = c * ROUTE_CHUNK + tid;
+    pdl_trigger();
+    pdl_wait();  // the ids may come from the previous kernel; the count table may still be read by it
+    const int e = s < S ? ids[s] : 0;
+    for (int i = tid; i < E; i += ROUTE_CHUNK) hist[i] = 0;
+    __syncthreads();
+    if (s < S) {
+        if ((unsigned)e < (unsigned)E) {
+            atomicAdd(&hist[e], 1);
+        } else {
+            set_device_error(err, DEVERR_BAD_EXPERT);
+            if (ynan) nan_row(ynan, s, ynan_w);
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < E; i += ROUTE_CHUNK) blk[(size_t)i * CP + c] = hist[i];
+}
+
+// Four consecutive entries of a count row, those at chunk C and beyond as 0.
+__device__ __forceinline__ int4 load_counts(const int *row, int c0, int C)
+{
+    int4 v = __ldcg(reinterpret_cast<const int4 *>(row + c0));
+    if (c0 + 0 >= C) v.x = 0;
+    if (c0 + 1 >= C) v.y = 0;
+    if (c0 + 2 >= C) v.z = 0;
+    if (c0 + 3 >= C) v.w = 0;
+    return v;
+}
+
+// One block of ROUTE_THREADS: per expert e, blk[e][c] becomes the number of
+// e's rows in chunks before c.  tpe lanes of a warp share an expert's row,
+// which they read in rounds of tpe consecutive 16-byte pieces (4 chunks
+// each; coalesced), scanning each round across the lanes and carrying its
+// total into the next; the experts' totals then give the exclusive scans,
+// the group tile table (groups) and pos[e] (the expert's first sorted row)
+// in posg.
+__global__ void __launch_bounds__(ROUTE_THREADS) moe_scan_kernel(int *__restrict__ blk, int C, int CP, int E,
+                                                                 int *__restrict__ groups, int *__restrict__ posg)
+{
     __shared__ int cnt[ROUTE_SMALL_E], pos[ROUTE_SMALL_E], tile0[ROUTE_SMALL_E];
-    __shared__ int bad;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int run = (S + NW - 1) / NW;
-    const int s0 = min(warp * run, S), s1 = min(s0 + run, S);
+    const int tid = threadIdx.x;
     pdl_trigger();
     pdl_wait();
-    for (int i = tid; i < NW * ROUTE_SMALL_E; i += ROUTE_THREADS) (&hist[0][0])[i] = 0;
-    if (tid == 0) bad = 0;
-    __syncthreads();
-    // ids are read ROUTE_BATCHES batches of 32 at a time, all loads in flight
-    // before the first is used
-    for (int b0 = s0; b0 < s1; b0 += 32 * ROUTE_BATCHES) {
-        int key[ROUTE_BATCHES];
+    int tpe = 32;  // lanes per expert: a power of two, within one warp
+    while (tpe > 1 && tpe * E > ROUTE_THREADS) tpe >>= 1;
+    const int e = tid / tpe, j = tid - e * tpe;
+    const bool mine = e < E;
+    int *row = blk + (size_t)(mine ? e : 0) * CP;
+    const int rounds = CP / (4 * tpe);  // at least 1: CP is a multiple of 128
+    int carry = 0;
+    for (int r0 = 0; r0 < rounds; r0 += 8) {
+        int4 v[8];
 #pragma unroll
-        for (int i = 0; i < ROUTE_BATCHES; ++i) {
-            const int s = b0 + 32 * i + lane;
-            key[i] = s < s1 ? ids[s] : 0;
-        }
+        for (int u = 0; u < 8; ++u)
+            v[u] = mine && r0 + u < rounds ? load_counts(row, 4 * ((r0 + u) * tpe + j), C) : make_int4(0, 0, 0, 0);
 #pragma unroll
-        for (int i = 0; i < ROUTE_BATCHES; ++i) {
-            const int s = b0 + 32 * i + lane;
-            if (s >= s1) continue;
-            if ((unsigned)key[i] < (unsigned)E) {
-                atomicAdd(&hist[warp][key[i]], 1);
-            } else {
-                bad = 1;
-                if (ynan) nan_row(ynan, s, ynan_w);
+        for (int u = 0; u < 8; ++u) {
+            if (r0 + u >= rounds) break;  // the same for every lane
+            const int sum = v[u].x + v[u].y + v[u].z + v[u].w;
+            int inc = sum;  // inclusive scan of the round over the expert's lanes
+            for (int o = 1; o < tpe; o <<= 1) {
+                const int t = __shfl_up_sync(0xFFFFFFFFu, inc, o, tpe);
+                if (j >= o) inc += t;
             }
+            const int total = __shfl_sync(0xFFFFFFFFu, inc, tpe - 1, tpe);
+            int run = carry + inc - sum;
+            int4 o4;
+            o4.x = run;
+            run += v[u].x;
+            o4.y = run;
+            run += v[u].y;
+            o4.z = run;
+            run += v[u].z;
+            o4.w = run;
+            if (mine) *reinterpret_cast<int4 *>(row + 4 * ((r0 + u) * tpe + j)) = o4;
+            carry += total;
         }
     }
-    __syncthreads();
-    for (int e = tid; e < E; e += ROUTE_THREADS) {
-        int off = 0;
-        for (int w = 0; w < NW; ++w) {
-            const int c = hist[w][e];
-            hist[w][e] = off;
-            off += c;
-        }
-        cnt[e] = off;
-    }
+    if (mine && j == 0) cnt[e] = carry;
     __syncthreads();
     route_scan_tiles(cnt, pos, tile0, E, groups);
-    for (int b0 = s0; b0 < s1; b0 += 32 * ROUTE_BATCHES) {
-        int key[ROUTE_BATCHES];
-#pragma unroll
-        for (int i = 0; i < ROUTE_BATCHES; ++i) {
-            const int s = b0 + 32 * i + lane;
-            key[i] = s < s1 ? ids[s] : -1;
+    for (int i = tid; i < E; i += ROUTE_THREADS) posg[i] = pos[i];
+}
+
+// Chunk blockIdx.x: each valid slot takes the next sorted row of its expert
+// (the chunk's first row of that expert, blk, plus a cursor; an expert's
+// rows are in no particular order: each output row depends on its own X row
+// only), records slot_of, and the chunk's X rows are copied to their sorted
+// rows (one warp per row, 16-byte copies, eight in flight per lane).
+__global__ void __launch_bounds__(GATHER_THREADS) moe_place_gather_kernel(
+    const int32_t *__restrict__ ids, int S, int E, const int *__restrict__ blk, int CP, const int *__restrict__ posg,
+    int *__restrict__ slot_of, const uint16_t *__restrict__ x, int topk, int K, uint16_t *__restrict__ xs)
+{
+    __shared__ int cur[ROUTE_SMALL_E];
+    __shared__ int prow[ROUTE_CHUNK];
+    const int tid = threadIdx.x, c = blockIdx.x;
+    const int s = c * ROUTE_CHUNK + tid;
+    pdl_trigger();
+    pdl_wait();
+    const int e = tid < ROUTE_CHUNK && s < S ? ids[s] : -1;
+    for (int i = tid; i < E; i += GATHER_THREADS) cur[i] = __ldcg(posg + i) + __ldcg(blk + (size_t)i * CP + c);
+    __syncthreads();
+    if (tid < ROUTE_CHUNK) {
+        int p = -1;
+        if ((unsigned)e < (unsigned)E) {
+            p = atomicAdd(&cur[e], 1);
+            slot_of[p] = s;
         }
-#pragma unroll
-        for (int i = 0; i < ROUTE_BATCHES; ++i)
-            if ((unsigned)key[i] < (unsigned)E)
-                slot_of[pos[key[i]] + atomicAdd(&hist[warp][key[i]], 1)] = b0 + 32 * i + lane;
+        prow[tid] = p;
     }
-    if (tid == 0 && bad) set_device_error(err, DEVERR_BAD_EXPERT);
+    __syncthreads();
+    const int warp = tid >> 5, lane = tid & 31;
+    const int vec = K / 8;  // 16-byte chunks per row
+    for (int i = warp; i < ROUTE_CHUNK; i += GATHER_THREADS / 32) {
+        const int p = prow[i];
+        if (p < 0) continue;
+        const int t = (c * ROUTE_CHUNK + i) / topk;
+        // x may have been written by the kernel before this one: coherent (L2) loads
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * K);
+        uint4 *dst = reinterpret_cast<uint4 *>(xs + (size_t)p * K);
+        int k = lane;
+        for (; k + 224 < vec; k += 256) {
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = __ldcg(src + k + 32 * u);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) dst[k + 32 * u] = v[u];
+        }
+        for (; k < vec; k += 32) dst[k] = __ldcg(src + k);
+    }
 }
 
 // xs[p] = x[slot_of[p] / topk] for the valid sorted rows, one warp per row.
@@ -298,6 +389,18 @@ static cudaError_t route_and_gather(const DeviceState &ds, cudaStream_t st, cons
     int *groups = reinterpret_cast<int *>(ws + p.off_groups);
     int *slot_of = reinterpret_cast<int *>(ws + p.off_slot);
     uint16_t *xs = reinterpret_cast<uint16_t *>(ws + p.off_xs);
+    if (E <= ROUTE_SMALL_E) {
+        const int C = route_chunks(p.S), CP = route_stride(C);
+        int *blk = reinterpret_cast<int *>(ws + p.off_blk);
+        int *posg = blk + (size_t)E * CP;
+        cudaError_t e = launch_k(moe_count_kernel, dim3(C), dim3(ROUTE_CHUNK), 0, st, ids, p.S, E, CP, blk, ynan,
+                                 ynan_w, ds.err);
+        if (e != cudaSuccess) return e;
+        e = launch_k(moe_scan_kernel, dim3(1), dim3(ROUTE_THREADS), 0, st, blk, C, CP, E, groups, posg);
+        if (e != cudaSuccess) return e;
+        return launch_k(moe_place_gather_kernel, dim3(C), dim3(GATHER_THREADS), 0, st, ids, p.S, E,
+                        (const int *)blk, CP, (const int *)posg, slot_of, x, topk, K, xs);
+    }
     // three [E] int tables: up to 48 KiB, plus the static shared memory
     static int configured_dev[64] = {0};
     if (ds.device < 64 && !configured_dev[ds.device]) {
@@ -306,11 +409,8 @@ static cudaError_t route_and_gather(const DeviceState &ds, cudaStream_t st, cons
         if (e != cudaSuccess) return e;
         configured_dev[ds.device] = 1;
     }
-    cudaError_t e = E <= ROUTE_SMALL_E
-                        ? launch_k(moe_group_route_small_kernel, dim3(1), dim3(ROUTE_THREADS), 0, st, ids, p.S, E,
-                                   groups, slot_of, ynan, ynan_w, ds.err)
-                        : launch_k(moe_group_route_kernel, dim3(1), dim3(ROUTE_THREADS), (size_t)3 * E * sizeof(int),
-                                   st, ids, p.S, E, groups, slot_of, ynan, ynan_w, ds.err);
+    cudaError_t e = launch_k(moe_group_route_kernel, dim3(1), dim3(ROUTE_THREADS), (size_t)3 * E * sizeof(int), st,
+                             ids, p.S, E, groups, slot_of, ynan, ynan_w, ds.err);
     if (e != cudaSuccess) return e;
     int blocks = (p.S + 7) / 8;  // 8 warps (rows) per block
     const int cap = ds.num_sms * 8;

@@ -205,8 +205,10 @@ int mx_qmm_qx(int fmt, const void *codes, const void *scales, const void *xcodes
  * (release post, section "Bandwidth utilisation per model"); here the
  * (token, slot) rows are grouped by expert on the device, gathered into
  * expert order and multiplied in tiles of up to 512 rows as in mx_qmm, so
- * each expert's weights are decoded once per 512 routed rows.  Launches: routing
- * (one block), the gather, the grouped GEMM.
+ * each expert's weights are decoded once per 512 routed rows.  Launches: for
+ * up to 256 experts, per-chunk row counts, one scan block (the group tile
+ * table) and the placement of each row with the gather of its x row; for
+ * more experts, one routing block and the gather; then the grouped GEMM.
  * workspace: caller-owned device memory of at least
  * mx_moe_qmm_workspace_size(T, E, topk, K) bytes, 256-byte aligned (else
  * MX_EINVAL / MX_EALIGN); the call overwrites it, so calls sharing one

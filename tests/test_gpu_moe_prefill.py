@@ -55,8 +55,8 @@ def test_moe_qmm_parity(orc, fmt, T, E, topk, N, K):
 
 
 def test_moe_qmm_many_experts(orc):
-    """More experts than the per-warp counting tables hold (E = 300): the
-    routing takes its shared-counter path."""
+    """More experts than the multi-block routing takes (E = 300): one routing
+    block with shared counters, then the separate gather."""
     need_gpu()
     fmt, T, E, topk, N, K = 0, 64, 300, 4, 256, 64
     codes, scales = synth.weights(fmt, N, K, 60, E=E)
@@ -68,6 +68,25 @@ def test_moe_qmm_many_experts(orc):
     want, rc = orc.moe_qmv(fmt, codes, scales, x, ids, T, E, topk, N, K)
     assert rc == 0
     check_close(bf16_bits_to_f64(y), want.reshape(T * topk, N), "moe_qmm E=300", bf16_out=True)
+
+
+@pytest.mark.parametrize("E", [256, 32, 7])
+def test_moe_qmm_route_chunks(orc, E):
+    """3000 routed rows in 24 chunks of 128 slots (the last one partial), one
+    expert taking a third of them across every chunk: per-chunk counts,
+    their scan over the chunks (4, 32 and 32 threads per expert) and the
+    placement with the gather."""
+    need_gpu()
+    fmt, T, topk, N, K = 0, 1500, 2, 128, 64
+    codes, scales = synth.weights(fmt, N, K, 68, E=E)
+    x = synth.activations(T, K, 69)
+    ids = synth.expert_ids(T, E, topk, 70)
+    ids[::3, 0] = E - 1
+    ids[::3, 1] = (ids[::3, 1] + 1) % (E - 1)  # distinct from the first slot
+    y = bf16_host(run_moe_qmm(fmt, codes, scales, x, ids, E, N)).reshape(T * topk, N)
+    want, rc = orc.moe_qmv(fmt, codes, scales, x, ids, T, E, topk, N, K)
+    assert rc == 0
+    check_close(bf16_bits_to_f64(y), want.reshape(T * topk, N), f"moe_qmm E={E} chunks", bf16_out=True)
 
 
 def test_moe_qmm_skewed_routing(orc):
