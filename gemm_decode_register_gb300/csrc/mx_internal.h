@@ -80,7 +80,7 @@ cudaError_t launch_qmm_grouped(const DeviceState &ds, cudaStream_t st, int fmt, 
 struct MoeGroupPlan {
     int S = 0;           // routed rows (T * topk)
     int max_groups = 0;  // most group tiles any routing can make
-    size_t off_groups = 0, off_slot = 0, off_xs = 0, off_hs = 0, off_blk = 0, bytes = 0;
+    size_t off_groups = 0, off_slot = 0, off_xs = 0, off_hs = 0, bytes = 0;
 };
 MoeGroupPlan moe_group_plan(int T, int E, int topk, int K, int I /* 0: no FFN */);
 cudaError_t launch_moe_qmm(const DeviceState &ds, cudaStream_t st, int fmt, const uint8_t *codes,

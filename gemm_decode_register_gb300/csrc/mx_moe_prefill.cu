@@ -35,16 +35,18 @@
 // Workspace (caller-owned, 256-byte aligned), in this order:
 //   groups   16 + 16 * max_groups bytes: tile count, valid rows, tiles
 //   slot_of  4 * S bytes (S = T * topk)
-//   xs       2 * S * K bytes: gathered activations (the FFN's down
-//            projection writes its per-slot outputs here afterwards)
-//   hs       2 * S * I bytes (FFN only): SwiGLU output in expert order
 //   blk      (up to 256 experts) 4 * E * (CP + 1) bytes: per expert, the
 //            chunks' counts, then their first sorted rows (row stride CP,
 //            the chunk count rounded up to 128), and pos[E]
+//   xs       2 * S * K bytes: gathered activations (the FFN's down
+//            projection writes its per-slot outputs here afterwards)
+//   hs       2 * S * I bytes (FFN only): SwiGLU output in expert order
 #include "mx_common.cuh"
 #include "mx_internal.h"
 
 namespace mx {
+
+static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 constexpr int GROUP_ROWS = 512;  // rows of a group tile (two 256-row pair MMAs sharing the decoded weights)
 constexpr int ROUTE_THREADS = 1024;
@@ -56,7 +58,13 @@ constexpr int GATHER_THREADS = 512;   // threads of a placing block (one warp pe
 static int route_chunks(long long S) { return (int)((S + ROUTE_CHUNK - 1) / ROUTE_CHUNK); }
 static int route_stride(int C) { return (C + 127) / 128 * 128; }
 
-static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+// Byte offset of the count table (right after slot_of) and its size.
+static size_t route_table_offset(size_t off_slot, long long S) { return align256(off_slot + 4 * (size_t)S); }
+static size_t route_table_bytes(long long S, int E)
+{
+    return E <= ROUTE_SMALL_E ? 4 * (size_t)E * (route_stride(route_chunks(S)) + 1) : 0;
+}
+
 
 MoeGroupPlan moe_group_plan(int T, int E, int topk, int K, int I)
 {
@@ -68,11 +76,9 @@ MoeGroupPlan moe_group_plan(int T, int E, int topk, int K, int I)
     p.max_groups = (int)((S + (long long)(GROUP_ROWS - 1) * active) / GROUP_ROWS);
     p.off_groups = 0;
     p.off_slot = align256(16 + 16 * (size_t)p.max_groups);
-    p.off_xs = align256(p.off_slot + 4 * (size_t)S);
+    p.off_xs = align256(route_table_offset(p.off_slot, S) + route_table_bytes(S, E));
     p.off_hs = align256(p.off_xs + 2 * (size_t)S * K);
-    p.off_blk = I > 0 ? align256(p.off_hs + 2 * (size_t)S * I) : p.off_hs;
-    const size_t blk = E <= ROUTE_SMALL_E ? 4 * (size_t)E * (route_stride(route_chunks(S)) + 1) : 0;
-    p.bytes = align256(p.off_blk + blk);
+    p.bytes = I > 0 ? align256(p.off_hs + 2 * (size_t)S * I) : p.off_hs;
     return p;
 }
 
@@ -391,7 +397,7 @@ static cudaError_t route_and_gather(const DeviceState &ds, cudaStream_t st, cons
     uint16_t *xs = reinterpret_cast<uint16_t *>(ws + p.off_xs);
     if (E <= ROUTE_SMALL_E) {
         const int C = route_chunks(p.S), CP = route_stride(C);
-        int *blk = reinterpret_cast<int *>(ws + p.off_blk);
+        int *blk = reinterpret_cast<int *>(ws + route_table_offset(p.off_slot, p.S));
         int *posg = blk + (size_t)E * CP;
         cudaError_t e = launch_k(moe_count_kernel, dim3(C), dim3(ROUTE_CHUNK), 0, st, ids, p.S, E, CP, blk, ynan,
                                  ynan_w, ds.err);

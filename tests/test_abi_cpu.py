@@ -106,19 +106,19 @@ def _align256(v):
 def test_prefill_workspace_sizes(lib, T, E, topk, K, I):
     """Workspace = tile table (16 bytes + 16 per group tile of up to 512
     rows, at most (S + 511 * min(S, E)) / 512 tiles for S = T * topk routed
-    rows) + sorted row -> slot (4 S) + gathered activations (2 S K)
-    [+ SwiGLU output 2 S I] + for E <= 256 the routing's count table (4
-    bytes per expert and chunk of 128 slots, the chunk count rounded up to
-    128, plus 4 bytes per expert), each part 256-byte aligned."""
+    rows) + sorted row -> slot (4 S) + for E <= 256 the routing's count
+    table (4 bytes per expert and chunk of 128 slots, the chunk count
+    rounded up to 128, plus 4 bytes per expert) + gathered activations
+    (2 S K) [+ SwiGLU output 2 S I], each part 256-byte aligned."""
     S = T * topk
     tiles = (S + 511 * min(S, E)) // 512
     chunks = (S + 127) // 128
     blk = 4 * E * ((chunks + 127) // 128 * 128 + 1) if E <= 256 else 0
-    plain = _align256(_align256(16 + 16 * tiles) + 4 * S) + 2 * S * K
-    assert lib.mx_moe_qmm_workspace_size(T, E, topk, K) == _align256(_align256(plain) + blk)
+    xs = _align256(_align256(_align256(16 + 16 * tiles) + 4 * S) + blk)
+    plain = _align256(xs + 2 * S * K)
+    assert lib.mx_moe_qmm_workspace_size(T, E, topk, K) == plain
     if I:
-        ffn = _align256(_align256(plain) + 2 * S * I)
-        assert lib.mx_moe_ffn_prefill_workspace_size(T, E, topk, K, I) == _align256(ffn + blk)
+        assert lib.mx_moe_ffn_prefill_workspace_size(T, E, topk, K, I) == _align256(plain + 2 * S * I)
     assert lib.mx_moe_qmm_workspace_size(0, E, topk, K) == 0
     assert lib.mx_moe_qmm_workspace_size(T, E, E + 1, K) == 0
 
