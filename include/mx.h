@@ -228,8 +228,8 @@ int mx_moe_qmm(int fmt, const void *expert_codes, const void *expert_scales, con
  *   yd[t][j] = bf16_rne( W_dn,e h[t][j] )
  *   out[t][n] = sum_j r[t][j] * yd[t][j][n]  (fp32 fused multiply-adds in slot order)
  * e = expert_ids[t][j]; gate-up stacks [E][2I][H], down stacks [E][H][I];
- * x bf16 [T][H]; r fp32 [T][topk]; out fp32 [T][H].  Launches: routing,
- * gather, grouped gate-up GEMM with the SwiGLU in its epilogue (CTA pairs
+ * x bf16 [T][H]; r fp32 [T][topk]; out fp32 [T][H].  Launches: routing and
+ * gather (as mx_moe_qmm), grouped gate-up GEMM with the SwiGLU in its epilogue (CTA pairs
  * whose two halves hold gate row i and up row I + i), grouped down GEMM,
  * combine.  workspace: at least mx_moe_ffn_prefill_workspace_size(T, E,
  * topk, H, I) bytes, 256-byte aligned.  H and I multiples of 32 (each is the
